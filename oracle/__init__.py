@@ -1,0 +1,236 @@
+"""CPU oracle for the block-FP8 fused MoE expert layer (TEST INFRASTRUCTURE).
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  The product path (``block_fp8_mixture_topk_gb300``)
+never imports it, and it imports nothing from there: the two share no code.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, fp64 sums, OpenMP over
+independent rows); this module only compiles it with gcc on first use and
+marshals numpy arrays.  Every function cites the passage it follows in the C
+source.  bf16 tensors are passed as ``uint16`` arrays holding the bf16 bits.
+
+Parity status: every function is pinned by ``tests/test_oracle_*.py`` except the
+bytes of the requantised intermediate (SiLU(gate)*up): those depend on fp32
+rounding order and are compared only within +-1 e4m3 code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_moe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cmd = ["gcc", "-O2", "-std=gnu11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            L = ctypes.c_long
+            I = ctypes.c_int
+            lib.orc_e4m3_value.argtypes = [I]
+            lib.orc_e4m3_value.restype = ctypes.c_double
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
+            lib.orc_bf16_from_f64.restype = ctypes.c_uint16
+            lib.orc_quant_1x128_f32.argtypes = [P, L, L, P, P]
+            lib.orc_quant_1x128_bf16.argtypes = [P, L, L, P, P]
+            lib.orc_quant_128x128_bf16.argtypes = [P, L, L, L, P, P]
+            lib.orc_route.argtypes = [P, P, L, I, I, I, I, I, I, ctypes.c_double, P, P]
+            lib.orc_route.restype = I
+            lib.orc_permute.argtypes = [P, L, I, P, P, P]
+            lib.orc_experts.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P]
+            lib.orc_combine.argtypes = [P, P, P, P, L, L, I, P]
+            lib.orc_num_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return _load().orc_num_threads()
+
+
+# --------------------------------------------------------------------------- e4m3 / bf16
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 e4m3fn codes (NaN for 0x7F / 0xFF)."""
+    lib = _load()
+    return np.array([lib.orc_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest e4m3fn code of each fp32 value (ties to even, saturating)."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    for i in range(flat_in.size):
+        flat_out[i] = lib.orc_e4m3_encode(float(flat_in[i]))
+    return out
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """fp64 value of e4m3 codes."""
+    return e4m3_values()[np.asarray(codes, dtype=np.uint8)]
+
+
+def bf16_from_f64(x) -> np.ndarray:
+    """Nearest-even bf16 bits (uint16) of fp64 values."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    fi, fo = x.reshape(-1), out.reshape(-1)
+    for i in range(fi.size):
+        fo[i] = lib.orc_bf16_from_f64(float(fi[i]))
+    return out
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bits."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------- quantisers
+
+def quant_1x128_bf16(x_bits: np.ndarray):
+    """1x128 group quantisation of bf16 rows: returns (codes [R,C] u8, scales [R,C/128] f32)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, C = x.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((R, C // 128), dtype=np.float32)
+    _load().orc_quant_1x128_bf16(_ptr(x), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_1x128_f32(x: np.ndarray):
+    """1x128 group quantisation of fp32 rows: returns (codes, scales)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((R, C // 128), dtype=np.float32)
+    _load().orc_quant_1x128_f32(_ptr(x), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_128x128_bf16(w_bits: np.ndarray):
+    """128x128 block quantisation of stacked bf16 weights [E,N,K]: (codes [E,N,K], scales [E,N/128,K/128])."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    E, N, K = w.shape
+    assert N % 128 == 0 and K % 128 == 0
+    q = np.empty((E, N, K), dtype=np.uint8)
+    s = np.empty((E, N // 128, K // 128), dtype=np.float32)
+    _load().orc_quant_128x128_bf16(_ptr(w), E, N, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+# --------------------------------------------------------------------------- routing / permute
+
+SOFTMAX, SIGMOID = 0, 1
+
+
+def route(logits: np.ndarray, topk: int, renormalize: bool = True, scoring: int = SOFTMAX,
+          bias: np.ndarray | None = None, n_group: int = 1, topk_group: int = 1,
+          routed_scaling: float = 1.0):
+    """Top-k routing: returns (ids [T,k] int32, weights [T,k] f32)."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = l.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    ids = np.empty((T, topk), dtype=np.int32)
+    w = np.empty((T, topk), dtype=np.float32)
+    rc = _load().orc_route(_ptr(l), _ptr(b), T, E, topk, int(bool(renormalize)), scoring,
+                           n_group, topk_group, float(routed_scaling), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError(f"oracle route rejected the arguments (rc={rc})")
+    return ids, w
+
+
+def permute(ids: np.ndarray, E: int):
+    """Stable sort of pairs by expert: returns (offsets [E+1], sorted [P], pos [P])."""
+    flat = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    P = flat.size
+    offsets = np.empty(E + 1, dtype=np.int32)
+    sorted_ = np.empty(P, dtype=np.int32)
+    pos = np.empty(P, dtype=np.int32)
+    _load().orc_permute(_ptr(flat), P, E, _ptr(offsets), _ptr(sorted_), _ptr(pos))
+    return offsets, sorted_, pos
+
+
+# --------------------------------------------------------------------------- full layer
+
+def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
+                scoring=SOFTMAX, bias=None, n_group=1, topk_group=1, routed_scaling=1.0,
+                tokens=None, want_c1=False):
+    """The whole layer on the CPU.
+
+    hidden_bits [T,H] uint16 (bf16 bits), logits [T,E] f32, w13 [E,2I,H] u8,
+    w13_scale [E,2I/128,H/128] f32, w2 [E,H,I] u8, w2_scale [E,H/128,I/128] f32.
+    ``tokens``: optional iterable of token indices to compute (others stay NaN).
+    Returns a dict with ids, weights, offsets, sorted, pos, a1q, a1s, a2q, a2s
+    (by sorted row), c2 (by sorted row), out (fp64 [T,H]) and out_bf16 bits.
+    """
+    hidden_bits = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
+    T, H = hidden_bits.shape
+    E, N1, H2 = w13.shape
+    assert H2 == H and N1 % 256 == 0
+    I = N1 // 2
+    assert w2.shape == (E, H, I)
+    ids, wts = route(logits, topk, renormalize, scoring, bias, n_group, topk_group, routed_scaling)
+    offsets, sorted_, pos = permute(ids, E)
+    a1q, a1s = quant_1x128_bf16(hidden_bits)
+    P = T * topk
+    need = np.zeros(T, dtype=np.uint8)
+    if tokens is None:
+        need[:] = 1
+    else:
+        need[np.asarray(list(tokens), dtype=np.int64)] = 1
+    a2q = np.zeros((P, I), dtype=np.uint8)
+    a2s = np.zeros((P, I // 128), dtype=np.float32)
+    c1 = np.full((P, N1), np.nan) if want_c1 else None
+    c2 = np.full((P, H), np.nan)
+    w13c = np.ascontiguousarray(w13, dtype=np.uint8)
+    w2c = np.ascontiguousarray(w2, dtype=np.uint8)
+    w13s = np.ascontiguousarray(w13_scale, dtype=np.float32)
+    w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
+    _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
+                        _ptr(offsets), _ptr(sorted_), _ptr(need), T, H, I, E, topk,
+                        _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2))
+    out = np.full((T, H), np.nan)
+    _load().orc_combine(_ptr(c2), _ptr(wts), _ptr(pos), _ptr(need), T, H, topk, _ptr(out))
+    out_bf16 = np.zeros((T, H), dtype=np.uint16)
+    rows = np.nonzero(need)[0]
+    if rows.size:
+        out_bf16[rows] = bf16_from_f64(out[rows])
+    return dict(ids=ids, weights=wts, offsets=offsets, sorted=sorted_, pos=pos, a1q=a1q, a1s=a1s,
+                a2q=a2q, a2s=a2s, c1=c1, c2=c2, out=out, out_bf16=out_bf16, need=need)
