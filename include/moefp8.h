@@ -1,0 +1,214 @@
+/*
+ * moefp8 — block-FP8 fused Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument documented "device" is caller-owned device
+ * memory of the current CUDA device; "host" pointers are caller-owned host
+ * memory.  The library allocates no memory per call: scratch space is the
+ * caller's workspace, whose size the matching *_workspace_size function gives.
+ * All calls are asynchronous on the given stream (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream) and never synchronise the host.
+ *
+ * Return value of every int function: MOE_OK (0) or a negative MOE_ERR_* code.
+ * Argument errors are detected on the host before anything is enqueued.
+ * Problems only the device can see (a routed expert id out of range, a pipeline
+ * wait that ran past its time limit) never trap: they set bits in a device
+ * status word, read with moe_get_device_status after synchronising.
+ *
+ * Tensor layouts (row-major, innermost dimension last):
+ *   hidden        bf16  [T, H]            (bf16 passed as uint16_t bit patterns)
+ *   router_logits fp32  [T, E]
+ *   w13           e4m3  [E, 2I, H]        rows [0, I) gate, rows [I, 2I) up
+ *   w13_scale     fp32  [E, 2I/128, H/128]
+ *   w2            e4m3  [E, H, I]
+ *   w2_scale      fp32  [E, H/128, I/128]
+ *   out           bf16  [T, H]
+ * "e4m3" is float8 e4m3fn (1-4-3, bias 7, max 448, no infinities) stored as
+ * uint8_t.  H and I must be multiples of 128.
+ *
+ * Sources: the pages "Quantization and MoE Optimizations" (vLLM wiki),
+ * "vllm.model_executor.layers.fused_moe.oracle.fp8" and
+ * "vllm.model_executor.layers.quantization.online.nvfp4" (vLLM API docs).
+ */
+#ifndef MOEFP8_H
+#define MOEFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)          /* null pointer, negative size, bad enum */
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2)    /* H or I not a multiple of 128, topk > E, ... */
+#define MOE_ERR_WORKSPACE_TOO_SMALL (-3)
+#define MOE_ERR_CUDA (-4)                 /* a CUDA runtime call failed */
+#define MOE_ERR_DEVICE (-5)               /* current device is not sm_103 (GB300) */
+
+/* device status bits (moe_get_device_status) */
+#define MOE_STATUS_WAIT_TIMEOUT 0x1u      /* a pipeline wait gave up; outputs invalid */
+#define MOE_STATUS_BAD_EXPERT_ID 0x2u     /* a routed id was outside [0, E); pair dropped */
+
+/* Limits of this implementation. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_GROUPS 32
+#define MOE_BLOCK_M 128                   /* rows per expert tile of the grouped GEMMs */
+
+/* ---- routing -------------------------------------------------------------- */
+#define MOE_SCORING_SOFTMAX 0
+#define MOE_SCORING_SIGMOID 1
+
+/* Router options ("router — top-K router" of the FusedMoE layer and the
+ * "fused grouped top-K routing" switch, page "Quantization and MoE
+ * Optimizations", sections FusedMoE Class and Key Environment Variables).
+ * A NULL moe_routing_params* means softmax scoring, no grouping, scaling 1.   */
+typedef struct moe_routing_params {
+    int32_t scoring;        /* MOE_SCORING_SOFTMAX or MOE_SCORING_SIGMOID */
+    int32_t n_group;        /* 1 = ungrouped; > 1 (sigmoid only): E/n_group consecutive experts per group */
+    int32_t topk_group;     /* groups kept when n_group > 1 */
+    float routed_scaling;   /* multiplies the final weights (1.0 = none) */
+    const float* bias;      /* device fp32 [E] selection bias, or NULL (sigmoid only) */
+} moe_routing_params;
+
+/* Top-k routing of T tokens over E experts.
+ *   softmax: the k largest logits (ties: lower index); weight = softmax
+ *            probability, renormalised over the chosen k if renormalize != 0.
+ *   sigmoid: s = fp32(1/(1+exp(-logit))) evaluated in fp64; b = s + bias
+ *            selects; grouped: group score = sum of its two largest b, the
+ *            topk_group best groups are kept (ties: lower group), the k largest
+ *            b among their experts are chosen; weight = s, renormalised over the
+ *            chosen k if renormalize != 0.
+ *   Both: weights *= routed_scaling.
+ * logits: device fp32 [T, E]; topk_ids: device int32 [T, topk] (descending
+ * score order); topk_weights: device fp32 [T, topk].
+ * Errors: INVALID_ARG (null pointer, T < 0), UNSUPPORTED_SHAPE (E > 1024,
+ * topk > min(E, 32), E % n_group, n_group > 32, grouping with softmax). */
+int moe_route_topk(const float* logits, int T, int E, int topk, int renormalize,
+                   const moe_routing_params* rp, int32_t* topk_ids, float* topk_weights,
+                   void* stream);
+
+/* ---- expert sort ("sorted token" pattern) ------------------------------------
+ * Page "Quantization and MoE Optimizations", section Triton Fused MoE Kernel:
+ * each program handles a block of tokens sorted by expert.  Pair p = t*topk + j
+ * goes to expert topk_ids[p].  Rows are grouped by expert, each expert's rows
+ * padded to a multiple of block_m, pairs of one expert in ascending p.
+ *
+ * Outputs (device):
+ *   expert_offsets  int32 [E+1]  exclusive prefix sum of the per-expert counts
+ *   padded_offsets  int32 [E+1]  the same with every count rounded up to block_m
+ *   sorted_pair_ids int32 [moe_max_padded_rows(...)]  pair of each padded row, -1 in padding
+ *   pos             int32 [T*topk]  padded row of each pair (-1 if its id was invalid)
+ *   tile_expert     int32 [moe_max_tiles(...)]  expert of each block_m-row tile
+ *   tile_row0       int32 [moe_max_tiles(...)]  first padded row of each tile
+ *   num_tiles       int32 [1]
+ * workspace: device scratch of moe_align_permute_workspace_size(T, topk, E) bytes.
+ * block_m: 1..1024.  Invalid ids set MOE_STATUS_BAD_EXPERT_ID and are dropped. */
+int64_t moe_max_padded_rows(int T, int topk, int E, int block_m);
+int64_t moe_max_tiles(int T, int topk, int E, int block_m);
+size_t moe_align_permute_workspace_size(int T, int topk, int E);
+int moe_align_permute(const int32_t* topk_ids, int T, int topk, int E, int block_m,
+                      int32_t* expert_offsets, int32_t* padded_offsets, int32_t* sorted_pair_ids,
+                      int32_t* pos, int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- FP8 quantisation ---------------------------------------------------------
+ * Dynamic per-token-group activation quantisation, groups of 1x128 ("computed
+ * per-token at runtime", page "Quantization and MoE Optimizations", section
+ * Fp8Config; activation key kFp8Dynamic128Sym, page
+ * "vllm.model_executor.layers.fused_moe.oracle.fp8", _get_priority_backends):
+ *   scale = max(amax, 1e-8) / 448 (fp32), q = e4m3(x / scale), round to
+ *   nearest even, saturate to +-448.
+ * x: device bf16 [rows, cols] with row stride ld (elements, >= cols, multiple
+ * of 8); q: device e4m3 [rows, cols] (dense); s: device fp32 [rows, cols/128].
+ * cols must be a multiple of 128. */
+int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s,
+                    void* stream);
+
+/* 128x128 block weight quantisation of stacked expert weights w [E, N, K]
+ * (bf16) with the same rule, amax over each block ("weight_block_size ...
+ * [128, 128]", Fp8Config; online quantisation at load time, page
+ * "Quantization", section Online quantization).  q: device e4m3 [E, N, K];
+ * s: device fp32 [E, N/128, K/128].  N and K multiples of 128. */
+int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
+                           void* stream);
+
+/* ---- grouped block-FP8 GEMM ------------------------------------------------------
+ * For every tile m < *num_tiles (rows tile_row0[m] .. +127 of A, all routed to
+ * expert e = tile_expert[m]) and every output column n:
+ *   C[r, n] = sum_kb a_scale[r, kb] * b_scale[e, n/128, kb]
+ *                   * sum_{k in block kb} A[r, k] * B[e, n, k]
+ * with the block scales applied per 128-wide K block in fp32 (tensor cores
+ * accumulate each K block, the scales are applied before the next one).
+ *   A        device e4m3 [a_rows, K]   (a_rows >= every tile_row0 + 128)
+ *   a_scale  device fp32, element (r, kb) at a_scale[r*a_scale_row_stride + kb*a_scale_kb_stride]
+ *   B        device e4m3 [E, N, K];  b_scale device fp32 [E, N/128, K/128]
+ *   tile_expert / tile_row0 device int32 [max_tiles]; num_tiles device int32 [1]
+ * Epilogues:
+ *   MOE_EPI_STORE_F32: out_f32[r, n] = C[r, n]  (out_f32: device fp32 [a_rows, N])
+ *   MOE_EPI_SILU_MUL_QUANT: h[r, i] = silu(C[r, i]) * C[r, N/2 + i] for i < N/2,
+ *       then 1x128 e4m3 quantisation of h ("SiLU(gate)*up with requantisation"):
+ *       out_q device e4m3 [a_rows, N/2]; out_scale element (r, g) at
+ *       out_scale[r*out_scale_row_stride + g*out_scale_kb_stride].
+ *   MOE_EPI_WEIGHTED_SCATTER: for rows with pair = sorted_pair_ids[r] >= 0,
+ *       out_f32[pair / topk, n] += topk_weights[pair] * C[r, n]  (out_f32: device
+ *       fp32 [T, N], accumulated with atomics; the caller zeroes it first).
+ * K, N multiples of 128 (N multiple of 256 for MOE_EPI_SILU_MUL_QUANT).
+ * Rows of a tile past its expert's count hold whatever A holds there; their
+ * results are written (store / silu epilogues) but belong to no pair. */
+#define MOE_EPI_STORE_F32 0
+#define MOE_EPI_SILU_MUL_QUANT 1
+#define MOE_EPI_WEIGHTED_SCATTER 2
+
+typedef struct moe_gemm_epilogue {
+    int32_t kind;                     /* MOE_EPI_* */
+    int32_t topk;                     /* MOE_EPI_WEIGHTED_SCATTER */
+    float* out_f32;
+    uint8_t* out_q;
+    float* out_scale;
+    int64_t out_scale_row_stride;
+    int64_t out_scale_kb_stride;
+    const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER */
+    const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER, [T*topk] */
+} moe_gemm_epilogue;
+
+int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
+                           int64_t a_scale_kb_stride, int64_t a_rows,
+                           const uint8_t* B, const float* b_scale, int N, int K, int E,
+                           const int32_t* tile_expert, const int32_t* tile_row0,
+                           const int32_t* num_tiles, int64_t max_tiles,
+                           const moe_gemm_epilogue* epilogue, void* stream);
+
+/* ---- the whole layer -------------------------------------------------------------
+ * Router -> sort by expert -> 1x128 quantisation of hidden -> GEMM over w13 with
+ * SiLU(gate)*up + requantisation -> GEMM over w2 with the top-k weighted
+ * scatter-add -> bf16 output (the modular pipeline Router -> Prepare/Finalize
+ * -> Permute/Experts/Unpermute, page "Quantization and MoE Optimizations",
+ * section Modular Kernel Architecture; weights "[num_experts, N, K]", section
+ * FusedMoE Class; 128x128 weight blocks with dynamic activations, section
+ * Fp8Config).
+ * workspace: device scratch of moe_fp8_block_workspace_size(T, H, I, E, topk)
+ * bytes (256-byte aligned).  out may not alias any input.  T == 0 is a no-op. */
+size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
+int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
+                          const uint8_t* w13, const float* w13_scale,
+                          const uint8_t* w2, const float* w2_scale,
+                          int T, int H, int I, int E, int topk, int renormalize,
+                          const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
+                          uint16_t* out, void* stream);
+
+/* ---- status -------------------------------------------------------------------- */
+/* Reads (and with clear != 0, resets) the device status word of the current
+ * device into *status (host).  Synchronises the device. */
+int moe_get_device_status(uint32_t* status, int clear);
+/* Human-readable name of a MOE_* return code. */
+const char* moe_error_string(int code);
+/* 1 if the current device can run these kernels (compute capability 10.3). */
+int moe_device_supported(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOEFP8_H */
