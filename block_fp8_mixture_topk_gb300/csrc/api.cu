@@ -1,0 +1,392 @@
+// C ABI of the block-FP8 MoE library: argument checks, workspace layout and the
+// launch sequence of the whole layer.  See include/moefp8.h for the contract.
+#include <mutex>
+
+#include "kernels.cuh"
+
+using namespace mfp8;
+
+namespace {
+
+// Device status word (MOE_STATUS_* bits), one per device that loads the library.
+__device__ uint32_t g_status_word;
+
+struct DeviceState {
+    bool init = false;
+    int rc = MOE_OK;
+    int num_sms = 0;
+    uint32_t* status = nullptr;  // device address of g_status_word on this device
+};
+constexpr int kMaxDevices = 128;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+// Once per device (with that device current): check it is a GB300, look up the
+// status word's device address and set the kernels' shared-memory limits.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
+    DeviceState& s = g_devices[dev];
+    if (!s.init) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            return MOE_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            s.rc = MOE_ERR_DEVICE;
+        } else {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || route_init_device() != cudaSuccess ||
+                permute_init_device() != cudaSuccess || gemm_init_device() != cudaSuccess) {
+                cudaGetLastError();
+                return MOE_ERR_CUDA;
+            }
+            s.status = static_cast<uint32_t*>(p);
+            s.rc = MOE_OK;
+        }
+        s.init = true;
+    }
+    *out = &s;
+    return s.rc;
+}
+
+inline int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_routing(int T, int E, int topk, const moe_routing_params* rp) {
+    if (T < 0 || E < 1 || topk < 1) return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS || topk > E || topk > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!rp) return MOE_OK;
+    if (rp->scoring != MOE_SCORING_SOFTMAX && rp->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (rp->n_group < 1) return MOE_ERR_INVALID_ARG;
+    if (rp->n_group > MOE_MAX_GROUPS || E % rp->n_group != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rp->bias && rp->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rp->n_group > 1) {
+        const int G = E / rp->n_group;
+        if (rp->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (rp->topk_group < 1 || rp->topk_group > rp->n_group) return MOE_ERR_INVALID_ARG;
+        if (G < 2 || topk > rp->topk_group * G) return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    return MOE_OK;
+}
+
+int64_t max_rows(int64_t P, int64_t E, int64_t bm) {
+    const int64_t busy = P < E ? P : E;
+    return P + busy * (bm - 1);
+}
+
+struct ForwardLayout {
+    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, outf, total;
+    int64_t rows, tiles;
+};
+
+ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
+    ForwardLayout L;
+    const int64_t P = static_cast<int64_t>(T) * topk;
+    L.rows = max_rows(P, E, MOE_BLOCK_M);
+    L.tiles = L.rows / MOE_BLOCK_M;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align_up(bytes, 256);
+        return o;
+    };
+    L.ids = take(P * 4);
+    L.wts = take(P * 4);
+    L.eoff = take((E + 1) * 4);
+    L.poff = take((E + 1) * 4);
+    L.sorted = take(L.rows * 4);
+    L.pos = take(P * 4);
+    L.tile_e = take(L.tiles * 4);
+    L.tile_r = take(L.tiles * 4);
+    L.ntiles = take(4);
+    L.counts = take(permute_chunks(P) * E * 4);
+    L.a1 = take(L.rows * H);
+    L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
+    L.a2 = take(L.rows * I);
+    L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
+    L.outf = take(static_cast<size_t>(T) * H * 4);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_device_supported(void) {
+    DeviceState* s = nullptr;
+    return device_state(&s) == MOE_OK ? 1 : 0;
+}
+
+const char* moe_error_string(int code) {
+    switch (code) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+int moe_get_device_status(uint32_t* status, int clear) {
+    if (!status) return MOE_ERR_INVALID_ARG;
+    DeviceState* s = nullptr;
+    int rc = device_state(&s);
+    if (rc != MOE_OK) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(status, s->status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (clear && cudaMemset(s->status, 0, sizeof(uint32_t)) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_route_topk(const float* logits, int T, int E, int topk, int renormalize, const moe_routing_params* rp,
+                   int32_t* topk_ids, float* topk_weights, void* stream) {
+    int rc = check_routing(T, E, topk, rp);
+    if (rc != MOE_OK) return rc;
+    if (T > 0 && (!logits || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+    DeviceState* s = nullptr;
+    if ((rc = device_state(&s)) != MOE_OK) return rc;
+    const int scoring = rp ? rp->scoring : MOE_SCORING_SOFTMAX;
+    const int n_group = rp ? rp->n_group : 1;
+    const int topk_group = rp ? rp->topk_group : 1;
+    const float scaling = rp ? rp->routed_scaling : 1.0f;
+    const float* bias = rp ? rp->bias : nullptr;
+    return cuda_rc(launch_route_topk(logits, T, E, topk, renormalize, scoring, n_group, topk_group, scaling, bias,
+                                     topk_ids, topk_weights, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t moe_max_padded_rows(int T, int topk, int E, int block_m) {
+    if (T < 0 || topk < 1 || E < 1 || block_m < 1) return -1;
+    return max_rows(static_cast<int64_t>(T) * topk, E, block_m);
+}
+
+int64_t moe_max_tiles(int T, int topk, int E, int block_m) {
+    const int64_t r = moe_max_padded_rows(T, topk, E, block_m);
+    return r < 0 ? -1 : r / block_m;
+}
+
+size_t moe_align_permute_workspace_size(int T, int topk, int E) {
+    if (T < 0 || topk < 1 || E < 1) return 0;
+    return align_up(static_cast<size_t>(permute_chunks(static_cast<int64_t>(T) * topk)) * E * 4, 256);
+}
+
+int moe_align_permute(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* expert_offsets,
+                      int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos, int32_t* tile_expert,
+                      int32_t* tile_row0, int32_t* num_tiles, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (T < 0 || topk < 1 || E < 1 || block_m < 1) return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS || block_m > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int64_t P = static_cast<int64_t>(T) * topk;
+    if (max_rows(P, E, block_m) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!expert_offsets || !padded_offsets || !num_tiles) return MOE_ERR_INVALID_ARG;
+    if (P > 0 && (!topk_ids || !sorted_pair_ids || !pos || !tile_expert || !tile_row0)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < moe_align_permute_workspace_size(T, topk, E)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (P > 0 && !workspace) return MOE_ERR_INVALID_ARG;
+    DeviceState* s = nullptr;
+    int rc = device_state(&s);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_align_permute(topk_ids, P, E, block_m, expert_offsets, padded_offsets, sorted_pair_ids, pos,
+                                        tile_expert, tile_row0, num_tiles, static_cast<int32_t*>(workspace),
+                                        s->status, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, void* stream) {
+    if (rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
+    if (cols % 128 != 0 || ld % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!x || !q || !s) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(q, 8) || !aligned(s, 4)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, s, cols / 128, 1, nullptr, 1,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0 || K > (1 << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (E > 65535 || N / 128 > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_block_quant_weight(w, E, N, K, q, s, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
+                           int64_t a_scale_kb_stride, int64_t a_rows, const uint8_t* B, const float* b_scale, int N,
+                           int K, int E, const int32_t* tile_expert, const int32_t* tile_row0,
+                           const int32_t* num_tiles, int64_t max_tiles, const moe_gemm_epilogue* ep, void* stream) {
+    if (!ep || N < 0 || K < 0 || E < 1 || max_tiles < 0 || a_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0 || N == 0 || K == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(E) * N >= (int64_t(1) << 31) || a_rows >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (ep->kind == MOE_EPI_SILU_MUL_QUANT && N % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (max_tiles == 0) return MOE_OK;
+    if (!A || !a_scale || !B || !b_scale || !tile_expert || !tile_row0 || !num_tiles) return MOE_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(B, 16)) return MOE_ERR_INVALID_ARG;
+    switch (ep->kind) {
+        case MOE_EPI_STORE_F32:
+            if (!ep->out_f32 || !aligned(ep->out_f32, 16)) return MOE_ERR_INVALID_ARG;
+            break;
+        case MOE_EPI_SILU_MUL_QUANT:
+            if (!ep->out_q || !ep->out_scale || !aligned(ep->out_q, 16)) return MOE_ERR_INVALID_ARG;
+            break;
+        case MOE_EPI_WEIGHTED_SCATTER:
+            if (!ep->out_f32 || !aligned(ep->out_f32, 16) || !ep->sorted_pair_ids || !ep->topk_weights ||
+                ep->topk < 1 || ep->num_pairs < 0)
+                return MOE_ERR_INVALID_ARG;
+            break;
+        default:
+            return MOE_ERR_INVALID_ARG;
+    }
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    GemmArgs g{};
+    g.A = A;
+    g.a_scale = a_scale;
+    g.as_row_stride = a_scale_row_stride;
+    g.as_kb_stride = a_scale_kb_stride;
+    g.a_rows = a_rows;
+    g.B = B;
+    g.b_scale = b_scale;
+    g.N = N;
+    g.K = K;
+    g.E = E;
+    g.tile_expert = tile_expert;
+    g.tile_row0 = tile_row0;
+    g.num_tiles = num_tiles;
+    g.max_tiles = max_tiles;
+    g.epi = ep->kind;
+    g.out_f32 = ep->out_f32;
+    g.out_q = ep->out_q;
+    g.out_scale = ep->out_scale;
+    g.os_row_stride = ep->out_scale_row_stride;
+    g.os_kb_stride = ep->out_scale_kb_stride;
+    g.sorted_pair_ids = ep->sorted_pair_ids;
+    g.topk_weights = ep->topk_weights;
+    g.topk = ep->topk;
+    g.num_pairs = ep->num_pairs;
+    g.status = st->status;
+    return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk) {
+    if (T < 0 || H < 0 || I < 0 || E < 1 || topk < 1) return 0;
+    return forward_layout(T, H, I, E, topk).total;
+}
+
+int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
+                          const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H, int I, int E,
+                          int topk, int renormalize, const moe_routing_params* rp, void* workspace,
+                          size_t workspace_bytes, uint16_t* out, void* stream) {
+    int rc = check_routing(T, E, topk, rp);
+    if (rc != MOE_OK) return rc;
+    if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) || static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    const ForwardLayout L = forward_layout(T, H, I, E, topk);
+    if (L.rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!hidden || !router_logits || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 8) ||
+        !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* st = nullptr;
+    if ((rc = device_state(&st)) != MOE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+    float* wts = reinterpret_cast<float*>(ws + L.wts);
+    int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+    int32_t* pos = reinterpret_cast<int32_t*>(ws + L.pos);
+    int32_t* tile_e = reinterpret_cast<int32_t*>(ws + L.tile_e);
+    int32_t* tile_r = reinterpret_cast<int32_t*>(ws + L.tile_r);
+    int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
+    uint8_t* a1 = ws + L.a1;
+    float* a1s = reinterpret_cast<float*>(ws + L.a1s);
+    uint8_t* a2 = ws + L.a2;
+    float* a2s = reinterpret_cast<float*>(ws + L.a2s);
+    float* outf = reinterpret_cast<float*>(ws + L.outf);
+    const int64_t P = static_cast<int64_t>(T) * topk;
+
+    const int scoring = rp ? rp->scoring : MOE_SCORING_SOFTMAX;
+    cudaError_t e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, rp ? rp->n_group : 1,
+                                      rp ? rp->topk_group : 1, rp ? rp->routed_scaling : 1.0f,
+                                      rp ? rp->bias : nullptr, ids, wts, s);
+    if (e == cudaSuccess)
+        e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
+                                 reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
+                                 reinterpret_cast<int32_t*>(ws + L.counts), st->status, s);
+    // each token quantised once, its codes written to the sorted rows of its pairs;
+    // the scales are stored transposed ([H/128][rows]) for the GEMM's per-row reads
+    if (e == cudaSuccess) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(outf, 0, static_cast<size_t>(T) * H * sizeof(float), s);
+    if (e == cudaSuccess) {
+        GemmArgs g{};
+        g.A = a1;
+        g.a_scale = a1s;
+        g.as_row_stride = 1;
+        g.as_kb_stride = L.rows;
+        g.a_rows = L.rows;
+        g.B = w13;
+        g.b_scale = w13_scale;
+        g.N = 2 * I;
+        g.K = H;
+        g.E = E;
+        g.tile_expert = tile_e;
+        g.tile_row0 = tile_r;
+        g.num_tiles = ntiles;
+        g.max_tiles = L.tiles;
+        g.epi = MOE_EPI_SILU_MUL_QUANT;
+        g.out_q = a2;
+        g.out_scale = a2s;
+        g.os_row_stride = 1;
+        g.os_kb_stride = L.rows;
+        g.status = st->status;
+        e = launch_grouped_gemm(g, st->num_sms, s);
+    }
+    if (e == cudaSuccess) {
+        GemmArgs g{};
+        g.A = a2;
+        g.a_scale = a2s;
+        g.as_row_stride = 1;
+        g.as_kb_stride = L.rows;
+        g.a_rows = L.rows;
+        g.B = w2;
+        g.b_scale = w2_scale;
+        g.N = H;
+        g.K = I;
+        g.E = E;
+        g.tile_expert = tile_e;
+        g.tile_row0 = tile_r;
+        g.num_tiles = ntiles;
+        g.max_tiles = L.tiles;
+        g.epi = MOE_EPI_WEIGHTED_SCATTER;
+        g.out_f32 = outf;
+        g.sorted_pair_ids = sorted;
+        g.topk_weights = wts;
+        g.topk = topk;
+        g.num_pairs = P;
+        g.status = st->status;
+        e = launch_grouped_gemm(g, st->num_sms, s);
+    }
+    if (e == cudaSuccess) e = launch_f32_to_bf16(outf, out, static_cast<int64_t>(T) * H, s);
+    return cuda_rc(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,423 @@
+// Grouped block-FP8 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// C[r, n] = sum_kb a_scale[r, kb] * b_scale[e, n/128, kb] * sum_{k in kb} A[r, k] * B[e, n, k]
+//
+// The weights of an expert are "[num_experts, N, K]" with 128x128 blocks
+// (page "Quantization and MoE Optimizations", sections FusedMoE Class and
+// Fp8Config); the activations carry one scale per 1x128 group.  Each CTA tile is
+// 128 sorted rows of one expert (the "sorted token" pattern, section Triton
+// Fused MoE Kernel) by 256 output columns.  Because the scales change with
+// every 128-wide K block and are fp32 (not the power-of-two scales of the
+// hardware block-scaled MMA), every K block is accumulated by the tensor cores
+// into its own TMEM buffer and then "promoted": the epilogue warps read it,
+// multiply by a_scale * b_scale and add it to fp32 register accumulators.  Two
+// TMEM buffers (2 x 256 columns) let the MMA of block kb+1 run while block kb
+// is promoted.  (The pages' Triton kernel dequantises after the K loop, which is
+// exact only for per-tensor / per-channel scales; blockwise scales vary along K.)
+//
+// Roles (320 threads, one CTA per SM, persistent over the tile list):
+//   warp 0, one thread : TMA producer, 4-stage ring of {A 128x128, B 256x128} e4m3 tiles
+//   warp 1, one thread : MMA issuer (4 x tcgen05.mma 128x256x32 per K block), TMEM owner
+//   warps 2..9         : promotion + epilogue; warp w reads TMEM lanes 32*(w%4)..+31
+//                        (its rows) and 128 of the 256 columns (column half (w-2)/4)
+// Epilogues:
+//   store     : fp32 rows to out_f32
+//   silu      : B tile = 128 gate rows + the 128 matching up rows; h = silu(g)*u in
+//               fp32, amax of the 128-wide group exchanged between the two column
+//               halves through shared memory, 1x128 e4m3 requantisation
+//   scatter   : out_f32[token] += router_weight * C (float4 atomics), the top-k
+//               weighted unpermute-sum
+// Every wait is bounded (mbar_wait); on expiry the CTA records
+// MOE_STATUS_WAIT_TIMEOUT, waits (bounded) for its TMA loads and MMAs in flight,
+// frees its TMEM and exits.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace mfp8 {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int STAGES = 4;
+constexpr int A_TILE = BM * BK;        // 16 KB
+constexpr int B_HALF = 128 * BK;       // 16 KB: 128 weight rows
+constexpr int B_TILE = 2 * B_HALF;     // 32 KB: 256 weight rows
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
+
+struct SmemCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t amax_bar[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    float amax_x[2][2][BM];            // [tile parity][column half][row]
+};
+constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
+
+struct Tile {
+    int64_t row0;
+    int e;
+    int n;
+    int bcol0, bcol1;
+    bool has1;
+    bool ok;
+};
+
+template <int EPI>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int64_t w, int NT) {
+    Tile t;
+    const int64_t m = w / NT;
+    t.n = static_cast<int>(w - m * NT);
+    t.e = a.tile_expert[m];
+    t.row0 = a.tile_row0[m];
+    t.ok = t.e >= 0 && t.e < a.E && t.row0 >= 0 && t.row0 + BM <= a.a_rows;
+    if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+        t.bcol0 = t.n * 128;
+        t.bcol1 = a.N / 2 + t.n * 128;
+        t.has1 = true;
+    } else {
+        t.bcol0 = t.n * 256;
+        t.bcol1 = t.bcol0 + 128;
+        t.has1 = t.bcol1 < a.N;
+    }
+    return t;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* smA = base;
+    uint8_t* smB = base + STAGES * A_TILE;
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smB + STAGES * B_TILE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NT = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 256 : (a.N + 255) / 256;
+    const int KB = a.K / BK;
+    int64_t ntiles = *a.num_tiles;
+    if (ntiles < 0) ntiles = 0;
+    if (ntiles > a.max_tiles) ntiles = a.max_tiles;
+    const int64_t total = ntiles * NT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&ctl->tfull[b]), 1);
+            mbar_init(smem_addr(&ctl->tempty[b]), NUM_EPI_WARPS);
+            mbar_init(smem_addr(&ctl->amax_bar[b]), NUM_EPI_WARPS * 32);
+        }
+        mbar_init(smem_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ producer
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Tile t = decode_tile<EPI>(a, w, NT);
+                if (!t.ok) {
+                    status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+                    continue;
+                }
+                const int32_t brow0 = t.e * a.N + t.bcol0, brow1 = t.e * a.N + t.bcol1;
+                const uint32_t bytes = A_TILE + (t.has1 ? B_TILE : B_HALF);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&ctl->full[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
+                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
+                    if (t.has1) tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every load already issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s) {
+                    const uint32_t n_s = (issued + STAGES - 1 - s) / STAGES;
+                    if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t idesc_full = idesc_e4m3_f32(BM, 256);
+            const uint32_t idesc_half = idesc_e4m3_f32(BM, 128);
+            int stage = 0;
+            uint32_t phase = 0, buf = 0, bphase = 0;
+            bool ok = true;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Tile t = decode_tile<EPI>(a, w, NT);
+                if (!t.ok) continue;
+                const uint32_t idesc = t.has1 ? idesc_full : idesc_half;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_addr(&ctl->tempty[buf]), bphase ^ 1u, abort_flag, a.status) ||
+                        !mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_addr(smA + stage * A_TILE);
+                    const uint32_t b0 = smem_addr(smB + stage * B_TILE);
+                    const uint32_t d = tmem + buf * 256;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_e4m3(d, smem_desc_k128_sw128(a0 + k * 32), smem_desc_k128_sw128(b0 + k * 32), idesc,
+                                 k > 0 ? 1u : 0u);
+                    mma_commit(smem_addr(&ctl->empty[stage]));
+                    mma_commit(smem_addr(&ctl->tfull[buf]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    buf ^= 1u;
+                    if (buf == 0) bphase ^= 1u;
+                }
+            }
+            if (!ok) {
+                mma_commit(smem_addr(&ctl->drain));
+                mbar_wait(smem_addr(&ctl->drain), 0, nullptr, a.status);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int g = (warp - 2) >> 2;          // column half
+        const int sp = warp & 3;                // TMEM lane quarter
+        const int row = sp * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        const int NBn = a.N / 128;
+        uint32_t buf = 0, bphase = 0, tile_iter = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Tile t = decode_tile<EPI>(a, w, NT);
+            if (!t.ok) continue;
+            const int64_t grow = t.row0 + row;
+            const bool active = (EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1;
+            const float* bs0;
+            const float* bs1;
+            if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+                bs0 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + t.n) * KB;             // gate block
+                bs1 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + NBn / 2 + t.n) * KB;   // up block
+            } else {
+                bs0 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + t.bcol0 / 128 + (active ? g : 0)) * KB;
+                bs1 = bs0;
+            }
+            const float* as = a.a_scale + grow * a.as_row_stride;
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+            for (int kb = 0; kb < KB; ++kb) {
+                const float sa = as[kb * a.as_kb_stride];
+                const float s0 = sa * bs0[kb];
+                const float s1 = sa * bs1[kb];
+                if (!mbar_wait(smem_addr(&ctl->tfull[buf]), bphase, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = lane_base + buf * 256;
+                float v[16];
+                if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+                    // gate columns g*64.. (scale s0) -> acc[0, 64); up columns 128+g*64.. (s1) -> acc[64, 128)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        tmem_ld16(col + (c < 4 ? 0 : 128) + g * 64 + (c & 3) * 16, v);
+                        const float sc = c < 4 ? s0 : s1;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(v[j], sc, acc[c * 16 + j]);
+                    }
+                } else if (active) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        tmem_ld16(col + g * 128 + c * 16, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(v[j], s0, acc[c * 16 + j]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty[buf]));
+                buf ^= 1u;
+                if (buf == 0) bphase ^= 1u;
+            }
+            if (!ok) break;
+
+            if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float gate = acc[j];
+                    const float h = gate / (1.0f + expf(-gate)) * acc[64 + j];
+                    acc[j] = h;
+                    amax = fmaxf(amax, fabsf(h));
+                }
+                const uint32_t par = tile_iter & 1u;
+                ctl->amax_x[par][g][row] = amax;
+                mbar_arrive(smem_addr(&ctl->amax_bar[par]));
+                if (!mbar_wait(smem_addr(&ctl->amax_bar[par]), (tile_iter >> 1) & 1u, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
+                const float sc = group_scale(amax);
+                uint32_t wbuf[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t lo = e4m3x2(__fdiv_rn(acc[4 * j], sc), __fdiv_rn(acc[4 * j + 1], sc));
+                    const uint32_t hi = e4m3x2(__fdiv_rn(acc[4 * j + 2], sc), __fdiv_rn(acc[4 * j + 3], sc));
+                    wbuf[j] = lo | (hi << 16);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(wbuf[4 * j], wbuf[4 * j + 1], wbuf[4 * j + 2], wbuf[4 * j + 3]);
+                if (g == 0) a.out_scale[grow * a.os_row_stride + static_cast<int64_t>(t.n) * a.os_kb_stride] = sc;
+            } else if (EPI == MOE_EPI_WEIGHTED_SCATTER) {
+                if (active) {
+                    const int32_t pair = a.sorted_pair_ids[grow];
+                    if (pair >= 0 && pair < a.num_pairs) {
+                        const int64_t tok = pair / a.topk;
+                        const float wgt = a.topk_weights[pair];
+                        float* dst = a.out_f32 + tok * a.N + t.bcol0 + g * 128;
+#pragma unroll
+                        for (int j = 0; j < 128; j += 4)
+                            atomicAdd(reinterpret_cast<float4*>(dst + j),
+                                      make_float4(wgt * acc[j], wgt * acc[j + 1], wgt * acc[j + 2], wgt * acc[j + 3]));
+                    }
+                }
+            } else {
+                if (active) {
+                    float4* dst = reinterpret_cast<float4*>(a.out_f32 + grow * a.N + t.bcol0 + g * 128);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                }
+            }
+            ++tile_iter;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 2-D e4m3 matrix [rows, cols] (row stride = cols bytes), 128x128 boxes, 128-byte swizzle
+cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t elem[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t gemm_init_device() {
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    const int bytes = static_cast<int>(SMEM_BYTES);
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_STORE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               bytes);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_SILU_MUL_QUANT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return err;
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
+    const int NT = (args.epi == MOE_EPI_SILU_MUL_QUANT) ? args.N / 256 : (args.N + 255) / 256;
+    const int64_t bound = args.max_tiles * NT;
+    if (bound == 0) return cudaSuccess;
+    CUtensorMap tmA, tmB;
+    cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows);
+    if (err != cudaSuccess) return err;
+    err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>(bound < num_sms ? bound : num_sms);
+    switch (args.epi) {
+        case MOE_EPI_STORE_F32:
+            grouped_gemm_kernel<MOE_EPI_STORE_F32><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            break;
+        case MOE_EPI_SILU_MUL_QUANT:
+            grouped_gemm_kernel<MOE_EPI_SILU_MUL_QUANT><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            break;
+        case MOE_EPI_WEIGHTED_SCATTER:
+            grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            break;
+        default:
+            return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mfp8

@@ -1,0 +1,64 @@
+// Host-side launchers of the sm_103a kernels (one translation unit each) and
+// their once-per-device set-up.  All launchers are asynchronous on `stream`
+// and return the launch's cudaError_t.
+#pragma once
+
+#include "common.cuh"
+
+namespace mfp8 {
+
+// route.cu
+cudaError_t route_init_device();
+cudaError_t launch_route_topk(const float* logits, int T, int E, int topk, int renormalize, int scoring,
+                              int n_group, int topk_group, float routed_scaling, const float* bias, int32_t* ids,
+                              float* weights, cudaStream_t stream);
+
+// permute.cu
+constexpr int kPermuteChunk = 1024;   // pairs per block of the counting / scatter kernels
+cudaError_t permute_init_device();
+int64_t permute_chunks(int64_t P);
+cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block_m, int32_t* expert_offsets,
+                                 int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
+                                 int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
+                                 int32_t* chunk_counts, uint32_t* status, cudaStream_t stream);
+
+// quant.cu
+// 1x128 group quantisation of bf16 rows.  Row r of x goes to output row r, or
+// (when pos != null) to output rows pos[r*topk + j], j < topk, skipping -1.
+// Scale of (output row o, group g) is stored at s[o*s_row_stride + g*s_group_stride].
+cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
+                               float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
+                               int topk, cudaStream_t stream);
+cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
+                                      cudaStream_t stream);
+// fp32 [n] -> bf16 bits [n], round to nearest even (n multiple of 4, 16-byte aligned)
+cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t stream);
+
+// gemm.cu
+struct GemmArgs {
+    const uint8_t* A;
+    const float* a_scale;
+    int64_t as_row_stride, as_kb_stride;
+    int64_t a_rows;
+    const uint8_t* B;
+    const float* b_scale;
+    int N, K, E;
+    const int32_t* tile_expert;
+    const int32_t* tile_row0;
+    const int32_t* num_tiles;
+    int64_t max_tiles;
+    int epi;
+    float* out_f32;
+    uint8_t* out_q;
+    float* out_scale;
+    int64_t os_row_stride, os_kb_stride;
+    const int32_t* sorted_pair_ids;
+    const float* topk_weights;
+    int topk;
+    int64_t num_pairs;
+    uint32_t* status;
+};
+cudaError_t gemm_init_device();
+cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+}  // namespace mfp8

@@ -1,0 +1,174 @@
+// FP8 quantisation kernels (HBM-bound).
+//
+// Activation groups of 1x128 ("computed per-token at runtime", page
+// "Quantization and MoE Optimizations", section Fp8Config; key
+// kFp8Dynamic128Sym, page "vllm.model_executor.layers.fused_moe.oracle.fp8"):
+// scale = max(amax, 1e-8)/448 in fp32, codes = e4m3(x / scale) with IEEE
+// division and the hardware's round-to-nearest-even, saturating conversion.
+// Sixteen threads own one group (8 bf16 = one 16-byte load each), reduce the
+// amax with four shuffles, and write 8 code bytes each.  The scatter form
+// writes each token's codes to the sorted rows of its top-k pairs, so the
+// expert GEMM reads one dense [rows, H] operand (the token is quantised once).
+//
+// Weight blocks of 128x128 ("weight_block_size ... [128, 128]", Fp8Config)
+// use the same rule with the amax over the whole block: one 256-thread CTA per
+// block keeps its 32 KB of bf16 in registers between the amax and the encode.
+#include <cuda_bf16.h>
+
+#include "kernels.cuh"
+
+namespace mfp8 {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+}
+
+__device__ __forceinline__ uint2 encode8(const float* f, float sc) {
+    uint32_t b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint16_t lo = e4m3x2(__fdiv_rn(f[2 * i], sc), __fdiv_rn(f[2 * i + 1], sc));
+        b[i] = lo;
+    }
+    return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+__global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols,
+                                                          int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
+                                                          float* __restrict__ s, int64_t s_rs, int64_t s_gs,
+                                                          const int32_t* __restrict__ pos, int topk) {
+    const int G = cols / 128;
+    const int64_t total = rows * G;
+    const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w * 2 < total;
+         w += nwarps) {
+        const int64_t gi = w * 2 + half;
+        const bool active = gi < total;
+        float f[8];
+        float amax = 0.0f;
+        int64_t r = 0;
+        int g = 0;
+        if (active) {
+            r = gi / G;
+            g = static_cast<int>(gi - r * G);
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + r * ld + g * 128 + sub * 8));
+            unpack8(v, f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (active) {
+            const float sc = group_scale(amax);
+            const uint2 code = encode8(f, sc);
+            if (pos) {
+                for (int j = 0; j < topk; ++j) {
+                    const int64_t o = pos[r * topk + j];
+                    if (o < 0) continue;
+                    *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
+                    if (sub == 0) s[o * s_rs + g * s_gs] = sc;
+                }
+            } else {
+                *reinterpret_cast<uint2*>(q + r * q_ld + g * 128 + sub * 8) = code;
+                if (sub == 0) s[r * s_rs + g * s_gs] = sc;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t* __restrict__ w, int N, int K,
+                                                                 uint8_t* __restrict__ q, float* __restrict__ s) {
+    __shared__ float warp_max[8];
+    const int kb = blockIdx.x, nb = blockIdx.y, e = blockIdx.z;
+    const int NB = N / 128, KB = K / 128;
+    const int row = threadIdx.x >> 1, part = threadIdx.x & 1;
+    const int64_t off = (static_cast<int64_t>(e) * N + nb * 128 + row) * K + kb * 128 + part * 64;
+    uint4 v[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[i] = __ldg(reinterpret_cast<const uint4*>(w + off) + i);
+        float f[8];
+        unpack8(v[i], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    const float sc = group_scale(amax);
+    uint2 out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        unpack8(v[i], f);
+        out[i] = encode8(f, sc);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        reinterpret_cast<uint4*>(q + off)[i] = make_uint4(out[2 * i].x, out[2 * i].y, out[2 * i + 1].x,
+                                                          out[2 * i + 1].y);
+    if (threadIdx.x == 0) s[(static_cast<int64_t>(e) * NB + nb) * KB + kb] = sc;
+}
+
+__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4* __restrict__ x, uint2* __restrict__ y,
+                                                          int64_t n4) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 v = x[i];
+        const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(v.x));
+        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v.y));
+        const uint32_t c = __bfloat16_as_ushort(__float2bfloat16_rn(v.z));
+        const uint32_t d = __bfloat16_as_ushort(__float2bfloat16_rn(v.w));
+        y[i] = make_uint2(a | (b << 16), c | (d << 16));
+    }
+}
+
+int grid_for(int64_t work_items, int per_block) {
+    int64_t b = (work_items + per_block - 1) / per_block;
+    if (b < 1) b = 1;
+    if (b > 152 * 32) b = 152 * 32;
+    return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
+                               float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
+                               int topk, cudaStream_t stream) {
+    const int64_t groups = rows * (cols / 128);
+    if (groups == 0) return cudaSuccess;
+    group_quant_kernel<<<grid_for(groups, 16), 256, 0, stream>>>(x, rows, cols, ld, q, q_ld, s, s_row_stride,
+                                                                 s_group_stride, pos, topk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
+                                      cudaStream_t stream) {
+    if (E == 0 || N == 0 || K == 0) return cudaSuccess;
+    dim3 grid(K / 128, N / 128, E);
+    block_quant_weight_kernel<<<grid, 256, 0, stream>>>(w, N, K, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int64_t n4 = n / 4;
+    f32_to_bf16_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(x),
+                                                               reinterpret_cast<uint2*>(y), n4);
+    return cudaGetLastError();
+}
+
+}  // namespace mfp8

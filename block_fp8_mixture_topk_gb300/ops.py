@@ -1,0 +1,264 @@
+"""ctypes binding of libmoefp8 (argument marshalling only).
+
+Function names and argument order follow the C ABI; tensors are torch CUDA
+tensors (bf16 as torch.bfloat16, e4m3 codes as torch.uint8 or
+torch.float8_e4m3fn), launched on torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_BLOCK_M = 128
+SCORING = {"softmax": 0, "sigmoid": 1}
+EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2}
+
+_ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE", -3: "MOE_ERR_WORKSPACE_TOO_SMALL",
+           -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {_ERRORS.get(code, code)}")
+        self.code = code
+
+
+class _RoutingParams(ctypes.Structure):
+    _fields_ = [("scoring", ctypes.c_int32), ("n_group", ctypes.c_int32), ("topk_group", ctypes.c_int32),
+                ("routed_scaling", ctypes.c_float), ("bias", ctypes.c_void_p)]
+
+
+class _Epilogue(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("topk", ctypes.c_int32), ("out_f32", ctypes.c_void_p),
+                ("out_q", ctypes.c_void_p), ("out_scale", ctypes.c_void_p),
+                ("out_scale_row_stride", ctypes.c_int64), ("out_scale_kb_stride", ctypes.c_int64),
+                ("sorted_pair_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
+                ("num_pairs", ctypes.c_int64)]
+
+
+@dataclasses.dataclass
+class RoutingParams:
+    """Router options of the C ABI's moe_routing_params (bias: CUDA fp32 [E] or None)."""
+    scoring: str = "softmax"
+    n_group: int = 1
+    topk_group: int = 1
+    routed_scaling: float = 1.0
+    bias: torch.Tensor | None = None
+
+    def to_c(self) -> _RoutingParams:
+        return _RoutingParams(SCORING[self.scoring], self.n_group, self.topk_group, float(self.routed_scaling),
+                              _ptr(self.bias))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded libmoefp8 (built on first use if absent; raises if that fails)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB_PATH):
+                _build.build()
+            L = ctypes.CDLL(_build.LIB_PATH)
+            P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            sig = {
+                "moe_route_topk": ([P, I, I, I, I, P, P, P, P], I),
+                "moe_max_padded_rows": ([I, I, I, I], I64),
+                "moe_max_tiles": ([I, I, I, I], I64),
+                "moe_align_permute_workspace_size": ([I, I, I], SZ),
+                "moe_align_permute": ([P, I, I, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
+                "fp8_group_quant": ([P, I, I, I, P, P, P], I),
+                "fp8_block_quant_weight": ([P, I, I, I, P, P, P], I),
+                "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
+                "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
+                "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
+                "moe_get_device_status": ([P, I], I),
+                "moe_error_string": ([I], ctypes.c_char_p),
+                "moe_device_supported": ([], I),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(name, rc):
+    if rc != 0:
+        raise MoeError(name, rc)
+
+
+def _codes(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"e4m3 codes must be uint8 or float8_e4m3fn, got {t.dtype}")
+    return t
+
+
+def _cuda(t, dtype=None, name="tensor"):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def moe_device_supported() -> bool:
+    return bool(lib().moe_device_supported())
+
+
+def moe_max_padded_rows(T, topk, E, block_m=MOE_BLOCK_M) -> int:
+    return int(lib().moe_max_padded_rows(T, topk, E, block_m))
+
+
+def moe_max_tiles(T, topk, E, block_m=MOE_BLOCK_M) -> int:
+    return int(lib().moe_max_tiles(T, topk, E, block_m))
+
+
+def moe_route_topk(logits, topk, renormalize=True, routing: RoutingParams | None = None):
+    """Top-k routing: returns (ids int32 [T,k], weights fp32 [T,k])."""
+    _cuda(logits, torch.float32, "logits")
+    T, E = logits.shape
+    ids = torch.empty(T, topk, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, topk, dtype=torch.float32, device=logits.device)
+    rp = routing.to_c() if routing else None
+    rc = lib().moe_route_topk(_ptr(logits), T, E, topk, int(bool(renormalize)),
+                              ctypes.byref(rp) if rp else None, _ptr(ids), _ptr(w), _stream())
+    _check("moe_route_topk", rc)
+    return ids, w
+
+
+def moe_align_permute(topk_ids, num_experts, block_m=MOE_BLOCK_M):
+    """Sort pairs by expert; returns a dict of the C ABI's outputs."""
+    _cuda(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    rows = moe_max_padded_rows(T, k, num_experts, block_m)
+    tiles = moe_max_tiles(T, k, num_experts, block_m)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = dict(expert_offsets=torch.empty(num_experts + 1, **i32),
+               padded_offsets=torch.empty(num_experts + 1, **i32),
+               sorted_pair_ids=torch.empty(max(rows, 1), **i32), pos=torch.empty(max(T * k, 1), **i32),
+               tile_expert=torch.empty(max(tiles, 1), **i32), tile_row0=torch.empty(max(tiles, 1), **i32),
+               num_tiles=torch.empty(1, **i32))
+    wsb = int(lib().moe_align_permute_workspace_size(T, k, num_experts))
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    rc = lib().moe_align_permute(_ptr(topk_ids), T, k, num_experts, block_m, _ptr(out["expert_offsets"]),
+                                 _ptr(out["padded_offsets"]), _ptr(out["sorted_pair_ids"]), _ptr(out["pos"]),
+                                 _ptr(out["tile_expert"]), _ptr(out["tile_row0"]), _ptr(out["num_tiles"]),
+                                 _ptr(ws), wsb, _stream())
+    _check("moe_align_permute", rc)
+    out["max_rows"], out["max_tiles"] = rows, tiles
+    return out
+
+
+def fp8_group_quant(x):
+    """1x128 group quantisation of bf16 [rows, cols]: returns (codes uint8, scales fp32 [rows, cols/128])."""
+    _cuda(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    s = torch.empty(rows, max(cols // 128, 1), dtype=torch.float32, device=x.device)
+    rc = lib().fp8_group_quant(_ptr(x), rows, cols, cols, _ptr(q), _ptr(s), _stream())
+    _check("fp8_group_quant", rc)
+    return q, s
+
+
+def fp8_block_quant_weight(w):
+    """128x128 block quantisation of bf16 [E, N, K]: returns (codes uint8 [E,N,K], scales [E,N/128,K/128])."""
+    _cuda(w, torch.bfloat16, "w")
+    E, N, K = w.shape
+    q = torch.empty(E, N, K, dtype=torch.uint8, device=w.device)
+    s = torch.empty(E, max(N // 128, 1), max(K // 128, 1), dtype=torch.float32, device=w.device)
+    rc = lib().fp8_block_quant_weight(_ptr(w), E, N, K, _ptr(q), _ptr(s), _stream())
+    _check("fp8_block_quant_weight", rc)
+    return q, s
+
+
+def fp8_block_grouped_gemm(A, a_scale, a_scale_strides, B, b_scale, tile_expert, tile_row0, num_tiles,
+                           epilogue="store", out_f32=None, out_q=None, out_scale=None, out_scale_strides=(0, 0),
+                           sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0):
+    """Grouped GEMM of the C ABI.  Outputs are caller-provided tensors (see include/moefp8.h)."""
+    A, B = _codes(_cuda(A, None, "A")), _codes(_cuda(B, None, "B"))
+    E, N, K = B.shape
+    ep = _Epilogue(EPILOGUE[epilogue], topk, _ptr(out_f32), _ptr(out_q), _ptr(out_scale),
+                   int(out_scale_strides[0]), int(out_scale_strides[1]), _ptr(sorted_pair_ids),
+                   _ptr(topk_weights), int(num_pairs))
+    rc = lib().fp8_block_grouped_gemm(_ptr(A), _ptr(a_scale), int(a_scale_strides[0]), int(a_scale_strides[1]),
+                                      A.shape[0], _ptr(B), _ptr(b_scale), N, K, E, _ptr(tile_expert),
+                                      _ptr(tile_row0), _ptr(num_tiles), tile_expert.numel(), ctypes.byref(ep),
+                                      _stream())
+    _check("fp8_block_grouped_gemm", rc)
+
+
+def moe_fp8_block_workspace_size(T, H, I, E, topk) -> int:
+    return int(lib().moe_fp8_block_workspace_size(T, H, I, E, topk))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes):
+    key = (device.type, device.index)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
+                          routing: RoutingParams | None = None, out=None, workspace=None):
+    """The whole layer: returns bf16 [T, H] (written into `out` when given)."""
+    _cuda(hidden, torch.bfloat16, "hidden")
+    _cuda(router_logits, torch.float32, "router_logits")
+    w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
+    _cuda(w13_scale, torch.float32, "w13_scale")
+    _cuda(w2_scale, torch.float32, "w2_scale")
+    T, H = hidden.shape
+    E, N1, _ = w13.shape
+    I = N1 // 2
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
+    nbytes = moe_fp8_block_workspace_size(T, H, I, E, topk)
+    if workspace is None:
+        workspace = _workspace(hidden.device, nbytes)
+    rp = routing.to_c() if routing else None
+    rc = lib().moe_fp8_block_forward(_ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+                                     _ptr(w2_scale), T, H, I, E, topk, int(bool(renormalize)),
+                                     ctypes.byref(rp) if rp else None, _ptr(workspace), workspace.numel(),
+                                     _ptr(out), _stream())
+    _check("moe_fp8_block_forward", rc)
+    return out
+
+
+def moe_get_device_status(clear=False) -> int:
+    """Device status bits (synchronises the device)."""
+    st = ctypes.c_uint32(0)
+    _check("moe_get_device_status", lib().moe_get_device_status(ctypes.byref(st), int(bool(clear))))
+    return st.value

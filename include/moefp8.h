@@ -172,6 +172,7 @@ typedef struct moe_gemm_epilogue {
     int64_t out_scale_kb_stride;
     const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER */
     const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER, [T*topk] */
+    int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER: T*topk; other pair ids are skipped */
 } moe_gemm_epilogue;
 
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,

@@ -1,0 +1,96 @@
+"""The C-ABI library loads without a GPU, exports every function include/moefp8.h
+declares, and rejects bad arguments on the host (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_fp8_mixture_topk_gb300 as moe
+from block_fp8_mixture_topk_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moefp8.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["moe_route_topk", "moe_align_permute", "fp8_group_quant", "fp8_block_grouped_gemm",
+                 "moe_fp8_block_forward", "moe_fp8_block_workspace_size", "moe_get_device_status"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(moe.library_path() if os.path.exists(moe.library_path()) else ops.lib()._name)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_only_queries():
+    L = ops.lib()
+    assert L.moe_error_string(0) == b"MOE_OK"
+    assert L.moe_error_string(-3) == b"MOE_ERR_WORKSPACE_TOO_SMALL"
+    # P + min(E, P) * (block_m - 1) padded rows, whole tiles
+    assert moe.moe_max_padded_rows(4096, 8, 256, 128) == 32768 + 256 * 127
+    assert moe.moe_max_padded_rows(1, 8, 256, 128) == 8 + 8 * 127
+    assert moe.moe_max_tiles(1, 8, 256, 128) == (8 + 8 * 127) // 128
+    assert moe.moe_max_padded_rows(-1, 8, 256, 128) == -1
+    ws = moe.moe_fp8_block_workspace_size(4096, 7168, 2048, 256, 8)
+    rows = 32768 + 256 * 127
+    assert ws >= rows * 7168 + rows * 2048 + 4096 * 7168 * 4
+    assert moe.moe_fp8_block_workspace_size(16, 256, 256, 4, 2) > 0
+
+
+@pytest.mark.parametrize("T,E,topk,rp,code", [
+    (-1, 8, 2, None, -1),
+    (4, 0, 1, None, -1),
+    (4, 2048, 2, None, -2),
+    (4, 8, 9, None, -2),
+    (4, 64, 33, None, -2),
+    (4, 8, 2, (1, 3, 1, 1.0), -2),     # E % n_group != 0
+    (4, 8, 2, (0, 2, 1, 1.0), -2),     # grouping with softmax
+    (4, 8, 2, (1, 2, 3, 1.0), -1),     # topk_group > n_group
+    (4, 8, 2, (7, 1, 1, 1.0), -1),     # unknown scoring
+])
+def test_route_rejects_bad_arguments_on_host(T, E, topk, rp, code):
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    rps = None
+    if rp is not None:
+        rps = ops._RoutingParams(rp[0], rp[1], rp[2], rp[3], None)
+    rc = L.moe_route_topk(p, T, E, topk, 1, ctypes.byref(rps) if rps else None, p, p, None)
+    assert rc == code
+
+
+def test_quant_and_gemm_reject_bad_shapes_on_host():
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    assert L.fp8_group_quant(p, 4, 100, 100, p, p, None) == -2          # cols % 128
+    assert L.fp8_group_quant(p, 4, 128, 100, p, p, None) == -1          # ld < cols
+    assert L.fp8_group_quant(p, 0, 128, 128, p, p, None) == 0           # empty: nothing to do
+    assert L.fp8_block_quant_weight(p, 1, 100, 128, p, p, None) == -2
+    ep = ops._Epilogue(1, 1, None, None, None, 0, 0, None, None, 0)
+    # silu epilogue needs N % 256 == 0
+    assert L.fp8_block_grouped_gemm(p, p, 1, 1, 128, p, p, 384, 128, 1, p, p, p, 1, ctypes.byref(ep), None) == -2
+    ep.kind = 9
+    assert L.fp8_block_grouped_gemm(p, p, 1, 1, 128, p, p, 256, 128, 1, p, p, p, 1, ctypes.byref(ep), None) == -1
+
+
+def test_forward_rejects_bad_arguments_on_host():
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    # H not a multiple of 128
+    assert L.moe_fp8_block_forward(p, p, p, p, p, p, 4, 100, 256, 4, 2, 1, None, p, 1 << 30, p, None) == -2
+    # T == 0 is a no-op
+    assert L.moe_fp8_block_forward(None, None, None, None, None, None, 0, 256, 256, 4, 2, 1, None, None, 0, None,
+                                   None) == 0
+    # workspace too small
+    assert L.moe_fp8_block_forward(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.c_void_p(0x10000), 16, p,
+                                   None) == -3
