@@ -1,0 +1,86 @@
+"""Helpers shared by the GPU parity tests: seeded inputs on both sides, the
+output tolerance, and the mapping between the GPU's padded sorted rows and
+the oracle's unpadded ones."""
+import numpy as np
+import torch
+
+import moe_inputs as mi
+import oracle
+import block_fp8_mixture_topk_gb300 as moe
+
+# Output tolerance of the layer: relative Frobenius error and per-element error
+# against the root-mean-square of the reference.
+REL_FRO = 1e-2
+MAX_REL_RMS = 5e-2
+
+
+def assert_output_close(got_bf16: torch.Tensor, ref: np.ndarray, rows=None):
+    got = got_bf16.float().cpu().double().numpy()
+    if rows is not None:
+        got, ref = got[rows], ref[rows]
+    assert np.all(np.isfinite(got)), "non-finite output"
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    rms = np.sqrt(np.mean(ref ** 2))
+    worst = np.abs(got - ref).max() / rms
+    assert rel <= REL_FRO and worst <= MAX_REL_RMS, f"rel_fro={rel:.3e} max|d|/rms={worst:.3e}"
+    return rel, worst
+
+
+def routing_of(wl: mi.Workload, device="cuda"):
+    bias = mi.expert_bias(wl)
+    if wl.scoring == mi.SIGMOID:
+        rp = moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling,
+                               None if bias is None else bias.to(device))
+    else:
+        rp = moe.RoutingParams("softmax", 1, 1, wl.routed_scaling)
+    okw = dict(scoring=wl.scoring, bias=None if bias is None else bias.numpy(), n_group=wl.n_group,
+               topk_group=wl.topk_group, routed_scaling=wl.routed_scaling)
+    return rp, okw
+
+
+class Layer:
+    """Quantised weights of a workload on the GPU (GPU quantiser), plus the
+    oracle's own quantisation of any subset of experts (from the same bf16)."""
+
+    def __init__(self, wl: mi.Workload, device="cuda", chunk=8):
+        self.wl, self.device = wl, device
+        E, H, I = wl.E, wl.H, wl.I
+        self.w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
+        self.w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
+        self.w2q = torch.empty(E, H, I, dtype=torch.uint8, device=device)
+        self.w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
+        for e0 in range(0, E, chunk):
+            ex = range(e0, min(E, e0 + chunk))
+            q, s = moe.fp8_block_quant_weight(mi.w13_bf16(wl, device, ex))
+            self.w13q[e0:e0 + len(ex)], self.w13s[e0:e0 + len(ex)] = q, s
+            q, s = moe.fp8_block_quant_weight(mi.w2_bf16(wl, device, ex))
+            self.w2q[e0:e0 + len(ex)], self.w2s[e0:e0 + len(ex)] = q, s
+        torch.cuda.synchronize()
+
+    def oracle_weights(self, experts):
+        """Oracle-quantised weights as full [E, ...] arrays with only `experts` filled."""
+        wl = self.wl
+        experts = sorted(set(int(e) for e in experts))
+        E, H, I = wl.E, wl.H, wl.I
+        w13q = np.zeros((E, 2 * I, H), dtype=np.uint8)
+        w13s = np.zeros((E, 2 * I // 128, H // 128), dtype=np.float32)
+        w2q = np.zeros((E, H, I), dtype=np.uint8)
+        w2s = np.zeros((E, H // 128, I // 128), dtype=np.float32)
+        for e in experts:
+            w13q[e], w13s[e] = [a[0] for a in oracle.quant_128x128_bf16(mi.bf16_bits(mi.w13_bf16(wl, self.device, [e])))]
+            w2q[e], w2s[e] = [a[0] for a in oracle.quant_128x128_bf16(mi.bf16_bits(mi.w2_bf16(wl, self.device, [e])))]
+        return w13q, w13s, w2q, w2s
+
+    def forward(self, hidden, logits, rp):
+        return moe.moe_fp8_block_forward(hidden, logits, self.w13q, self.w13s, self.w2q, self.w2s, self.wl.topk,
+                                         self.wl.renormalize, rp)
+
+
+def unpadded_rows(padded_offsets: np.ndarray, offsets: np.ndarray):
+    """Index array mapping the oracle's sorted row i to the GPU's padded row."""
+    E = offsets.size - 1
+    out = np.empty(offsets[-1], dtype=np.int64)
+    for e in range(E):
+        n = offsets[e + 1] - offsets[e]
+        out[offsets[e]:offsets[e + 1]] = padded_offsets[e] + np.arange(n)
+    return out

@@ -1,0 +1,336 @@
+"""GPU parity: every kernel of the layer against the CPU oracle, through the C ABI.
+
+Bit-exact: routing ids, the expert sort, quantised activation / weight bytes
+and scales.  Floating point: the layer's output within relative Frobenius
+1e-2 and per-element 5e-2 * rms(reference); the GEMM stages in isolation
+within 1e-5 (fp32 accumulation against fp64); requantised intermediate bytes
+within one e4m3 code (>= 99% identical), since fp32 rounding order decides them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import block_fp8_mixture_topk_gb300 as moe
+from moe_testutil import Layer, assert_output_close, routing_of, unpadded_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def device_status_stays_clean():
+    moe.moe_get_device_status(clear=True)
+    yield
+    assert moe.moe_get_device_status(clear=True) == 0
+
+
+def bits(t):
+    return mi.bf16_bits(t)
+
+
+# ----------------------------------------------------------------------------- quantisation
+
+def special_rows(rows, cols, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * torch.exp2(torch.randint(-12, 12, (rows, 1), generator=g).float())
+    if rows > 3:
+        x[0] = 0.0                                   # zero groups -> floor scale, zero codes
+        x[1] = 1e-12                                 # below the 1e-8 amax floor
+        x[2, :128] = 3e38                            # near the bf16 maximum
+        x[3, 5] = -x[3].abs().max() * 1.5            # negative group maximum
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 128), (37, 384), (300, 2048), (4096, 7168)])
+def test_group_quant_bit_exact(rows, cols):
+    x = special_rows(rows, cols, rows + cols)
+    q, s = moe.fp8_group_quant(x.to(DEV))
+    oq, os_ = oracle.quant_1x128_bf16(bits(x))
+    assert np.array_equal(s.cpu().numpy(), os_)
+    assert np.array_equal(q.cpu().numpy(), oq)
+
+
+@pytest.mark.parametrize("name,experts", [("tiny", None), ("dsv3", [0, 255])])
+def test_block_quant_weight_bit_exact(name, experts):
+    wl = mi.WORKLOADS[name]
+    for w in (mi.w13_bf16(wl, DEV, experts), mi.w2_bf16(wl, DEV, experts)):
+        q, s = moe.fp8_block_quant_weight(w)
+        oq, os_ = oracle.quant_128x128_bf16(bits(w))
+        assert np.array_equal(s.cpu().numpy(), os_)
+        assert np.array_equal(q.cpu().numpy(), oq)
+
+
+# ----------------------------------------------------------------------------- routing / sort
+
+ROUTE_CASES = [
+    ("tiny", None), ("mixtral", None), ("dsv3", None), ("dsv3_decode", 1), ("dsv3_decode", 128),
+    ("qwen3_skew", None),
+]
+
+
+def workload(name, T=None):
+    wl = mi.WORKLOADS[name]
+    return wl.with_tokens(T) if T else wl
+
+
+@pytest.mark.parametrize("name,T", ROUTE_CASES)
+def test_route_bit_exact_ids(name, T):
+    wl = workload(name, T)
+    logits = mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    ids, w = moe.moe_route_topk(logits.to(DEV), wl.topk, wl.renormalize, rp)
+    oids, ow = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("E,topk,scoring", [(1024, 32, "softmax"), (1024, 32, "sigmoid"), (1, 1, "softmax"),
+                                            (8, 8, "softmax"), (96, 7, "sigmoid")])
+def test_route_limits(E, topk, scoring):
+    g = torch.Generator().manual_seed(E + topk)
+    logits = torch.randn(33, E, generator=g)
+    logits[0] = 0.5                                   # all ties -> lowest indices
+    sc = 1 if scoring == "sigmoid" else 0
+    ids, w = moe.moe_route_topk(logits.to(DEV), topk, True, moe.RoutingParams(scoring, 1, 1, 1.0))
+    oids, ow = oracle.route(logits.numpy(), topk, True, scoring=sc)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+    assert ids.cpu()[0].tolist() == list(range(topk))
+
+
+def test_route_without_renormalize():
+    g = torch.Generator().manual_seed(2)
+    logits = torch.randn(50, 64, generator=g)
+    for scoring, sc in (("softmax", 0), ("sigmoid", 1)):
+        ids, w = moe.moe_route_topk(logits.to(DEV), 6, False, moe.RoutingParams(scoring, 1, 1, 1.5))
+        oids, ow = oracle.route(logits.numpy(), 6, False, scoring=sc, routed_scaling=1.5)
+        assert np.array_equal(ids.cpu().numpy(), oids)
+        np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+
+
+def check_sort(perm, ids_np, E, block_m=128):
+    off, sorted_, pos = oracle.permute(ids_np, E)
+    counts = np.diff(off)
+    padded = (counts + block_m - 1) // block_m * block_m
+    poff = np.concatenate([[0], np.cumsum(padded)])
+    assert np.array_equal(perm["expert_offsets"].cpu().numpy(), off)
+    assert np.array_equal(perm["padded_offsets"].cpu().numpy(), poff)
+    rows = unpadded_rows(poff, off)
+    sp = perm["sorted_pair_ids"].cpu().numpy()
+    assert np.array_equal(sp[rows], sorted_)
+    pad = np.ones(poff[-1], dtype=bool)
+    pad[rows] = False
+    assert np.all(sp[:poff[-1]][pad] == -1)
+    assert np.array_equal(perm["pos"].cpu().numpy()[:ids_np.size], rows[pos])
+    nt = int(perm["num_tiles"].item())
+    assert nt == poff[-1] // block_m
+    te = perm["tile_expert"].cpu().numpy()[:nt]
+    tr = perm["tile_row0"].cpu().numpy()[:nt]
+    assert np.array_equal(tr, np.arange(nt) * block_m)
+    assert np.array_equal(te, np.searchsorted(poff, tr, side="right") - 1)
+
+
+@pytest.mark.parametrize("name,T", ROUTE_CASES)
+def test_align_permute_exact(name, T):
+    wl = workload(name, T)
+    rp, okw = routing_of(wl)
+    oids, _ = oracle.route(mi.router_logits(wl).numpy(), wl.topk, wl.renormalize, **okw)
+    perm = moe.moe_align_permute(torch.from_numpy(oids).to(DEV), wl.E)
+    check_sort(perm, oids, wl.E)
+
+
+@pytest.mark.parametrize("T,k,E,block_m", [(3000, 4, 16, 128), (1, 1, 1, 128), (700, 3, 1024, 64), (5, 2, 4, 1)])
+def test_align_permute_shapes(T, k, E, block_m):
+    g = torch.Generator().manual_seed(T)
+    ids = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32)
+    ids[: T // 2, 0] = 0                              # skew towards expert 0
+    perm = moe.moe_align_permute(ids.to(DEV), E, block_m)
+    check_sort(perm, ids.numpy(), E, block_m)
+
+
+def test_align_permute_drops_invalid_ids_and_reports():
+    ids = torch.tensor([[0, 1], [5, 1], [-1, 0]], dtype=torch.int32)
+    perm = moe.moe_align_permute(ids.to(DEV), 4)
+    assert moe.moe_get_device_status(clear=True) & 2
+    pos = perm["pos"].cpu().numpy()[:6]
+    assert pos[2] == -1 and pos[4] == -1
+    assert perm["expert_offsets"].cpu().tolist() == [0, 2, 4, 4, 4]
+
+
+# ----------------------------------------------------------------------------- grouped GEMM stages
+
+GEMM_CASES = [
+    dict(T=24, H=384, I=256, E=4, topk=2),
+    dict(T=300, H=256, I=384, E=2, topk=1),           # several tiles per expert
+    dict(T=200, H=512, I=128, E=16, topk=4),          # many small experts, some empty
+]
+
+
+def stage_inputs(c, seed):
+    wl = mi.Workload("stage", seed, c["T"], c["H"], c["I"], c["E"], c["topk"])
+    layer = Layer(wl)
+    hidden = mi.hidden(wl)
+    logits = mi.router_logits(wl)
+    oids, ow = oracle.route(logits.numpy(), wl.topk, True)
+    ids = torch.from_numpy(oids).to(DEV)
+    perm = moe.moe_align_permute(ids, wl.E)
+    q, s = moe.fp8_group_quant(hidden.to(DEV))
+    sp = perm["sorted_pair_ids"].long()
+    valid = sp >= 0
+    tok = torch.where(valid, sp // wl.topk, torch.zeros_like(sp))
+    rows = perm["max_rows"]
+    A = torch.zeros(rows, wl.H, dtype=torch.uint8, device=DEV)
+    As = torch.ones(rows, wl.H // 128, dtype=torch.float32, device=DEV)
+    A[valid] = q[tok[valid]]
+    As[valid] = s[tok[valid]]
+    w13q, w13s, w2q, w2s = layer.oracle_weights(range(wl.E))
+    ref = oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, wl.topk, want_c1=True)
+    m = unpadded_rows(perm["padded_offsets"].cpu().numpy(), ref["offsets"])
+    return wl, layer, perm, A, As, ref, m, torch.from_numpy(ow).to(DEV)
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_store_matches_oracle(ci):
+    wl, layer, perm, A, As, ref, m, _ = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    out = torch.full((A.shape[0], 2 * wl.I), float("nan"), dtype=torch.float32, device=DEV)
+    moe.fp8_block_grouped_gemm(A, As, (wl.H // 128, 1), layer.w13q, layer.w13s, perm["tile_expert"],
+                               perm["tile_row0"], perm["num_tiles"], "store", out_f32=out)
+    got = out.cpu().double().numpy()[m]
+    want = ref["c1"]
+    err = np.abs(got - want)
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+    assert err.max() <= 1e-4 * np.sqrt(np.mean(want ** 2))
+
+
+def test_gemm_store_ragged_n():
+    """N = 384: the last 256-wide tile is half empty (128-column MMA)."""
+    g = torch.Generator().manual_seed(3)
+    E, N, K, M = 2, 384, 256, 256
+    B = torch.randint(0, 256, (E, N, K), generator=g, dtype=torch.uint8)
+    B[(B & 0x7F) == 0x7F] = 0x3E
+    A = torch.randint(0, 256, (M, K), generator=g, dtype=torch.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x3E
+    bs = torch.rand(E, N // 128, K // 128, generator=g) + 0.5
+    as_ = torch.rand(M, K // 128, generator=g) + 0.5
+    te = torch.tensor([1, 0], dtype=torch.int32)
+    tr = torch.tensor([0, 128], dtype=torch.int32)
+    nt = torch.tensor([2], dtype=torch.int32)
+    out = torch.full((M, N), float("nan"), device=DEV)
+    moe.fp8_block_grouped_gemm(A.to(DEV), as_.to(DEV), (K // 128, 1), B.to(DEV), bs.to(DEV), te.to(DEV), tr.to(DEV),
+                               nt.to(DEV), "store", out_f32=out)
+    Ad = A.view(torch.float8_e4m3fn).double() * as_.double().repeat_interleave(128, 1)
+    Bd = B.view(torch.float8_e4m3fn).double() * bs.double().repeat_interleave(128, 1).repeat_interleave(128, 2)
+    want = torch.cat([Ad[:128] @ Bd[1].T, Ad[128:] @ Bd[0].T]).numpy()
+    got = out.cpu().double().numpy()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_silu_requant_matches_oracle(ci):
+    wl, layer, perm, A, As, ref, m, _ = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    rows = A.shape[0]
+    oq = torch.empty(rows, wl.I, dtype=torch.uint8, device=DEV)
+    osc = torch.empty(rows, wl.I // 128, dtype=torch.float32, device=DEV)
+    moe.fp8_block_grouped_gemm(A, As, (wl.H // 128, 1), layer.w13q, layer.w13s, perm["tile_expert"],
+                               perm["tile_row0"], perm["num_tiles"], "silu_mul_quant", out_q=oq, out_scale=osc,
+                               out_scale_strides=(wl.I // 128, 1))
+    gs = osc.cpu().numpy()[m]
+    np.testing.assert_allclose(gs, ref["a2s"], rtol=2e-5)
+    gq = oq.cpu().numpy()[m].astype(np.int32)
+    rq = ref["a2q"].astype(np.int32)
+    same = gq == rq
+    assert same.mean() >= 0.99, same.mean()
+    # where they differ: same sign, adjacent codes (or +-0 around zero)
+    diff = ~same
+    mag_g, mag_r = gq[diff] & 0x7F, rq[diff] & 0x7F
+    sign_ok = ((gq[diff] ^ rq[diff]) & 0x80 == 0) | ((mag_g <= 1) & (mag_r <= 1))
+    assert np.all(sign_ok) and np.all(np.abs(mag_g - mag_r) <= 1)
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_weighted_scatter_matches_oracle(ci):
+    """GEMM2 on the oracle's own intermediate codes, so only GEMM2 + scatter are compared."""
+    wl, layer, perm, A, As, ref, m, w = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    rows = A.shape[0]
+    A2 = torch.zeros(rows, wl.I, dtype=torch.uint8)
+    A2s = torch.ones(rows, wl.I // 128, dtype=torch.float32)
+    A2[torch.from_numpy(m)] = torch.from_numpy(ref["a2q"])
+    A2s[torch.from_numpy(m)] = torch.from_numpy(ref["a2s"])
+    out = torch.zeros(wl.T, wl.H, dtype=torch.float32, device=DEV)
+    moe.fp8_block_grouped_gemm(A2.to(DEV), A2s.to(DEV), (wl.I // 128, 1), layer.w2q, layer.w2s, perm["tile_expert"],
+                               perm["tile_row0"], perm["num_tiles"], "weighted_scatter", out_f32=out,
+                               sorted_pair_ids=perm["sorted_pair_ids"], topk_weights=w.reshape(-1),
+                               topk=wl.topk, num_pairs=wl.T * wl.topk)
+    got = out.cpu().double().numpy()
+    want = ref["out"]
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+
+
+# ----------------------------------------------------------------------------- whole layer
+
+def run_layer(wl, tokens=None, layer=None):
+    layer = layer or Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    out = layer.forward(hidden.to(DEV), logits.to(DEV), rp)
+    torch.cuda.synchronize()
+    oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    toks = range(wl.T) if tokens is None else tokens
+    experts = set(oids[list(toks)].reshape(-1).tolist())
+    w13q, w13s, w2q, w2s = layer.oracle_weights(experts)
+    ref = oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, wl.topk, wl.renormalize,
+                             tokens=tokens, **okw)
+    return out, ref
+
+
+def test_forward_tiny_all_tokens():
+    wl = mi.WORKLOADS["tiny"]
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("name", ["mixtral", "dsv3", "qwen3_skew"])
+def test_forward_full_size_sampled_tokens(name):
+    wl = mi.WORKLOADS[name]
+    tokens = [0, 1, wl.T // 2, wl.T - 1]
+    out, ref = run_layer(wl, tokens)
+    assert_output_close(out, ref["out"], rows=tokens)
+
+
+@pytest.mark.parametrize("T", mi.DECODE_TOKENS)
+def test_forward_decode_sampled_tokens(T):
+    wl = mi.WORKLOADS["dsv3_decode"].with_tokens(T)
+    tokens = sorted(set([0, T // 2, T - 1]))
+    out, ref = run_layer(wl, tokens)
+    assert_output_close(out, ref["out"], rows=tokens)
+
+
+@pytest.mark.parametrize("T,H,I,E,topk", [(1, 128, 128, 1, 1), (5, 256, 128, 8, 8), (70, 128, 256, 3, 2)])
+def test_forward_small_shapes(T, H, I, E, topk):
+    wl = mi.Workload("edge", 60 + T, T, H, I, E, topk)
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
+def test_forward_all_tokens_to_one_expert():
+    """300 tokens, top-1, every token on expert 2: three tiles of one expert, the other experts empty."""
+    wl = mi.Workload("skew", 77, 300, 256, 256, 4, 1)
+    layer = Layer(wl)
+    hidden = mi.hidden(wl)
+    logits = mi.router_logits(wl)
+    logits[:, 2] += 100.0
+    out = layer.forward(hidden.to(DEV), logits.to(DEV), None)
+    w13q, w13s, w2q, w2s = layer.oracle_weights([2])
+    ref = oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, 1)
+    assert_output_close(out, ref["out"])
+
+
+def test_forward_zero_tokens_is_noop():
+    wl = mi.WORKLOADS["tiny"]
+    layer = Layer(wl)
+    hidden = torch.empty(0, wl.H, dtype=torch.bfloat16, device=DEV)
+    logits = torch.empty(0, wl.E, dtype=torch.float32, device=DEV)
+    out = layer.forward(hidden, logits, None)
+    assert out.shape == (0, wl.H)
