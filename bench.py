@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Throughput of the block-FP8 fused MoE layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one moe_fp8_block_forward over one batch of synthetic tokens (routing,
+expert sort, activation quantisation, both grouped GEMMs with their fused
+epilogues, bf16 output), inputs already resident in HBM.  The default workload
+is the DeepSeek-V3-shaped prefill layer (T=4096, H=7168, I=2048, E=256, top-8,
+sigmoid grouped routing); its 11.3 GB of expert weights exceed the 129 MB L2, so
+no flush is needed between steps.  Under torchrun each rank runs its own replica
+on its own batch (no collective on the data path): scaling is weak.
+
+--impl reference times the CPU oracle (oracle/) on a bounded token sample of the
+same workload on the host cores; it needs no GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+LAUNCHES_PER_STEP = 8      # route 1 + expert sort 3 + quantise 1 + two grouped GEMMs + bf16 conversion
+FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
+PROFILE = os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md")
+GEMM_SOURCES = [os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc", f) for f in ("gemm.cu", "common.cuh")]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="dsv3", choices=sorted(mi.WORKLOADS))
+    p.add_argument("--tokens", type=int, default=None, help="override T (decode sweeps)")
+    p.add_argument("--cpu-sample", type=int, default=None, help="tokens the oracle computes")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sust=d.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, source="fallback")
+
+
+def describe(wl, world):
+    routing = ("sigmoid + bias, n_group=%d topk_group=%d, scaling %.1f" % (wl.n_group, wl.topk_group,
+                                                                           wl.routed_scaling)
+               if wl.scoring == mi.SIGMOID else "softmax")
+    wbytes = wl.E * 3 * wl.H * wl.I
+    return {"workload": f"{wl.name}: MoE layer T={wl.T} H={wl.H} I={wl.I} E={wl.E} top-{wl.topk}, {routing}"
+                        + (", renormalize" if wl.renormalize else "")
+                        + (f", Zipf s={wl.zipf_s} router offsets" if wl.zipf_s else ""),
+            "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "topk": wl.topk,
+            "expert_weight_bytes": wbytes,
+            "l2": "inputs larger than L2" if wbytes > 129e6 else "L2 flushed between steps",
+            "parallelism": f"replicas x{world}"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        self.index = ids[device_index] if device_index < len(ids) and ids[device_index].isdigit() else str(device_index)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", self.index, "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def oracle_inputs(wl, tokens, device):
+    """CPU copies of the workload's inputs and the oracle's own quantisation of the experts
+    the sampled tokens use (untimed preparation)."""
+    import numpy as np
+    import oracle
+    hidden, logits = mi.hidden(wl, device), mi.router_logits(wl, device)
+    bias = mi.expert_bias(wl, device)
+    okw = dict(scoring=wl.scoring, bias=None if bias is None else bias.cpu().numpy(), n_group=wl.n_group,
+               topk_group=wl.topk_group, routed_scaling=wl.routed_scaling)
+    ids, _ = oracle.route(logits.cpu().numpy(), wl.topk, wl.renormalize, **okw)
+    experts = sorted(set(ids[tokens].reshape(-1).tolist()))
+    E, H, I = wl.E, wl.H, wl.I
+    w13q = np.zeros((E, 2 * I, H), np.uint8)
+    w13s = np.zeros((E, 2 * I // 128, H // 128), np.float32)
+    w2q = np.zeros((E, H, I), np.uint8)
+    w2s = np.zeros((E, H // 128, I // 128), np.float32)
+    for e in experts:
+        q, s = oracle.quant_128x128_bf16(mi.bf16_bits(mi.w13_bf16(wl, device, [e])))
+        w13q[e], w13s[e] = q[0], s[0]
+        q, s = oracle.quant_128x128_bf16(mi.bf16_bits(mi.w2_bf16(wl, device, [e])))
+        w2q[e], w2s[e] = q[0], s[0]
+    args = (mi.bf16_bits(hidden), logits.cpu().numpy(), w13q, w13s, w2q, w2s, wl.topk, wl.renormalize)
+    return args, okw, len(experts)
+
+
+def default_sample(wl):
+    return max(1, min(wl.T, 2 if wl.E * wl.H * wl.I > 1e9 else 16))
+
+
+def time_oracle(wl, n_tokens, device, runs=1, warmup=0):
+    import oracle
+    tokens = list(range(n_tokens))
+    args, okw, n_exp = oracle_inputs(wl, tokens, device)
+    for _ in range(warmup):
+        oracle.moe_forward(*args, tokens=tokens, **okw)
+    times = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        oracle.moe_forward(*args, tokens=tokens, **okw)
+        times.append(time.perf_counter() - t0)
+    sample = (f"first {n_tokens} of {wl.T} tokens ({n_tokens * wl.topk} routed pairs over {n_exp} experts); "
+              f"routing, sort and quantisation of all {wl.T} tokens included")
+    return times, sample, oracle.num_threads()
+
+
+def run_reference(args, wl):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    n = args.cpu_sample or default_sample(wl)
+    times, sample, cores = time_oracle(wl, n, "cpu", runs=args.steps, warmup=args.warmup)
+    ms = 1000.0 * sum(times) / len(times)
+    value = n / (ms / 1000.0)
+    line = {"impl": "reference", "metric": "block-FP8 fused-MoE tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
+            "config": describe(wl, 1),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- ours (GPU)
+def gemm_source_sha():
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(wl):
+    """dram bytes per launch of the w13 GEMM from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    if not os.path.exists(PROFILE):
+        return None
+    kv = {}
+    for line in open(PROFILE):
+        if "=" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split("=", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("source_sha") != gemm_source_sha() or kv.get("workload") != wl.name:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, wl):
+    import numpy as np
+    import block_fp8_mixture_topk_gb300 as moe
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # inputs: each rank its own batch (seed offset by rank), weights quantised on the GPU (untimed)
+    wl_r = wl.with_(number=wl.number + 100 * rank) if rank else wl
+    hidden, logits = mi.hidden(wl_r, dev), mi.router_logits(wl_r, dev)
+    bias = mi.expert_bias(wl, dev)
+    rp = (moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling, bias)
+          if wl.scoring == mi.SIGMOID else moe.RoutingParams("softmax", 1, 1, wl.routed_scaling))
+    E, H, I = wl.E, wl.H, wl.I
+    w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+    w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+    w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+    for e0 in range(0, E, 8):
+        ex = range(e0, min(E, e0 + 8))
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex))
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex))
+    out = torch.empty(wl.T, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, H, I, E, wl.topk), dtype=torch.uint8, device=dev)
+    ids, _ = moe.moe_route_topk(logits, wl.topk, wl.renormalize, rp)
+    touched = int(torch.unique(ids).numel())
+    P = wl.P
+
+    def step(events=None):
+        moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
+                                  workspace=ws, events=events)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    n_ev = len(moe.ops.FORWARD_STAGES) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier()
+    if clocks:
+        clocks.start()
+    t0.record()
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record()
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1) / args.steps
+    stage_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, name in enumerate(moe.ops.FORWARD_STAGES)}
+    if moe.moe_get_device_status(clear=True):
+        raise RuntimeError("device status word set during the benchmark")
+
+    # end to end through the public API: pinned host inputs in, bf16 output back, every step
+    hid_h, log_h = hidden.cpu().pin_memory(), logits.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hid_d, log_d = torch.empty_like(hidden), torch.empty_like(logits)
+
+    def e2e_step():
+        hid_d.copy_(hid_h, non_blocking=True)
+        log_d.copy_(log_h, non_blocking=True)
+        moe.moe_fp8_block_forward(hid_d, log_d, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
+                                  workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    if dist:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    tokens_s = world * wl.T / (ms / 1000.0)
+    flops = wl.flops()
+    per_expert_w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+    per_expert = 3 * H * I + ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+    layer_bytes = touched * per_expert + wl.T * H * 2 * 2 + wl.T * E * 4
+    # algorithmic bytes of one w13 GEMM launch: touched experts' w13 + scales, the sorted activation
+    # rows and scales read once, the requantised intermediate and its scales written once
+    gemm_bytes = touched * per_expert_w13 + P * (H + H // 128 * 4) + P * (I + I // 128 * 4)
+    gemm_flops = 4 * P * H * I
+    g_ms = stage_ms["gemm_w13"]
+    fp8_peak = pk["bf16"] * FP8_OVER_BF16
+    ridge = fp8_peak * 1e12 / (pk["hbm"] * 1e9)
+    if gemm_flops / gemm_bytes > ridge:
+        roof = {"bound": "tensor", "achieved": gemm_flops / (g_ms / 1e3) / 1e12, "peak": fp8_peak,
+                "unit": "TFLOP/s", "peak_source": f"{pk['source']} bf16 burst x {FP8_OVER_BF16} (fp8/bf16 nominal)"}
+    else:
+        roof = {"bound": "hbm", "achieved": gemm_bytes / (g_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                "peak_source": f"{pk['source']} copy bandwidth"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)"
+    roof["algorithmic_bytes_per_launch"] = gemm_bytes
+    roof["ms_per_launch"] = g_ms
+    roof["traffic"] = profiled_traffic(wl)
+
+    line = {"metric": "block-FP8 fused-MoE tokens/s", "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
+            "config": describe(wl, world),
+            "tflops": world * flops / (ms / 1e3) / 1e12,
+            "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
+            "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,
+            "experts_touched": touched, "weight_bytes_touched": touched * per_expert,
+            "stage_ms": stage_ms, "clocks": clk,
+            "e2e": {"value": world * wl.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
+                    "d2h_bytes_per_step": out.numel() * 2},
+            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "roofline": roof}
+    if world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample(wl)
+        times, sample, cores = time_oracle(wl, n, dev, runs=1)
+        line["cpu_baseline"] = {"value": n / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    _ = np
+
+
+def main():
+    args = parse()
+    wl = mi.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -291,6 +291,15 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
                           const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H, int I, int E,
                           int topk, int renormalize, const moe_routing_params* rp, void* workspace,
                           size_t workspace_bytes, uint16_t* out, void* stream) {
+    return moe_fp8_block_forward_events(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
+                                        renormalize, rp, workspace, workspace_bytes, out, stream, nullptr);
+}
+
+int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
+                                 int I, int E, int topk, int renormalize, const moe_routing_params* rp,
+                                 void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
+                                 void* const* events) {
     int rc = check_routing(T, E, topk, rp);
     if (rc != MOE_OK) return rc;
     if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
@@ -324,18 +333,26 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
     float* outf = reinterpret_cast<float*>(ws + L.outf);
     const int64_t P = static_cast<int64_t>(T) * topk;
 
+    auto mark = [&](int i) {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+    };
     const int scoring = rp ? rp->scoring : MOE_SCORING_SOFTMAX;
-    cudaError_t e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, rp ? rp->n_group : 1,
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess)
+        e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, rp ? rp->n_group : 1,
                                       rp ? rp->topk_group : 1, rp ? rp->routed_scaling : 1.0f,
                                       rp ? rp->bias : nullptr, ids, wts, s);
+    if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
                                  reinterpret_cast<int32_t*>(ws + L.counts), st->status, s);
     // each token quantised once, its codes written to the sorted rows of its pairs;
     // the scales are stored transposed ([H/128][rows]) for the GEMM's per-row reads
+    if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(outf, 0, static_cast<size_t>(T) * H * sizeof(float), s);
+    if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
         GemmArgs g{};
         g.A = a1;
@@ -360,6 +377,7 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
     }
+    if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess) {
         GemmArgs g{};
         g.A = a2;
@@ -385,7 +403,9 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
     }
+    if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess) e = launch_f32_to_bf16(outf, out, static_cast<int64_t>(T) * H, s);
+    if (e == cudaSuccess) e = mark(6);
     return cuda_rc(e);
 }
 

@@ -84,6 +84,7 @@ def lib():
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
+                "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, P], I),
                 "moe_get_device_status": ([P, I], I),
                 "moe_error_string": ([I], ctypes.c_char_p),
                 "moe_device_supported": ([], I),
@@ -164,7 +165,7 @@ def moe_align_permute(topk_ids, num_experts, block_m=MOE_BLOCK_M):
     i32 = dict(dtype=torch.int32, device=dev)
     out = dict(expert_offsets=torch.empty(num_experts + 1, **i32),
                padded_offsets=torch.empty(num_experts + 1, **i32),
-               sorted_pair_ids=torch.empty(max(rows, 1), **i32), pos=torch.empty(max(T * k, 1), **i32),
+               sorted_pair_ids=torch.full((max(rows, 1),), -1, **i32), pos=torch.empty(max(T * k, 1), **i32),
                tile_expert=torch.empty(max(tiles, 1), **i32), tile_row0=torch.empty(max(tiles, 1), **i32),
                num_tiles=torch.empty(1, **i32))
     wsb = int(lib().moe_align_permute_workspace_size(T, k, num_experts))
@@ -232,9 +233,15 @@ def _workspace(device, nbytes):
     return ws
 
 
+FORWARD_STAGES = ("route", "sort", "quant", "gemm_w13", "gemm_w2", "to_bf16")
+
+
 def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
-                          routing: RoutingParams | None = None, out=None, workspace=None):
-    """The whole layer: returns bf16 [T, H] (written into `out` when given)."""
+                          routing: RoutingParams | None = None, out=None, workspace=None, events=None):
+    """The whole layer: returns bf16 [T, H] (written into `out` when given).
+
+    events: optional list of 7 torch.cuda.Event recorded between the stages
+    (FORWARD_STAGES) on the current stream, for per-stage timing."""
     _cuda(hidden, torch.bfloat16, "hidden")
     _cuda(router_logits, torch.float32, "router_logits")
     w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
@@ -249,10 +256,16 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     if workspace is None:
         workspace = _workspace(hidden.device, nbytes)
     rp = routing.to_c() if routing else None
-    rc = lib().moe_fp8_block_forward(_ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w13_scale), _ptr(w2),
-                                     _ptr(w2_scale), T, H, I, E, topk, int(bool(renormalize)),
-                                     ctypes.byref(rp) if rp else None, _ptr(workspace), workspace.numel(),
-                                     _ptr(out), _stream())
+    args = [_ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), T, H, I, E,
+            topk, int(bool(renormalize)), ctypes.byref(rp) if rp else None, _ptr(workspace), workspace.numel(),
+            _ptr(out), _stream()]
+    if events is None:
+        rc = lib().moe_fp8_block_forward(*args)
+    else:
+        if len(events) != len(FORWARD_STAGES) + 1:
+            raise ValueError("events: one more than the number of stages")
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+        rc = lib().moe_fp8_block_forward_events(*args, arr)
     _check("moe_fp8_block_forward", rc)
     return out
 

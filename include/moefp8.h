@@ -200,6 +200,20 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
                           uint16_t* out, void* stream);
 
+/* The same layer, recording CUDA events between its stages for per-stage timing
+ * (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the
+ * caller, recorded on `stream` in this order: before routing, before the expert
+ * sort, before the activation quantisation, before the w13 GEMM, before the w2
+ * GEMM, before the bf16 conversion, after it).  Arguments and errors as
+ * moe_fp8_block_forward; events == NULL behaves exactly like it. */
+#define MOE_FORWARD_NUM_EVENTS 7
+int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits,
+                                 const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale,
+                                 int T, int H, int I, int E, int topk, int renormalize,
+                                 const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
+                                 uint16_t* out, void* stream, void* const* events);
+
 /* ---- status -------------------------------------------------------------------- */
 /* Reads (and with clear != 0, resets) the device status word of the current
  * device into *status (host).  Synchronises the device. */

@@ -177,14 +177,18 @@ def stage_inputs(c, seed):
     ids = torch.from_numpy(oids).to(DEV)
     perm = moe.moe_align_permute(ids, wl.E)
     q, s = moe.fp8_group_quant(hidden.to(DEV))
-    sp = perm["sorted_pair_ids"].long()
-    valid = sp >= 0
-    tok = torch.where(valid, sp // wl.topk, torch.zeros_like(sp))
+    # gather the sorted activation rows on the host, from indices checked against their bounds
+    used = int(perm["padded_offsets"][-1].item())
+    sp = perm["sorted_pair_ids"].cpu().numpy()[:used].astype(np.int64)
+    assert used <= perm["max_rows"] and np.all(sp < wl.T * wl.topk) and np.all(sp >= -1)
+    valid = np.nonzero(sp >= 0)[0]
+    tok = sp[valid] // wl.topk
     rows = perm["max_rows"]
-    A = torch.zeros(rows, wl.H, dtype=torch.uint8, device=DEV)
-    As = torch.ones(rows, wl.H // 128, dtype=torch.float32, device=DEV)
-    A[valid] = q[tok[valid]]
-    As[valid] = s[tok[valid]]
+    A = torch.zeros(rows, wl.H, dtype=torch.uint8)
+    As = torch.ones(rows, wl.H // 128, dtype=torch.float32)
+    A[torch.from_numpy(valid)] = q.cpu()[torch.from_numpy(tok)]
+    As[torch.from_numpy(valid)] = s.cpu()[torch.from_numpy(tok)]
+    A, As = A.to(DEV), As.to(DEV)
     w13q, w13s, w2q, w2s = layer.oracle_weights(range(wl.E))
     ref = oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, wl.topk, want_c1=True)
     m = unpadded_rows(perm["padded_offsets"].cpu().numpy(), ref["offsets"])
