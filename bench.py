@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="dsv3", choices=sorted(mi.WORKLOADS))
     p.add_argument("--tokens", type=int, default=None, help="override T (decode sweeps)")
+    p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     p.add_argument("--cpu-sample", type=int, default=None, help="tokens the oracle computes")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -365,6 +366,8 @@ def main():
     wl = mi.WORKLOADS[args.workload]
     if args.tokens:
         wl = wl.with_tokens(args.tokens)
+    if args.experts:
+        wl = wl.with_(E=args.experts)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
