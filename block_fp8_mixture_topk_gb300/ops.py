@@ -264,6 +264,9 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     else:
         if len(events) != len(FORWARD_STAGES) + 1:
             raise ValueError("events: one more than the number of stages")
+        for ev in events:
+            if not ev.cuda_event:       # torch creates the CUDA event on its first record()
+                ev.record()
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
         rc = lib().moe_fp8_block_forward_events(*args, arr)
     _check("moe_fp8_block_forward", rc)
