@@ -21,4 +21,5 @@ from .ops import (  # noqa: F401
     moe_max_padded_rows,
     moe_max_tiles,
     moe_route_topk,
+    moe_unpermute_sum,
 )

@@ -81,7 +81,7 @@ int64_t max_rows(int64_t P, int64_t E, int64_t bm) {
 }
 
 struct ForwardLayout {
-    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, outf, total;
+    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, y, total;
     int64_t rows, tiles;
 };
 
@@ -110,7 +110,7 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
-    L.outf = take(static_cast<size_t>(T) * H * 4);
+    L.y = take(static_cast<size_t>(L.rows) * H * 4);
     L.total = off;
     return L;
 }
@@ -243,6 +243,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
             if (!ep->out_q || !ep->out_scale || !aligned(ep->out_q, 16)) return MOE_ERR_INVALID_ARG;
             break;
         case MOE_EPI_WEIGHTED_SCATTER:
+        case MOE_EPI_WEIGHTED_ROWS:
             if (!ep->out_f32 || !aligned(ep->out_f32, 16) || !ep->sorted_pair_ids || !ep->topk_weights ||
                 ep->topk < 1 || ep->num_pairs < 0)
                 return MOE_ERR_INVALID_ARG;
@@ -280,6 +281,19 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.num_pairs = ep->num_pairs;
     g.status = st->status;
     return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int T, int topk, int H, uint16_t* out,
+                      void* stream) {
+    if (T < 0 || topk < 1 || H < 0 || y_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0 || H == 0) return MOE_OK;
+    if (!y || !pos || !out || !aligned(y, 16) || !aligned(out, 8)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_unpermute_sum(y, y_rows, pos, T, topk, H, out, st->status,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk) {
@@ -330,7 +344,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     float* a1s = reinterpret_cast<float*>(ws + L.a1s);
     uint8_t* a2 = ws + L.a2;
     float* a2s = reinterpret_cast<float*>(ws + L.a2s);
-    float* outf = reinterpret_cast<float*>(ws + L.outf);
+    float* yrows = reinterpret_cast<float*>(ws + L.y);
     const int64_t P = static_cast<int64_t>(T) * topk;
 
     auto mark = [&](int i) {
@@ -351,7 +365,6 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     // the scales are stored transposed ([H/128][rows]) for the GEMM's per-row reads
     if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(outf, 0, static_cast<size_t>(T) * H * sizeof(float), s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
         GemmArgs g{};
@@ -370,6 +383,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
         g.epi = MOE_EPI_SILU_MUL_QUANT;
+        g.sorted_pair_ids = sorted;
         g.out_q = a2;
         g.out_scale = a2s;
         g.os_row_stride = 1;
@@ -394,8 +408,8 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.tile_row0 = tile_r;
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
-        g.epi = MOE_EPI_WEIGHTED_SCATTER;
-        g.out_f32 = outf;
+        g.epi = MOE_EPI_WEIGHTED_ROWS;
+        g.out_f32 = yrows;
         g.sorted_pair_ids = sorted;
         g.topk_weights = wts;
         g.topk = topk;
@@ -404,7 +418,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         e = launch_grouped_gemm(g, st->num_sms, s);
     }
     if (e == cudaSuccess) e = mark(5);
-    if (e == cudaSuccess) e = launch_f32_to_bf16(outf, out, static_cast<int64_t>(T) * H, s);
+    if (e == cudaSuccess) e = launch_unpermute_sum(yrows, L.rows, pos, T, topk, H, out, st->status, s);
     if (e == cudaSuccess) e = mark(6);
     return cuda_rc(e);
 }

@@ -15,18 +15,20 @@
 // is promoted.  (The pages' Triton kernel dequantises after the K loop, which is
 // exact only for per-tensor / per-channel scales; blockwise scales vary along K.)
 //
-// Roles (320 threads, one CTA per SM, persistent over the tile list):
+// Roles (384 threads, one CTA per SM, persistent over the tile list):
 //   warp 0, one thread : TMA producer, 4-stage ring of {A 128x128, B 256x128} e4m3 tiles
 //   warp 1, one thread : MMA issuer (4 x tcgen05.mma 128x256x32 per K block), TMEM owner
-//   warps 2..9         : promotion + epilogue; warp w reads TMEM lanes 32*(w%4)..+31
-//                        (its rows) and 128 of the 256 columns (column half (w-2)/4)
+//   warps 2, 3         : idle (they complete warpgroup 0, which gives registers away)
+//   warps 4..11        : promotion + epilogue; warp w reads TMEM lanes 32*(w%4)..+31
+//                        (its rows) and 128 of the 256 columns (column half (w-4)/4)
 // Epilogues:
 //   store     : fp32 rows to out_f32
 //   silu      : B tile = 128 gate rows + the 128 matching up rows; h = silu(g)*u in
 //               fp32, amax of the 128-wide group exchanged between the two column
 //               halves through shared memory, 1x128 e4m3 requantisation
-//   scatter   : out_f32[token] += router_weight * C (float4 atomics), the top-k
-//               weighted unpermute-sum
+//   scatter   : out_f32[token] += router_weight * C (float4 atomics)
+//   rows      : out_f32[row] = router_weight * C in sorted-row order (plain stores); the
+//               layer sums each token's k rows afterwards (moe_unpermute_sum), in a fixed order
 // Every wait is bounded (mbar_wait); on expiry the CTA records
 // MOE_STATUS_WAIT_TIMEOUT, waits (bounded) for its TMA loads and MMAs in flight,
 // frees its TMEM and exits.
@@ -45,7 +47,12 @@ constexpr int A_TILE = BM * BK;        // 16 KB
 constexpr int B_HALF = 128 * BK;       // 16 KB: 128 weight rows
 constexpr int B_TILE = 2 * B_HALF;     // 32 KB: 256 weight rows
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int FIRST_EPI_WARP = 4;       // warpgroup 0: TMA warp, MMA warp, two idle warps
+constexpr int NUM_THREADS = (FIRST_EPI_WARP + NUM_EPI_WARPS) * 32;
+// registers per thread: 168 at launch (384 threads); warpgroup 0 gives back down to 80,
+// the two epilogue warpgroups take up to 208: 128*80 + 256*208 <= 384*168
+constexpr uint32_t REGS_CONTROL = 80;
+constexpr uint32_t REGS_EPILOGUE = 208;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 
 struct SmemCtl {
@@ -58,7 +65,9 @@ struct SmemCtl {
     uint32_t tmem_base;
     int abort_flag;
     float amax_x[2][2][BM];            // [tile parity][column half][row]
+    alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
 };
+constexpr int STAGE_ROW = 20;          // floats per staged row (80 B: conflict-free 16-byte slots)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
 
 struct Tile {
@@ -70,6 +79,8 @@ struct Tile {
     bool ok;
 };
 
+// Work item w -> (tile m = w / NT, column block n = w % NT): consecutive CTAs take
+// the column blocks of one tile, so its A rows are shared in L2.
 template <int EPI>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int64_t w, int NT) {
     Tile t;
@@ -136,8 +147,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
-
-    if (warp == 0) {
+    if (warp < FIRST_EPI_WARP) {
+      regs_decrease<REGS_CONTROL>();
+      if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ producer
             int stage = 0;
@@ -217,9 +229,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_wait(smem_addr(&ctl->drain), 0, nullptr, a.status);
             }
         }
+      }
     } else {
+        regs_increase<REGS_EPILOGUE>();
         // ---------------------------------------------------------------- epilogue
-        const int g = (warp - 2) >> 2;          // column half
+        const int g = (warp - FIRST_EPI_WARP) >> 2;   // column half
         const int sp = warp & 3;                // TMEM lane quarter
         const int row = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
@@ -230,7 +244,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const Tile t = decode_tile<EPI>(a, w, NT);
             if (!t.ok) continue;
             const int64_t grow = t.row0 + row;
-            const bool active = (EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1;
+            // rows whose sorted pair id is -1 are padding: a warp with no real row skips the
+            // promotion (decode tiles hold a few real rows out of 128)
+            const bool row_real = a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0;
+            const bool warp_live = __any_sync(0xffffffffu, row_real);
+            const bool active = ((EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1) && warp_live;
             const float* bs0;
             const float* bs1;
             if (EPI == MOE_EPI_SILU_MUL_QUANT) {
@@ -245,32 +263,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
 
+            // the scales of K block kb+2 are loaded while block kb is promoted (L2 latency
+            // is longer than one K block of MMA)
+            float pa0 = as[0], pb0 = bs0[0], pc0 = bs1[0];
+            float pa1 = 0.0f, pb1 = 0.0f, pc1 = 0.0f;
+            if (KB > 1) {
+                pa1 = as[a.as_kb_stride];
+                pb1 = bs0[1];
+                pc1 = bs1[1];
+            }
             for (int kb = 0; kb < KB; ++kb) {
-                const float sa = as[kb * a.as_kb_stride];
-                const float s0 = sa * bs0[kb];
-                const float s1 = sa * bs1[kb];
+                const float s0 = pa0 * pb0;
+                const float s1 = pa0 * pc0;
+                pa0 = pa1;
+                pb0 = pb1;
+                pc0 = pc1;
+                if (kb + 2 < KB) {
+                    pa1 = as[(kb + 2) * a.as_kb_stride];
+                    pb1 = bs0[kb + 2];
+                    pc1 = bs1[kb + 2];
+                }
                 if (!mbar_wait(smem_addr(&ctl->tfull[buf]), bphase, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t col = lane_base + buf * 256;
-                float v[16];
-                if (EPI == MOE_EPI_SILU_MUL_QUANT) {
-                    // gate columns g*64.. (scale s0) -> acc[0, 64); up columns 128+g*64.. (s1) -> acc[64, 128)
+                if (active) {
+                    // two rounds of 64 columns: two 32-column TMEM loads, one wait, 32 packed FMAs.
+                    // silu: round 0 = gate columns g*64.. (scale s0) -> acc[0, 64),
+                    //       round 1 = up columns 128+g*64.. (scale s1) -> acc[64, 128)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        tmem_ld16(col + (c < 4 ? 0 : 128) + g * 64 + (c & 3) * 16, v);
-                        const float sc = c < 4 ? s0 : s1;
+                    for (int r = 0; r < 2; ++r) {
+                        const uint32_t c0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? col + r * 128 + g * 64
+                                                                            : col + g * 128 + r * 64;
+                        const float sc = (EPI == MOE_EPI_SILU_MUL_QUANT && r == 1) ? s1 : s0;
+                        float va[32], vb[32];
+                        tmem_ld32x2(c0, c0 + 32, va, vb);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(v[j], sc, acc[c * 16 + j]);
-                    }
-                } else if (active) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        tmem_ld16(col + g * 128 + c * 16, v);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(v[j], s0, acc[c * 16 + j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            ffma2(acc + r * 64 + j, va + j, sc);
+                            ffma2(acc + r * 64 + 32 + j, vb + j, sc);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -285,8 +319,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float amax = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
+                    // silu(g) * u = g * u / (1 + e^-g); its fp32 rounding is not part of the
+                    // definition (the requantised bytes are compared within one code)
                     const float gate = acc[j];
-                    const float h = gate / (1.0f + expf(-gate)) * acc[64 + j];
+                    const float h = __fdividef(gate * acc[64 + j], 1.0f + __expf(-gate));
                     acc[j] = h;
                     amax = fmaxf(amax, fabsf(h));
                 }
@@ -299,17 +335,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
                 const float sc = group_scale(amax);
-                uint32_t wbuf[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint32_t lo = e4m3x2(__fdiv_rn(acc[4 * j], sc), __fdiv_rn(acc[4 * j + 1], sc));
-                    const uint32_t hi = e4m3x2(__fdiv_rn(acc[4 * j + 2], sc), __fdiv_rn(acc[4 * j + 3], sc));
-                    wbuf[j] = lo | (hi << 16);
-                }
+                const float rsc = __frcp_rn(sc);
                 uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    dst[j] = make_uint4(wbuf[4 * j], wbuf[4 * j + 1], wbuf[4 * j + 2], wbuf[4 * j + 3]);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float* h = acc + c * 16 + j * 4;
+                        const uint32_t lo = e4m3x2(div_by_scale(h[0], sc, rsc), div_by_scale(h[1], sc, rsc));
+                        const uint32_t hi = e4m3x2(div_by_scale(h[2], sc, rsc), div_by_scale(h[3], sc, rsc));
+                        wv[j] = lo | (hi << 16);
+                    }
+                    dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
                 if (g == 0) a.out_scale[grow * a.os_row_stride + static_cast<int64_t>(t.n) * a.os_kb_stride] = sc;
             } else if (EPI == MOE_EPI_WEIGHTED_SCATTER) {
                 if (active) {
@@ -325,11 +364,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             } else {
+                // fp32 rows (times the router weight for the rows epilogue) written through a
+                // per-warp staging buffer, 16 columns at a time, so that each store instruction
+                // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
                 if (active) {
-                    float4* dst = reinterpret_cast<float4*>(a.out_f32 + grow * a.N + t.bcol0 + g * 128);
+                    bool keep = true;
+                    float wgt = 1.0f;
+                    if (EPI == MOE_EPI_WEIGHTED_ROWS) {
+                        const int32_t pair = a.sorted_pair_ids[grow];
+                        keep = pair >= 0 && pair < a.num_pairs;
+                        wgt = keep ? a.topk_weights[pair] : 0.0f;
+                    }
+                    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+                    float* stg = ctl->stage[warp - FIRST_EPI_WARP];
+                    const int r_out = lane >> 2, q_out = lane & 3;
+                    float* gbase = a.out_f32 + (t.row0 + sp * 32) * a.N + t.bcol0 + g * 128 + q_out * 4;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float* v = acc + c * 16 + q * 4;
+                            *reinterpret_cast<float4*>(stg + lane * STAGE_ROW + q * 4) =
+                                make_float4(wgt * v[0], wgt * v[1], wgt * v[2], wgt * v[3]);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = i * 8 + r_out;
+                            const float4 v = *reinterpret_cast<const float4*>(stg + r * STAGE_ROW + q_out * 4);
+                            if ((keep_mask >> r) & 1u)
+                                *reinterpret_cast<float4*>(gbase + static_cast<int64_t>(r) * a.N + c * 16) = v;
+                        }
+                        __syncwarp();
+                    }
                 }
             }
             ++tile_iter;
@@ -391,6 +458,9 @@ cudaError_t gemm_init_device() {
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return err;
 }
 
@@ -413,6 +483,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
             break;
         case MOE_EPI_WEIGHTED_SCATTER:
             grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            break;
+        case MOE_EPI_WEIGHTED_ROWS:
+            grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
             break;
         default:
             return cudaErrorInvalidValue;

@@ -31,8 +31,9 @@ cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_
                                int topk, cudaStream_t stream);
 cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
                                       cudaStream_t stream);
-// fp32 [n] -> bf16 bits [n], round to nearest even (n multiple of 4, 16-byte aligned)
-cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t stream);
+// out[t] = bf16(sum_j y[pos[t*topk + j]]) in j order (H multiple of 4, y / out 16- / 8-byte aligned)
+cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,
+                                 uint16_t* out, uint32_t* status, cudaStream_t stream);
 
 // gemm.cu
 struct GemmArgs {

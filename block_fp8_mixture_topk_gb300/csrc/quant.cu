@@ -3,8 +3,9 @@
 // Activation groups of 1x128 ("computed per-token at runtime", page
 // "Quantization and MoE Optimizations", section Fp8Config; key
 // kFp8Dynamic128Sym, page "vllm.model_executor.layers.fused_moe.oracle.fp8"):
-// scale = max(amax, 1e-8)/448 in fp32, codes = e4m3(x / scale) with IEEE
-// division and the hardware's round-to-nearest-even, saturating conversion.
+// scale = max(amax, 1e-8)/448 in fp32, codes = e4m3(x / scale) with the
+// correctly rounded quotient and the hardware's round-to-nearest-even, saturating
+// conversion.
 // Sixteen threads own one group (8 bf16 = one 16-byte load each), reduce the
 // amax with four shuffles, and write 8 code bytes each.  The scatter form
 // writes each token's codes to the sorted rows of its top-k pairs, so the
@@ -13,6 +14,9 @@
 // Weight blocks of 128x128 ("weight_block_size ... [128, 128]", Fp8Config)
 // use the same rule with the amax over the whole block: one 256-thread CTA per
 // block keeps its 32 KB of bf16 in registers between the amax and the encode.
+//
+// The weighted unpermute-sum adds each token's k router-weighted expert rows
+// (written in sorted order by the w2 GEMM) in a fixed order and rounds to bf16.
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
@@ -30,11 +34,12 @@ __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
     }
 }
 
-__device__ __forceinline__ uint2 encode8(const float* f, float sc) {
+// codes of 8 values x / sc (correctly rounded quotient, see div_by_scale; rsc = 1/sc rounded)
+__device__ __forceinline__ uint2 encode8(const float* f, float sc, float rsc) {
     uint32_t b[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint16_t lo = e4m3x2(__fdiv_rn(f[2 * i], sc), __fdiv_rn(f[2 * i + 1], sc));
+        const uint16_t lo = e4m3x2(div_by_scale(f[2 * i], sc, rsc), div_by_scale(f[2 * i + 1], sc, rsc));
         b[i] = lo;
     }
     return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
         for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (active) {
             const float sc = group_scale(amax);
-            const uint2 code = encode8(f, sc);
+            const uint2 code = encode8(f, sc, __frcp_rn(sc));
             if (pos) {
                 for (int j = 0; j < topk; ++j) {
                     const int64_t o = pos[r * topk + j];
@@ -109,12 +114,13 @@ __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t*
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
     const float sc = group_scale(amax);
+    const float rsc = __frcp_rn(sc);
     uint2 out[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         unpack8(v[i], f);
-        out[i] = encode8(f, sc);
+        out[i] = encode8(f, sc, rsc);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -123,16 +129,34 @@ __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t*
     if (threadIdx.x == 0) s[(static_cast<int64_t>(e) * NB + nb) * KB + kb] = sc;
 }
 
-__global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4* __restrict__ x, uint2* __restrict__ y,
-                                                          int64_t n4) {
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float4 v = x[i];
-        const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(v.x));
-        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v.y));
-        const uint32_t c = __bfloat16_as_ushort(__float2bfloat16_rn(v.z));
-        const uint32_t d = __bfloat16_as_ushort(__float2bfloat16_rn(v.w));
-        y[i] = make_uint2(a | (b << 16), c | (d << 16));
+// out[t] = bf16(sum_j y[pos[t*topk + j]]): thread = 4 consecutive columns of one token,
+// the k rows summed in j order in fp32.
+__global__ void __launch_bounds__(256) unpermute_sum_kernel(const float4* __restrict__ y, int64_t y_rows,
+                                                            const int32_t* __restrict__ pos, int64_t T, int topk,
+                                                            int H4, uint2* __restrict__ out, uint32_t* status) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= H4) return;
+    for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int j = 0; j < topk; ++j) {
+            const int64_t r = pos[t * topk + j];
+            if (r < 0) continue;
+            if (r >= y_rows) {
+                if (c == 0) status_set(status, MOE_STATUS_BAD_EXPERT_ID);
+                continue;
+            }
+            const float4 v = __ldg(y + r * H4 + c);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x));
+        const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(acc.y));
+        const uint32_t cc = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z));
+        const uint32_t d = __bfloat16_as_ushort(__float2bfloat16_rn(acc.w));
+        out[t * H4 + c] = make_uint2(a | (b << 16), cc | (d << 16));
     }
 }
 
@@ -163,11 +187,13 @@ cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, ui
     return cudaGetLastError();
 }
 
-cudaError_t launch_f32_to_bf16(const float* x, uint16_t* y, int64_t n, cudaStream_t stream) {
-    if (n == 0) return cudaSuccess;
-    const int64_t n4 = n / 4;
-    f32_to_bf16_kernel<<<grid_for(n4, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(x),
-                                                               reinterpret_cast<uint2*>(y), n4);
+cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,
+                                 uint16_t* out, uint32_t* status, cudaStream_t stream) {
+    if (T == 0 || H == 0) return cudaSuccess;
+    const int H4 = H / 4;
+    dim3 grid((H4 + 255) / 256, static_cast<unsigned>(T < 65535 ? T : 65535));
+    unpermute_sum_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y), y_rows, pos, T, topk, H4,
+                                                   reinterpret_cast<uint2*>(out), status);
     return cudaGetLastError();
 }
 

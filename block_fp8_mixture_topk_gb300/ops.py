@@ -17,7 +17,7 @@ from . import build as _build
 
 MOE_BLOCK_M = 128
 SCORING = {"softmax": 0, "sigmoid": 1}
-EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2}
+EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3}
 
 _ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE", -3: "MOE_ERR_WORKSPACE_TOO_SMALL",
            -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
@@ -85,6 +85,7 @@ def lib():
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, P], I),
+                "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
                 "moe_error_string": ([I], ctypes.c_char_p),
                 "moe_device_supported": ([], I),
@@ -217,6 +218,18 @@ def fp8_block_grouped_gemm(A, a_scale, a_scale_strides, B, b_scale, tile_expert,
     _check("fp8_block_grouped_gemm", rc)
 
 
+def moe_unpermute_sum(y, pos, T, topk, out=None):
+    """out[t] = bf16(sum_j y[pos[t*topk + j]]) for y fp32 [rows, H] and pos int32 [T*topk]."""
+    _cuda(y, torch.float32, "y")
+    _cuda(pos, torch.int32, "pos")
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
+    rc = lib().moe_unpermute_sum(_ptr(y), y.shape[0], _ptr(pos), T, topk, H, _ptr(out), _stream())
+    _check("moe_unpermute_sum", rc)
+    return out
+
+
 def moe_fp8_block_workspace_size(T, H, I, E, topk) -> int:
     return int(lib().moe_fp8_block_workspace_size(T, H, I, E, topk))
 
@@ -233,7 +246,7 @@ def _workspace(device, nbytes):
     return ws
 
 
-FORWARD_STAGES = ("route", "sort", "quant", "gemm_w13", "gemm_w2", "to_bf16")
+FORWARD_STAGES = ("route", "sort", "quant", "gemm_w13", "gemm_w2", "unpermute_sum")
 
 
 def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,

@@ -155,24 +155,32 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
  *   MOE_EPI_WEIGHTED_SCATTER: for rows with pair = sorted_pair_ids[r] >= 0,
  *       out_f32[pair / topk, n] += topk_weights[pair] * C[r, n]  (out_f32: device
  *       fp32 [T, N], accumulated with atomics; the caller zeroes it first).
+ *   MOE_EPI_WEIGHTED_ROWS: for rows with pair = sorted_pair_ids[r] >= 0,
+ *       out_f32[r, n] = topk_weights[pair] * C[r, n]  (out_f32: device fp32
+ *       [a_rows, N] in sorted-row order; padding rows are not written).
  * K, N multiples of 128 (N multiple of 256 for MOE_EPI_SILU_MUL_QUANT).
- * Rows of a tile past its expert's count hold whatever A holds there; their
- * results are written (store / silu epilogues) but belong to no pair. */
+ * Optional epilogue field sorted_pair_ids (store / silu epilogues; NULL =
+ * unused): rows with id -1 are padding; a group of 32 padding rows is not
+ * computed and its output rows are left unspecified (the scatter and rows
+ * epilogues always require it and skip padding rows).
+ * Otherwise rows of a tile past its expert's count are computed from whatever
+ * A holds there and belong to no pair. */
 #define MOE_EPI_STORE_F32 0
 #define MOE_EPI_SILU_MUL_QUANT 1
 #define MOE_EPI_WEIGHTED_SCATTER 2
+#define MOE_EPI_WEIGHTED_ROWS 3
 
 typedef struct moe_gemm_epilogue {
     int32_t kind;                     /* MOE_EPI_* */
-    int32_t topk;                     /* MOE_EPI_WEIGHTED_SCATTER */
+    int32_t topk;                     /* MOE_EPI_WEIGHTED_SCATTER / _ROWS */
     float* out_f32;
     uint8_t* out_q;
     float* out_scale;
     int64_t out_scale_row_stride;
     int64_t out_scale_kb_stride;
-    const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER */
-    const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER, [T*topk] */
-    int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER: T*topk; other pair ids are skipped */
+    const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER / _ROWS */
+    const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER / _ROWS, [T*topk] */
+    int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER / _ROWS: T*topk; other pair ids are skipped */
 } moe_gemm_epilogue;
 
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
@@ -181,6 +189,16 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
                            const int32_t* tile_expert, const int32_t* tile_row0,
                            const int32_t* num_tiles, int64_t max_tiles,
                            const moe_gemm_epilogue* epilogue, void* stream);
+
+/* ---- weighted unpermute-sum -------------------------------------------------------
+ * out[t, :] = bf16( sum_{j < topk, pos[t*topk+j] >= 0} y[pos[t*topk+j], :] ), summed in
+ * j order in fp32, rounded to nearest even ("gathers results", page
+ * "Quantization and MoE Optimizations", section Modular Kernel Architecture).
+ * y: device fp32 [y_rows, H] (the router-weighted rows of MOE_EPI_WEIGHTED_ROWS);
+ * pos: device int32 [T*topk] (moe_align_permute); out: device bf16 [T, H].
+ * H multiple of 4; positions >= y_rows are skipped and set MOE_STATUS_BAD_EXPERT_ID. */
+int moe_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int T, int topk, int H,
+                      uint16_t* out, void* stream);
 
 /* ---- the whole layer -------------------------------------------------------------
  * Router -> sort by expert -> 1x128 quantisation of hidden -> GEMM over w13 with
@@ -204,7 +222,7 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
  * (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the
  * caller, recorded on `stream` in this order: before routing, before the expert
  * sort, before the activation quantisation, before the w13 GEMM, before the w2
- * GEMM, before the bf16 conversion, after it).  Arguments and errors as
+ * GEMM, before the weighted unpermute-sum, after it).  Arguments and errors as
  * moe_fp8_block_forward; events == NULL behaves exactly like it. */
 #define MOE_FORWARD_NUM_EVENTS 7
 int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits,

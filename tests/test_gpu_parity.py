@@ -52,6 +52,28 @@ def test_group_quant_bit_exact(rows, cols):
     assert np.array_equal(q.cpu().numpy(), oq)
 
 
+def test_group_quant_bit_exact_wide_range():
+    """8M values, per-group magnitudes from 2^-60 to 2^60, and groups whose scale is an exact power
+    of two holding e4m3 tie midpoints (ties to even) -- the quotient x/scale must round exactly as
+    IEEE division does."""
+    g = torch.Generator().manual_seed(77)
+    rows, cols = 2048, 4096
+    x = torch.randn(rows, cols, generator=g)
+    x = x * torch.exp2(torch.randint(-60, 60, (rows, cols // 128), generator=g).float()).repeat_interleave(128, 1)
+    vals = oracle.e4m3_values()
+    mids = torch.from_numpy(((vals[1:126] + vals[2:127]) / 2).astype(np.float32))
+    for r in range(0, rows, 64):                       # tie rows: amax 448 * 2^k, the rest midpoints * 2^k
+        k = float(r % 17 - 8)
+        row = mids[torch.randint(0, mids.numel(), (cols,), generator=g)] * (2.0 ** k)
+        row[::128] = 448.0 * 2.0 ** k
+        x[r] = row * torch.where(torch.rand(cols, generator=g) < 0.5, -1.0, 1.0)
+    x = x.to(torch.bfloat16)
+    q, s = moe.fp8_group_quant(x.to(DEV))
+    oq, os_ = oracle.quant_1x128_bf16(bits(x))
+    assert np.array_equal(s.cpu().numpy(), os_)
+    assert np.array_equal(q.cpu().numpy(), oq)
+
+
 @pytest.mark.parametrize("name,experts", [("tiny", None), ("dsv3", [0, 255])])
 def test_block_quant_weight_bit_exact(name, experts):
     wl = mi.WORKLOADS[name]
@@ -270,6 +292,48 @@ def test_gemm_weighted_scatter_matches_oracle(ci):
     got = out.cpu().double().numpy()
     want = ref["out"]
     assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_weighted_rows_then_unpermute_sum_matches_oracle(ci):
+    """GEMM2 writing router-weighted rows in sorted order, then the j-ordered sum of each token's
+    rows, on the oracle's own intermediate codes."""
+    wl, layer, perm, A, As, ref, m, w = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    rows = A.shape[0]
+    A2 = torch.zeros(rows, wl.I, dtype=torch.uint8)
+    A2s = torch.ones(rows, wl.I // 128, dtype=torch.float32)
+    A2[torch.from_numpy(m)] = torch.from_numpy(ref["a2q"])
+    A2s[torch.from_numpy(m)] = torch.from_numpy(ref["a2s"])
+    y = torch.full((rows, wl.H), float("nan"), dtype=torch.float32, device=DEV)
+    moe.fp8_block_grouped_gemm(A2.to(DEV), A2s.to(DEV), (wl.I // 128, 1), layer.w2q, layer.w2s, perm["tile_expert"],
+                               perm["tile_row0"], perm["num_tiles"], "weighted_rows", out_f32=y,
+                               sorted_pair_ids=perm["sorted_pair_ids"], topk_weights=w.reshape(-1),
+                               topk=wl.topk, num_pairs=wl.T * wl.topk)
+    # each real row holds weight * C2 of its pair
+    wflat = ref["weights"].reshape(-1).astype(np.float64)
+    got_rows = y.cpu().double().numpy()[m]
+    want_rows = ref["c2"] * wflat[ref["sorted"]][:, None]
+    assert np.linalg.norm(got_rows - want_rows) / np.linalg.norm(want_rows) < 1e-5
+    out = moe.moe_unpermute_sum(y, perm["pos"][: wl.T * wl.topk].contiguous(), wl.T, wl.topk)
+    got = out.float().cpu().double().numpy()
+    want = ref["out"]
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 4e-3      # bf16 output rounding
+    assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-6 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("T,k,H,rows", [(1, 1, 4, 3), (37, 3, 384, 200), (300, 8, 2048, 2500)])
+def test_unpermute_sum_bit_exact_against_fp32_j_order(T, k, H, rows):
+    g = torch.Generator().manual_seed(T * k)
+    y = torch.randn(rows, H, generator=g)
+    pos = torch.randint(0, rows, (T * k,), generator=g, dtype=torch.int32)
+    pos[::5] = -1                                    # dropped pairs are skipped
+    out = moe.moe_unpermute_sum(y.to(DEV), pos.to(DEV), T, k)
+    acc = torch.zeros(T, H, dtype=torch.float32)
+    p2 = pos.view(T, k).long()
+    for j in range(k):
+        valid = p2[:, j] >= 0
+        acc[valid] = acc[valid] + y[p2[valid, j]]
+    assert torch.equal(out.cpu(), acc.to(torch.bfloat16))
 
 
 # ----------------------------------------------------------------------------- whole layer
