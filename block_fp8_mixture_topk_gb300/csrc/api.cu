@@ -117,6 +117,16 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
 
 }  // namespace
 
+namespace mfp8 {
+// Device set-up and the status word's device address, for entry points in other files.
+int device_status_word(uint32_t** status) {
+    DeviceState* s = nullptr;
+    const int rc = device_state(&s);
+    if (rc == MOE_OK) *status = s->status;
+    return rc;
+}
+}  // namespace mfp8
+
 extern "C" {
 
 int moe_device_supported(void) {

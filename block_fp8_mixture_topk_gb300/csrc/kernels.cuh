@@ -60,6 +60,9 @@ struct GemmArgs {
     uint32_t* status;
 };
 cudaError_t gemm_init_device();
+
+// api.cu: once-per-device set-up; on MOE_OK, *status = the device status word's address
+int device_status_word(uint32_t** status);
 cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 }  // namespace mfp8

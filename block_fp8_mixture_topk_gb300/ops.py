@@ -79,6 +79,7 @@ def lib():
                 "moe_max_tiles": ([I, I, I, I], I64),
                 "moe_align_permute_workspace_size": ([I, I, I], SZ),
                 "moe_align_permute": ([P, I, I, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
+                "moe_align_permute_noalloc": ([P, I, I, I, I, P, P, P, P, P, P, P, P], I),
                 "fp8_group_quant": ([P, I, I, I, P, P, P], I),
                 "fp8_block_quant_weight": ([P, I, I, I, P, P, P], I),
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),

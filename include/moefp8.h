@@ -114,6 +114,29 @@ int moe_align_permute(const int32_t* topk_ids, int T, int topk, int E, int block
                       int32_t* pos, int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same expert sort without a workspace argument.  The pages have no
+ * counterpart to this entry point: it is for callers that cannot allocate device
+ * memory when they call (a plugin inside a host program whose pool owns all
+ * device memory, or a serving loop that must not call cudaMalloc, which may
+ * synchronise the device).  Its scratch is one fixed array of
+ * MOE_NOALLOC_SORT_SCRATCH_INTS int32 inside the library, present on every GPU
+ * that loads the library until the process exits.
+ *   - Arguments, outputs and results are those of moe_align_permute.
+ *   - A problem needing more than the fixed scratch, i.e.
+ *     ceil(T*topk / 1024) * E > MOE_NOALLOC_SORT_SCRATCH_INTS, is rejected with
+ *     MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.  Nothing
+ *     in it has to start at zero (each call writes every count it reads), but calls
+ *     that overlap on the GPU (e.g. on two streams) race on it: order them.
+ *   - Allocates no memory (no cudaMalloc / cudaFree). */
+#define MOE_NOALLOC_SORT_SCRATCH_INTS 262144
+int moe_align_permute_noalloc(const int32_t* topk_ids, int T, int topk, int E, int block_m,
+                              int32_t* expert_offsets, int32_t* padded_offsets, int32_t* sorted_pair_ids,
+                              int32_t* pos, int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
+                              void* stream);
+
 /* ---- FP8 quantisation ---------------------------------------------------------
  * Dynamic per-token-group activation quantisation, groups of 1x128 ("computed
  * per-token at runtime", page "Quantization and MoE Optimizations", section
