@@ -88,7 +88,8 @@ struct ForwardLayout {
 ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     ForwardLayout L;
     const int64_t P = static_cast<int64_t>(T) * topk;
-    L.rows = max_rows(P, E, MOE_BLOCK_M);
+    // whole tiles, and a multiple of 4 so that each K block's row scales start 16-byte aligned
+    L.rows = (max_rows(P, E, MOE_BLOCK_M) + MOE_BLOCK_M - 1) / MOE_BLOCK_M * MOE_BLOCK_M;
     L.tiles = L.rows / MOE_BLOCK_M;
     size_t off = 0;
     auto take = [&](size_t bytes) {

@@ -49,11 +49,19 @@ constexpr int B_TILE = 2 * B_HALF;     // 32 KB: 256 weight rows
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int FIRST_EPI_WARP = 4;       // warpgroup 0: TMA warp, MMA warp, two idle warps
 constexpr int NUM_THREADS = (FIRST_EPI_WARP + NUM_EPI_WARPS) * 32;
-// registers per thread: 168 at launch (384 threads); warpgroup 0 gives back down to 80,
-// the two epilogue warpgroups take up to 208: 128*80 + 256*208 <= 384*168
-constexpr uint32_t REGS_CONTROL = 80;
-constexpr uint32_t REGS_EPILOGUE = 208;
+// registers per thread: 168 at launch (384 threads).  Warpgroup 0 (TMA and MMA warps)
+// gives some back and the two epilogue warpgroups take them: 128*c + 256*e <= 384*168.
+// The SiLU epilogue holds more live values (gate and up halves), the others more
+// producer state, hence two splits.
+template <int EPI>
+struct RegSplit {
+    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 72 : 104;
+    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 216 : 192;
+    static_assert(128 * control + 256 * epilogue <= 384 * 168, "register split over the launch budget");
+};
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
+constexpr int SR = 8;                  // slots of the scale ring (K blocks in flight)
+constexpr int SCL = 132;               // floats per slot: 128 row scales, 2 weight-block scales, pad
 
 struct SmemCtl {
     uint64_t full[STAGES];
@@ -61,14 +69,18 @@ struct SmemCtl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t amax_bar[2];
+    uint64_t sfull[SR];                // scales of a K block landed (32 producer-lane arrivals)
+    uint64_t sempty[SR];               // the epilogue warps have read them (8 arrivals)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
     float amax_x[2][2][BM];            // [tile parity][column half][row]
     alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
+    alignas(16) float scl[SR][SCL];    // scale ring: a_scale of the tile's 128 rows, then the two weight scales
 };
 constexpr int STAGE_ROW = 20;          // floats per staged row (80 B: conflict-free 16-byte slots)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA exceeds the sm_103 limit");
 
 struct Tile {
     int64_t row0;
@@ -130,6 +142,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_addr(&ctl->tempty[b]), NUM_EPI_WARPS);
             mbar_init(smem_addr(&ctl->amax_bar[b]), NUM_EPI_WARPS * 32);
         }
+        for (int r = 0; r < SR; ++r) {
+            mbar_init(smem_addr(&ctl->sfull[r]), 32);
+            mbar_init(smem_addr(&ctl->sempty[r]), NUM_EPI_WARPS);
+        }
         mbar_init(smem_addr(&ctl->drain), 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
@@ -148,46 +164,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     if (warp < FIRST_EPI_WARP) {
-      regs_decrease<REGS_CONTROL>();
+      regs_decrease<RegSplit<EPI>::control>();
       if (warp == 0) {
-        if (lane == 0) {
             // ------------------------------------------------------------ producer
+            // Lane 0 issues the TMA tile loads; all 32 lanes copy the K block's scales
+            // (the tile's 128 row scales and its two weight-block scales) into the scale
+            // ring with cp.async, so the epilogue reads them from shared memory.
+            const bool vec = a.as_row_stride == 1 && (a.as_kb_stride & 3) == 0 &&
+                             (reinterpret_cast<uintptr_t>(a.a_scale) & 15) == 0;
+            const int NBn = a.N / 128;
             int stage = 0;
-            uint32_t phase = 0, issued = 0;
+            uint32_t phase = 0, issued = 0, q = 0;
             bool ok = true;
             for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 const Tile t = decode_tile<EPI>(a, w, NT);
                 if (!t.ok) {
-                    status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+                    if (lane == 0) status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
                 }
                 const int32_t brow0 = t.e * a.N + t.bcol0, brow1 = t.e * a.N + t.bcol1;
                 const uint32_t bytes = A_TILE + (t.has1 ? B_TILE : B_HALF);
+                const int nb0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? t.n : t.bcol0 / 128;
+                const int nb1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? NBn / 2 + t.n : (t.has1 ? nb0 + 1 : nb0);
+                const float* bsa = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb0) * KB;
+                const float* bsb = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb1) * KB;
+                const float* asr = a.a_scale + t.row0 * a.as_row_stride;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status))) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_addr(&ctl->full[stage]);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
-                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
-                    if (t.has1) tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
+                    if (lane == 0) {
+                        const uint32_t fb = smem_addr(&ctl->full[stage]);
+                        mbar_arrive_expect_tx(fb, bytes);
+                        tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0),
+                                    fb);
+                        tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
+                        if (t.has1)
+                            tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    const uint32_t slot = q % SR, use = q / SR;
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->sempty[slot]), (use & 1u) ^ 1u,
+                                                           abort_flag, a.status))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = smem_addr(&ctl->scl[slot][0]);
+                    const float* src = asr + static_cast<int64_t>(kb) * a.as_kb_stride;
+                    if (vec) {
+                        cp_async_16(dst + lane * 16, src + lane * 4);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            cp_async_4(dst + (lane * 4 + i) * 4, src + (lane * 4 + i) * a.as_row_stride);
+                    }
+                    if (lane == 0) cp_async_4(dst + 128 * 4, bsa + kb);
+                    if (lane == 1) cp_async_4(dst + 129 * 4, bsb + kb);
+                    cp_async_arrive(smem_addr(&ctl->sfull[slot]));
+                    ++q;
                 }
             }
-            if (!ok) {
-                // let every load already issued land before the CTA exits
+            cp_async_wait_all();
+            if (!ok && lane == 0) {
+                // let every tile load already issued land before the CTA exits
                 for (int s = 0; s < STAGES; ++s) {
                     const uint32_t n_s = (issued + STAGES - 1 - s) / STAGES;
                     if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
                 }
             }
-        }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
@@ -231,14 +281,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     } else {
-        regs_increase<REGS_EPILOGUE>();
+        regs_increase<RegSplit<EPI>::epilogue>();
         // ---------------------------------------------------------------- epilogue
         const int g = (warp - FIRST_EPI_WARP) >> 2;   // column half
         const int sp = warp & 3;                // TMEM lane quarter
         const int row = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
-        const int NBn = a.N / 128;
-        uint32_t buf = 0, bphase = 0, tile_iter = 0;
+        uint32_t buf = 0, bphase = 0, tile_iter = 0, q = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const Tile t = decode_tile<EPI>(a, w, NT);
@@ -249,44 +298,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool row_real = a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0;
             const bool warp_live = __any_sync(0xffffffffu, row_real);
             const bool active = ((EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1) && warp_live;
-            const float* bs0;
-            const float* bs1;
-            if (EPI == MOE_EPI_SILU_MUL_QUANT) {
-                bs0 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + t.n) * KB;             // gate block
-                bs1 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + NBn / 2 + t.n) * KB;   // up block
-            } else {
-                bs0 = a.b_scale + (static_cast<int64_t>(t.e) * NBn + t.bcol0 / 128 + (active ? g : 0)) * KB;
-                bs1 = bs0;
-            }
-            const float* as = a.a_scale + grow * a.as_row_stride;
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
 
-            // the scales of K block kb+2 are loaded while block kb is promoted (L2 latency
-            // is longer than one K block of MMA)
-            float pa0 = as[0], pb0 = bs0[0], pc0 = bs1[0];
-            float pa1 = 0.0f, pb1 = 0.0f, pc1 = 0.0f;
-            if (KB > 1) {
-                pa1 = as[a.as_kb_stride];
-                pb1 = bs0[1];
-                pc1 = bs1[1];
-            }
             for (int kb = 0; kb < KB; ++kb) {
-                const float s0 = pa0 * pb0;
-                const float s1 = pa0 * pc0;
-                pa0 = pa1;
-                pb0 = pb1;
-                pc0 = pc1;
-                if (kb + 2 < KB) {
-                    pa1 = as[(kb + 2) * a.as_kb_stride];
-                    pb1 = bs0[kb + 2];
-                    pc1 = bs1[kb + 2];
-                }
-                if (!mbar_wait(smem_addr(&ctl->tfull[buf]), bphase, abort_flag, a.status)) {
+                const uint32_t slot = q % SR;
+                if (!mbar_wait(smem_addr(&ctl->sfull[slot]), (q / SR) & 1u, abort_flag, a.status) ||
+                    !mbar_wait(smem_addr(&ctl->tfull[buf]), bphase, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
+                const float sa = ctl->scl[slot][row];
+                // silu: s0 = gate block, s1 = up block; otherwise column half g's weight block
+                const float s0 = sa * ctl->scl[slot][128 + ((EPI == MOE_EPI_SILU_MUL_QUANT) ? 0 : g)];
+                const float s1 = sa * ctl->scl[slot][129];
                 tc_fence_after();
                 const uint32_t col = lane_base + buf * 256;
                 if (active) {
@@ -309,9 +335,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty[buf]));
+                if (lane == 0) {
+                    mbar_arrive(smem_addr(&ctl->tempty[buf]));
+                    mbar_arrive(smem_addr(&ctl->sempty[slot]));
+                }
                 buf ^= 1u;
                 if (buf == 0) bphase ^= 1u;
+                ++q;
             }
             if (!ok) break;
 
