@@ -321,6 +321,37 @@ def test_gemm_weighted_rows_then_unpermute_sum_matches_oracle(ci):
     assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-6 * np.abs(want).max())
 
 
+def test_gemm_weighted_rows_many_tiles_per_cta():
+    """The w2 GEMM alone on the DeepSeek-V3 decode shapes with T=8 (~20 tiles per CTA, both epilogue
+    warpgroups cycling through their accumulators and scale rings many times), fed the oracle's own
+    intermediate codes, three launches in a row."""
+    wl = mi.WORKLOADS["dsv3_decode"].with_tokens(8)
+    layer = Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    oids, ow = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    w13q, w13s, w2q, w2s = layer.oracle_weights(set(oids.reshape(-1).tolist()))
+    ref = oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, **okw)
+    perm = moe.moe_align_permute(torch.from_numpy(oids).to(DEV), wl.E)
+    m = unpadded_rows(perm["padded_offsets"].cpu().numpy(), ref["offsets"])
+    rows = perm["max_rows"]
+    A2 = torch.zeros(rows, wl.I, dtype=torch.uint8)
+    A2s = torch.ones(rows, wl.I // 128, dtype=torch.float32)
+    A2[torch.from_numpy(m)] = torch.from_numpy(ref["a2q"])
+    A2s[torch.from_numpy(m)] = torch.from_numpy(ref["a2s"])
+    want = ref["c2"] * ow.reshape(-1).astype(np.float64)[ref["sorted"]][:, None]
+    for _ in range(3):
+        y = torch.full((rows, wl.H), float("nan"), dtype=torch.float32, device=DEV)
+        moe.fp8_block_grouped_gemm(A2.to(DEV), A2s.to(DEV), (wl.I // 128, 1), layer.w2q, layer.w2s,
+                                   perm["tile_expert"], perm["tile_row0"], perm["num_tiles"], "weighted_rows",
+                                   out_f32=y, sorted_pair_ids=perm["sorted_pair_ids"],
+                                   topk_weights=torch.from_numpy(ow).to(DEV).reshape(-1), topk=wl.topk,
+                                   num_pairs=wl.T * wl.topk)
+        got = y.cpu().double().numpy()[m]
+        assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+        assert np.abs(got - want).max() <= 1e-4 * np.abs(want).max()
+
+
 @pytest.mark.parametrize("T,k,H,rows", [(1, 1, 4, 3), (37, 3, 384, 200), (300, 8, 2048, 2500)])
 def test_unpermute_sum_bit_exact_against_fp32_j_order(T, k, H, rows):
     g = torch.Generator().manual_seed(T * k)
