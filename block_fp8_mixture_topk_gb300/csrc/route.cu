@@ -3,11 +3,13 @@
 // The router of the FusedMoE layer ("router — top-K router", page "Quantization
 // and MoE Optimizations", section FusedMoE Class) with the fused grouped top-k
 // variant ("VLLM_USE_FUSED_MOE_GROUPED_TOPK", section Key Environment
-// Variables).  Scores live in shared memory (E floats per warp, two arrays for
-// sigmoid scoring); the k winners are found by k rounds of a warp-shuffle
-// argmax with ties resolved to the lower expert index, so the chosen ids are
-// exactly those of the definition.  Sigmoid scores are evaluated in fp64 and
-// rounded to fp32; weights are formed in fp64 and rounded to fp32.
+// Variables).  Scores live in shared memory (E floats per warp); the k winners are
+// found by k rounds of a warp-shuffle argmax with ties resolved to the lower
+// expert index, so the chosen ids are exactly those of the definition.  Sigmoid
+// scores are defined as fp64 sigmoids rounded to fp32; the selection first runs on
+// fp32 sigmoids and keeps the result when every decision clears the fp32 error
+// (nearly always), else repeats the token on the exact scores.  Weights are formed
+// in fp64 from the exact scores of the chosen experts and rounded to fp32.
 #include "kernels.cuh"
 
 namespace mfp8 {
@@ -38,35 +40,18 @@ __device__ __forceinline__ Cand warp_argmax(Cand c) {
     return c;
 }
 
-__global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
-    int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
-    float* __restrict__ weights) {
-    extern __shared__ float route_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long t = static_cast<long>(blockIdx.x) * kWarps + warp;
-    if (t >= T) return;
-    float* sel = route_smem + static_cast<size_t>(warp) * 2 * E;  // selection score
-    float* sig = sel + E;                                        // sigmoid score (weights)
-    const float* lrow = logits + t * E;
-    const bool sigmoid = scoring == MOE_SCORING_SIGMOID;
-
-    for (int e = lane; e < E; e += 32) {
-        const float l = lrow[e];
-        if (sigmoid) {
-            const float s = static_cast<float>(1.0 / (1.0 + exp(-static_cast<double>(l))));
-            sig[e] = s;
-            sel[e] = bias ? s + bias[e] : s;
-        } else {
-            sel[e] = l;
-        }
-    }
-    __syncwarp();
-
-    // bit j of `taken`: expert lane + 32*j is chosen or excluded (E <= 1024)
-    uint32_t taken = 0;
+// Chooses the experts from the scores sel[0..E) (shared memory): with n_group > 1,
+// the topk_group groups with the largest sum of their two best scores are kept
+// first (ties: lower group), then the topk best experts among them (ties: lower
+// index).  Returns, on lane j < topk, the j-th chosen expert.  With check set,
+// *thin tells whether a decision was closer than the error of the scores: two
+// consecutive chosen scores (down to the first one not chosen), or the last kept
+// and the first dropped group score, within their error bound.
+__device__ int select_experts(const float* sel, int E, int topk, int n_group, int topk_group, int lane, bool check,
+                              bool* thin) {
+    uint32_t taken = 0;  // bit j: expert lane + 32*j is chosen or excluded (E <= 1024)
     const int per_lane = (E + 31) / 32;
-
+    bool close = false;
     if (n_group > 1) {
         const int G = E / n_group;
         Cand gs{0.0f, INT32_MAX};
@@ -80,21 +65,30 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
             gs.idx = lane;
         }
         uint32_t kept = 0;
+        float last = 0.0f;
         for (int r = 0; r < topk_group; ++r) {
             Cand c = gs;
             if (c.idx != INT32_MAX && ((kept >> c.idx) & 1u)) c.idx = INT32_MAX;
             const Cand win = warp_argmax(c);
             kept |= 1u << win.idx;
+            last = win.v;
         }
-        // experts outside the kept groups are never candidates
+        if (check && topk_group < n_group) {
+            Cand c = gs;
+            if (c.idx != INT32_MAX && ((kept >> c.idx) & 1u)) c.idx = INT32_MAX;
+            const Cand next = warp_argmax(c);
+            const float bound = 0x1p-17f + 0x1p-19f * fmaxf(fabsf(last), fabsf(next.v));
+            if (last - next.v <= bound) close = true;
+        }
         for (int j = 0; j < per_lane; ++j) {
             const int e = lane + 32 * j;
             if (e < E && !((kept >> (e / G)) & 1u)) taken |= 1u << j;
         }
     }
-
-    int my_id = -1;  // lane j < topk ends up holding the j-th chosen expert
-    for (int j = 0; j < topk; ++j) {
+    int my_id = -1;
+    float prev = 0.0f;
+    const int rounds = check ? topk + 1 : topk;
+    for (int j = 0; j < rounds; ++j) {
         Cand c{0.0f, INT32_MAX};
         for (int jj = 0; jj < per_lane; ++jj) {
             const int e = lane + 32 * jj;
@@ -104,31 +98,83 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
             }
         }
         const Cand win = warp_argmax(c);
-        if ((win.idx & 31) == lane) taken |= 1u << (win.idx >> 5);
-        if (lane == j) my_id = win.idx;
+        if (win.idx == INT32_MAX) break;  // fewer candidates than rounds (only the extra round)
+        if (check && j > 0) {
+            const float bound = 0x1p-19f + 0x1p-20f * fmaxf(fabsf(prev), fabsf(win.v));
+            if (prev - win.v <= bound) close = true;
+        }
+        prev = win.v;
+        if (j < topk) {
+            if ((win.idx & 31) == lane) taken |= 1u << (win.idx >> 5);
+            if (lane == j) my_id = win.idx;
+        }
+    }
+    if (thin) *thin = close;
+    return my_id;
+}
+
+// Sigmoid score of a logit as the layer defines it: evaluated in fp64, rounded to fp32.
+__device__ __forceinline__ float sigmoid_exact(float l) {
+    return static_cast<float>(1.0 / (1.0 + exp(-static_cast<double>(l))));
+}
+
+__global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
+    int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
+    float* __restrict__ weights) {
+    extern __shared__ float route_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long t = static_cast<long>(blockIdx.x) * kWarps + warp;
+    if (t >= T) return;
+    float* sel = route_smem + static_cast<size_t>(warp) * E;  // selection scores
+    const float* lrow = logits + t * E;
+    const bool sigmoid = scoring == MOE_SCORING_SIGMOID;
+
+    int my_id;
+    if (sigmoid) {
+        // Fast path: fp32 scores 1/(1+expf(-l)) (expf is within 2 ulp, so each biased score is
+        // within 2^-21 + 1 ulp of the exact one).  The choice is kept only if every decision had
+        // a margin above that error; otherwise the token is redone with the exact scores.
+        for (int e = lane; e < E; e += 32) {
+            const float s = 1.0f / (1.0f + expf(-lrow[e]));
+            sel[e] = bias ? s + bias[e] : s;
+        }
+        __syncwarp();
+        bool thin = false;
+        my_id = select_experts(sel, E, topk, n_group, topk_group, lane, true, &thin);
+        if (__any_sync(0xffffffffu, thin)) {
+            __syncwarp();
+            for (int e = lane; e < E; e += 32) {
+                const float s = sigmoid_exact(lrow[e]);
+                sel[e] = bias ? s + bias[e] : s;
+            }
+            __syncwarp();
+            my_id = select_experts(sel, E, topk, n_group, topk_group, lane, false, nullptr);
+        }
+    } else {
+        for (int e = lane; e < E; e += 32) sel[e] = lrow[e];
+        __syncwarp();
+        my_id = select_experts(sel, E, topk, n_group, topk_group, lane, false, nullptr);
     }
 
-    // weights (fp64, sums in the order of the chosen list / expert index)
-    __shared__ int chosen_s[kWarps][MOE_MAX_TOPK];
-    if (lane < topk) chosen_s[warp][lane] = my_id;
-    __syncwarp();
-    double z = 0.0, mine = 0.0;
+    // weights (fp64; sums in the order of the chosen list, or of the expert index)
+    double mine = 0.0, z = 0.0;
     if (sigmoid) {
-        for (int j = 0; j < topk; ++j) z += static_cast<double>(sig[chosen_s[warp][j]]);
-        if (lane < topk) mine = static_cast<double>(sig[my_id]);
+        if (lane < topk) mine = static_cast<double>(sigmoid_exact(lrow[my_id]));
+        for (int j = 0; j < topk; ++j) z += __shfl_sync(0xffffffffu, mine, j);
         if (!renormalize) z = 1.0;
     } else {
-        const double lmax = static_cast<double>(sel[chosen_s[warp][0]]);
+        const double lmax = static_cast<double>(lrow[__shfl_sync(0xffffffffu, my_id, 0)]);
+        if (lane < topk) mine = exp(static_cast<double>(lrow[my_id]) - lmax);
         if (renormalize) {
-            for (int j = 0; j < topk; ++j) z += exp(static_cast<double>(sel[chosen_s[warp][j]]) - lmax);
+            for (int j = 0; j < topk; ++j) z += __shfl_sync(0xffffffffu, mine, j);
         } else {
             double part = 0.0;
-            for (int e = lane; e < E; e += 32) part += exp(static_cast<double>(sel[e]) - lmax);
+            for (int e = lane; e < E; e += 32) part += exp(static_cast<double>(lrow[e]) - lmax);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             z = part;
         }
-        if (lane < topk) mine = exp(static_cast<double>(sel[my_id]) - lmax);
     }
     if (lane < topk) {
         ids[t * topk + lane] = my_id;
@@ -140,14 +186,14 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
 
 cudaError_t route_init_device() {
     return cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kWarps * 2 * MOE_MAX_EXPERTS * static_cast<int>(sizeof(float)));
+                                kWarps * MOE_MAX_EXPERTS * static_cast<int>(sizeof(float)));
 }
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int topk, int renormalize, int scoring,
                               int n_group, int topk_group, float routed_scaling, const float* bias, int32_t* ids,
                               float* weights, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(kWarps) * 2 * E * sizeof(float);
+    const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(float);
     const int blocks = (T + kWarps - 1) / kWarps;
     route_topk_kernel<<<blocks, kWarps * 32, smem, stream>>>(logits, T, E, topk, renormalize, scoring, n_group,
                                                               topk_group, routed_scaling, bias, ids, weights);

@@ -122,6 +122,23 @@ def test_route_limits(E, topk, scoring):
     assert ids.cpu()[0].tolist() == list(range(topk))
 
 
+@pytest.mark.parametrize("n_group,topk_group,with_bias", [(1, 1, False), (8, 4, True), (4, 2, False)])
+def test_route_near_ties_fall_back_to_exact_scores(n_group, topk_group, with_bias):
+    """Logits a few fp32 ulps apart make the fp32 sigmoids too close to decide: the kernel must
+    repeat those tokens on the exact (fp64-evaluated) scores and still match the oracle bit-exactly."""
+    g = torch.Generator().manual_seed(n_group * 10 + topk_group)
+    T, E, k = 512, 64, 6
+    logits = (0.5 + torch.randint(0, 6, (T, E), generator=g).float() * 2.0 ** -22).float()
+    logits[T // 2:] = torch.randn(T - T // 2, E, generator=g)       # ordinary rows take the fast path
+    bias = (torch.randint(0, 3, (E,), generator=g).float() * 2.0 ** -24) if with_bias else None
+    rp = moe.RoutingParams("sigmoid", n_group, topk_group, 1.0, None if bias is None else bias.to(DEV))
+    ids, w = moe.moe_route_topk(logits.to(DEV), k, True, rp)
+    oids, ow = oracle.route(logits.numpy(), k, True, scoring=oracle.SIGMOID,
+                            bias=None if bias is None else bias.numpy(), n_group=n_group, topk_group=topk_group)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+
+
 def test_route_without_renormalize():
     g = torch.Generator().manual_seed(2)
     logits = torch.randn(50, 64, generator=g)
