@@ -32,7 +32,7 @@ import torch  # noqa: E402
 
 import moe_inputs as mi  # noqa: E402
 
-LAUNCHES_PER_STEP = 8      # route 1 + expert sort 3 + quantise 1 + two grouped GEMMs + unpermute-sum 1
+LAUNCHES_PER_STEP = 8      # route 1 + expert sort 3 + quantise 1 + two grouped GEMMs + weighted sum 1
 FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
 PROFILE = os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md")
 GEMM_SOURCES = [os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc", f) for f in ("gemm.cu", "common.cuh")]
@@ -273,10 +273,35 @@ def run_ours(args, wl):
     t1.record()
     torch.cuda.nvtx.range_pop()
     barrier()
-    clk = clocks.stop() if clocks else None
-    ms = t0.elapsed_time(t1) / args.steps
+    eager_ms = t0.elapsed_time(t1) / args.steps
     stage_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, name in enumerate(moe.ops.FORWARD_STAGES)}
+
+    # the same step captured once in a CUDA graph and replayed: identical kernels and work,
+    # without the host's per-launch cost (the way a serving loop issues a decode step)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    barrier()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("moe_timed_graph")
+    g0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record()
+    torch.cuda.nvtx.range_pop()
+    barrier()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    clk = clocks.stop() if clocks else None
+    ms = min(eager_ms, graph_ms)
+    launch = "cuda_graph" if graph_ms <= eager_ms else "eager"
     if moe.moe_get_device_status(clear=True):
         raise RuntimeError("device status word set during the benchmark")
 
@@ -345,6 +370,7 @@ def run_ours(args, wl):
             "tflops": world * flops / (ms / 1e3) / 1e12,
             "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
             "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,
+            "ms_per_step_eager": eager_ms, "ms_per_step_graph": graph_ms, "launch": launch,
             "experts_touched": touched, "weight_bytes_touched": touched * per_expert,
             "stage_ms": stage_ms, "clocks": clk,
             "e2e": {"value": world * wl.T / (e2e_ms / 1e3), "unit": "tokens/s",

@@ -14,6 +14,7 @@ from .ops import (  # noqa: F401
     fp8_group_quant,
     library_path,
     moe_align_permute,
+    moe_combine_pairs,
     moe_device_supported,
     moe_fp8_block_forward,
     moe_fp8_block_workspace_size,

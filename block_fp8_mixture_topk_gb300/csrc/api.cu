@@ -111,7 +111,7 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
-    L.y = take(static_cast<size_t>(L.rows) * H * 4);
+    L.y = take(static_cast<size_t>(P) * H * 2);
     L.total = off;
     return L;
 }
@@ -259,6 +259,11 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
                 ep->topk < 1 || ep->num_pairs < 0)
                 return MOE_ERR_INVALID_ARG;
             break;
+        case MOE_EPI_WEIGHTED_PAIRS_BF16:
+            if (!ep->out_bf16 || !aligned(ep->out_bf16, 16) || !ep->sorted_pair_ids || !ep->topk_weights ||
+                ep->topk < 1 || ep->num_pairs < 0)
+                return MOE_ERR_INVALID_ARG;
+            break;
         default:
             return MOE_ERR_INVALID_ARG;
     }
@@ -290,6 +295,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.topk_weights = ep->topk_weights;
     g.topk = ep->topk;
     g.num_pairs = ep->num_pairs;
+    g.out_bf16 = ep->out_bf16;
     g.status = st->status;
     return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -305,6 +311,17 @@ int moe_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int T,
     if (rc != MOE_OK) return rc;
     return cuda_rc(launch_unpermute_sum(y, y_rows, pos, T, topk, H, out, st->status,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, int H, uint16_t* out, void* stream) {
+    if (T < 0 || topk < 1 || H < 0) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0 || H == 0) return MOE_OK;
+    if (!y || !pos || !out || !aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_combine_pairs(y, pos, T, topk, H, out, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk) {
@@ -336,7 +353,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     if (L.rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!hidden || !router_logits || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace)
         return MOE_ERR_INVALID_ARG;
-    if (!aligned(hidden, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 8) ||
+    if (!aligned(hidden, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
         !aligned(workspace, 256))
         return MOE_ERR_INVALID_ARG;
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -355,7 +372,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     float* a1s = reinterpret_cast<float*>(ws + L.a1s);
     uint8_t* a2 = ws + L.a2;
     float* a2s = reinterpret_cast<float*>(ws + L.a2s);
-    float* yrows = reinterpret_cast<float*>(ws + L.y);
+    uint16_t* ypairs = reinterpret_cast<uint16_t*>(ws + L.y);
     const int64_t P = static_cast<int64_t>(T) * topk;
 
     auto mark = [&](int i) {
@@ -419,8 +436,8 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.tile_row0 = tile_r;
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
-        g.epi = MOE_EPI_WEIGHTED_ROWS;
-        g.out_f32 = yrows;
+        g.epi = MOE_EPI_WEIGHTED_PAIRS_BF16;
+        g.out_bf16 = ypairs;
         g.sorted_pair_ids = sorted;
         g.topk_weights = wts;
         g.topk = topk;
@@ -429,7 +446,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         e = launch_grouped_gemm(g, st->num_sms, s);
     }
     if (e == cudaSuccess) e = mark(5);
-    if (e == cudaSuccess) e = launch_unpermute_sum(yrows, L.rows, pos, T, topk, H, out, st->status, s);
+    if (e == cudaSuccess) e = launch_combine_pairs(ypairs, pos, T, topk, H, out, s);
     if (e == cudaSuccess) e = mark(6);
     return cuda_rc(e);
 }

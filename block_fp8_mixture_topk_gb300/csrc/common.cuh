@@ -206,6 +206,13 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Two fp32 values to a packed bf16 pair (round to nearest even): `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // acc[0..1] += v[0..1] * s with one packed fp32x2 FMA (round to nearest)
 __device__ __forceinline__ void ffma2(float* acc, const float* v, float s) {
     const float2 r = __ffma2_rn(make_float2(v[0], v[1]), make_float2(s, s), make_float2(acc[0], acc[1]));

@@ -29,6 +29,8 @@
 //   scatter   : out_f32[token] += router_weight * C (float4 atomics)
 //   rows      : out_f32[row] = router_weight * C in sorted-row order (plain stores); the
 //               layer sums each token's k rows afterwards (moe_unpermute_sum), in a fixed order
+//   pairs     : out_bf16[pair] = bf16(router_weight * C) in pair order (pair = t*topk + j), so
+//               that a token's k rows are contiguous for the sum that follows (moe_combine_pairs)
 // Every wait is bounded (mbar_wait); on expiry the CTA records
 // MOE_STATUS_WAIT_TIMEOUT, waits (bounded) for its TMA loads and MMAs in flight,
 // frees its TMEM and exits.
@@ -393,6 +395,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                       make_float4(wgt * acc[j], wgt * acc[j + 1], wgt * acc[j + 2], wgt * acc[j + 3]));
                     }
                 }
+            } else if (EPI == MOE_EPI_WEIGHTED_PAIRS_BF16) {
+                // bf16 rows (times the router weight) to out_bf16[pair], through a per-warp
+                // staging buffer of 32 rows x 32 columns (64 B per row, 16-byte chunks swizzled
+                // by row so that both the row-wise writes and the column-wise reads are free
+                // of bank conflicts): each store instruction covers 8 rows x 64 contiguous bytes
+                if (active) {
+                    const int32_t pair = a.sorted_pair_ids[grow];
+                    const bool keep = pair >= 0 && pair < a.num_pairs;
+                    const float wgt = keep ? a.topk_weights[pair] : 0.0f;
+                    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+                    uint32_t* stg = reinterpret_cast<uint32_t*>(ctl->stage[warp - FIRST_EPI_WARP]);
+                    const int r_out = lane >> 2, q_out = lane & 3;
+                    uint16_t* dst[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t p = __shfl_sync(0xffffffffu, pair, i * 8 + r_out);
+                        dst[i] = a.out_bf16 + p * a.N + t.bcol0 + g * 128 + q_out * 8;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float* v = acc + c * 32 + q * 8;
+                            const int slot = q ^ ((lane >> 1) & 3);
+                            *reinterpret_cast<uint4*>(stg + lane * 16 + slot * 4) =
+                                make_uint4(bf16x2(wgt * v[0], wgt * v[1]), bf16x2(wgt * v[2], wgt * v[3]),
+                                           bf16x2(wgt * v[4], wgt * v[5]), bf16x2(wgt * v[6], wgt * v[7]));
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = i * 8 + r_out;
+                            const int slot = q_out ^ ((r >> 1) & 3);
+                            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 16 + slot * 4);
+                            if ((keep_mask >> r) & 1u) *reinterpret_cast<uint4*>(dst[i] + c * 32) = v;
+                        }
+                        __syncwarp();
+                    }
+                }
             } else {
                 // fp32 rows (times the router weight for the rows epilogue) written through a
                 // per-warp staging buffer, 16 columns at a time, so that each store instruction
@@ -491,6 +532,9 @@ cudaError_t gemm_init_device() {
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     return err;
 }
 
@@ -516,6 +560,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
             break;
         case MOE_EPI_WEIGHTED_ROWS:
             grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            break;
+        case MOE_EPI_WEIGHTED_PAIRS_BF16:
+            grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB,
+                                                                                                       args);
             break;
         default:
             return cudaErrorInvalidValue;

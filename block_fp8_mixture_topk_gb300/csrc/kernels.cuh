@@ -34,6 +34,10 @@ cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, ui
 // out[t] = bf16(sum_j y[pos[t*topk + j]]) in j order (H multiple of 4, y / out 16- / 8-byte aligned)
 cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,
                                  uint16_t* out, uint32_t* status, cudaStream_t stream);
+// out[t] = bf16(sum_j float(y[t*topk + j])) in j order over the pairs with pos >= 0
+// (y bf16 [T*topk, H] in pair order; H multiple of 8, y / out 16-byte aligned)
+cudaError_t launch_combine_pairs(const uint16_t* y, const int32_t* pos, int64_t T, int topk, int H, uint16_t* out,
+                                 cudaStream_t stream);
 
 // gemm.cu
 struct GemmArgs {
@@ -57,6 +61,7 @@ struct GemmArgs {
     const float* topk_weights;
     int topk;
     int64_t num_pairs;
+    uint16_t* out_bf16;
     uint32_t* status;
 };
 cudaError_t gemm_init_device();

@@ -16,7 +16,9 @@
 // block keeps its 32 KB of bf16 in registers between the amax and the encode.
 //
 // The weighted unpermute-sum adds each token's k router-weighted expert rows
-// (written in sorted order by the w2 GEMM) in a fixed order and rounds to bf16.
+// in a fixed order (j) and rounds to bf16: from fp32 rows in sorted order
+// (unpermute_sum_kernel), or from bf16 rows in pair order, where a token's k
+// rows are contiguous (combine_pairs_kernel, the layer's path).
 #include <cuda_bf16.h>
 
 #include "kernels.cuh"
@@ -160,6 +162,53 @@ __global__ void __launch_bounds__(256) unpermute_sum_kernel(const float4* __rest
     }
 }
 
+// out[t] = bf16(sum_j float(y[t*topk + j])) over the pairs with pos >= 0: one thread per 8
+// consecutive columns of one token, the token's k rows (contiguous in pair order) loaded
+// together and summed in j order in fp32.
+template <int K>
+__global__ void __launch_bounds__(256) combine_pairs_kernel(const uint4* __restrict__ y,
+                                                            const int32_t* __restrict__ pos, int64_t T, int topk,
+                                                            int H8, uint4* __restrict__ out) {
+    const int64_t total = T * H8;
+    const int kk = K > 0 ? K : topk;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / H8;
+        const int c = static_cast<int>(i - t * H8);
+        const uint4* src = y + t * kk * H8 + c;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        if (K > 0) {
+            // all k rows in flight at once
+            bool live[K > 0 ? K : 1];
+            uint4 v[K > 0 ? K : 1];
+#pragma unroll
+            for (int j = 0; j < K; ++j) live[j] = __ldg(pos + t * K + j) >= 0;
+#pragma unroll
+            for (int j = 0; j < K; ++j) v[j] = live[j] ? __ldg(src + static_cast<int64_t>(j) * H8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                if (!live[j]) continue;
+                float f[8];
+                unpack8(v[j], f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += f[q];
+            }
+        } else {
+            for (int j = 0; j < kk; ++j) {
+                if (__ldg(pos + t * kk + j) < 0) continue;
+                float f[8];
+                unpack8(__ldg(src + static_cast<int64_t>(j) * H8), f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] += f[q];
+            }
+        }
+        out[i] = make_uint4(bf16x2(acc[0], acc[1]), bf16x2(acc[2], acc[3]), bf16x2(acc[4], acc[5]),
+                            bf16x2(acc[6], acc[7]));
+    }
+}
+
 int grid_for(int64_t work_items, int per_block) {
     int64_t b = (work_items + per_block - 1) / per_block;
     if (b < 1) b = 1;
@@ -194,6 +243,25 @@ cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* 
     dim3 grid((H4 + 255) / 256, static_cast<unsigned>(T < 65535 ? T : 65535));
     unpermute_sum_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y), y_rows, pos, T, topk, H4,
                                                    reinterpret_cast<uint2*>(out), status);
+    return cudaGetLastError();
+}
+
+}  // namespace mfp8
+
+namespace mfp8 {
+
+cudaError_t launch_combine_pairs(const uint16_t* y, const int32_t* pos, int64_t T, int topk, int H, uint16_t* out,
+                                 cudaStream_t stream) {
+    if (T == 0 || H == 0) return cudaSuccess;
+    const int H8 = H / 8;
+    const int grid = grid_for(T * H8, 256);
+    const uint4* y4 = reinterpret_cast<const uint4*>(y);
+    uint4* o4 = reinterpret_cast<uint4*>(out);
+    switch (topk) {
+        case 8: combine_pairs_kernel<8><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
+        case 2: combine_pairs_kernel<2><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
+        default: combine_pairs_kernel<0><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
+    }
     return cudaGetLastError();
 }
 

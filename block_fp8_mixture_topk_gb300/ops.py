@@ -17,7 +17,7 @@ from . import build as _build
 
 MOE_BLOCK_M = 128
 SCORING = {"softmax": 0, "sigmoid": 1}
-EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3}
+EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
 
 _ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE", -3: "MOE_ERR_WORKSPACE_TOO_SMALL",
            -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE"}
@@ -39,7 +39,7 @@ class _Epilogue(ctypes.Structure):
                 ("out_q", ctypes.c_void_p), ("out_scale", ctypes.c_void_p),
                 ("out_scale_row_stride", ctypes.c_int64), ("out_scale_kb_stride", ctypes.c_int64),
                 ("sorted_pair_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
-                ("num_pairs", ctypes.c_int64)]
+                ("num_pairs", ctypes.c_int64), ("out_bf16", ctypes.c_void_p)]
 
 
 @dataclasses.dataclass
@@ -87,6 +87,7 @@ def lib():
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, P], I),
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
+                "moe_combine_pairs": ([P, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
                 "moe_error_string": ([I], ctypes.c_char_p),
                 "moe_device_supported": ([], I),
@@ -205,13 +206,13 @@ def fp8_block_quant_weight(w):
 
 def fp8_block_grouped_gemm(A, a_scale, a_scale_strides, B, b_scale, tile_expert, tile_row0, num_tiles,
                            epilogue="store", out_f32=None, out_q=None, out_scale=None, out_scale_strides=(0, 0),
-                           sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0):
+                           sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0, out_bf16=None):
     """Grouped GEMM of the C ABI.  Outputs are caller-provided tensors (see include/moefp8.h)."""
     A, B = _codes(_cuda(A, None, "A")), _codes(_cuda(B, None, "B"))
     E, N, K = B.shape
     ep = _Epilogue(EPILOGUE[epilogue], topk, _ptr(out_f32), _ptr(out_q), _ptr(out_scale),
                    int(out_scale_strides[0]), int(out_scale_strides[1]), _ptr(sorted_pair_ids),
-                   _ptr(topk_weights), int(num_pairs))
+                   _ptr(topk_weights), int(num_pairs), _ptr(out_bf16))
     rc = lib().fp8_block_grouped_gemm(_ptr(A), _ptr(a_scale), int(a_scale_strides[0]), int(a_scale_strides[1]),
                                       A.shape[0], _ptr(B), _ptr(b_scale), N, K, E, _ptr(tile_expert),
                                       _ptr(tile_row0), _ptr(num_tiles), tile_expert.numel(), ctypes.byref(ep),
@@ -228,6 +229,18 @@ def moe_unpermute_sum(y, pos, T, topk, out=None):
         out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
     rc = lib().moe_unpermute_sum(_ptr(y), y.shape[0], _ptr(pos), T, topk, H, _ptr(out), _stream())
     _check("moe_unpermute_sum", rc)
+    return out
+
+
+def moe_combine_pairs(y, pos, T, topk, out=None):
+    """out[t] = bf16(sum_j y[t*topk + j]) over pairs with pos >= 0, for y bf16 [T*topk, H] in pair order."""
+    _cuda(y, torch.bfloat16, "y")
+    _cuda(pos, torch.int32, "pos")
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=y.device)
+    rc = lib().moe_combine_pairs(_ptr(y), _ptr(pos), T, topk, H, _ptr(out), _stream())
+    _check("moe_combine_pairs", rc)
     return out
 
 

@@ -181,6 +181,14 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
  *   MOE_EPI_WEIGHTED_ROWS: for rows with pair = sorted_pair_ids[r] >= 0,
  *       out_f32[r, n] = topk_weights[pair] * C[r, n]  (out_f32: device fp32
  *       [a_rows, N] in sorted-row order; padding rows are not written).
+ *   MOE_EPI_WEIGHTED_PAIRS_BF16: for rows with pair = sorted_pair_ids[r] in
+ *       [0, num_pairs), out_bf16[pair, n] = bf16_rn(topk_weights[pair] * C[r, n])
+ *       (out_bf16: device bf16 [num_pairs, N] in pair order p = t*topk + j, rows
+ *       16-byte aligned; rows of pairs that no tile holds are not written).  The
+ *       router weight is applied after dequantisation, in fp32, as the pages'
+ *       Triton kernel orders it (section Triton Fused MoE Kernel); the weighted
+ *       row is then held in the output's own type until the k-way sum
+ *       (moe_combine_pairs).
  * K, N multiples of 128 (N multiple of 256 for MOE_EPI_SILU_MUL_QUANT).
  * Optional epilogue field sorted_pair_ids (store / silu epilogues; NULL =
  * unused): rows with id -1 are padding; a group of 32 padding rows is not
@@ -192,18 +200,20 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
 #define MOE_EPI_SILU_MUL_QUANT 1
 #define MOE_EPI_WEIGHTED_SCATTER 2
 #define MOE_EPI_WEIGHTED_ROWS 3
+#define MOE_EPI_WEIGHTED_PAIRS_BF16 4
 
 typedef struct moe_gemm_epilogue {
     int32_t kind;                     /* MOE_EPI_* */
-    int32_t topk;                     /* MOE_EPI_WEIGHTED_SCATTER / _ROWS */
+    int32_t topk;                     /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16 */
     float* out_f32;
     uint8_t* out_q;
     float* out_scale;
     int64_t out_scale_row_stride;
     int64_t out_scale_kb_stride;
-    const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER / _ROWS */
-    const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER / _ROWS, [T*topk] */
-    int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER / _ROWS: T*topk; other pair ids are skipped */
+    const int32_t* sorted_pair_ids;   /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16 */
+    const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16, [T*topk] */
+    int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16: T*topk; other pair ids are skipped */
+    uint16_t* out_bf16;               /* MOE_EPI_WEIGHTED_PAIRS_BF16 */
 } moe_gemm_epilogue;
 
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
@@ -223,16 +233,27 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
 int moe_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int T, int topk, int H,
                       uint16_t* out, void* stream);
 
+/* The same sum over rows held in pair order (MOE_EPI_WEIGHTED_PAIRS_BF16):
+ * out[t, :] = bf16( sum_{j < topk, pos[t*topk+j] >= 0} y[t*topk+j, :] ), each term
+ * widened to fp32, summed in j order, rounded to nearest even once.
+ * y: device bf16 [T*topk, H]; pos: device int32 [T*topk] (used only to skip the
+ * pairs that were dropped, pos < 0); out: device bf16 [T, H].  H multiple of 8,
+ * y and out 16-byte aligned. */
+int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, int H, uint16_t* out,
+                      void* stream);
+
 /* ---- the whole layer -------------------------------------------------------------
  * Router -> sort by expert -> 1x128 quantisation of hidden -> GEMM over w13 with
- * SiLU(gate)*up + requantisation -> GEMM over w2 with the top-k weighted
- * scatter-add -> bf16 output (the modular pipeline Router -> Prepare/Finalize
+ * SiLU(gate)*up + requantisation -> GEMM over w2 writing each pair's
+ * router-weighted row (bf16, pair order) -> per-token sum of its k rows in j
+ * order -> bf16 output (the modular pipeline Router -> Prepare/Finalize
  * -> Permute/Experts/Unpermute, page "Quantization and MoE Optimizations",
  * section Modular Kernel Architecture; weights "[num_experts, N, K]", section
  * FusedMoE Class; 128x128 weight blocks with dynamic activations, section
  * Fp8Config).
  * workspace: device scratch of moe_fp8_block_workspace_size(T, H, I, E, topk)
- * bytes (256-byte aligned).  out may not alias any input.  T == 0 is a no-op. */
+ * bytes (256-byte aligned).  hidden, w13, w2 and out 16-byte aligned.  out may
+ * not alias any input.  T == 0 is a no-op. */
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
 int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const uint8_t* w13, const float* w13_scale,

@@ -33,6 +33,14 @@ def test_library_exports_every_declared_symbol():
     assert not missing, missing
 
 
+def test_package_reexports_every_binding():
+    """Each C entry point the binding wraps in ops.py is importable from the package."""
+    wrapped = [n for n in declared_functions() if callable(getattr(ops, n, None))]
+    assert "moe_combine_pairs" in wrapped
+    missing = [n for n in wrapped if not hasattr(moe, n)]
+    assert not missing, missing
+
+
 def test_host_only_queries():
     L = ops.lib()
     assert L.moe_error_string(0) == b"MOE_OK"

@@ -338,7 +338,8 @@ def test_gemm_weighted_rows_then_unpermute_sum_matches_oracle(ci):
     assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-6 * np.abs(want).max())
 
 
-def test_gemm_weighted_rows_many_tiles_per_cta():
+@pytest.mark.parametrize("epilogue", ["weighted_rows", "weighted_pairs_bf16"])
+def test_gemm_weighted_rows_many_tiles_per_cta(epilogue):
     """The w2 GEMM alone on the DeepSeek-V3 decode shapes with T=8 (~20 tiles per CTA, both epilogue
     warpgroups cycling through their accumulators and scale rings many times), fed the oracle's own
     intermediate codes, three launches in a row."""
@@ -357,16 +358,26 @@ def test_gemm_weighted_rows_many_tiles_per_cta():
     A2[torch.from_numpy(m)] = torch.from_numpy(ref["a2q"])
     A2s[torch.from_numpy(m)] = torch.from_numpy(ref["a2s"])
     want = ref["c2"] * ow.reshape(-1).astype(np.float64)[ref["sorted"]][:, None]
+    P = wl.T * wl.topk
     for _ in range(3):
-        y = torch.full((rows, wl.H), float("nan"), dtype=torch.float32, device=DEV)
+        if epilogue == "weighted_rows":
+            y = torch.full((rows, wl.H), float("nan"), dtype=torch.float32, device=DEV)
+            kw = dict(out_f32=y)
+        else:
+            y = torch.full((P, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+            kw = dict(out_bf16=y)
         moe.fp8_block_grouped_gemm(A2.to(DEV), A2s.to(DEV), (wl.I // 128, 1), layer.w2q, layer.w2s,
-                                   perm["tile_expert"], perm["tile_row0"], perm["num_tiles"], "weighted_rows",
-                                   out_f32=y, sorted_pair_ids=perm["sorted_pair_ids"],
+                                   perm["tile_expert"], perm["tile_row0"], perm["num_tiles"], epilogue,
+                                   sorted_pair_ids=perm["sorted_pair_ids"],
                                    topk_weights=torch.from_numpy(ow).to(DEV).reshape(-1), topk=wl.topk,
-                                   num_pairs=wl.T * wl.topk)
-        got = y.cpu().double().numpy()[m]
-        assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
-        assert np.abs(got - want).max() <= 1e-4 * np.abs(want).max()
+                                   num_pairs=P, **kw)
+        if epilogue == "weighted_rows":
+            got = y.cpu().double().numpy()[m]
+            assert np.linalg.norm(got - want) / np.linalg.norm(want) < 1e-5
+            assert np.abs(got - want).max() <= 1e-4 * np.abs(want).max()
+        else:
+            got = y.float().cpu().double().numpy()[ref["sorted"]]
+            assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-4 * np.abs(want).max())
 
 
 @pytest.mark.parametrize("T,k,H,rows", [(1, 1, 4, 3), (37, 3, 384, 200), (300, 8, 2048, 2500)])
@@ -381,6 +392,63 @@ def test_unpermute_sum_bit_exact_against_fp32_j_order(T, k, H, rows):
     for j in range(k):
         valid = p2[:, j] >= 0
         acc[valid] = acc[valid] + y[p2[valid, j]]
+    assert torch.equal(out.cpu(), acc.to(torch.bfloat16))
+
+
+def pair_rows_reference(ref, wl):
+    """The oracle's router-weighted w2 rows in pair order ([P, H], fp64) and, per token and
+    column, the sum of the magnitudes of its k terms (scale of the bf16 rounding error)."""
+    P = wl.T * wl.topk
+    wflat = ref["weights"].reshape(-1).astype(np.float64)
+    rows = np.zeros((P, wl.H))
+    rows[ref["sorted"]] = ref["c2"] * wflat[ref["sorted"]][:, None]
+    sum_abs = np.abs(rows).reshape(wl.T, wl.topk, wl.H).sum(axis=1)
+    return rows, sum_abs
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_weighted_pairs_bf16_then_combine_matches_oracle(ci):
+    """GEMM2 writing bf16 router-weighted rows in pair order, then the j-ordered sum of each
+    token's k contiguous rows, on the oracle's own intermediate codes."""
+    wl, layer, perm, A, As, ref, m, w = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    rows = A.shape[0]
+    P = wl.T * wl.topk
+    A2 = torch.zeros(rows, wl.I, dtype=torch.uint8)
+    A2s = torch.ones(rows, wl.I // 128, dtype=torch.float32)
+    A2[torch.from_numpy(m)] = torch.from_numpy(ref["a2q"])
+    A2s[torch.from_numpy(m)] = torch.from_numpy(ref["a2s"])
+    y = torch.full((P, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.fp8_block_grouped_gemm(A2.to(DEV), A2s.to(DEV), (wl.I // 128, 1), layer.w2q, layer.w2s, perm["tile_expert"],
+                               perm["tile_row0"], perm["num_tiles"], "weighted_pairs_bf16", out_bf16=y,
+                               sorted_pair_ids=perm["sorted_pair_ids"], topk_weights=w.reshape(-1),
+                               topk=wl.topk, num_pairs=P)
+    want_rows, sum_abs = pair_rows_reference(ref, wl)
+    got_rows = y.float().cpu().double().numpy()
+    # every pair row written once: bf16 rounding (half an ulp, 2^-8 relative) of an fp32 value
+    # within the GEMM's fp32 accumulation error of the fp64 reference
+    scale = np.abs(want_rows).max()
+    assert np.all(np.abs(got_rows - want_rows) <= 2.0 ** -8 * np.abs(want_rows) + 1e-4 * scale)
+    out = moe.moe_combine_pairs(y, perm["pos"][:P].contiguous(), wl.T, wl.topk)
+    got = out.float().cpu().double().numpy()
+    want = ref["out"]
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) < 6e-3
+    # each term rounded to bf16, the sum rounded once more, against the oracle's single rounding
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * (2 * np.abs(want) + sum_abs) * 1.01 + 1e-4 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("T,k,H", [(1, 1, 8), (37, 3, 384), (300, 8, 2048), (5, 2, 7168), (64, 8, 7168)])
+def test_combine_pairs_bit_exact_against_fp32_j_order(T, k, H):
+    g = torch.Generator().manual_seed(T * k + H)
+    y = torch.randn(T * k, H, generator=g).to(torch.bfloat16)
+    pos = torch.arange(T * k, dtype=torch.int32)
+    pos[::5] = -1                                    # dropped pairs are skipped ...
+    y[pos < 0] = float("nan")                        # ... and their rows never read
+    out = moe.moe_combine_pairs(y.to(DEV), pos.to(DEV), T, k)
+    acc = torch.zeros(T, H, dtype=torch.float32)
+    yv, pv = y.view(T, k, H), pos.view(T, k)
+    for j in range(k):
+        valid = pv[:, j] >= 0
+        acc[valid] = acc[valid] + yv[valid, j].float()
     assert torch.equal(out.cpu(), acc.to(torch.bfloat16))
 
 
