@@ -389,8 +389,9 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
                                  reinterpret_cast<int32_t*>(ws + L.counts), st->status, s);
-    // each token quantised once, its codes written to the sorted rows of its pairs;
-    // the scales are stored transposed ([H/128][rows]) for the GEMM's per-row reads
+    // each token quantised once, its codes written to the sorted rows of its pairs (one
+    // dense tile load per K block in the GEMM); the scales are stored transposed
+    // ([H/128][rows]) for the GEMM's per-row reads
     if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
     if (e == cudaSuccess) e = mark(3);

@@ -5,11 +5,14 @@
 // rows, page "vllm.model_executor.layers.fused_moe.oracle.fp8",
 // _get_priority_backends).
 //
-// Three kernels, no global atomics:
-//   1. per chunk of 1024 pairs, a shared-memory histogram over experts;
+// Three kernels, no atomics:
+//   1. per chunk of 1024 pairs, a histogram over experts: each warp counts its
+//      pairs with a warp match (the lowest lane of each set of equal ids writes
+//      the set's size into the warp's own row of counts), then the block sums
+//      the warp rows;
 //   2. one block scans the chunk histograms (per expert over chunks, then over
 //      experts), producing offsets, padded offsets, the tile table and the
-//      first padded row of every (chunk, expert);
+//      first row of every (chunk, expert) relative to its expert's padded start;
 //   3. per chunk, each pair's rank among the pairs of its expert in that chunk
 //      (warp match + per-warp counts), which keeps pairs of one expert in
 //      ascending pair order: the sort is stable and deterministic.
@@ -25,22 +28,39 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-__global__ void __launch_bounds__(256) chunk_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
-                                                          int32_t* __restrict__ counts, uint32_t* status) {
-    extern __shared__ int hist[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+constexpr int kCountWarps = 8;
+
+__global__ void __launch_bounds__(kCountWarps * 32) chunk_count_kernel(const int32_t* __restrict__ ids, int64_t P,
+                                                                       int E, int32_t* __restrict__ counts,
+                                                                       uint32_t* status) {
+    extern __shared__ int warp_hist[];  // [kCountWarps][E]
+    for (int i = threadIdx.x; i < kCountWarps * E; i += blockDim.x) warp_hist[i] = 0;
     __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int* hist = warp_hist + warp * E;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermuteChunk;
-    for (int i = threadIdx.x; i < kPermuteChunk; i += blockDim.x) {
-        const int64_t p = base + i;
+    // the warp's pairs: 32 at a time, kPermuteChunk / kCountWarps of them
+    for (int i = warp * 32; i < kPermuteChunk; i += kCountWarps * 32) {
+        const int64_t p = base + i + lane;
+        int id = -1;
         if (p < P) {
-            const int id = ids[p];
-            if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
-            else status_set(status, MOE_STATUS_BAD_EXPERT_ID);
+            id = ids[p];
+            if (id < 0 || id >= E) {
+                status_set(status, MOE_STATUS_BAD_EXPERT_ID);
+                id = -1;
+            }
         }
+        const uint32_t same = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && (same & lanemask_lt()) == 0) hist[id] += __popc(same);
+        __syncwarp();
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kCountWarps; ++w) c += warp_hist[w * E + e];
+        counts[static_cast<int64_t>(blockIdx.x) * E + e] = c;
+    }
 }
 
 // exclusive scan over the 1024 threads of the block
@@ -102,7 +122,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t n_chunks, int E, int
             padded_offsets[E] = poff + padded;
             *num_tiles = (poff + padded) / block_m;
         }
-        for (int64_t c = 0; c < n_chunks; ++c) counts[c * E + e] += poff;
         for (int i = poff / block_m; i < (poff + padded) / block_m; ++i) {
             tile_expert[i] = e;
             tile_row0[i] = i * block_m;
@@ -113,6 +132,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t n_chunks, int E, int
 
 __global__ void __launch_bounds__(kPermuteChunk) scatter_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
                                                                 const int32_t* __restrict__ bases,
+                                                                const int32_t* __restrict__ padded_offsets,
                                                                 int32_t* __restrict__ sorted_pair_ids,
                                                                 int32_t* __restrict__ pos) {
     extern __shared__ int16_t warp_count[];  // [32][E]
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(kPermuteChunk) scatter_kernel(const int32_t* _
     if (id >= 0) {
         int before = 0;
         for (int w = 0; w < warp; ++w) before += warp_count[w * E + id];
-        const int r = bases[static_cast<int64_t>(blockIdx.x) * E + id] + before + rank;
+        const int r = padded_offsets[id] + bases[static_cast<int64_t>(blockIdx.x) * E + id] + before + rank;
         pos[p] = r;
         sorted_pair_ids[r] = static_cast<int32_t>(p);
     } else if (valid) {
@@ -145,8 +165,12 @@ __global__ void __launch_bounds__(kPermuteChunk) scatter_kernel(const int32_t* _
 int64_t permute_chunks(int64_t P) { return (P + kPermuteChunk - 1) / kPermuteChunk; }
 
 cudaError_t permute_init_device() {
-    return cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                32 * MOE_MAX_EXPERTS * static_cast<int>(sizeof(int16_t)));
+    cudaError_t e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         32 * MOE_MAX_EXPERTS * static_cast<int>(sizeof(int16_t)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kCountWarps * MOE_MAX_EXPERTS * static_cast<int>(sizeof(int)));
+    return e;
 }
 
 cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block_m, int32_t* expert_offsets,
@@ -155,13 +179,13 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
                                  int32_t* chunk_counts, uint32_t* status, cudaStream_t stream) {
     const int64_t n_chunks = permute_chunks(P);
     if (n_chunks > 0)
-        chunk_count_kernel<<<static_cast<unsigned>(n_chunks), 256, E * sizeof(int), stream>>>(ids, P, E, chunk_counts,
-                                                                                             status);
+        chunk_count_kernel<<<static_cast<unsigned>(n_chunks), kCountWarps * 32, kCountWarps * E * sizeof(int),
+                             stream>>>(ids, P, E, chunk_counts, status);
     scan_kernel<<<1, 1024, 0, stream>>>(n_chunks, E, block_m, chunk_counts, expert_offsets, padded_offsets,
                                         sorted_pair_ids, tile_expert, tile_row0, num_tiles);
     if (n_chunks > 0)
         scatter_kernel<<<static_cast<unsigned>(n_chunks), kPermuteChunk, 32 * E * sizeof(int16_t), stream>>>(
-            ids, P, E, chunk_counts, sorted_pair_ids, pos);
+            ids, P, E, chunk_counts, padded_offsets, sorted_pair_ids, pos);
     return cudaGetLastError();
 }
 

@@ -182,6 +182,197 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
     }
 }
 
+// ---------------------------------------------------------------- register-resident variant
+// The same routing with each lane holding V consecutive experts (e = lane*V + v) in
+// registers: for E <= 32*V and groups that are whole runs of lanes (n_group == 1, or a
+// group's G = E/n_group experts a multiple of V spanning a power-of-two number of lanes).
+// A group's two best scores are merged across its lanes with shuffles (the group score
+// is the fp32 sum of the two largest values, whichever experts hold them); the topk_group
+// best groups are found by ranking the group scores; the k winners by k rounds of a lane
+// maximum plus a warp argmax (ties to the lower expert index).  Same fast path, margin
+// checks and exact fallback as route_topk_kernel.
+template <int V>
+__device__ int select_experts_reg(const float (&sel)[V], uint32_t live, int E, int topk, int n_group,
+                                  int topk_group, int lane, bool check, bool* thin) {
+    bool close = false;
+    if (n_group > 1) {
+        const int lpg = (E / n_group) / V;   // lanes per group
+        float a1 = -INFINITY, a2 = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            if (!((live >> v) & 1u)) continue;
+            if (sel[v] > a1) {
+                a2 = a1;
+                a1 = sel[v];
+            } else if (sel[v] > a2) {
+                a2 = sel[v];
+            }
+        }
+        for (int o = 1; o < lpg; o <<= 1) {
+            const float b1 = __shfl_xor_sync(0xffffffffu, a1, o);
+            const float b2 = __shfl_xor_sync(0xffffffffu, a2, o);
+            const float hi = fmaxf(a1, b1);
+            a2 = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
+            a1 = hi;
+        }
+        const float gs = a1 + a2;
+        const int my_group = lane / lpg;
+        int rank = 0;
+        for (int g = 0; g < n_group; ++g) {
+            const float o = __shfl_sync(0xffffffffu, gs, g * lpg);
+            rank += (o > gs || (o == gs && g < my_group)) ? 1 : 0;
+        }
+        if (check && topk_group < n_group) {
+            float last = (my_group < n_group && rank == topk_group - 1) ? gs : -INFINITY;
+            float next = (my_group < n_group && rank == topk_group) ? gs : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                last = fmaxf(last, __shfl_xor_sync(0xffffffffu, last, o));
+                next = fmaxf(next, __shfl_xor_sync(0xffffffffu, next, o));
+            }
+            const float bound = 0x1p-17f + 0x1p-19f * fmaxf(fabsf(last), fabsf(next));
+            if (last - next <= bound) close = true;
+        }
+        if (my_group >= n_group || rank >= topk_group) live = 0;
+    }
+    int my_id = -1;
+    float prev = 0.0f;
+    const int rounds = check ? topk + 1 : topk;
+    for (int j = 0; j < rounds; ++j) {
+        Cand c{0.0f, INT32_MAX};
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+            if (((live >> v) & 1u) && (c.idx == INT32_MAX || sel[v] > c.v)) c = Cand{sel[v], lane * V + v};
+        const Cand win = warp_argmax(c);
+        if (win.idx == INT32_MAX) break;  // fewer candidates than rounds (only the extra round)
+        if (check && j > 0) {
+            const float bound = 0x1p-19f + 0x1p-20f * fmaxf(fabsf(prev), fabsf(win.v));
+            if (prev - win.v <= bound) close = true;
+        }
+        prev = win.v;
+        if (j < topk) {
+            if (win.idx / V == lane) live &= ~(1u << (win.idx % V));
+            if (lane == j) my_id = win.idx;
+        }
+    }
+    if (thin) *thin = close;
+    return my_id;
+}
+
+// One warp selects the experts of one token (fp32 registers); the fp64 weights of the
+// block's kWarps tokens are then formed together, one thread per (token, choice), so that
+// the fp64 instructions (a small fraction of the fp32 rate on this GPU) run on full warps.
+template <int V>
+__global__ void __launch_bounds__(kWarps * 32) route_topk_reg_kernel(
+    const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
+    int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
+    float* __restrict__ weights, bool vec_loads) {
+    __shared__ int s_id[kWarps * MOE_MAX_TOPK];
+    __shared__ double s_val[kWarps * MOE_MAX_TOPK];
+    __shared__ double s_zall[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long tb = static_cast<long>(blockIdx.x) * kWarps;      // first token of the block
+    const long t = tb + warp;
+    const bool sigmoid = scoring == MOE_SCORING_SIGMOID;
+    if (t < T) {
+        const float* lrow = logits + t * E;
+        const int e0 = lane * V;
+        uint32_t live = 0;
+        float x[V];
+        if (vec_loads) {
+            // E == 32*V, V >= 4, rows 16-byte aligned
+#pragma unroll
+            for (int v = 0; v < V; v += 4) {
+                const float4 q = __ldg(reinterpret_cast<const float4*>(lrow + e0 + v));
+                x[v] = q.x;
+                x[v + 1] = q.y;
+                x[v + 2] = q.z;
+                x[v + 3] = q.w;
+            }
+            live = V >= 32 ? 0xffffffffu : (1u << V) - 1u;
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const bool ok = e0 + v < E;
+                x[v] = ok ? __ldg(lrow + e0 + v) : 0.0f;
+                if (ok) live |= 1u << v;
+            }
+        }
+        float sel[V];
+        int my_id;
+        if (sigmoid) {
+            // fast path on fp32 sigmoids, kept only when every decision clears their error
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const float sg = 1.0f / (1.0f + expf(-x[v]));
+                sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldg(bias + e0 + v) : sg;
+            }
+            bool thin = false;
+            my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, true, &thin);
+            if (__any_sync(0xffffffffu, thin)) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const float sg = sigmoid_exact(x[v]);
+                    sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldg(bias + e0 + v) : sg;
+                }
+                my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) sel[v] = x[v];
+            my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
+            if (!renormalize) {
+                const double lmax = static_cast<double>(lrow[__shfl_sync(0xffffffffu, my_id, 0)]);
+                double part = 0.0;
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    if ((live >> v) & 1u) part += exp(static_cast<double>(x[v]) - lmax);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lane == 0) s_zall[warp] = part;
+            }
+        }
+        if (lane < topk) s_id[warp * topk + lane] = my_id;
+    }
+    __syncthreads();
+
+    // fp64 weight terms, one thread per (token, choice) of the block
+    const long left = T - tb;
+    const int ntok = static_cast<int>(left < kWarps ? left : kWarps);
+    const int slots = ntok * topk;
+    for (int sl = threadIdx.x; sl < slots; sl += blockDim.x) {
+        const int w = sl / topk;
+        const float* lrow = logits + (tb + w) * E;
+        const int id = s_id[sl];
+        s_val[sl] = sigmoid ? static_cast<double>(sigmoid_exact(lrow[id]))
+                            : exp(static_cast<double>(lrow[id]) - static_cast<double>(lrow[s_id[w * topk]]));
+    }
+    __syncthreads();
+    // sums in the order of the chosen list; weights rounded once to fp32
+    for (int sl = threadIdx.x; sl < slots; sl += blockDim.x) {
+        const int w = sl / topk;
+        double z = 0.0;
+        for (int jj = 0; jj < topk; ++jj) z += s_val[w * topk + jj];
+        if (!renormalize) z = sigmoid ? 1.0 : s_zall[w];
+        ids[tb * topk + sl] = s_id[sl];
+        weights[tb * topk + sl] = static_cast<float>(s_val[sl] / z * static_cast<double>(routed_scaling));
+    }
+}
+
+// experts per lane of the register variant for this shape, or 0 when it does not apply
+int reg_experts_per_lane(int E, int n_group) {
+    int V = 1;
+    while (32 * V < E) V *= 2;
+    if (V > 32) return 0;
+    if (n_group > 1) {
+        const int G = E / n_group;
+        if (G % V != 0) return 0;
+        const int lpg = G / V;
+        if (lpg > 32 || (lpg & (lpg - 1)) != 0) return 0;
+    }
+    return V;
+}
+
 }  // namespace
 
 cudaError_t route_init_device() {
@@ -193,8 +384,25 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int topk, int r
                               int n_group, int topk_group, float routed_scaling, const float* bias, int32_t* ids,
                               float* weights, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(float);
     const int blocks = (T + kWarps - 1) / kWarps;
+    const int V = reg_experts_per_lane(E, n_group);
+    if (V > 0) {
+        const bool vec = V >= 4 && E == 32 * V && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+#define MOE_ROUTE_REG(VV)                                                                                          \
+    route_topk_reg_kernel<VV><<<blocks, kWarps * 32, 0, stream>>>(logits, T, E, topk, renormalize, scoring, n_group, \
+                                                                  topk_group, routed_scaling, bias, ids, weights, vec)
+        switch (V) {
+            case 1: MOE_ROUTE_REG(1); break;
+            case 2: MOE_ROUTE_REG(2); break;
+            case 4: MOE_ROUTE_REG(4); break;
+            case 8: MOE_ROUTE_REG(8); break;
+            case 16: MOE_ROUTE_REG(16); break;
+            default: MOE_ROUTE_REG(32); break;
+        }
+#undef MOE_ROUTE_REG
+        return cudaGetLastError();
+    }
+    const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(float);
     route_topk_kernel<<<blocks, kWarps * 32, smem, stream>>>(logits, T, E, topk, renormalize, scoring, n_group,
                                                               topk_group, routed_scaling, bias, ids, weights);
     return cudaGetLastError();

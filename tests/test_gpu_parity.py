@@ -122,6 +122,27 @@ def test_route_limits(E, topk, scoring):
     assert ids.cpu()[0].tolist() == list(range(topk))
 
 
+@pytest.mark.parametrize("E,n_group,topk_group,topk", [
+    (96, 4, 2, 6),      # 24-expert groups over 6 lanes: the shared-memory kernel
+    (72, 6, 3, 5),      # 12-expert groups over 3 lanes: the shared-memory kernel
+    (48, 3, 2, 5),      # 16-expert groups over 8 lanes: the register kernel
+    (160, 5, 3, 8),     # 32-expert groups over 4 lanes, 20 of 32 lanes used: the register kernel
+    (512, 16, 5, 12),   # 32-expert groups over 2 lanes: the register kernel
+])
+def test_route_grouped_shapes_bit_exact(E, n_group, topk_group, topk):
+    g = torch.Generator().manual_seed(E + n_group)
+    T = 300
+    logits = torch.randn(T, E, generator=g)
+    logits[0] = 0.25                                  # all ties: lowest groups, lowest indices
+    bias = torch.randn(E, generator=g) * 0.01
+    rp = moe.RoutingParams("sigmoid", n_group, topk_group, 2.5, bias.to(DEV))
+    ids, w = moe.moe_route_topk(logits.to(DEV), topk, True, rp)
+    oids, ow = oracle.route(logits.numpy(), topk, True, scoring=oracle.SIGMOID, bias=bias.numpy(),
+                            n_group=n_group, topk_group=topk_group, routed_scaling=2.5)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
+
+
 @pytest.mark.parametrize("n_group,topk_group,with_bias", [(1, 1, False), (8, 4, True), (4, 2, False)])
 def test_route_near_ties_fall_back_to_exact_scores(n_group, topk_group, with_bias):
     """Logits a few fp32 ulps apart make the fp32 sigmoids too close to decide: the kernel must
