@@ -18,7 +18,8 @@
 // Roles (384 threads, one CTA per SM, persistent over the tile list):
 //   warp 0, one thread : TMA producer, 4-stage ring of {A 128x128, B 256x128} e4m3 tiles
 //   warp 1, one thread : MMA issuer (4 x tcgen05.mma 128x256x32 per K block), TMEM owner
-//   warps 2, 3         : idle (they complete warpgroup 0, which gives registers away)
+//   warp 2             : scale producer, an 8-slot ring of each K block's row and weight scales
+//   warp 3             : idle (it completes warpgroup 0, which gives registers away)
 //   warps 4..11        : promotion + epilogue; warp w reads TMEM lanes 32*(w%4)..+31
 //                        (its rows) and 128 of the 256 columns (column half (w-4)/4)
 // Epilogues:
@@ -51,10 +52,10 @@ constexpr int B_TILE = 2 * B_HALF;     // 32 KB: 256 weight rows
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int FIRST_EPI_WARP = 4;       // warpgroup 0: TMA warp, MMA warp, two idle warps
 constexpr int NUM_THREADS = (FIRST_EPI_WARP + NUM_EPI_WARPS) * 32;
-// registers per thread: 168 at launch (384 threads).  Warpgroup 0 (TMA and MMA warps)
-// gives some back and the two epilogue warpgroups take them: 128*c + 256*e <= 384*168.
-// The SiLU epilogue holds more live values (gate and up halves), the others more
-// producer state, hence two splits.
+// registers per thread: 168 at launch (384 threads).  Warpgroup 0 (the TMA, MMA and
+// scale warps) gives some back and the two epilogue warpgroups take them: 128*c + 256*e
+// <= 384*168.  The SiLU epilogue holds more live values (gate and up halves); the
+// splits are the ones with the fewest spills.
 template <int EPI>
 struct RegSplit {
     static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 72 : 104;
@@ -168,78 +169,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp < FIRST_EPI_WARP) {
       regs_decrease<RegSplit<EPI>::control>();
       if (warp == 0) {
-            // ------------------------------------------------------------ producer
-            // Lane 0 issues the TMA tile loads; all 32 lanes copy the K block's scales
-            // (the tile's 128 row scales and its two weight-block scales) into the scale
-            // ring with cp.async, so the epilogue reads them from shared memory.
-            const bool vec = a.as_row_stride == 1 && (a.as_kb_stride & 3) == 0 &&
-                             (reinterpret_cast<uintptr_t>(a.a_scale) & 15) == 0;
-            const int NBn = a.N / 128;
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            // one thread, nothing but the tile loads: the 4-stage ring refills as soon as
+            // the MMAs release a stage
             int stage = 0;
-            uint32_t phase = 0, issued = 0, q = 0;
+            uint32_t phase = 0, issued = 0;
             bool ok = true;
             for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 const Tile t = decode_tile<EPI>(a, w, NT);
                 if (!t.ok) {
-                    if (lane == 0) status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+                    status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
                 }
                 const int32_t brow0 = t.e * a.N + t.bcol0, brow1 = t.e * a.N + t.bcol1;
                 const uint32_t bytes = A_TILE + (t.has1 ? B_TILE : B_HALF);
-                const int nb0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? t.n : t.bcol0 / 128;
-                const int nb1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? NBn / 2 + t.n : (t.has1 ? nb0 + 1 : nb0);
-                const float* bsa = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb0) * KB;
-                const float* bsb = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb1) * KB;
-                const float* asr = a.a_scale + t.row0 * a.as_row_stride;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status))) {
+                    if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) {
-                        const uint32_t fb = smem_addr(&ctl->full[stage]);
-                        mbar_arrive_expect_tx(fb, bytes);
-                        tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0),
-                                    fb);
-                        tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
-                        if (t.has1)
-                            tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
-                    }
+                    const uint32_t fb = smem_addr(&ctl->full[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
+                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
+                    if (t.has1) tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    const uint32_t slot = q % SR, use = q / SR;
-                    if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->sempty[slot]), (use & 1u) ^ 1u,
-                                                           abort_flag, a.status))) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dst = smem_addr(&ctl->scl[slot][0]);
-                    const float* src = asr + static_cast<int64_t>(kb) * a.as_kb_stride;
-                    if (vec) {
-                        cp_async_16(dst + lane * 16, src + lane * 4);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            cp_async_4(dst + (lane * 4 + i) * 4, src + (lane * 4 + i) * a.as_row_stride);
-                    }
-                    if (lane == 0) cp_async_4(dst + 128 * 4, bsa + kb);
-                    if (lane == 1) cp_async_4(dst + 129 * 4, bsb + kb);
-                    cp_async_arrive(smem_addr(&ctl->sfull[slot]));
-                    ++q;
                 }
             }
-            cp_async_wait_all();
-            if (!ok && lane == 0) {
+            if (!ok) {
                 // let every tile load already issued land before the CTA exits
                 for (int s = 0; s < STAGES; ++s) {
                     const uint32_t n_s = (issued + STAGES - 1 - s) / STAGES;
                     if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
                 }
             }
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- scale producer
+        // all 32 lanes copy each K block's scales (the tile's 128 row scales and its two
+        // weight-block scales) into the scale ring with cp.async, so that the epilogue
+        // reads them from shared memory
+        const bool vec = a.as_row_stride == 1 && (a.as_kb_stride & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(a.a_scale) & 15) == 0;
+        const int NBn = a.N / 128;
+        uint32_t q = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Tile t = decode_tile<EPI>(a, w, NT);
+            if (!t.ok) continue;
+            const int nb0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? t.n : t.bcol0 / 128;
+            const int nb1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? NBn / 2 + t.n : (t.has1 ? nb0 + 1 : nb0);
+            const float* bsa = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb0) * KB;
+            const float* bsb = a.b_scale + (static_cast<int64_t>(t.e) * NBn + nb1) * KB;
+            const float* asr = a.a_scale + t.row0 * a.as_row_stride;
+            for (int kb = 0; kb < KB; ++kb) {
+                const uint32_t slot = q % SR, use = q / SR;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->sempty[slot]), (use & 1u) ^ 1u,
+                                                       abort_flag, a.status))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = smem_addr(&ctl->scl[slot][0]);
+                const float* src = asr + static_cast<int64_t>(kb) * a.as_kb_stride;
+                if (vec) {
+                    cp_async_16(dst + lane * 16, src + lane * 4);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        cp_async_4(dst + (lane * 4 + i) * 4, src + (lane * 4 + i) * a.as_row_stride);
+                }
+                if (lane == 0) cp_async_4(dst + 128 * 4, bsa + kb);
+                if (lane == 1) cp_async_4(dst + 129 * 4, bsb + kb);
+                cp_async_arrive(smem_addr(&ctl->sfull[slot]));
+                ++q;
+            }
+        }
+        cp_async_wait_all();
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
