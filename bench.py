@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     p.add_argument("--cpu-sample", type=int, default=None, help="tokens the oracle computes")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--weights", choices=["tiled", "nk"], default="tiled",
+                   help="expert weight layout: tile-packed at load time (default) or the pages' [E, N, K]")
     return p.parse_args()
 
 
@@ -73,6 +75,11 @@ def describe(wl, world):
             "expert_weight_bytes": wbytes,
             "l2": "inputs larger than L2" if wbytes > 129e6 else "L2 flushed between steps",
             "parallelism": f"replicas x{world}"}
+
+
+def describe_weights(args):
+    return ("e4m3 128x128 blocks, tile-packed at load time (moe_fp8_block_pack_weights)"
+            if args.weights == "tiled" else "e4m3 128x128 blocks, [E, N, K] layout")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -242,6 +249,12 @@ def run_ours(args, wl):
         ex = range(e0, min(E, e0 + 8))
         w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex))
         w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex))
+    if args.weights == "tiled":
+        # load-time conversion into the kernels' tile-packed layout (untimed, like the quantisation)
+        w13q = moe.moe_fp8_block_pack_weights(w13q)
+        w2q = moe.moe_fp8_block_pack_weights(w2q)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     out = torch.empty(wl.T, H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, H, I, E, wl.topk), dtype=torch.uint8, device=dev)
     ids, _ = moe.moe_route_topk(logits, wl.topk, wl.renormalize, rp)
@@ -366,7 +379,7 @@ def run_ours(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
-            "config": describe(wl, world),
+            "config": {**describe(wl, world), "weights": describe_weights(args)},
             "tflops": world * flops / (ms / 1e3) / 1e12,
             "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
             "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,

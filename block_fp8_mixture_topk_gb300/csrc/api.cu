@@ -234,6 +234,21 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
     return cuda_rc(launch_block_quant_weight(w, E, N, K, q, s, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<int64_t>(E) * N * (K / 128) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (!w || !packed || !aligned(w, 16) || !aligned(packed, 16)) return MOE_ERR_INVALID_ARG;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(w), b0 = reinterpret_cast<uintptr_t>(packed);
+    const uintptr_t n = static_cast<uintptr_t>(E) * N * K;
+    if (a0 < b0 + n && b0 < a0 + n) return MOE_ERR_INVALID_ARG;   // the conversion is not in place
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_pack_weights(w, E, N, K, packed, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
                            int64_t a_scale_kb_stride, int64_t a_rows, const uint8_t* B, const float* b_scale, int N,
                            int K, int E, const int32_t* tile_expert, const int32_t* tile_row0,
@@ -246,6 +261,9 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     if (max_tiles == 0) return MOE_OK;
     if (!A || !a_scale || !B || !b_scale || !tile_expert || !tile_row0 || !num_tiles) return MOE_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16)) return MOE_ERR_INVALID_ARG;
+    if (ep->b_layout != MOE_WEIGHTS_NK && ep->b_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (ep->b_layout == MOE_WEIGHTS_TILED && static_cast<int64_t>(E) * N * (K / 128) >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     switch (ep->kind) {
         case MOE_EPI_STORE_F32:
             if (!ep->out_f32 || !aligned(ep->out_f32, 16)) return MOE_ERR_INVALID_ARG;
@@ -296,6 +314,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.topk = ep->topk;
     g.num_pairs = ep->num_pairs;
     g.out_bf16 = ep->out_bf16;
+    g.b_tiled = ep->b_layout == MOE_WEIGHTS_TILED;
     g.status = st->status;
     return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -334,16 +353,30 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
                           int topk, int renormalize, const moe_routing_params* rp, void* workspace,
                           size_t workspace_bytes, uint16_t* out, void* stream) {
     return moe_fp8_block_forward_events(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
-                                        renormalize, rp, workspace, workspace_bytes, out, stream, nullptr);
+                                        renormalize, rp, workspace, workspace_bytes, out, stream, MOE_WEIGHTS_NK,
+                                        nullptr);
+}
+
+int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
+                                 int I, int E, int topk, int renormalize, const moe_routing_params* rp,
+                                 void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
+    return moe_fp8_block_forward_events(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
+                                        renormalize, rp, workspace, workspace_bytes, out, stream, MOE_WEIGHTS_TILED,
+                                        nullptr);
 }
 
 int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
                                  const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
                                  int I, int E, int topk, int renormalize, const moe_routing_params* rp,
                                  void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
-                                 void* const* events) {
+                                 int weight_layout, void* const* events) {
     int rc = check_routing(T, E, topk, rp);
     if (rc != MOE_OK) return rc;
+    if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (weight_layout == MOE_WEIGHTS_TILED &&
+        static_cast<int64_t>(E) * 2 * I * (H / 128) >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
     if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) || static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
@@ -403,6 +436,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.as_kb_stride = L.rows;
         g.a_rows = L.rows;
         g.B = w13;
+        g.b_tiled = weight_layout == MOE_WEIGHTS_TILED;
         g.b_scale = w13_scale;
         g.N = 2 * I;
         g.K = H;
@@ -429,6 +463,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.as_kb_stride = L.rows;
         g.a_rows = L.rows;
         g.B = w2;
+        g.b_tiled = weight_layout == MOE_WEIGHTS_TILED;
         g.b_scale = w2_scale;
         g.N = H;
         g.K = I;

@@ -182,7 +182,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
                 }
-                const int32_t brow0 = t.e * a.N + t.bcol0, brow1 = t.e * a.N + t.bcol1;
+                // weight tile coordinates: [E*N, K] rows in the pages' layout (x advances along
+                // K), or one 128-row block per 128 map rows in the tile-packed layout (each
+                // 128x128 block a contiguous 16 KB, consecutive K blocks adjacent: y advances)
+                int32_t by0, by1, bdx, bdy;
+                if (a.b_tiled) {
+                    by0 = ((t.e * (a.N / 128) + t.bcol0 / 128) * KB) * 128;
+                    by1 = ((t.e * (a.N / 128) + t.bcol1 / 128) * KB) * 128;
+                    bdx = 0;
+                    bdy = 128;
+                } else {
+                    by0 = t.e * a.N + t.bcol0;
+                    by1 = t.e * a.N + t.bcol1;
+                    bdx = BK;
+                    bdy = 0;
+                }
                 const uint32_t bytes = A_TILE + (t.has1 ? B_TILE : B_HALF);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
@@ -192,8 +206,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t fb = smem_addr(&ctl->full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
-                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * BK, brow0, fb);
-                    if (t.has1) tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * BK, brow1, fb);
+                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
+                    if (t.has1)
+                        tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * bdx, by1 + kb * bdy, fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -555,7 +570,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     CUtensorMap tmA, tmB;
     cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows);
     if (err != cudaSuccess) return err;
-    err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
+    if (args.b_tiled)   // [E][N/128][K/128] blocks of 128 rows x 128 bytes, stacked
+        err = make_map(&tmB, args.B, 128, static_cast<int64_t>(args.E) * args.N * (args.K / 128));
+    else
+        err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(bound < num_sms ? bound : num_sms);
     switch (args.epi) {

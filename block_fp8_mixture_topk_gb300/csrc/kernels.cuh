@@ -31,6 +31,8 @@ cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_
                                int topk, cudaStream_t stream);
 cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
                                       cudaStream_t stream);
+// [E, N, K] e4m3 -> [E][N/128][K/128][128][128] (each 128x128 block contiguous)
+cudaError_t launch_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, cudaStream_t stream);
 // out[t] = bf16(sum_j y[pos[t*topk + j]]) in j order (H multiple of 4, y / out 16- / 8-byte aligned)
 cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,
                                  uint16_t* out, uint32_t* status, cudaStream_t stream);
@@ -46,6 +48,7 @@ struct GemmArgs {
     int64_t as_row_stride, as_kb_stride;
     int64_t a_rows;
     const uint8_t* B;
+    int b_tiled;               // B in the tile-packed layout (moe_fp8_block_pack_weights)
     const float* b_scale;
     int N, K, E;
     const int32_t* tile_expert;

@@ -209,6 +209,20 @@ __global__ void __launch_bounds__(256) combine_pairs_kernel(const uint4* __restr
     }
 }
 
+// [E, N, K] -> [E][N/128][K/128][128 rows][128 bytes]: one thread per 16 bytes of the output
+// (coalesced writes; each source row segment of 128 bytes is read by 8 consecutive threads)
+__global__ void __launch_bounds__(256) pack_weights_kernel(const uint4* __restrict__ w, int64_t N, int64_t K,
+                                                           int64_t total16, uint4* __restrict__ out) {
+    const int64_t NB = N / 128, KB = K / 128;
+    for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total16;
+         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t blk = o >> 10;                 // 1024 x 16 B per block
+        const int r = static_cast<int>((o >> 3) & 127), c = static_cast<int>(o & 7);
+        const int64_t kb = blk % KB, nb = (blk / KB) % NB, e = blk / (KB * NB);
+        out[o] = __ldg(w + (((e * N + nb * 128 + r) * K + kb * 128) >> 4) + c);
+    }
+}
+
 int grid_for(int64_t work_items, int per_block) {
     int64_t b = (work_items + per_block - 1) / per_block;
     if (b < 1) b = 1;
@@ -262,6 +276,18 @@ cudaError_t launch_combine_pairs(const uint16_t* y, const int32_t* pos, int64_t 
         case 2: combine_pairs_kernel<2><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
         default: combine_pairs_kernel<0><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
     }
+    return cudaGetLastError();
+}
+
+}  // namespace mfp8
+
+namespace mfp8 {
+
+cudaError_t launch_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, cudaStream_t stream) {
+    const int64_t total16 = static_cast<int64_t>(E) * N * K / 16;
+    if (total16 == 0) return cudaSuccess;
+    pack_weights_kernel<<<grid_for(total16, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(w), N, K, total16,
+                                                                     reinterpret_cast<uint4*>(packed));
     return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@ import torch
 from . import build as _build
 
 MOE_BLOCK_M = 128
+MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED = 0, 1
 SCORING = {"softmax": 0, "sigmoid": 1}
 EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
 
@@ -39,7 +40,7 @@ class _Epilogue(ctypes.Structure):
                 ("out_q", ctypes.c_void_p), ("out_scale", ctypes.c_void_p),
                 ("out_scale_row_stride", ctypes.c_int64), ("out_scale_kb_stride", ctypes.c_int64),
                 ("sorted_pair_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
-                ("num_pairs", ctypes.c_int64), ("out_bf16", ctypes.c_void_p)]
+                ("num_pairs", ctypes.c_int64), ("out_bf16", ctypes.c_void_p), ("b_layout", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -85,7 +86,9 @@ def lib():
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
-                "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, P], I),
+                "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
+                "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, I, P], I),
+                "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
                 "moe_combine_pairs": ([P, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
@@ -204,15 +207,33 @@ def fp8_block_quant_weight(w):
     return q, s
 
 
+def moe_fp8_block_pack_weights(w):
+    """e4m3 expert weights [E, N, K] -> the tile-packed layout, a uint8 tensor of shape
+    [E, N/128, K/128, 128, 128] (each 128x128 block contiguous; load-time, once)."""
+    w = _codes(_cuda(w, None, "w"))
+    E, N, K = w.shape
+    packed = torch.empty(E, N // 128, K // 128, 128, 128, dtype=torch.uint8, device=w.device)
+    _check("moe_fp8_block_pack_weights", lib().moe_fp8_block_pack_weights(_ptr(w), E, N, K, _ptr(packed), _stream()))
+    return packed
+
+
+def _weight_shape(w):
+    """(E, N, K, layout) of expert weights in either layout."""
+    if w.dim() == 5:
+        return w.shape[0], w.shape[1] * 128, w.shape[2] * 128, MOE_WEIGHTS_TILED
+    E, N, K = w.shape
+    return E, N, K, MOE_WEIGHTS_NK
+
+
 def fp8_block_grouped_gemm(A, a_scale, a_scale_strides, B, b_scale, tile_expert, tile_row0, num_tiles,
                            epilogue="store", out_f32=None, out_q=None, out_scale=None, out_scale_strides=(0, 0),
                            sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0, out_bf16=None):
     """Grouped GEMM of the C ABI.  Outputs are caller-provided tensors (see include/moefp8.h)."""
     A, B = _codes(_cuda(A, None, "A")), _codes(_cuda(B, None, "B"))
-    E, N, K = B.shape
+    E, N, K, layout = _weight_shape(B)
     ep = _Epilogue(EPILOGUE[epilogue], topk, _ptr(out_f32), _ptr(out_q), _ptr(out_scale),
                    int(out_scale_strides[0]), int(out_scale_strides[1]), _ptr(sorted_pair_ids),
-                   _ptr(topk_weights), int(num_pairs), _ptr(out_bf16))
+                   _ptr(topk_weights), int(num_pairs), _ptr(out_bf16), layout)
     rc = lib().fp8_block_grouped_gemm(_ptr(A), _ptr(a_scale), int(a_scale_strides[0]), int(a_scale_strides[1]),
                                       A.shape[0], _ptr(B), _ptr(b_scale), N, K, E, _ptr(tile_expert),
                                       _ptr(tile_row0), _ptr(num_tiles), tile_expert.numel(), ctypes.byref(ep),
@@ -267,6 +288,7 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
                           routing: RoutingParams | None = None, out=None, workspace=None, events=None):
     """The whole layer: returns bf16 [T, H] (written into `out` when given).
 
+    w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D).
     events: optional list of 7 torch.cuda.Event recorded between the stages
     (FORWARD_STAGES) on the current stream, for per-stage timing."""
     _cuda(hidden, torch.bfloat16, "hidden")
@@ -275,7 +297,9 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     _cuda(w13_scale, torch.float32, "w13_scale")
     _cuda(w2_scale, torch.float32, "w2_scale")
     T, H = hidden.shape
-    E, N1, _ = w13.shape
+    E, N1, _, layout = _weight_shape(w13)
+    if _weight_shape(w2)[3] != layout:
+        raise ValueError("w13 and w2 must share one layout")
     I = N1 // 2
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=hidden.device)
@@ -287,7 +311,7 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
             topk, int(bool(renormalize)), ctypes.byref(rp) if rp else None, _ptr(workspace), workspace.numel(),
             _ptr(out), _stream()]
     if events is None:
-        rc = lib().moe_fp8_block_forward(*args)
+        rc = (lib().moe_fp8_block_forward_packed if layout == MOE_WEIGHTS_TILED else lib().moe_fp8_block_forward)(*args)
     else:
         if len(events) != len(FORWARD_STAGES) + 1:
             raise ValueError("events: one more than the number of stages")
@@ -295,7 +319,7 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
             if not ev.cuda_event:       # torch creates the CUDA event on its first record()
                 ev.record()
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
-        rc = lib().moe_fp8_block_forward_events(*args, arr)
+        rc = lib().moe_fp8_block_forward_events(*args, layout, arr)
     _check("moe_fp8_block_forward", rc)
     return out
 

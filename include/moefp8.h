@@ -158,6 +158,20 @@ int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, f
 int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
                            void* stream);
 
+/* Load-time conversion of e4m3 expert weights from the pages' layout [E, N, K]
+ * into the tile-packed layout the GEMMs stream fastest: packed[e][nb][kb][r][c] =
+ * w[e, nb*128 + r, kb*128 + c], i.e. [E][N/128][K/128][128][128], each 128x128
+ * block one contiguous 16 KB run and the K blocks of a 128-row band adjacent.
+ * The pages convert checkpoint weights into each kernel's own format once, at
+ * load time (process_weights_after_loading -> convert_to_nvfp4_moe_kernel_format,
+ * page "vllm.model_executor.layers.quantization.online.nvfp4"); this is that step
+ * for the block-FP8 kernels.  The block scales keep their layout.
+ * w, packed: device, 16-byte aligned, E*N*K bytes, not overlapping.  N and K
+ * multiples of 128, E*N*K/128 < 2^31. */
+#define MOE_WEIGHTS_NK 0      /* [E, N, K] row-major, the pages' layout */
+#define MOE_WEIGHTS_TILED 1   /* moe_fp8_block_pack_weights output */
+int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, void* stream);
+
 /* ---- grouped block-FP8 GEMM ------------------------------------------------------
  * For every tile m < *num_tiles (rows tile_row0[m] .. +127 of A, all routed to
  * expert e = tile_expert[m]) and every output column n:
@@ -214,6 +228,7 @@ typedef struct moe_gemm_epilogue {
     const float* topk_weights;        /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16, [T*topk] */
     int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16: T*topk; other pair ids are skipped */
     uint16_t* out_bf16;               /* MOE_EPI_WEIGHTED_PAIRS_BF16 */
+    int32_t b_layout;                 /* layout of B: MOE_WEIGHTS_NK (0) or MOE_WEIGHTS_TILED */
 } moe_gemm_epilogue;
 
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
@@ -262,19 +277,29 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
                           uint16_t* out, void* stream);
 
+/* The same layer with w13 and w2 in the tile-packed layout (moe_fp8_block_pack_weights);
+ * identical results, the weights streamed as contiguous 16 KB blocks. */
+int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_logits,
+                                 const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale,
+                                 int T, int H, int I, int E, int topk, int renormalize,
+                                 const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
+                                 uint16_t* out, void* stream);
+
 /* The same layer, recording CUDA events between its stages for per-stage timing
  * (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the
  * caller, recorded on `stream` in this order: before routing, before the expert
  * sort, before the activation quantisation, before the w13 GEMM, before the w2
- * GEMM, before the weighted unpermute-sum, after it).  Arguments and errors as
- * moe_fp8_block_forward; events == NULL behaves exactly like it. */
+ * GEMM, before the weighted unpermute-sum, after it).  weight_layout:
+ * MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED for w13 and w2.  Other arguments and errors
+ * as moe_fp8_block_forward; events == NULL behaves exactly like it. */
 #define MOE_FORWARD_NUM_EVENTS 7
 int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits,
                                  const uint8_t* w13, const float* w13_scale,
                                  const uint8_t* w2, const float* w2_scale,
                                  int T, int H, int I, int E, int topk, int renormalize,
                                  const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
-                                 uint16_t* out, void* stream, void* const* events);
+                                 uint16_t* out, void* stream, int weight_layout, void* const* events);
 
 /* ---- status -------------------------------------------------------------------- */
 /* Reads (and with clear != 0, resets) the device status word of the current

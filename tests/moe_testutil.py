@@ -71,8 +71,11 @@ class Layer:
             w2q[e], w2s[e] = [a[0] for a in oracle.quant_128x128_bf16(mi.bf16_bits(mi.w2_bf16(wl, self.device, [e])))]
         return w13q, w13s, w2q, w2s
 
-    def forward(self, hidden, logits, rp):
-        return moe.moe_fp8_block_forward(hidden, logits, self.w13q, self.w13s, self.w2q, self.w2s, self.wl.topk,
+    def forward(self, hidden, logits, rp, packed=False):
+        w13, w2 = self.w13q, self.w2q
+        if packed:
+            w13, w2 = moe.moe_fp8_block_pack_weights(w13), moe.moe_fp8_block_pack_weights(w2)
+        return moe.moe_fp8_block_forward(hidden, logits, w13, self.w13s, w2, self.w2s, self.wl.topk,
                                          self.wl.renormalize, rp)
 
 

@@ -473,6 +473,45 @@ def test_combine_pairs_bit_exact_against_fp32_j_order(T, k, H):
     assert torch.equal(out.cpu(), acc.to(torch.bfloat16))
 
 
+# ----------------------------------------------------------------------------- tile-packed weights
+
+@pytest.mark.parametrize("E,N,K", [(1, 128, 128), (3, 384, 256), (2, 4096, 7168)])
+def test_pack_weights_is_the_block_permutation(E, N, K):
+    g = torch.Generator().manual_seed(E * N + K)
+    w = torch.randint(0, 256, (E, N, K), generator=g, dtype=torch.uint8)
+    packed = moe.moe_fp8_block_pack_weights(w.to(DEV))
+    want = w.view(E, N // 128, 128, K // 128, 128).permute(0, 1, 3, 2, 4).contiguous()
+    assert torch.equal(packed.cpu(), want)
+
+
+@pytest.mark.parametrize("ci", range(len(GEMM_CASES)))
+def test_gemm_packed_weights_bit_identical(ci):
+    """Every epilogue reads the tile-packed weights to exactly the same bits as the [E, N, K] ones."""
+    wl, layer, perm, A, As, ref, m, w = stage_inputs(GEMM_CASES[ci], 40 + ci)
+    w13p, w2p = moe.moe_fp8_block_pack_weights(layer.w13q), moe.moe_fp8_block_pack_weights(layer.w2q)
+    rows, P = A.shape[0], wl.T * wl.topk
+    outs = []
+    for b13, b2 in ((layer.w13q, layer.w2q), (w13p, w2p)):
+        c1 = torch.zeros(rows, 2 * wl.I, dtype=torch.float32, device=DEV)
+        moe.fp8_block_grouped_gemm(A, As, (wl.H // 128, 1), b13, layer.w13s, perm["tile_expert"],
+                                   perm["tile_row0"], perm["num_tiles"], "store", out_f32=c1)
+        oq = torch.zeros(rows, wl.I, dtype=torch.uint8, device=DEV)
+        osc = torch.zeros(rows, wl.I // 128, dtype=torch.float32, device=DEV)
+        moe.fp8_block_grouped_gemm(A, As, (wl.H // 128, 1), b13, layer.w13s, perm["tile_expert"],
+                                   perm["tile_row0"], perm["num_tiles"], "silu_mul_quant", out_q=oq, out_scale=osc,
+                                   out_scale_strides=(wl.I // 128, 1))
+        y = torch.zeros(P, wl.H, dtype=torch.bfloat16, device=DEV)
+        moe.fp8_block_grouped_gemm(oq, osc, (wl.I // 128, 1), b2, layer.w2s, perm["tile_expert"],
+                                   perm["tile_row0"], perm["num_tiles"], "weighted_pairs_bf16", out_bf16=y,
+                                   sorted_pair_ids=perm["sorted_pair_ids"], topk_weights=w.reshape(-1),
+                                   topk=wl.topk, num_pairs=P)
+        outs.append((c1, oq, osc, y))
+    mt = torch.from_numpy(m).to(DEV)
+    (c1a, oqa, osa, ya), (c1b, oqb, osb, yb) = outs
+    assert torch.equal(c1a[mt], c1b[mt]) and torch.equal(oqa[mt], oqb[mt]) and torch.equal(osa[mt], osb[mt])
+    assert torch.equal(ya, yb)
+
+
 # ----------------------------------------------------------------------------- whole layer
 
 def run_layer(wl, tokens=None, layer=None):
@@ -480,7 +519,10 @@ def run_layer(wl, tokens=None, layer=None):
     hidden, logits = mi.hidden(wl), mi.router_logits(wl)
     rp, okw = routing_of(wl)
     out = layer.forward(hidden.to(DEV), logits.to(DEV), rp)
+    # the same layer on the tile-packed weights gives the same bits
+    out_packed = layer.forward(hidden.to(DEV), logits.to(DEV), rp, packed=True)
     torch.cuda.synchronize()
+    assert torch.equal(out, out_packed)
     oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
     toks = range(wl.T) if tokens is None else tokens
     experts = set(oids[list(toks)].reshape(-1).tolist())
