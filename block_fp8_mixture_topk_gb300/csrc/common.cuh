@@ -20,6 +20,13 @@ __device__ __forceinline__ void status_set(uint32_t* status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Programmatic dependent launch: every kernel of this library is launched so that it
+// may start while the previous kernel in the stream finishes; before it reads anything
+// an earlier kernel wrote (or writes anything an earlier kernel reads) it waits here for
+// the previous grid to complete and its memory to be visible.  Every kernel calls it on
+// every path, so the wait also covers all grids before that one.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

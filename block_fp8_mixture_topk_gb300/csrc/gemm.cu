@@ -130,10 +130,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 256 : (a.N + 255) / 256;
     const int KB = a.K / BK;
-    int64_t ntiles = *a.num_tiles;
-    if (ntiles < 0) ntiles = 0;
-    if (ntiles > a.max_tiles) ntiles = a.max_tiles;
-    const int64_t total = ntiles * NT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -164,6 +160,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the set-up above overlaps the previous kernel's tail; its outputs are read from here on
+    grid_dependency_wait();
+    int64_t ntiles = *a.num_tiles;
+    if (ntiles < 0) ntiles = 0;
+    if (ntiles > a.max_tiles) ntiles = a.max_tiles;
+    const int64_t total = ntiles * NT;
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     if (warp < FIRST_EPI_WARP) {
@@ -578,25 +580,29 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     const unsigned grid = static_cast<unsigned>(bound < num_sms ? bound : num_sms);
     switch (args.epi) {
         case MOE_EPI_STORE_F32:
-            grouped_gemm_kernel<MOE_EPI_STORE_F32><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            err = launch_pdl(grouped_gemm_kernel<MOE_EPI_STORE_F32>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
+                             tmB, args);
             break;
         case MOE_EPI_SILU_MUL_QUANT:
-            grouped_gemm_kernel<MOE_EPI_SILU_MUL_QUANT><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            err = launch_pdl(grouped_gemm_kernel<MOE_EPI_SILU_MUL_QUANT>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
+                             tmB, args);
             break;
         case MOE_EPI_WEIGHTED_SCATTER:
-            grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
+                             tmB, args);
             break;
         case MOE_EPI_WEIGHTED_ROWS:
-            grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, args);
+            err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
+                             tmB, args);
             break;
         case MOE_EPI_WEIGHTED_PAIRS_BF16:
-            grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB,
-                                                                                                       args);
+            err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
+                             tmB, args);
             break;
         default:
             return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace mfp8

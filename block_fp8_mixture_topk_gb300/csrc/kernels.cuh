@@ -3,9 +3,29 @@
 // and return the launch's cudaError_t.
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace mfp8 {
+
+// Launch on `stream` with programmatic stream serialisation allowed (the kernel must call
+// grid_dependency_wait before touching data of earlier kernels).
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // route.cu
 cudaError_t route_init_device();

@@ -33,6 +33,7 @@ constexpr int kCountWarps = 8;
 __global__ void __launch_bounds__(kCountWarps * 32) chunk_count_kernel(const int32_t* __restrict__ ids, int64_t P,
                                                                        int E, int32_t* __restrict__ counts,
                                                                        uint32_t* status) {
+    grid_dependency_wait();
     extern __shared__ int warp_hist[];  // [kCountWarps][E]
     for (int i = threadIdx.x; i < kCountWarps * E; i += blockDim.x) warp_hist[i] = 0;
     __syncthreads();
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t n_chunks, int E, int
                                                     int32_t* __restrict__ sorted_pair_ids,
                                                     int32_t* __restrict__ tile_expert,
                                                     int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles) {
+    grid_dependency_wait();
     __shared__ int warp_sums[32];
     const int e = threadIdx.x;
     int total = 0;
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(kPermuteChunk) scatter_kernel(const int32_t* _
                                                                 const int32_t* __restrict__ padded_offsets,
                                                                 int32_t* __restrict__ sorted_pair_ids,
                                                                 int32_t* __restrict__ pos) {
+    grid_dependency_wait();
     extern __shared__ int16_t warp_count[];  // [32][E]
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) warp_count[i] = 0;
     __syncthreads();
@@ -178,15 +181,18 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
                                  int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
                                  int32_t* chunk_counts, uint32_t* status, cudaStream_t stream) {
     const int64_t n_chunks = permute_chunks(P);
+    cudaError_t e = cudaSuccess;
     if (n_chunks > 0)
-        chunk_count_kernel<<<static_cast<unsigned>(n_chunks), kCountWarps * 32, kCountWarps * E * sizeof(int),
-                             stream>>>(ids, P, E, chunk_counts, status);
-    scan_kernel<<<1, 1024, 0, stream>>>(n_chunks, E, block_m, chunk_counts, expert_offsets, padded_offsets,
-                                        sorted_pair_ids, tile_expert, tile_row0, num_tiles);
-    if (n_chunks > 0)
-        scatter_kernel<<<static_cast<unsigned>(n_chunks), kPermuteChunk, 32 * E * sizeof(int16_t), stream>>>(
-            ids, P, E, chunk_counts, padded_offsets, sorted_pair_ids, pos);
-    return cudaGetLastError();
+        e = launch_pdl(chunk_count_kernel, dim3(static_cast<unsigned>(n_chunks)), dim3(kCountWarps * 32),
+                       kCountWarps * E * sizeof(int), stream, ids, P, E, chunk_counts, status);
+    if (e == cudaSuccess)
+        e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, stream, n_chunks, E, block_m, chunk_counts,
+                       expert_offsets, padded_offsets, sorted_pair_ids, tile_expert, tile_row0, num_tiles);
+    if (e == cudaSuccess && n_chunks > 0)
+        e = launch_pdl(scatter_kernel, dim3(static_cast<unsigned>(n_chunks)), dim3(kPermuteChunk),
+                       32 * E * sizeof(int16_t), stream, ids, P, E, chunk_counts, padded_offsets, sorted_pair_ids,
+                       pos);
+    return e;
 }
 
 }  // namespace mfp8

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
                                                           int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
                                                           float* __restrict__ s, int64_t s_rs, int64_t s_gs,
                                                           const int32_t* __restrict__ pos, int topk) {
+    grid_dependency_wait();
     const int G = cols / 128;
     const int64_t total = rows * G;
     const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
 
 __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t* __restrict__ w, int N, int K,
                                                                  uint8_t* __restrict__ q, float* __restrict__ s) {
+    grid_dependency_wait();
     __shared__ float warp_max[8];
     const int kb = blockIdx.x, nb = blockIdx.y, e = blockIdx.z;
     const int NB = N / 128, KB = K / 128;
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t*
 __global__ void __launch_bounds__(256) unpermute_sum_kernel(const float4* __restrict__ y, int64_t y_rows,
                                                             const int32_t* __restrict__ pos, int64_t T, int topk,
                                                             int H4, uint2* __restrict__ out, uint32_t* status) {
+    grid_dependency_wait();
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= H4) return;
     for (int64_t t = blockIdx.y; t < T; t += gridDim.y) {
@@ -169,6 +172,7 @@ template <int K>
 __global__ void __launch_bounds__(256) combine_pairs_kernel(const uint4* __restrict__ y,
                                                             const int32_t* __restrict__ pos, int64_t T, int topk,
                                                             int H8, uint4* __restrict__ out) {
+    grid_dependency_wait();
     const int64_t total = T * H8;
     const int kk = K > 0 ? K : topk;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(256) combine_pairs_kernel(const uint4* __restr
 // (coalesced writes; each source row segment of 128 bytes is read by 8 consecutive threads)
 __global__ void __launch_bounds__(256) pack_weights_kernel(const uint4* __restrict__ w, int64_t N, int64_t K,
                                                            int64_t total16, uint4* __restrict__ out) {
+    grid_dependency_wait();
     const int64_t NB = N / 128, KB = K / 128;
     for (int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; o < total16;
          o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -237,17 +242,15 @@ cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_
                                int topk, cudaStream_t stream) {
     const int64_t groups = rows * (cols / 128);
     if (groups == 0) return cudaSuccess;
-    group_quant_kernel<<<grid_for(groups, 16), 256, 0, stream>>>(x, rows, cols, ld, q, q_ld, s, s_row_stride,
-                                                                 s_group_stride, pos, topk);
-    return cudaGetLastError();
+    return launch_pdl(group_quant_kernel, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, rows, cols, ld, q,
+                      q_ld, s, s_row_stride, s_group_stride, pos, topk);
 }
 
 cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
                                       cudaStream_t stream) {
     if (E == 0 || N == 0 || K == 0) return cudaSuccess;
     dim3 grid(K / 128, N / 128, E);
-    block_quant_weight_kernel<<<grid, 256, 0, stream>>>(w, N, K, q, s);
-    return cudaGetLastError();
+    return launch_pdl(block_quant_weight_kernel, grid, dim3(256), 0, stream, w, N, K, q, s);
 }
 
 cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,
@@ -255,9 +258,8 @@ cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* 
     if (T == 0 || H == 0) return cudaSuccess;
     const int H4 = H / 4;
     dim3 grid((H4 + 255) / 256, static_cast<unsigned>(T < 65535 ? T : 65535));
-    unpermute_sum_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(y), y_rows, pos, T, topk, H4,
-                                                   reinterpret_cast<uint2*>(out), status);
-    return cudaGetLastError();
+    return launch_pdl(unpermute_sum_kernel, grid, dim3(256), 0, stream, reinterpret_cast<const float4*>(y), y_rows,
+                      pos, T, topk, H4, reinterpret_cast<uint2*>(out), status);
 }
 
 }  // namespace mfp8
@@ -272,11 +274,13 @@ cudaError_t launch_combine_pairs(const uint16_t* y, const int32_t* pos, int64_t 
     const uint4* y4 = reinterpret_cast<const uint4*>(y);
     uint4* o4 = reinterpret_cast<uint4*>(out);
     switch (topk) {
-        case 8: combine_pairs_kernel<8><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
-        case 2: combine_pairs_kernel<2><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
-        default: combine_pairs_kernel<0><<<grid, 256, 0, stream>>>(y4, pos, T, topk, H8, o4); break;
+        case 8:
+            return launch_pdl(combine_pairs_kernel<8>, dim3(grid), dim3(256), 0, stream, y4, pos, T, topk, H8, o4);
+        case 2:
+            return launch_pdl(combine_pairs_kernel<2>, dim3(grid), dim3(256), 0, stream, y4, pos, T, topk, H8, o4);
+        default:
+            return launch_pdl(combine_pairs_kernel<0>, dim3(grid), dim3(256), 0, stream, y4, pos, T, topk, H8, o4);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace mfp8
@@ -286,9 +290,8 @@ namespace mfp8 {
 cudaError_t launch_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, cudaStream_t stream) {
     const int64_t total16 = static_cast<int64_t>(E) * N * K / 16;
     if (total16 == 0) return cudaSuccess;
-    pack_weights_kernel<<<grid_for(total16, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(w), N, K, total16,
-                                                                     reinterpret_cast<uint4*>(packed));
-    return cudaGetLastError();
+    return launch_pdl(pack_weights_kernel, dim3(grid_for(total16, 256)), dim3(256), 0, stream,
+                      reinterpret_cast<const uint4*>(w), N, K, total16, reinterpret_cast<uint4*>(packed));
 }
 
 }  // namespace mfp8

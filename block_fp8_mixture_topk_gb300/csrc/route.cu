@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
     int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
     float* __restrict__ weights) {
+    grid_dependency_wait();
     extern __shared__ float route_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long t = static_cast<long>(blockIdx.x) * kWarps + warp;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_reg_kernel(
     const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
     int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
     float* __restrict__ weights, bool vec_loads) {
+    grid_dependency_wait();
     __shared__ int s_id[kWarps * MOE_MAX_TOPK];
     __shared__ double s_val[kWarps * MOE_MAX_TOPK];
     __shared__ double s_zall[kWarps];
@@ -388,24 +390,22 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int topk, int r
     const int V = reg_experts_per_lane(E, n_group);
     if (V > 0) {
         const bool vec = V >= 4 && E == 32 * V && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-#define MOE_ROUTE_REG(VV)                                                                                          \
-    route_topk_reg_kernel<VV><<<blocks, kWarps * 32, 0, stream>>>(logits, T, E, topk, renormalize, scoring, n_group, \
-                                                                  topk_group, routed_scaling, bias, ids, weights, vec)
+#define MOE_ROUTE_REG(VV)                                                                                    \
+    return launch_pdl(route_topk_reg_kernel<VV>, dim3(blocks), dim3(kWarps * 32), 0, stream, logits, T, E, topk, \
+                      renormalize, scoring, n_group, topk_group, routed_scaling, bias, ids, weights, vec)
         switch (V) {
-            case 1: MOE_ROUTE_REG(1); break;
-            case 2: MOE_ROUTE_REG(2); break;
-            case 4: MOE_ROUTE_REG(4); break;
-            case 8: MOE_ROUTE_REG(8); break;
-            case 16: MOE_ROUTE_REG(16); break;
-            default: MOE_ROUTE_REG(32); break;
+            case 1: MOE_ROUTE_REG(1);
+            case 2: MOE_ROUTE_REG(2);
+            case 4: MOE_ROUTE_REG(4);
+            case 8: MOE_ROUTE_REG(8);
+            case 16: MOE_ROUTE_REG(16);
+            default: MOE_ROUTE_REG(32);
         }
 #undef MOE_ROUTE_REG
-        return cudaGetLastError();
     }
     const size_t smem = static_cast<size_t>(kWarps) * E * sizeof(float);
-    route_topk_kernel<<<blocks, kWarps * 32, smem, stream>>>(logits, T, E, topk, renormalize, scoring, n_group,
-                                                              topk_group, routed_scaling, bias, ids, weights);
-    return cudaGetLastError();
+    return launch_pdl(route_topk_kernel, dim3(blocks), dim3(kWarps * 32), smem, stream, logits, T, E, topk,
+                      renormalize, scoring, n_group, topk_group, routed_scaling, bias, ids, weights);
 }
 
 }  // namespace mfp8
