@@ -418,7 +418,15 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
                                       rp ? rp->topk_group : 1, rp ? rp->routed_scaling : 1.0f,
                                       rp ? rp->bias : nullptr, ids, wts, s);
     if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess)
+    // a small batch (decode) is sorted and quantised by one block in one launch (the
+    // quantisation stage is then empty); larger ones by the three sort kernels and the
+    // grid-wide quantiser
+    const bool small = P <= kSmallPairs;
+    if (e == cudaSuccess && small)
+        e = launch_sort_quant_small(ids, static_cast<int>(P), E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
+                                    reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
+                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, s);
+    if (e == cudaSuccess && !small)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
                                  reinterpret_cast<int32_t*>(ws + L.counts), st->status, s);
@@ -426,7 +434,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     // dense tile load per K block in the GEMM); the scales are stored transposed
     // ([H/128][rows]) for the GEMM's per-row reads
     if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
+    if (e == cudaSuccess && !small) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
         GemmArgs g{};

@@ -247,4 +247,52 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
+// ---------------------------------------------------------------- bf16 / e4m3 groups of 8
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+}
+
+// codes of 8 values x / sc (correctly rounded quotient, see div_by_scale; rsc = 1/sc rounded)
+__device__ __forceinline__ uint2 encode8(const float* f, float sc, float rsc) {
+    uint32_t b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint16_t lo = e4m3x2(div_by_scale(f[2 * i], sc, rsc), div_by_scale(f[2 * i + 1], sc, rsc));
+        b[i] = lo;
+    }
+    return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+}
+
+// ---------------------------------------------------------------- block scan
+// exclusive scan over the 1024 threads of the block
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int res = (warp ? warp_sums[warp - 1] : 0) + x - v;
+    __syncthreads();
+    return res;
+}
+
 }  // namespace mfp8

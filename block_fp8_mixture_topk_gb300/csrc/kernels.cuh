@@ -42,6 +42,14 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
                                  int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
                                  int32_t* chunk_counts, uint32_t* status, cudaStream_t stream);
 
+// prologue.cu: expert sort + scattering quantisation of a small batch in one block
+constexpr int kSmallPairs = 512;   // routed pairs the one-block path takes
+cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_m, int32_t* expert_offsets,
+                                    int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
+                                    int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
+                                    const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
+                                    int64_t s_rs, int64_t s_gs, cudaStream_t stream);
+
 // quant.cu
 // 1x128 group quantisation of bf16 rows.  Row r of x goes to output row r, or
 // (when pos != null) to output rows pos[r*topk + j], j < topk, skipping -1.

@@ -64,32 +64,6 @@ __global__ void __launch_bounds__(kCountWarps * 32) chunk_count_kernel(const int
     }
 }
 
-// exclusive scan over the 1024 threads of the block
-__device__ int block_exclusive_scan(int v, int* warp_sums) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = warp_sums[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        warp_sums[lane] = w;
-    }
-    __syncthreads();
-    const int res = (warp ? warp_sums[warp - 1] : 0) + x - v;
-    __syncthreads();
-    return res;
-}
-
 __global__ void __launch_bounds__(1024) scan_kernel(int64_t n_chunks, int E, int block_m,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ expert_offsets,
                                                     int32_t* __restrict__ padded_offsets,

@@ -1,0 +1,134 @@
+// Expert sort and activation quantisation of a small batch in one launch.
+//
+// For up to kSmallPairs routed pairs, one launch of 1024-thread blocks does what the
+// three sort kernels (permute.cu) and the scattering quantiser (quant.cu) do for large
+// batches.  Every block sorts the (few) pairs itself in shared memory, block 0 writes the
+// sort's outputs, and the blocks share the quantisation of the tokens' groups:
+// the "sorted token" layout of the pages' Triton fused-MoE kernel (page "Quantization
+// and MoE Optimizations", section Triton Fused MoE Kernel) with each expert's rows
+// padded to whole tiles, then each token's 1x128 group quantisation (section Fp8Config;
+// kFp8Dynamic128Sym) written to the sorted rows of its pairs.  The results are the
+// same, element for element: per-expert counts, exclusive scans, the stable order by
+// (expert, pair) -- a pair's rank is the number of earlier pairs with its expert,
+// counted, so no atomics -- the tile table, and the codes and scales.  In a decode step
+// this removes three launches and the gaps between them.
+#include "kernels.cuh"
+
+namespace mfp8 {
+
+namespace {
+
+__global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
+    const int32_t* __restrict__ ids, int P, int E, int block_m, int32_t* __restrict__ expert_offsets,
+    int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
+    int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles,
+    uint32_t* status, const uint16_t* __restrict__ x, int T, int H, int topk, uint8_t* __restrict__ q,
+    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs) {
+    grid_dependency_wait();
+    __shared__ int s_id[kSmallPairs];
+    __shared__ int s_pos[kSmallPairs];
+    __shared__ int s_poff[MOE_MAX_EXPERTS];
+    __shared__ int warp_sums[32];
+    const int tid = threadIdx.x;
+
+    // routed ids (an id out of range drops its pair and is reported, as in the large sort)
+    for (int p = tid; p < P; p += blockDim.x) {
+        int id = ids[p];
+        if (id < 0 || id >= E) {
+            status_set(status, MOE_STATUS_BAD_EXPERT_ID);
+            id = -1;
+        }
+        s_id[p] = id;
+    }
+    __syncthreads();
+
+    // per-expert counts and padded counts; exclusive scans over the experts (E <= 1024)
+    int total = 0;
+    if (tid < E)
+        for (int p = 0; p < P; ++p) total += s_id[p] == tid ? 1 : 0;
+    const int padded = (total + block_m - 1) / block_m * block_m;
+    const int off = block_exclusive_scan(total, warp_sums);
+    const int poff = block_exclusive_scan(padded, warp_sums);
+    const bool writer = blockIdx.x == 0;
+    if (tid < E) s_poff[tid] = poff;
+    if (writer && tid < E) {
+        expert_offsets[tid] = off;
+        padded_offsets[tid] = poff;
+        if (tid == E - 1) {
+            expert_offsets[E] = off + total;
+            padded_offsets[E] = poff + padded;
+            *num_tiles = (poff + padded) / block_m;
+        }
+        for (int i = poff / block_m; i < (poff + padded) / block_m; ++i) {
+            tile_expert[i] = tid;
+            tile_row0[i] = i * block_m;
+        }
+        for (int r = poff + total; r < poff + padded; ++r) sorted_pair_ids[r] = -1;
+    }
+    __syncthreads();
+
+    // stable order: pair p goes after the earlier pairs of its expert
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int id = s_id[p];
+        int r = -1;
+        if (id >= 0) {
+            int before = 0;
+            for (int o = 0; o < p; ++o) before += s_id[o] == id ? 1 : 0;
+            r = s_poff[id] + before;
+            if (writer) sorted_pair_ids[r] = p;
+        }
+        if (writer) pos[p] = r;
+        s_pos[p] = r;
+    }
+    __syncthreads();
+
+    // 1x128 groups of each token: 16 threads per group (8 values each), codes and scale
+    // written to the sorted rows of the token's pairs
+    const int G = H / 128;
+    const int half = (tid >> 4) & 1, sub = tid & 15;
+    const int per_pass = (blockDim.x >> 5) * 2;   // groups per block and pass
+    for (int gi0 = blockIdx.x * per_pass + (tid >> 5) * 2; gi0 < T * G; gi0 += gridDim.x * per_pass) {
+        const int gi = gi0 + half;
+        const bool active = gi < T * G;
+        float f[8];
+        float amax = 0.0f;
+        int t = 0, g = 0;
+        if (active) {
+            t = gi / G;
+            g = gi - t * G;
+            unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + g * 128 + sub * 8)), f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (active) {
+            const float sc = group_scale(amax);
+            const uint2 code = encode8(f, sc, __frcp_rn(sc));
+            for (int j = 0; j < topk; ++j) {
+                const int64_t o = s_pos[t * topk + j];
+                if (o < 0) continue;
+                *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
+                if (sub == 0) s[o * s_rs + g * s_gs] = sc;
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_m, int32_t* expert_offsets,
+                                    int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
+                                    int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
+                                    const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
+                                    int64_t s_rs, int64_t s_gs, cudaStream_t stream) {
+    const int groups = T * (H / 128);
+    int blocks = (groups + 63) / 64;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 148) blocks = 148;
+    return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
+                      padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
+                      q, q_ld, s, s_rs, s_gs);
+}
+
+}  // namespace mfp8

@@ -27,26 +27,6 @@ namespace mfp8 {
 
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-        f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-}
-
-// codes of 8 values x / sc (correctly rounded quotient, see div_by_scale; rsc = 1/sc rounded)
-__device__ __forceinline__ uint2 encode8(const float* f, float sc, float rsc) {
-    uint32_t b[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint16_t lo = e4m3x2(div_by_scale(f[2 * i], sc, rsc), div_by_scale(f[2 * i + 1], sc, rsc));
-        b[i] = lo;
-    }
-    return make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
-}
-
 __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols,
                                                           int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
                                                           float* __restrict__ s, int64_t s_rs, int64_t s_gs,
