@@ -131,6 +131,29 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+# The layer is data-parallel over tokens: every rank runs its own replica on its own batch
+# (no collective on the data path); only the step time is reduced, as the maximum over ranks.
+
+def replica_workload(wl, rank):
+    """The batch rank `rank` processes: the same shapes and weights, its own seeded tokens."""
+    return wl.with_(number=wl.number + 100 * rank) if rank else wl
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of a list of floats over all ranks (no-op without a process group)."""
+    if dist is None:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world, units_per_rank, ms):
+    """Units per second processed by all ranks together in `ms` milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- oracle (CPU)
 def oracle_inputs(wl, tokens, device):
     """CPU copies of the workload's inputs and the oracle's own quantisation of the experts
@@ -235,7 +258,7 @@ def run_ours(args, wl):
         dist.init_process_group("nccl", device_id=dev)
 
     # inputs: each rank its own batch (seed offset by rank), weights quantised on the GPU (untimed)
-    wl_r = wl.with_(number=wl.number + 100 * rank) if rank else wl
+    wl_r = replica_workload(wl, rank)
     hidden, logits = mi.hidden(wl_r, dev), mi.router_logits(wl_r, dev)
     bias = mi.expert_bias(wl, dev)
     rp = (moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling, bias)
@@ -341,17 +364,14 @@ def run_ours(args, wl):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
-    if dist:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
     pk = peaks()
-    tokens_s = world * wl.T / (ms / 1000.0)
+    tokens_s = whole_job_rate(world, wl.T, ms)
     flops = wl.flops()
     per_expert_w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
     per_expert = 3 * H * I + ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
@@ -386,7 +406,7 @@ def run_ours(args, wl):
             "ms_per_step_eager": eager_ms, "ms_per_step_graph": graph_ms, "launch": launch,
             "experts_touched": touched, "weight_bytes_touched": touched * per_expert,
             "stage_ms": stage_ms, "clocks": clk,
-            "e2e": {"value": world * wl.T / (e2e_ms / 1e3), "unit": "tokens/s",
+            "e2e": {"value": whole_job_rate(world, wl.T, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
                     "d2h_bytes_per_step": out.numel() * 2},
             "gpu_launches": LAUNCHES_PER_STEP * args.steps,
