@@ -399,7 +399,7 @@ def run_ours(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
-            "config": {**describe(wl, world), "weights": describe_weights(args)},
+            "config": describe(wl, world), "weights_layout": describe_weights(args),
             "tflops": world * flops / (ms / 1e3) / 1e12,
             "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
             "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,
