@@ -32,7 +32,6 @@ import torch  # noqa: E402
 
 import moe_inputs as mi  # noqa: E402
 
-LAUNCHES_PER_STEP = 8      # route 1 + expert sort 3 + quantise 1 + two grouped GEMMs + weighted sum 1
 FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
 PROFILE = os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md")
 GEMM_SOURCES = [os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc", f) for f in ("gemm.cu", "common.cuh")]
@@ -409,7 +408,7 @@ def run_ours(args, wl):
             "e2e": {"value": whole_job_rate(world, wl.T, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
                     "d2h_bytes_per_step": out.numel() * 2},
-            "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk) * args.steps,
             "roofline": roof}
     if world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or default_sample(wl)

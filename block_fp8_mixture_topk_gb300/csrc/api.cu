@@ -343,6 +343,13 @@ int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, in
     return cuda_rc(launch_combine_pairs(y, pos, T, topk, H, out, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || topk < 1) return -1;
+    if (T == 0) return 0;
+    const int64_t P = static_cast<int64_t>(T) * topk;
+    return 1 + (P <= kSmallPairs ? 1 : 4) + 2 + 1;
+}
+
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk) {
     if (T < 0 || H < 0 || I < 0 || E < 1 || topk < 1) return 0;
     return forward_layout(T, H, I, E, topk).total;

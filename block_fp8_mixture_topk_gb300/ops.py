@@ -85,6 +85,7 @@ def lib():
                 "fp8_block_quant_weight": ([P, I, I, I, P, P, P], I),
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
+                "moe_fp8_block_forward_kernel_count": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, I, P], I),
@@ -263,6 +264,11 @@ def moe_combine_pairs(y, pos, T, topk, out=None):
     rc = lib().moe_combine_pairs(_ptr(y), _ptr(pos), T, topk, H, _ptr(out), _stream())
     _check("moe_combine_pairs", rc)
     return out
+
+
+def moe_fp8_block_forward_kernel_count(T, H, I, E, topk) -> int:
+    """Kernels one moe_fp8_block_forward launches for these sizes."""
+    return int(lib().moe_fp8_block_forward_kernel_count(T, H, I, E, topk))
 
 
 def moe_fp8_block_workspace_size(T, H, I, E, topk) -> int:

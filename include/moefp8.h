@@ -270,6 +270,11 @@ int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, in
  * bytes (256-byte aligned).  hidden, w13, w2 and out 16-byte aligned.  out may
  * not alias any input.  T == 0 is a no-op. */
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
+/* Number of kernels one moe_fp8_block_forward launches for these sizes (host only):
+ * routing, the expert sort and quantisation (one kernel for up to 512 routed pairs,
+ * four otherwise), the two grouped GEMMs and the weighted sum; 0 when T == 0, -1 for
+ * invalid sizes. */
+int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk);
 int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const uint8_t* w13, const float* w13_scale,
                           const uint8_t* w2, const float* w2_scale,

@@ -55,6 +55,12 @@ def test_host_only_queries():
     # sorted activation codes, the sorted intermediate, bf16 weighted rows in pair order
     assert ws >= rows * 7168 + rows * 2048 + 32768 * 7168 * 2
     assert moe.moe_fp8_block_workspace_size(16, 256, 256, 4, 2) > 0
+    # route + sort/quantise (one kernel up to 512 pairs, four above) + two GEMMs + weighted sum
+    assert moe.moe_fp8_block_forward_kernel_count(1, 7168, 2048, 256, 8) == 5
+    assert moe.moe_fp8_block_forward_kernel_count(64, 7168, 2048, 256, 8) == 5
+    assert moe.moe_fp8_block_forward_kernel_count(65, 7168, 2048, 256, 8) == 8
+    assert moe.moe_fp8_block_forward_kernel_count(0, 7168, 2048, 256, 8) == 0
+    assert moe.moe_fp8_block_forward_kernel_count(-1, 7168, 2048, 256, 8) == -1
 
 
 @pytest.mark.parametrize("T,E,topk,rp,code", [
