@@ -234,3 +234,47 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
         out_bf16[rows] = bf16_from_f64(out[rows])
     return dict(ids=ids, weights=wts, offsets=offsets, sorted=sorted_, pos=pos, a1q=a1q, a1s=a1s,
                 a2q=a2q, a2s=a2s, c1=c1, c2=c2, out=out, out_bf16=out_bf16, need=need)
+
+
+# --------------------------------------------------------------------------- masked batched layout
+
+def moe_forward_masked(hidden_bits, counts, w13, w13_scale, w2, w2_scale):
+    """The expert MLP on rows already grouped by expert ("[num_experts, max_tokens, hidden]"
+    with per-expert counts, the batched layout the low-latency expert-parallel path hands to
+    the experts, page "Quantization and MoE Optimizations", BatchedDeepGemmExperts): for
+    every expert e and row i < counts[e], the same 1x128 quantisation, GEMM over w13,
+    SiLU(gate)*up with requantisation and GEMM over w2 as the routed layer computes for a
+    pair of that expert, with no router weight (the combine belongs to the dispatcher).
+
+    hidden_bits [E, M, H] uint16 (bf16 bits), counts [E] ints in [0, M].
+    Returns (out fp64 [E, M, H] with NaN in rows i >= counts[e], out_bf16 bits [E, M, H]).
+    """
+    hidden_bits = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
+    E, M, H = hidden_bits.shape
+    counts = np.asarray(counts, dtype=np.int64)
+    assert counts.shape == (E,) and np.all((counts >= 0) & (counts <= M))
+    N1 = w13.shape[1]
+    I = N1 // 2
+    a1q, a1s = quant_1x128_bf16(hidden_bits.reshape(E * M, H))
+    # one pair per valid row (topk = 1): expert e's rows in order
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    sorted_ = np.concatenate([e * M + np.arange(counts[e]) for e in range(E)]).astype(np.int32) \
+        if offsets[-1] else np.zeros(0, dtype=np.int32)
+    P = int(offsets[-1])
+    need = np.ones(E * M, dtype=np.uint8)
+    a2q = np.zeros((max(P, 1), I), dtype=np.uint8)
+    a2s = np.zeros((max(P, 1), I // 128), dtype=np.float32)
+    c2 = np.full((max(P, 1), H), np.nan)
+    w13c, w2c = np.ascontiguousarray(w13, dtype=np.uint8), np.ascontiguousarray(w2, dtype=np.uint8)
+    w13s = np.ascontiguousarray(w13_scale, dtype=np.float32)
+    w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
+    _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
+                        _ptr(offsets), _ptr(sorted_), _ptr(need), E * M, H, I, E, 1,
+                        _ptr(a2q), _ptr(a2s), None, _ptr(c2))
+    out = np.full((E * M, H), np.nan)
+    out_bf16 = np.zeros((E * M, H), dtype=np.uint16)
+    if P:
+        out[sorted_] = c2[:P]
+        out_bf16[sorted_] = bf16_from_f64(c2[:P])
+    return out.reshape(E, M, H), out_bf16.reshape(E, M, H)

@@ -223,3 +223,24 @@ def test_sampled_tokens_match_full_run():
     part = oracle.moe_forward(hid, logits, w13q, w13s, w2q, w2s, k, tokens=[2, 7])
     assert np.array_equal(part["out"][[2, 7]], full["out"][[2, 7]])
     assert np.all(np.isnan(part["out"][[0, 1, 3]]))
+
+
+def test_masked_layout_equals_dense_chain_per_expert():
+    """The masked batched layout ([E, M, H] rows already grouped by expert, counts[e] valid rows):
+    every valid row of expert e equals the dense block-FP8 chain through expert e's weights
+    (torch float64), rows past the count stay empty, and an empty expert computes nothing."""
+    rng = np.random.default_rng(23)
+    E, M, H, I = 3, 40, 256, 256
+    counts = [0, 40, 17]
+    hid = bf16_bits(rng.standard_normal((E, M, H)))
+    w13q, w13s = oracle.quant_128x128_bf16(bf16_bits(rng.standard_normal((E, 2 * I, H)) * 0.02))
+    w2q, w2s = oracle.quant_128x128_bf16(bf16_bits(rng.standard_normal((E, H, I)) * 0.02))
+    out, out_bf16 = oracle.moe_forward_masked(hid, counts, w13q, w13s, w2q, w2s)
+    for e, c in enumerate(counts):
+        assert np.all(np.isnan(out[e, c:]))
+        if c:
+            ref = _dense_chain_torch(hid[e, :c], w13q[e:e + 1], w13s[e:e + 1], w2q[e:e + 1], w2s[e:e + 1])
+            assert np.allclose(out[e, :c], ref, rtol=1e-12, atol=1e-14)
+            assert np.array_equal(out_bf16[e, :c], oracle.bf16_from_f64(out[e, :c]))
+    empty, _ = oracle.moe_forward_masked(hid, [0, 0, 0], w13q, w13s, w2q, w2s)
+    assert np.all(np.isnan(empty))
