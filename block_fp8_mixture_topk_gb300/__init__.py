@@ -17,6 +17,8 @@ from .ops import (  # noqa: F401
     moe_combine_pairs,
     moe_device_supported,
     moe_fp8_block_forward,
+    moe_fp8_block_forward_masked,
+    moe_fp8_block_masked_workspace_size,
     moe_fp8_block_forward_kernel_count,
     moe_fp8_block_pack_weights,
     moe_fp8_block_workspace_size,

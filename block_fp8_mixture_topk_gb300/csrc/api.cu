@@ -116,6 +116,37 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     return L;
 }
 
+struct MaskedLayout {
+    size_t row_map, pos, ones, tile_e, tile_r, ntiles, a1, a1s, a2, a2s, total;
+    int64_t Mp, rows, tiles;
+};
+
+MaskedLayout masked_layout(int E, int M, int H, int I) {
+    MaskedLayout L;
+    L.Mp = (static_cast<int64_t>(M) + MOE_BLOCK_M - 1) / MOE_BLOCK_M * MOE_BLOCK_M;
+    L.rows = static_cast<int64_t>(E) * L.Mp;
+    L.tiles = L.rows / MOE_BLOCK_M;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align_up(bytes, 256);
+        return o;
+    };
+    const size_t EM = static_cast<size_t>(E) * M;
+    L.row_map = take(L.rows * 4);
+    L.pos = take(EM * 4);
+    L.ones = take(EM * 4);
+    L.tile_e = take(L.tiles * 4);
+    L.tile_r = take(L.tiles * 4);
+    L.ntiles = take(4);
+    L.a1 = take(L.rows * H);
+    L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
+    L.a2 = take(L.rows * I);
+    L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
+    L.total = off;
+    return L;
+}
+
 }  // namespace
 
 namespace mfp8 {
@@ -499,6 +530,106 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess) e = launch_combine_pairs(ypairs, pos, T, topk, H, out, s);
     if (e == cudaSuccess) e = mark(6);
+    return cuda_rc(e);
+}
+
+
+size_t moe_fp8_block_masked_workspace_size(int E, int max_tokens, int H, int I) {
+    if (E < 0 || max_tokens < 0 || H < 0 || I < 0) return 0;
+    return masked_layout(E, max_tokens, H, I).total;
+}
+
+int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2, const float* w2_scale, int E,
+                                 int max_tokens, int H, int I, int weight_layout, void* workspace,
+                                 size_t workspace_bytes, uint16_t* out, void* stream) {
+    if (E < 0 || max_tokens < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (H % 128 != 0 || I % 128 != 0 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || max_tokens == 0) return MOE_OK;
+    const MaskedLayout L = masked_layout(E, max_tokens, H, I);
+    if (L.rows >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I * (H / 128) >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!hidden || !counts || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* row_map = reinterpret_cast<int32_t*>(ws + L.row_map);
+    int32_t* pos = reinterpret_cast<int32_t*>(ws + L.pos);
+    float* ones = reinterpret_cast<float*>(ws + L.ones);
+    int32_t* tile_e = reinterpret_cast<int32_t*>(ws + L.tile_e);
+    int32_t* tile_r = reinterpret_cast<int32_t*>(ws + L.tile_r);
+    int32_t* ntiles = reinterpret_cast<int32_t*>(ws + L.ntiles);
+    uint8_t* a1 = ws + L.a1;
+    float* a1s = reinterpret_cast<float*>(ws + L.a1s);
+    uint8_t* a2 = ws + L.a2;
+    float* a2s = reinterpret_cast<float*>(ws + L.a2s);
+    const int64_t EM = static_cast<int64_t>(E) * max_tokens;
+
+    cudaError_t e = launch_masked_map(counts, E, max_tokens, static_cast<int>(L.Mp), row_map, pos, ones, tile_e,
+                                      tile_r, ntiles, st->status, s);
+    // valid rows quantised into their padded rows; scales transposed ([H/128][rows])
+    if (e == cudaSuccess) e = launch_group_quant(hidden, EM, H, H, a1, H, a1s, 1, L.rows, pos, 1, s);
+    if (e == cudaSuccess) {
+        GemmArgs g{};
+        g.A = a1;
+        g.a_scale = a1s;
+        g.as_row_stride = 1;
+        g.as_kb_stride = L.rows;
+        g.a_rows = L.rows;
+        g.B = w13;
+        g.b_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        g.b_scale = w13_scale;
+        g.N = 2 * I;
+        g.K = H;
+        g.E = E;
+        g.tile_expert = tile_e;
+        g.tile_row0 = tile_r;
+        g.num_tiles = ntiles;
+        g.max_tiles = L.tiles;
+        g.epi = MOE_EPI_SILU_MUL_QUANT;
+        g.sorted_pair_ids = row_map;
+        g.out_q = a2;
+        g.out_scale = a2s;
+        g.os_row_stride = 1;
+        g.os_kb_stride = L.rows;
+        g.status = st->status;
+        e = launch_grouped_gemm(g, st->num_sms, s);
+    }
+    if (e == cudaSuccess) {
+        // one "pair" per input row: unit weight, written to the row's place in out
+        GemmArgs g{};
+        g.A = a2;
+        g.a_scale = a2s;
+        g.as_row_stride = 1;
+        g.as_kb_stride = L.rows;
+        g.a_rows = L.rows;
+        g.B = w2;
+        g.b_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        g.b_scale = w2_scale;
+        g.N = H;
+        g.K = I;
+        g.E = E;
+        g.tile_expert = tile_e;
+        g.tile_row0 = tile_r;
+        g.num_tiles = ntiles;
+        g.max_tiles = L.tiles;
+        g.epi = MOE_EPI_WEIGHTED_PAIRS_BF16;
+        g.out_bf16 = out;
+        g.sorted_pair_ids = row_map;
+        g.topk_weights = ones;
+        g.topk = 1;
+        g.num_pairs = EM;
+        g.status = st->status;
+        e = launch_grouped_gemm(g, st->num_sms, s);
+    }
     return cuda_rc(e);
 }
 

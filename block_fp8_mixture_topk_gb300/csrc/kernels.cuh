@@ -50,6 +50,12 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
                                     int64_t s_rs, int64_t s_gs, cudaStream_t stream);
 
+// masked.cu: row maps and tile table of the masked batched layout [E, M, H] (Mp = M rounded
+// up to 128): row_map [E*Mp] (input row or -1), pos [E*M] (padded row or -1), ones [E*M]
+cudaError_t launch_masked_map(const int32_t* counts, int E, int M, int Mp, int32_t* row_map, int32_t* pos,
+                              float* ones, int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
+                              uint32_t* status, cudaStream_t stream);
+
 // quant.cu
 // 1x128 group quantisation of bf16 rows.  Row r of x goes to output row r, or
 // (when pos != null) to output rows pos[r*topk + j], j < topk, skipping -1.

@@ -90,6 +90,8 @@ def lib():
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, I, P], I),
                 "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
+                "moe_fp8_block_masked_workspace_size": ([I, I, I, I], SZ),
+                "moe_fp8_block_forward_masked": ([P, P, P, P, P, P, I, I, I, I, I, P, SZ, P, P], I),
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
                 "moe_combine_pairs": ([P, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
@@ -327,6 +329,35 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
         rc = lib().moe_fp8_block_forward_events(*args, layout, arr)
     _check("moe_fp8_block_forward", rc)
+    return out
+
+
+def moe_fp8_block_masked_workspace_size(E, max_tokens, H, I) -> int:
+    return int(lib().moe_fp8_block_masked_workspace_size(E, max_tokens, H, I))
+
+
+def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, out=None, workspace=None):
+    """Expert MLP on the masked batched layout: hidden bf16 [E, M, H] with counts int32 [E]
+    (CUDA) valid rows per expert; returns bf16 [E, M, H] (rows past the counts not written)."""
+    _cuda(hidden, torch.bfloat16, "hidden")
+    _cuda(counts, torch.int32, "counts")
+    w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
+    _cuda(w13_scale, torch.float32, "w13_scale")
+    _cuda(w2_scale, torch.float32, "w2_scale")
+    E, M, H = hidden.shape
+    _, N1, _, layout = _weight_shape(w13)
+    if _weight_shape(w2)[3] != layout:
+        raise ValueError("w13 and w2 must share one layout")
+    I = N1 // 2
+    if out is None:
+        out = torch.empty(E, M, H, dtype=torch.bfloat16, device=hidden.device)
+    nbytes = moe_fp8_block_masked_workspace_size(E, M, H, I)
+    if workspace is None:
+        workspace = _workspace(hidden.device, nbytes)
+    rc = lib().moe_fp8_block_forward_masked(_ptr(hidden), _ptr(counts), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+                                            _ptr(w2_scale), E, M, H, I, layout, _ptr(workspace), workspace.numel(),
+                                            _ptr(out), _stream())
+    _check("moe_fp8_block_forward_masked", rc)
     return out
 
 

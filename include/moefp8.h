@@ -50,6 +50,7 @@ extern "C" {
 /* device status bits (moe_get_device_status) */
 #define MOE_STATUS_WAIT_TIMEOUT 0x1u      /* a pipeline wait gave up; outputs invalid */
 #define MOE_STATUS_BAD_EXPERT_ID 0x2u     /* a routed id was outside [0, E); pair dropped */
+#define MOE_STATUS_BAD_COUNT 0x4u         /* a masked-layout count was outside [0, max_tokens]; clamped */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024
@@ -305,6 +306,27 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
                                  int T, int H, int I, int E, int topk, int renormalize,
                                  const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
                                  uint16_t* out, void* stream, int weight_layout, void* const* events);
+
+/* ---- the masked batched layout -----------------------------------------------------
+ * The expert MLP on rows already grouped by expert: hidden [E, max_tokens, H] bf16 with
+ * counts[e] valid rows for expert e (the "[num_experts, max_tokens, hidden]" batched format
+ * that low-latency expert-parallel dispatch produces, BatchedDeepGemmExperts, page
+ * "Quantization and MoE Optimizations").  For every e and i < counts[e]:
+ *   out[e, i, :] = bf16( w2-GEMM( requant( SiLU(gate) * up ( w13-GEMM( quant(hidden[e, i]) ) ) ) ) )
+ * with the same 1x128 activation groups, 128x128 weight blocks and fp32 block-scale
+ * promotion as moe_fp8_block_forward, and no router weight (the combine belongs to the
+ * dispatcher).  Rows i >= counts[e] of out are not written.
+ * counts: device int32 [E], read on the device (no host synchronisation); a count
+ * outside [0, max_tokens] is clamped and sets MOE_STATUS_BAD_COUNT.
+ * w13, w2 in weight_layout (MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED); hidden, w13, w2, out
+ * 16-byte aligned; workspace of moe_fp8_block_masked_workspace_size bytes, 256-byte
+ * aligned.  H, I multiples of 128, E <= 1024.  max_tokens == 0 or E == 0 is a no-op. */
+size_t moe_fp8_block_masked_workspace_size(int E, int max_tokens, int H, int I);
+int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts,
+                                 const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale,
+                                 int E, int max_tokens, int H, int I, int weight_layout,
+                                 void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---- status -------------------------------------------------------------------- */
 /* Reads (and with clear != 0, resets) the device status word of the current
