@@ -48,6 +48,10 @@ def parse():
     p.add_argument("--experts", type=int, default=None, help="override E (smaller profiling cases)")
     p.add_argument("--cpu-sample", type=int, default=None, help="tokens the oracle computes")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layout", choices=["routed", "masked"], default="routed",
+                   help="routed: the whole layer (default); masked: moe_fp8_block_forward_masked on rows "
+                        "grouped by expert, counts from routing the workload's tokens")
+    p.add_argument("--max-tokens", type=int, default=None, help="masked layout: rows per expert (default: max count)")
     p.add_argument("--weights", choices=["tiled", "nk"], default="tiled",
                    help="expert weight layout: tile-packed at load time (default) or the pages' [E, N, K]")
     return p.parse_args()
@@ -421,6 +425,103 @@ def run_ours(args, wl):
     _ = np
 
 
+def run_masked(args, wl):
+    """The expert MLP on the masked batched layout [E, M, H] (rows already grouped by expert, as
+    expert-parallel dispatch delivers them): counts from routing the workload's tokens, M the
+    largest count (or --max-tokens), timed as CUDA-graph replays; one GPU."""
+    import numpy as np
+    import block_fp8_mixture_topk_gb300 as moe
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E, H, I = wl.E, wl.H, wl.I
+    bias = mi.expert_bias(wl, dev)
+    rp = (moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling, bias)
+          if wl.scoring == mi.SIGMOID else moe.RoutingParams("softmax", 1, 1, wl.routed_scaling))
+    ids, _ = moe.moe_route_topk(mi.router_logits(wl, dev), wl.topk, wl.renormalize, rp)
+    counts = torch.bincount(ids.reshape(-1).long(), minlength=E).to(torch.int32)
+    M = args.max_tokens or int(counts.max().item())
+    counts = counts.clamp(max=M)
+    rows = int(counts.sum().item())
+    touched = int((counts > 0).sum().item())
+    g = torch.Generator(device=dev).manual_seed(wl.seed + 7)
+    hidden = torch.randn(E, M, H, generator=g, device=dev).to(torch.bfloat16)
+    w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+    w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+    w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+    for e0 in range(0, E, 8):
+        ex = range(e0, min(E, e0 + 8))
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex))
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex))
+    w13p, w2p = (moe.moe_fp8_block_pack_weights(w13q), moe.moe_fp8_block_pack_weights(w2q)) \
+        if args.weights == "tiled" else (w13q, w2q)
+    out = torch.empty(E, M, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(moe.moe_fp8_block_masked_workspace_size(E, M, H, I), dtype=torch.uint8, device=dev)
+
+    def step():
+        moe.moe_fp8_block_forward_masked(hidden, counts, w13p, w13s, w2p, w2s, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    if moe.moe_get_device_status(clear=True):
+        raise RuntimeError("device status word set during the benchmark")
+    pk = peaks()
+    per_expert = 3 * H * I + ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+    layer_bytes = touched * per_expert + rows * H * 2 * 2
+    line = {"metric": "block-FP8 masked-layout expert rows/s", "value": rows / (ms / 1e3), "unit": "rows/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded; counts from routing the workload's tokens)",
+            "config": {**describe(wl, 1), "layout": f"masked [E={E}, M={M}, H={H}], {rows} valid rows"},
+            "weights_layout": describe_weights(args), "launch": "cuda_graph",
+            "tflops": 6 * rows * H * I / (ms / 1e3) / 1e12, "layer_gbs": layer_bytes / (ms / 1e3) / 1e9,
+            "hbm_frac": layer_bytes / (ms / 1e3) / 1e9 / pk["hbm"], "experts_touched": touched,
+            "clocks": clk, "gpu_launches": 4 * args.steps}
+    if not args.no_cpu_baseline:
+        # the oracle on the rows of the first two touched experts
+        cnt = counts.cpu().numpy()
+        sample = [int(e) for e in np.nonzero(cnt)[0][:2]]
+        sub = np.zeros(E, dtype=np.int64)
+        sub[sample] = cnt[sample]
+        w13o = np.zeros((E, 2 * I, H), np.uint8)
+        w13so = np.zeros((E, 2 * I // 128, H // 128), np.float32)
+        w2o = np.zeros((E, H, I), np.uint8)
+        w2so = np.zeros((E, H // 128, I // 128), np.float32)
+        for e in sample:
+            q, s_ = oracle.quant_128x128_bf16(mi.bf16_bits(mi.w13_bf16(wl, dev, [e])))
+            w13o[e], w13so[e] = q[0], s_[0]
+            q, s_ = oracle.quant_128x128_bf16(mi.bf16_bits(mi.w2_bf16(wl, dev, [e])))
+            w2o[e], w2so[e] = q[0], s_[0]
+        hb = mi.bf16_bits(hidden.cpu())
+        t_start = time.perf_counter()
+        oracle.moe_forward_masked(hb, sub, w13o, w13so, w2o, w2so)
+        dt = time.perf_counter() - t_start
+        line["cpu_baseline"] = {"value": int(sub.sum()) / dt, "unit": "rows/s", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": f"{int(sub.sum())} rows of experts {sample}"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     wl = mi.WORKLOADS[args.workload]
@@ -430,6 +531,8 @@ def main():
         wl = wl.with_(E=args.experts)
     if args.impl == "reference":
         run_reference(args, wl)
+    elif args.layout == "masked":
+        run_masked(args, wl)
     else:
         run_ours(args, wl)
 
