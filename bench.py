@@ -344,28 +344,56 @@ def run_ours(args, wl):
     if moe.moe_get_device_status(clear=True):
         raise RuntimeError("device status word set during the benchmark")
 
-    # end to end through the public API: pinned host inputs in, bf16 output back, every step
+    # end to end through the public API: every step uploads its inputs from pinned host memory
+    # and downloads its bf16 output, all inside the timed region.  As a serving loop would, the
+    # uploads and downloads run on their own streams, double-buffered, so that step i+1's
+    # upload and step i-1's download overlap step i's forward.
+    comp, up, down = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nbuf = 2
     hid_h, log_h = hidden.cpu().pin_memory(), logits.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hid_d, log_d = torch.empty_like(hidden), torch.empty_like(logits)
+    hid_d = [torch.empty_like(hidden) for _ in range(nbuf)]
+    log_d = [torch.empty_like(logits) for _ in range(nbuf)]
+    out_d = [torch.empty_like(out) for _ in range(nbuf)]
+    out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(nbuf)]
+    h2d_done = [torch.cuda.Event() for _ in range(nbuf)]
+    fwd_done = [torch.cuda.Event() for _ in range(nbuf)]
+    d2h_done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_step():
-        hid_d.copy_(hid_h, non_blocking=True)
-        log_d.copy_(log_h, non_blocking=True)
-        moe.moe_fp8_block_forward(hid_d, log_d, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
-                                  workspace=ws)
-        out_h.copy_(out, non_blocking=True)
+    def e2e_run(n, start_event):
+        up.wait_event(start_event)
+        for i in range(n):
+            b = i % nbuf
+            with torch.cuda.stream(up):
+                if i >= nbuf:
+                    up.wait_event(fwd_done[b])          # the forward that read buffer b is done
+                hid_d[b].copy_(hid_h, non_blocking=True)
+                log_d[b].copy_(log_h, non_blocking=True)
+                h2d_done[b].record(up)
+            comp.wait_event(h2d_done[b])
+            if i >= nbuf:
+                comp.wait_event(d2h_done[b])            # output buffer b was downloaded
+            moe.moe_fp8_block_forward(hid_d[b], log_d[b], w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp,
+                                      out=out_d[b], workspace=ws)
+            fwd_done[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(fwd_done[b])
+                out_h[b].copy_(out_d[b], non_blocking=True)
+                d2h_done[b].record(down)
+        for b in range(min(n, nbuf)):
+            comp.wait_event(d2h_done[b])
 
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
+    w0 = torch.cuda.Event()
+    w0.record(comp)
+    e2e_run(max(3, args.warmup), w0)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
+    e0.record(comp)
+    e2e_run(args.steps, e0)
+    e1.record(comp)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
+    if not torch.equal(out_h[(args.steps - 1) % nbuf].to(dev), out):
+        raise RuntimeError("end-to-end output differs from the device-resident run")
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
     if rank != 0:
