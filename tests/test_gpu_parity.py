@@ -561,6 +561,18 @@ def test_forward_small_shapes(T, H, I, E, topk):
     assert_output_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("T,H,I,E,topk", [
+    (64, 128, 128, 16, 8),       # 512 routed pairs: the one-launch sort + quantisation
+    (65, 128, 128, 16, 8),       # 520 pairs: the three sort kernels and the grid-wide quantiser
+    (5, 128, 128, 1024, 4),      # the largest expert count, small batch
+    (40, 128, 256, 1024, 16),    # the largest expert count, 640 pairs
+])
+def test_forward_sort_path_boundaries(T, H, I, E, topk):
+    wl = mi.Workload("bounds", 70 + T + E, T, H, I, E, topk)
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
 def test_forward_all_tokens_to_one_expert():
     """300 tokens, top-1, every token on expert 2: three tiles of one expert, the other experts empty."""
     wl = mi.Workload("skew", 77, 300, 256, 256, 4, 1)
