@@ -54,13 +54,13 @@ def _load():
             lib.orc_e4m3_encode.restype = ctypes.c_uint8
             lib.orc_bf16_from_f64.argtypes = [ctypes.c_double]
             lib.orc_bf16_from_f64.restype = ctypes.c_uint16
-            lib.orc_quant_1x128_f32.argtypes = [P, L, L, P, P]
-            lib.orc_quant_1x128_bf16.argtypes = [P, L, L, P, P]
-            lib.orc_quant_128x128_bf16.argtypes = [P, L, L, L, P, P]
+            lib.orc_quant_1x128_f32.argtypes = [P, L, L, P, P, I]
+            lib.orc_quant_1x128_bf16.argtypes = [P, L, L, P, P, I]
+            lib.orc_quant_128x128_bf16.argtypes = [P, L, L, L, P, P, I]
             lib.orc_route.argtypes = [P, P, L, I, I, I, I, I, I, ctypes.c_double, P, P]
             lib.orc_route.restype = I
             lib.orc_permute.argtypes = [P, L, I, P, P, P]
-            lib.orc_experts.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P]
+            lib.orc_experts.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P, I]
             lib.orc_combine.argtypes = [P, P, P, P, L, L, I, P]
             lib.orc_num_threads.restype = I
             _lib = lib
@@ -122,36 +122,40 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------- quantisers
 
-def quant_1x128_bf16(x_bits: np.ndarray):
+# scale formats: fp32 amax/448, or that scale rounded up to a power of two (FLOAT32_CEIL_UE8M0)
+SCALE_F32, SCALE_UE8M0 = 0, 1
+
+
+def quant_1x128_bf16(x_bits: np.ndarray, scale_fmt: int = SCALE_F32):
     """1x128 group quantisation of bf16 rows: returns (codes [R,C] u8, scales [R,C/128] f32)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     R, C = x.shape
     assert C % 128 == 0
     q = np.empty((R, C), dtype=np.uint8)
     s = np.empty((R, C // 128), dtype=np.float32)
-    _load().orc_quant_1x128_bf16(_ptr(x), R, C, _ptr(q), _ptr(s))
+    _load().orc_quant_1x128_bf16(_ptr(x), R, C, _ptr(q), _ptr(s), scale_fmt)
     return q, s
 
 
-def quant_1x128_f32(x: np.ndarray):
+def quant_1x128_f32(x: np.ndarray, scale_fmt: int = SCALE_F32):
     """1x128 group quantisation of fp32 rows: returns (codes, scales)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     R, C = x.shape
     assert C % 128 == 0
     q = np.empty((R, C), dtype=np.uint8)
     s = np.empty((R, C // 128), dtype=np.float32)
-    _load().orc_quant_1x128_f32(_ptr(x), R, C, _ptr(q), _ptr(s))
+    _load().orc_quant_1x128_f32(_ptr(x), R, C, _ptr(q), _ptr(s), scale_fmt)
     return q, s
 
 
-def quant_128x128_bf16(w_bits: np.ndarray):
+def quant_128x128_bf16(w_bits: np.ndarray, scale_fmt: int = SCALE_F32):
     """128x128 block quantisation of stacked bf16 weights [E,N,K]: (codes [E,N,K], scales [E,N/128,K/128])."""
     w = np.ascontiguousarray(w_bits, dtype=np.uint16)
     E, N, K = w.shape
     assert N % 128 == 0 and K % 128 == 0
     q = np.empty((E, N, K), dtype=np.uint8)
     s = np.empty((E, N // 128, K // 128), dtype=np.float32)
-    _load().orc_quant_128x128_bf16(_ptr(w), E, N, K, _ptr(q), _ptr(s))
+    _load().orc_quant_128x128_bf16(_ptr(w), E, N, K, _ptr(q), _ptr(s), scale_fmt)
     return q, s
 
 
@@ -191,7 +195,7 @@ def permute(ids: np.ndarray, E: int):
 
 def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
                 scoring=SOFTMAX, bias=None, n_group=1, topk_group=1, routed_scaling=1.0,
-                tokens=None, want_c1=False):
+                tokens=None, want_c1=False, scale_fmt=SCALE_F32):
     """The whole layer on the CPU.
 
     hidden_bits [T,H] uint16 (bf16 bits), logits [T,E] f32, w13 [E,2I,H] u8,
@@ -208,7 +212,7 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
     assert w2.shape == (E, H, I)
     ids, wts = route(logits, topk, renormalize, scoring, bias, n_group, topk_group, routed_scaling)
     offsets, sorted_, pos = permute(ids, E)
-    a1q, a1s = quant_1x128_bf16(hidden_bits)
+    a1q, a1s = quant_1x128_bf16(hidden_bits, scale_fmt)
     P = T * topk
     need = np.zeros(T, dtype=np.uint8)
     if tokens is None:
@@ -225,7 +229,7 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
     w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
     _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
                         _ptr(offsets), _ptr(sorted_), _ptr(need), T, H, I, E, topk,
-                        _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2))
+                        _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2), scale_fmt)
     out = np.full((T, H), np.nan)
     _load().orc_combine(_ptr(c2), _ptr(wts), _ptr(pos), _ptr(need), T, H, topk, _ptr(out))
     out_bf16 = np.zeros((T, H), dtype=np.uint16)
@@ -238,7 +242,7 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
 
 # --------------------------------------------------------------------------- masked batched layout
 
-def moe_forward_masked(hidden_bits, counts, w13, w13_scale, w2, w2_scale):
+def moe_forward_masked(hidden_bits, counts, w13, w13_scale, w2, w2_scale, scale_fmt=SCALE_F32):
     """The expert MLP on rows already grouped by expert ("[num_experts, max_tokens, hidden]"
     with per-expert counts, the batched layout the low-latency expert-parallel path hands to
     the experts, page "Quantization and MoE Optimizations", BatchedDeepGemmExperts): for
@@ -255,7 +259,7 @@ def moe_forward_masked(hidden_bits, counts, w13, w13_scale, w2, w2_scale):
     assert counts.shape == (E,) and np.all((counts >= 0) & (counts <= M))
     N1 = w13.shape[1]
     I = N1 // 2
-    a1q, a1s = quant_1x128_bf16(hidden_bits.reshape(E * M, H))
+    a1q, a1s = quant_1x128_bf16(hidden_bits.reshape(E * M, H), scale_fmt)
     # one pair per valid row (topk = 1): expert e's rows in order
     offsets = np.zeros(E + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
@@ -271,7 +275,7 @@ def moe_forward_masked(hidden_bits, counts, w13, w13_scale, w2, w2_scale):
     w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
     _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
                         _ptr(offsets), _ptr(sorted_), _ptr(need), E * M, H, I, E, 1,
-                        _ptr(a2q), _ptr(a2s), None, _ptr(c2))
+                        _ptr(a2q), _ptr(a2s), None, _ptr(c2), scale_fmt)
     out = np.full((E * M, H), np.nan)
     out_bf16 = np.zeros((E * M, H), dtype=np.uint16)
     if P:

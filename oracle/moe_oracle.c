@@ -131,13 +131,24 @@ uint16_t orc_bf16_from_f64(double x) {
  * key kFp8Dynamic128Sym ([FP8O] _get_priority_backends); the 1e-8 floor on amax
  * follows [NVFP4] _quantize_moe_weight_to_nvfp4. */
 
-static float group_scale(float amax) {
+/* Scale formats: 0 = fp32 (amax/448 as computed); 1 = FLOAT32_CEIL_UE8M0, the fp32
+ * scale rounded up to a power of two ("Float32 scales rounded up to UE8M0", DeepGEMM
+ * scale formats, [QMO] DeepGEMM Scale Formats), so that every scale is exactly
+ * representable as an 8-bit exponent. */
+static float ceil_pow2(float t) {
+    int e;
+    float m = frexpf(t, &e);                       /* t = m * 2^e, 0.5 <= m < 1 */
+    return m == 0.5f ? t : ldexpf(1.0f, e);
+}
+
+static float group_scale(float amax, int fmt) {
     float floored = amax > 1e-8f ? amax : 1e-8f;
-    return floored / 448.0f;                       /* fp32 IEEE division */
+    float t = floored / 448.0f;                    /* fp32 IEEE division */
+    return fmt == 1 ? ceil_pow2(t) : t;
 }
 
 /* x: fp32 [rows, cols] (cols % 128 == 0) -> q [rows, cols], s [rows, cols/128] */
-void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float* s) {
+void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
     long G = cols / 128;
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
@@ -148,7 +159,7 @@ void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float
                 float a = fabsf(xg[i]);
                 if (a > amax) amax = a;
             }
-            float sc = group_scale(amax);
+            float sc = group_scale(amax, fmt);
             s[r * G + g] = sc;
             for (int i = 0; i < 128; ++i) q[r * cols + g * 128 + i] = orc_e4m3_encode(xg[i] / sc);
         }
@@ -156,7 +167,7 @@ void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float
 }
 
 /* bf16 input version of the 1x128 activation quantiser */
-void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, float* s) {
+void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
     long G = cols / 128;
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
@@ -168,7 +179,7 @@ void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, f
                 float a = fabsf(row[i]);
                 if (a > amax) amax = a;
             }
-            float sc = group_scale(amax);
+            float sc = group_scale(amax, fmt);
             s[r * G + g] = sc;
             for (int i = 0; i < 128; ++i) q[r * cols + g * 128 + i] = orc_e4m3_encode(row[i] / sc);
         }
@@ -179,7 +190,7 @@ void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, f
  * ("weight_block_size ... [128, 128]", [QMO] Fp8Config; the static block key
  * kFp8Static128BlockSym, [FP8O] _get_priority_backends).  Same rule as the
  * groups, amax over the whole block.  s: [E, N/128, K/128]. */
-void orc_quant_128x128_bf16(const uint16_t* w, long E, long N, long K, uint8_t* q, float* s) {
+void orc_quant_128x128_bf16(const uint16_t* w, long E, long N, long K, uint8_t* q, float* s, int fmt) {
     long NB = N / 128, KB = K / 128;
 #pragma omp parallel for collapse(2) schedule(static)
     for (long e = 0; e < E; ++e) {
@@ -191,7 +202,7 @@ void orc_quant_128x128_bf16(const uint16_t* w, long E, long N, long K, uint8_t* 
                         float a = fabsf(bf16_to_f32(w[(e * N + n) * K + k]));
                         if (a > amax) amax = a;
                     }
-                float sc = group_scale(amax);
+                float sc = group_scale(amax, fmt);
                 s[(e * NB + nb) * KB + kb] = sc;
                 for (long n = nb * 128; n < nb * 128 + 128; ++n)
                     for (long k = kb * 128; k < kb * 128 + 128; ++k) {
@@ -364,7 +375,7 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
                  const uint8_t* w13, const float* w13s, const uint8_t* w2, const float* w2s,
                  const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
                  long T, long H, long I, int E, int topk,
-                 uint8_t* a2q, float* a2s, double* c1, double* c2) {
+                 uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
     (void)T;
     e4m3_build();
     long N1 = 2 * I, HB = H / 128, IB = I / 128;
@@ -399,7 +410,7 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
                 double gate = g[i], up = g[I + i];
                 h1[i] = (float)(gate / (1.0 + exp(-gate)) * up);
             }
-            orc_quant_1x128_f32(h1, 1, I, a2q + r * I, a2s + r * IB);
+            orc_quant_1x128_f32(h1, 1, I, a2q + r * I, a2s + r * IB, fmt);
             free(a); free(g); free(h1);
         }
         /* dequantised w2[e] */

@@ -191,3 +191,45 @@ def test_f32_and_bf16_quantisers_agree(rows, cols):
     q1, s1 = oracle.quant_1x128_bf16(bits)
     q2, s2 = oracle.quant_1x128_f32(oracle.bf16_to_f64(bits).astype(np.float32))
     assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+
+
+def test_ue8m0_scales_round_the_fp32_scale_up_to_a_power_of_two():
+    """FLOAT32_CEIL_UE8M0: each scale is the smallest power of two not below fp32(amax/448)
+    (numpy's float32 division and float64 log2, not the oracle's frexp), exact powers stay, and
+    the codes are torch's float8 cast of x / scale (exact, the scale being a power of two)."""
+    rng = np.random.default_rng(31)
+    rows, cols = 64, 512
+    x = rng.standard_normal((rows, cols)) * np.exp2(rng.integers(-30, 30, (rows, 1)))
+    x[0, :128] = 0.0                                       # floor group
+    x[1, :128] = 0.0
+    x[1, 7] = 448.0 * 2.0 ** 5                             # t = 2^5 exactly: kept
+    x[2, 128:256] = 0.0
+    x[2, 130] = -(448.0 * 2.0 ** -3) * 1.5                 # t = 1.5 * 2^-3: rounded up to 2^-2
+    bits = oracle.bf16_from_f64(x)
+    q, s = oracle.quant_1x128_bf16(bits, oracle.SCALE_UE8M0)
+    xb = oracle.bf16_to_f64(bits).astype(np.float32)
+    amax = np.abs(xb.reshape(rows, -1, 128)).max(axis=2)
+    t = np.maximum(amax, np.float32(1e-8)).astype(np.float32) / np.float32(448.0)
+    want = np.exp2(np.ceil(np.log2(t.astype(np.float64)))).astype(np.float32)
+    assert np.array_equal(s, want)
+    assert s[1, 0] == 2.0 ** 5 and s[2, 1] == 2.0 ** -2
+    assert np.all(np.frexp(s)[0] == 0.5)
+    # codes: float8 cast of the exact quotient
+    y = torch.from_numpy(xb.reshape(rows, -1, 128) / s[..., None])
+    tq = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy().reshape(rows, cols)
+    assert np.array_equal(q, tq)
+    # the fp32 mode on the same rows is unchanged
+    q32, s32 = oracle.quant_1x128_bf16(bits)
+    assert np.array_equal(s32, t)
+
+
+def test_ue8m0_weight_blocks():
+    rng = np.random.default_rng(32)
+    w = oracle.bf16_from_f64(rng.standard_normal((2, 256, 384)) * 0.02)
+    q, s = oracle.quant_128x128_bf16(w, oracle.SCALE_UE8M0)
+    wf = oracle.bf16_to_f64(w).astype(np.float32)
+    amax = np.abs(wf.reshape(2, 2, 128, 3, 128)).max(axis=(2, 4))
+    t = np.maximum(amax, np.float32(1e-8)).astype(np.float32) / np.float32(448.0)
+    assert np.array_equal(s, np.exp2(np.ceil(np.log2(t.astype(np.float64)))).astype(np.float32))
+    y = wf / np.repeat(np.repeat(s, 128, axis=1), 128, axis=2)
+    assert np.array_equal(q, torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy())

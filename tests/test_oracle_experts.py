@@ -155,8 +155,9 @@ def test_random_gemms_against_torch_float64():
     assert np.array_equal(r["sorted"][r["pos"]], np.arange(T * k))
 
 
-def _dense_chain_torch(hid_bits, w13q, w13s, w2q, w2s):
-    """E=1, top-1: quantise -> GEMM -> SiLU*up -> requantise -> GEMM, all in torch."""
+def _dense_chain_torch(hid_bits, w13q, w13s, w2q, w2s, ue8m0=False):
+    """E=1, top-1: quantise -> GEMM -> SiLU*up -> requantise -> GEMM, all in torch (with ue8m0:
+    every activation scale rounded up to a power of two)."""
     x = torch.from_numpy(oracle.bf16_to_f64(hid_bits)).float()
     T, H = x.shape
     I = w2q.shape[2]
@@ -164,6 +165,8 @@ def _dense_chain_torch(hid_bits, w13q, w13s, w2q, w2s):
     def quant(v):
         g = v.view(v.shape[0], -1, 128)
         s = g.abs().amax(2).clamp_min(1e-8) / 448.0
+        if ue8m0:
+            s = torch.exp2(torch.ceil(torch.log2(s.double()))).float()
         q = (g / s[..., None]).to(torch.float8_e4m3fn)
         return q.double().view(v.shape[0], -1) * s.double().repeat_interleave(128, 1)
 
@@ -244,3 +247,22 @@ def test_masked_layout_equals_dense_chain_per_expert():
             assert np.array_equal(out_bf16[e, :c], oracle.bf16_from_f64(out[e, :c]))
     empty, _ = oracle.moe_forward_masked(hid, [0, 0, 0], w13q, w13s, w2q, w2s)
     assert np.all(np.isnan(empty))
+
+
+
+def test_ue8m0_single_expert_reduces_to_dense_chain():
+    """The FLOAT32_CEIL_UE8M0 mode end to end: weights, activations and the requantised
+    intermediate all on power-of-two scales; E=1, top-1 equals the torch chain."""
+    rng = np.random.default_rng(9)
+    T, H, I = 7, 256, 256
+    hid = bf16_bits(rng.standard_normal((T, H)) * 3.0)
+    w13q, w13s = oracle.quant_128x128_bf16(bf16_bits(rng.standard_normal((1, 2 * I, H)) * 0.02), oracle.SCALE_UE8M0)
+    w2q, w2s = oracle.quant_128x128_bf16(bf16_bits(rng.standard_normal((1, H, I)) * 0.02), oracle.SCALE_UE8M0)
+    assert np.all(np.frexp(w13s)[0] == 0.5) and np.all(np.frexp(w2s)[0] == 0.5)
+    r = oracle.moe_forward(hid, np.zeros((T, 1), np.float32), w13q, w13s, w2q, w2s, 1, scale_fmt=oracle.SCALE_UE8M0)
+    assert np.all(np.frexp(r["a1s"])[0] == 0.5) and np.all(np.frexp(r["a2s"][:T])[0] == 0.5)
+    ref = _dense_chain_torch(hid, w13q, w13s, w2q, w2s, ue8m0=True)
+    assert np.allclose(r["out"], ref, rtol=1e-12, atol=1e-14)
+    # and it differs from the fp32-scale layer on the same weights
+    r32 = oracle.moe_forward(hid, np.zeros((T, 1), np.float32), w13q, w13s, w2q, w2s, 1)
+    assert not np.array_equal(r["out"], r32["out"])
