@@ -241,7 +241,13 @@ int moe_align_permute(const int32_t* topk_ids, int T, int topk, int E, int block
 }
 
 int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, void* stream) {
+    return fp8_group_quant_ex(x, rows, cols, ld, q, s, MOE_SCALE_F32, stream);
+}
+
+int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, int scale_fmt,
+                       void* stream) {
     if (rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
+    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (cols % 128 != 0 || ld % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     if (!x || !q || !s) return MOE_ERR_INVALID_ARG;
@@ -249,12 +255,18 @@ int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, f
     DeviceState* st = nullptr;
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
-    return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, s, cols / 128, 1, nullptr, 1,
+    return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, s, cols / 128, 1, nullptr, 1, scale_fmt,
                                       static_cast<cudaStream_t>(stream)));
 }
 
 int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, void* stream) {
+    return fp8_block_quant_weight_ex(w, E, N, K, q, s, MOE_SCALE_F32, stream);
+}
+
+int fp8_block_quant_weight_ex(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
+                              void* stream) {
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (N % 128 != 0 || K % 128 != 0 || K > (1 << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (E == 0 || N == 0 || K == 0) return MOE_OK;
     if (E > 65535 || N / 128 > 65535) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -262,7 +274,7 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
     DeviceState* st = nullptr;
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
-    return cuda_rc(launch_block_quant_weight(w, E, N, K, q, s, static_cast<cudaStream_t>(stream)));
+    return cuda_rc(launch_block_quant_weight(w, E, N, K, q, s, scale_fmt, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, void* stream) {
@@ -293,6 +305,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     if (!A || !a_scale || !B || !b_scale || !tile_expert || !tile_row0 || !num_tiles) return MOE_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16)) return MOE_ERR_INVALID_ARG;
     if (ep->b_layout != MOE_WEIGHTS_NK && ep->b_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (ep->scale_fmt != MOE_SCALE_F32 && ep->scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (ep->b_layout == MOE_WEIGHTS_TILED && static_cast<int64_t>(E) * N * (K / 128) >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     switch (ep->kind) {
@@ -346,6 +359,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.num_pairs = ep->num_pairs;
     g.out_bf16 = ep->out_bf16;
     g.b_tiled = ep->b_layout == MOE_WEIGHTS_TILED;
+    g.scale_fmt = ep->scale_fmt;
     g.status = st->status;
     return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -390,28 +404,30 @@ int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits, co
                           const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H, int I, int E,
                           int topk, int renormalize, const moe_routing_params* rp, void* workspace,
                           size_t workspace_bytes, uint16_t* out, void* stream) {
-    return moe_fp8_block_forward_events(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
-                                        renormalize, rp, workspace, workspace_bytes, out, stream, MOE_WEIGHTS_NK,
-                                        nullptr);
+    return moe_fp8_block_forward_ex(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
+                                    renormalize, rp, nullptr, workspace, workspace_bytes, out, stream, nullptr);
 }
 
 int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
                                  const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
                                  int I, int E, int topk, int renormalize, const moe_routing_params* rp,
                                  void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
-    return moe_fp8_block_forward_events(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
-                                        renormalize, rp, workspace, workspace_bytes, out, stream, MOE_WEIGHTS_TILED,
-                                        nullptr);
+    const moe_forward_options opts{MOE_WEIGHTS_TILED, MOE_SCALE_F32};
+    return moe_fp8_block_forward_ex(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
+                                    renormalize, rp, &opts, workspace, workspace_bytes, out, stream, nullptr);
 }
 
-int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
-                                 const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
-                                 int I, int E, int topk, int renormalize, const moe_routing_params* rp,
-                                 void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
-                                 int weight_layout, void* const* events) {
+int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits, const uint8_t* w13,
+                             const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H, int I,
+                             int E, int topk, int renormalize, const moe_routing_params* rp,
+                             const moe_forward_options* opts, void* workspace, size_t workspace_bytes,
+                             uint16_t* out, void* stream, void* const* events) {
     int rc = check_routing(T, E, topk, rp);
     if (rc != MOE_OK) return rc;
+    const int weight_layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
+    const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (weight_layout == MOE_WEIGHTS_TILED &&
         static_cast<int64_t>(E) * 2 * I * (H / 128) >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -463,7 +479,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     if (e == cudaSuccess && small)
         e = launch_sort_quant_small(ids, static_cast<int>(P), E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                     reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
-                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, s);
+                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, scale_fmt, s);
     if (e == cudaSuccess && !small)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
@@ -472,7 +488,8 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
     // dense tile load per K block in the GEMM); the scales are stored transposed
     // ([H/128][rows]) for the GEMM's per-row reads
     if (e == cudaSuccess) e = mark(2);
-    if (e == cudaSuccess && !small) e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, s);
+    if (e == cudaSuccess && !small)
+        e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, scale_fmt, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
         GemmArgs g{};
@@ -492,6 +509,7 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
         g.epi = MOE_EPI_SILU_MUL_QUANT;
+        g.scale_fmt = scale_fmt;
         g.sorted_pair_ids = sorted;
         g.out_q = a2;
         g.out_scale = a2s;
@@ -541,10 +559,13 @@ size_t moe_fp8_block_masked_workspace_size(int E, int max_tokens, int H, int I) 
 
 int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, const uint8_t* w13,
                                  const float* w13_scale, const uint8_t* w2, const float* w2_scale, int E,
-                                 int max_tokens, int H, int I, int weight_layout, void* workspace,
+                                 int max_tokens, int H, int I, const moe_forward_options* opts, void* workspace,
                                  size_t workspace_bytes, uint16_t* out, void* stream) {
     if (E < 0 || max_tokens < 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    const int weight_layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
+    const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (H % 128 != 0 || I % 128 != 0 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (E == 0 || max_tokens == 0) return MOE_OK;
     const MaskedLayout L = masked_layout(E, max_tokens, H, I);
@@ -576,7 +597,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     cudaError_t e = launch_masked_map(counts, E, max_tokens, static_cast<int>(L.Mp), row_map, pos, ones, tile_e,
                                       tile_r, ntiles, st->status, s);
     // valid rows quantised into their padded rows; scales transposed ([H/128][rows])
-    if (e == cudaSuccess) e = launch_group_quant(hidden, EM, H, H, a1, H, a1s, 1, L.rows, pos, 1, s);
+    if (e == cudaSuccess) e = launch_group_quant(hidden, EM, H, H, a1, H, a1s, 1, L.rows, pos, 1, scale_fmt, s);
     if (e == cudaSuccess) {
         GemmArgs g{};
         g.A = a1;
@@ -595,6 +616,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
         g.epi = MOE_EPI_SILU_MUL_QUANT;
+        g.scale_fmt = scale_fmt;
         g.sorted_pair_ids = row_map;
         g.out_q = a2;
         g.out_scale = a2s;

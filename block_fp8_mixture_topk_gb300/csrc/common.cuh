@@ -243,6 +243,16 @@ __device__ __forceinline__ float group_scale(float amax) {
     return __fdiv_rn(fmaxf(amax, 1e-8f), 448.0f);
 }
 
+// The same scale in format fmt: MOE_SCALE_F32 as is, MOE_SCALE_UE8M0 rounded up to a power
+// of two (a positive normal float whose mantissa bits are not all zero goes to the next
+// exponent), so that it is exactly an 8-bit exponent.
+__device__ __forceinline__ float group_scale_fmt(float amax, int fmt) {
+    const float t = group_scale(amax);
+    if (fmt != MOE_SCALE_UE8M0) return t;
+    const uint32_t b = __float_as_uint(t);
+    return (b & 0x007FFFFFu) ? __uint_as_float((b & 0x7F800000u) + 0x00800000u) : t;
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }

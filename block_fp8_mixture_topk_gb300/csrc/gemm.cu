@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
-                const float sc = group_scale(amax);
+                const float sc = group_scale_fmt(amax, a.scale_fmt);
                 const float rsc = __frcp_rn(sc);
                 uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
 #pragma unroll

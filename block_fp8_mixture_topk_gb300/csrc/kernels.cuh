@@ -48,7 +48,7 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, cudaStream_t stream);
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream);
 
 // masked.cu: row maps and tile table of the masked batched layout [E, M, H] (Mp = M rounded
 // up to 128): row_map [E*Mp] (input row or -1), pos [E*M] (padded row or -1), ones [E*M]
@@ -62,8 +62,8 @@ cudaError_t launch_masked_map(const int32_t* counts, int E, int M, int Mp, int32
 // Scale of (output row o, group g) is stored at s[o*s_row_stride + g*s_group_stride].
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, cudaStream_t stream);
-cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
+                               int topk, int scale_fmt, cudaStream_t stream);
+cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
                                       cudaStream_t stream);
 // [E, N, K] e4m3 -> [E][N/128][K/128][128][128] (each 128x128 block contiguous)
 cudaError_t launch_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, cudaStream_t stream);
@@ -99,6 +99,7 @@ struct GemmArgs {
     int topk;
     int64_t num_pairs;
     uint16_t* out_bf16;
+    int scale_fmt;             // MOE_SCALE_*: the SiLU epilogue's requantisation scales
     uint32_t* status;
 };
 cudaError_t gemm_init_device();

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles,
     uint32_t* status, const uint16_t* __restrict__ x, int T, int H, int topk, uint8_t* __restrict__ q,
-    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs) {
+    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt) {
     grid_dependency_wait();
     __shared__ int s_id[kSmallPairs];
     __shared__ int s_pos[kSmallPairs];
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (active) {
-            const float sc = group_scale(amax);
+            const float sc = group_scale_fmt(amax, scale_fmt);
             const uint2 code = encode8(f, sc, __frcp_rn(sc));
             for (int j = 0; j < topk; ++j) {
                 const int64_t o = s_pos[t * topk + j];
@@ -121,14 +121,14 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, cudaStream_t stream) {
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream) {
     const int groups = T * (H / 128);
     int blocks = (groups + 63) / 64;
     if (blocks < 1) blocks = 1;
     if (blocks > 148) blocks = 148;
     return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
                       padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
-                      q, q_ld, s, s_rs, s_gs);
+                      q, q_ld, s, s_rs, s_gs, scale_fmt);
 }
 
 }  // namespace mfp8

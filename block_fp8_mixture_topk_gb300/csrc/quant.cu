@@ -30,7 +30,7 @@ namespace {
 __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols,
                                                           int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
                                                           float* __restrict__ s, int64_t s_rs, int64_t s_gs,
-                                                          const int32_t* __restrict__ pos, int topk) {
+                                                          const int32_t* __restrict__ pos, int topk, int scale_fmt) {
     grid_dependency_wait();
     const int G = cols / 128;
     const int64_t total = rows * G;
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (active) {
-            const float sc = group_scale(amax);
+            const float sc = group_scale_fmt(amax, scale_fmt);
             const uint2 code = encode8(f, sc, __frcp_rn(sc));
             if (pos) {
                 for (int j = 0; j < topk; ++j) {
@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
 }
 
 __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t* __restrict__ w, int N, int K,
-                                                                 uint8_t* __restrict__ q, float* __restrict__ s) {
+                                                                 uint8_t* __restrict__ q, float* __restrict__ s,
+                                                                 int scale_fmt) {
     grid_dependency_wait();
     __shared__ float warp_max[8];
     const int kb = blockIdx.x, nb = blockIdx.y, e = blockIdx.z;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t*
     amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
-    const float sc = group_scale(amax);
+    const float sc = group_scale_fmt(amax, scale_fmt);
     const float rsc = __frcp_rn(sc);
     uint2 out[8];
 #pragma unroll
@@ -219,18 +220,18 @@ int grid_for(int64_t work_items, int per_block) {
 
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, cudaStream_t stream) {
+                               int topk, int scale_fmt, cudaStream_t stream) {
     const int64_t groups = rows * (cols / 128);
     if (groups == 0) return cudaSuccess;
     return launch_pdl(group_quant_kernel, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, rows, cols, ld, q,
-                      q_ld, s, s_row_stride, s_group_stride, pos, topk);
+                      q_ld, s, s_row_stride, s_group_stride, pos, topk, scale_fmt);
 }
 
-cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s,
+cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
                                       cudaStream_t stream) {
     if (E == 0 || N == 0 || K == 0) return cudaSuccess;
     dim3 grid(K / 128, N / 128, E);
-    return launch_pdl(block_quant_weight_kernel, grid, dim3(256), 0, stream, w, N, K, q, s);
+    return launch_pdl(block_quant_weight_kernel, grid, dim3(256), 0, stream, w, N, K, q, s, scale_fmt);
 }
 
 cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* pos, int64_t T, int topk, int H,

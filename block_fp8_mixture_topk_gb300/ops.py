@@ -17,6 +17,7 @@ from . import build as _build
 
 MOE_BLOCK_M = 128
 MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED = 0, 1
+SCALE_FMT = {"f32": 0, "ue8m0": 1}      # fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)
 SCORING = {"softmax": 0, "sigmoid": 1}
 EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
 
@@ -40,7 +41,12 @@ class _Epilogue(ctypes.Structure):
                 ("out_q", ctypes.c_void_p), ("out_scale", ctypes.c_void_p),
                 ("out_scale_row_stride", ctypes.c_int64), ("out_scale_kb_stride", ctypes.c_int64),
                 ("sorted_pair_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
-                ("num_pairs", ctypes.c_int64), ("out_bf16", ctypes.c_void_p), ("b_layout", ctypes.c_int32)]
+                ("num_pairs", ctypes.c_int64), ("out_bf16", ctypes.c_void_p), ("b_layout", ctypes.c_int32),
+                ("scale_fmt", ctypes.c_int32)]
+
+
+class _ForwardOptions(ctypes.Structure):
+    _fields_ = [("weight_layout", ctypes.c_int32), ("scale_fmt", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -82,16 +88,18 @@ def lib():
                 "moe_align_permute": ([P, I, I, I, I, P, P, P, P, P, P, P, P, SZ, P], I),
                 "moe_align_permute_noalloc": ([P, I, I, I, I, P, P, P, P, P, P, P, P], I),
                 "fp8_group_quant": ([P, I, I, I, P, P, P], I),
+                "fp8_group_quant_ex": ([P, I, I, I, P, P, I, P], I),
+                "fp8_block_quant_weight_ex": ([P, I, I, I, P, P, I, P], I),
                 "fp8_block_quant_weight": ([P, I, I, I, P, P, P], I),
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward_kernel_count": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
-                "moe_fp8_block_forward_events": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P, I, P], I),
+                "moe_fp8_block_forward_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P, P, P], I),
                 "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
                 "moe_fp8_block_masked_workspace_size": ([I, I, I, I], SZ),
-                "moe_fp8_block_forward_masked": ([P, P, P, P, P, P, I, I, I, I, I, P, SZ, P, P], I),
+                "moe_fp8_block_forward_masked": ([P, P, P, P, P, P, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
                 "moe_combine_pairs": ([P, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
@@ -188,24 +196,25 @@ def moe_align_permute(topk_ids, num_experts, block_m=MOE_BLOCK_M):
     return out
 
 
-def fp8_group_quant(x):
-    """1x128 group quantisation of bf16 [rows, cols]: returns (codes uint8, scales fp32 [rows, cols/128])."""
+def fp8_group_quant(x, scale_fmt="f32"):
+    """1x128 group quantisation of bf16 [rows, cols]: returns (codes uint8, scales fp32 [rows, cols/128]).
+    scale_fmt: "f32" (amax/448) or "ue8m0" (rounded up to a power of two)."""
     _cuda(x, torch.bfloat16, "x")
     rows, cols = x.shape
     q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
     s = torch.empty(rows, max(cols // 128, 1), dtype=torch.float32, device=x.device)
-    rc = lib().fp8_group_quant(_ptr(x), rows, cols, cols, _ptr(q), _ptr(s), _stream())
+    rc = lib().fp8_group_quant_ex(_ptr(x), rows, cols, cols, _ptr(q), _ptr(s), SCALE_FMT[scale_fmt], _stream())
     _check("fp8_group_quant", rc)
     return q, s
 
 
-def fp8_block_quant_weight(w):
+def fp8_block_quant_weight(w, scale_fmt="f32"):
     """128x128 block quantisation of bf16 [E, N, K]: returns (codes uint8 [E,N,K], scales [E,N/128,K/128])."""
     _cuda(w, torch.bfloat16, "w")
     E, N, K = w.shape
     q = torch.empty(E, N, K, dtype=torch.uint8, device=w.device)
     s = torch.empty(E, max(N // 128, 1), max(K // 128, 1), dtype=torch.float32, device=w.device)
-    rc = lib().fp8_block_quant_weight(_ptr(w), E, N, K, _ptr(q), _ptr(s), _stream())
+    rc = lib().fp8_block_quant_weight_ex(_ptr(w), E, N, K, _ptr(q), _ptr(s), SCALE_FMT[scale_fmt], _stream())
     _check("fp8_block_quant_weight", rc)
     return q, s
 
@@ -230,13 +239,14 @@ def _weight_shape(w):
 
 def fp8_block_grouped_gemm(A, a_scale, a_scale_strides, B, b_scale, tile_expert, tile_row0, num_tiles,
                            epilogue="store", out_f32=None, out_q=None, out_scale=None, out_scale_strides=(0, 0),
-                           sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0, out_bf16=None):
+                           sorted_pair_ids=None, topk_weights=None, topk=1, num_pairs=0, out_bf16=None,
+                           scale_fmt="f32"):
     """Grouped GEMM of the C ABI.  Outputs are caller-provided tensors (see include/moefp8.h)."""
     A, B = _codes(_cuda(A, None, "A")), _codes(_cuda(B, None, "B"))
     E, N, K, layout = _weight_shape(B)
     ep = _Epilogue(EPILOGUE[epilogue], topk, _ptr(out_f32), _ptr(out_q), _ptr(out_scale),
                    int(out_scale_strides[0]), int(out_scale_strides[1]), _ptr(sorted_pair_ids),
-                   _ptr(topk_weights), int(num_pairs), _ptr(out_bf16), layout)
+                   _ptr(topk_weights), int(num_pairs), _ptr(out_bf16), layout, SCALE_FMT[scale_fmt])
     rc = lib().fp8_block_grouped_gemm(_ptr(A), _ptr(a_scale), int(a_scale_strides[0]), int(a_scale_strides[1]),
                                       A.shape[0], _ptr(B), _ptr(b_scale), N, K, E, _ptr(tile_expert),
                                       _ptr(tile_row0), _ptr(num_tiles), tile_expert.numel(), ctypes.byref(ep),
@@ -293,7 +303,8 @@ FORWARD_STAGES = ("route", "sort", "quant", "gemm_w13", "gemm_w2", "unpermute_su
 
 
 def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
-                          routing: RoutingParams | None = None, out=None, workspace=None, events=None):
+                          routing: RoutingParams | None = None, out=None, workspace=None, events=None,
+                          scale_fmt="f32"):
     """The whole layer: returns bf16 [T, H] (written into `out` when given).
 
     w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D).
@@ -315,19 +326,19 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     if workspace is None:
         workspace = _workspace(hidden.device, nbytes)
     rp = routing.to_c() if routing else None
-    args = [_ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), T, H, I, E,
-            topk, int(bool(renormalize)), ctypes.byref(rp) if rp else None, _ptr(workspace), workspace.numel(),
-            _ptr(out), _stream()]
-    if events is None:
-        rc = (lib().moe_fp8_block_forward_packed if layout == MOE_WEIGHTS_TILED else lib().moe_fp8_block_forward)(*args)
-    else:
+    opts = _ForwardOptions(layout, SCALE_FMT[scale_fmt])
+    arr = None
+    if events is not None:
         if len(events) != len(FORWARD_STAGES) + 1:
             raise ValueError("events: one more than the number of stages")
         for ev in events:
             if not ev.cuda_event:       # torch creates the CUDA event on its first record()
                 ev.record()
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
-        rc = lib().moe_fp8_block_forward_events(*args, layout, arr)
+    rc = lib().moe_fp8_block_forward_ex(_ptr(hidden), _ptr(router_logits), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+                                        _ptr(w2_scale), T, H, I, E, topk, int(bool(renormalize)),
+                                        ctypes.byref(rp) if rp else None, ctypes.byref(opts), _ptr(workspace),
+                                        workspace.numel(), _ptr(out), _stream(), arr)
     _check("moe_fp8_block_forward", rc)
     return out
 
@@ -336,7 +347,8 @@ def moe_fp8_block_masked_workspace_size(E, max_tokens, H, I) -> int:
     return int(lib().moe_fp8_block_masked_workspace_size(E, max_tokens, H, I))
 
 
-def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, out=None, workspace=None):
+def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, out=None, workspace=None,
+                                 scale_fmt="f32"):
     """Expert MLP on the masked batched layout: hidden bf16 [E, M, H] with counts int32 [E]
     (CUDA) valid rows per expert; returns bf16 [E, M, H] (rows past the counts not written)."""
     _cuda(hidden, torch.bfloat16, "hidden")
@@ -355,7 +367,8 @@ def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, o
     if workspace is None:
         workspace = _workspace(hidden.device, nbytes)
     rc = lib().moe_fp8_block_forward_masked(_ptr(hidden), _ptr(counts), _ptr(w13), _ptr(w13_scale), _ptr(w2),
-                                            _ptr(w2_scale), E, M, H, I, layout, _ptr(workspace), workspace.numel(),
+                                            _ptr(w2_scale), E, M, H, I, ctypes.byref(_ForwardOptions(layout,
+                                            SCALE_FMT[scale_fmt])), _ptr(workspace), workspace.numel(),
                                             _ptr(out), _stream())
     _check("moe_fp8_block_forward_masked", rc)
     return out

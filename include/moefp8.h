@@ -173,6 +173,21 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
 #define MOE_WEIGHTS_TILED 1   /* moe_fp8_block_pack_weights output */
 int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, void* stream);
 
+/* ---- scale formats ------------------------------------------------------------------
+ * Every 1x128 group and 128x128 block scale is max(amax, 1e-8)/448 in fp32 (MOE_SCALE_F32),
+ * or that value rounded up to a power of two (MOE_SCALE_UE8M0: the "FLOAT32_CEIL_UE8M0"
+ * format, fp32 scales rounded up to UE8M0, page "Quantization and MoE Optimizations",
+ * section DeepGEMM Scale Formats), so that each scale is exactly an 8-bit exponent.  The
+ * GEMMs take either (scales are fp32 values); the format decides how the activations and
+ * the requantised intermediate are scaled, and should match the weights'. */
+#define MOE_SCALE_F32 0
+#define MOE_SCALE_UE8M0 1
+/* fp8_group_quant / fp8_block_quant_weight with a scale format. */
+int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, int scale_fmt,
+                       void* stream);
+int fp8_block_quant_weight_ex(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
+                              void* stream);
+
 /* ---- grouped block-FP8 GEMM ------------------------------------------------------
  * For every tile m < *num_tiles (rows tile_row0[m] .. +127 of A, all routed to
  * expert e = tile_expert[m]) and every output column n:
@@ -230,6 +245,7 @@ typedef struct moe_gemm_epilogue {
     int64_t num_pairs;                /* MOE_EPI_WEIGHTED_SCATTER / _ROWS / _PAIRS_BF16: T*topk; other pair ids are skipped */
     uint16_t* out_bf16;               /* MOE_EPI_WEIGHTED_PAIRS_BF16 */
     int32_t b_layout;                 /* layout of B: MOE_WEIGHTS_NK (0) or MOE_WEIGHTS_TILED */
+    int32_t scale_fmt;                /* MOE_EPI_SILU_MUL_QUANT: scale format of the requantisation */
 } moe_gemm_epilogue;
 
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
@@ -292,20 +308,27 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
                                  const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
                                  uint16_t* out, void* stream);
 
-/* The same layer, recording CUDA events between its stages for per-stage timing
- * (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the
+/* Options of the layer: the expert weights' layout and the scale format of the activations
+ * and of the requantised intermediate (NULL options = MOE_WEIGHTS_NK, MOE_SCALE_F32). */
+typedef struct moe_forward_options {
+    int32_t weight_layout;            /* MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED */
+    int32_t scale_fmt;                /* MOE_SCALE_F32 or MOE_SCALE_UE8M0 */
+} moe_forward_options;
+
+/* The same layer with options, optionally recording CUDA events between its stages for
+ * per-stage timing (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the
  * caller, recorded on `stream` in this order: before routing, before the expert
  * sort, before the activation quantisation, before the w13 GEMM, before the w2
- * GEMM, before the weighted unpermute-sum, after it).  weight_layout:
- * MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED for w13 and w2.  Other arguments and errors
- * as moe_fp8_block_forward; events == NULL behaves exactly like it. */
+ * GEMM, before the weighted unpermute-sum, after it), with options (may be NULL).
+ * Other arguments and errors as moe_fp8_block_forward; events == NULL records none. */
 #define MOE_FORWARD_NUM_EVENTS 7
-int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_logits,
-                                 const uint8_t* w13, const float* w13_scale,
-                                 const uint8_t* w2, const float* w2_scale,
-                                 int T, int H, int I, int E, int topk, int renormalize,
-                                 const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
-                                 uint16_t* out, void* stream, int weight_layout, void* const* events);
+int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
+                             const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale,
+                             int T, int H, int I, int E, int topk, int renormalize,
+                             const moe_routing_params* rp, const moe_forward_options* opts,
+                             void* workspace, size_t workspace_bytes, uint16_t* out, void* stream,
+                             void* const* events);
 
 /* ---- the masked batched layout -----------------------------------------------------
  * The expert MLP on rows already grouped by expert: hidden [E, max_tokens, H] bf16 with
@@ -318,14 +341,14 @@ int moe_fp8_block_forward_events(const uint16_t* hidden, const float* router_log
  * dispatcher).  Rows i >= counts[e] of out are not written.
  * counts: device int32 [E], read on the device (no host synchronisation); a count
  * outside [0, max_tokens] is clamped and sets MOE_STATUS_BAD_COUNT.
- * w13, w2 in weight_layout (MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED); hidden, w13, w2, out
+ * opts (may be NULL): the weights' layout and the scale format; hidden, w13, w2, out
  * 16-byte aligned; workspace of moe_fp8_block_masked_workspace_size bytes, 256-byte
  * aligned.  H, I multiples of 128, E <= 1024.  max_tokens == 0 or E == 0 is a no-op. */
 size_t moe_fp8_block_masked_workspace_size(int E, int max_tokens, int H, int I);
 int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts,
                                  const uint8_t* w13, const float* w13_scale,
                                  const uint8_t* w2, const float* w2_scale,
-                                 int E, int max_tokens, int H, int I, int weight_layout,
+                                 int E, int max_tokens, int H, int I, const moe_forward_options* opts,
                                  void* workspace, size_t workspace_bytes, uint16_t* out, void* stream);
 
 /* ---- status -------------------------------------------------------------------- */

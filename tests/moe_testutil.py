@@ -42,8 +42,8 @@ class Layer:
     """Quantised weights of a workload on the GPU (GPU quantiser), plus the
     oracle's own quantisation of any subset of experts (from the same bf16)."""
 
-    def __init__(self, wl: mi.Workload, device="cuda", chunk=8):
-        self.wl, self.device = wl, device
+    def __init__(self, wl: mi.Workload, device="cuda", chunk=8, scale_fmt="f32"):
+        self.wl, self.device, self.scale_fmt = wl, device, scale_fmt
         E, H, I = wl.E, wl.H, wl.I
         self.w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=device)
         self.w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=device)
@@ -51,9 +51,9 @@ class Layer:
         self.w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=device)
         for e0 in range(0, E, chunk):
             ex = range(e0, min(E, e0 + chunk))
-            q, s = moe.fp8_block_quant_weight(mi.w13_bf16(wl, device, ex))
+            q, s = moe.fp8_block_quant_weight(mi.w13_bf16(wl, device, ex), scale_fmt)
             self.w13q[e0:e0 + len(ex)], self.w13s[e0:e0 + len(ex)] = q, s
-            q, s = moe.fp8_block_quant_weight(mi.w2_bf16(wl, device, ex))
+            q, s = moe.fp8_block_quant_weight(mi.w2_bf16(wl, device, ex), scale_fmt)
             self.w2q[e0:e0 + len(ex)], self.w2s[e0:e0 + len(ex)] = q, s
         torch.cuda.synchronize()
 
@@ -66,9 +66,12 @@ class Layer:
         w13s = np.zeros((E, 2 * I // 128, H // 128), dtype=np.float32)
         w2q = np.zeros((E, H, I), dtype=np.uint8)
         w2s = np.zeros((E, H // 128, I // 128), dtype=np.float32)
+        fmt = oracle.SCALE_UE8M0 if self.scale_fmt == "ue8m0" else oracle.SCALE_F32
         for e in experts:
-            w13q[e], w13s[e] = [a[0] for a in oracle.quant_128x128_bf16(mi.bf16_bits(mi.w13_bf16(wl, self.device, [e])))]
-            w2q[e], w2s[e] = [a[0] for a in oracle.quant_128x128_bf16(mi.bf16_bits(mi.w2_bf16(wl, self.device, [e])))]
+            w13q[e], w13s[e] = [a[0] for a in oracle.quant_128x128_bf16(
+                mi.bf16_bits(mi.w13_bf16(wl, self.device, [e])), fmt)]
+            w2q[e], w2s[e] = [a[0] for a in oracle.quant_128x128_bf16(
+                mi.bf16_bits(mi.w2_bf16(wl, self.device, [e])), fmt)]
         return w13q, w13s, w2q, w2s
 
     def forward(self, hidden, logits, rp, packed=False):
@@ -76,7 +79,7 @@ class Layer:
         if packed:
             w13, w2 = moe.moe_fp8_block_pack_weights(w13), moe.moe_fp8_block_pack_weights(w2)
         return moe.moe_fp8_block_forward(hidden, logits, w13, self.w13s, w2, self.w2s, self.wl.topk,
-                                         self.wl.renormalize, rp)
+                                         self.wl.renormalize, rp, scale_fmt=self.scale_fmt)
 
 
 def unpadded_rows(padded_offsets: np.ndarray, offsets: np.ndarray):
