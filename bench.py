@@ -52,6 +52,8 @@ def parse():
                    help="routed: the whole layer (default); masked: moe_fp8_block_forward_masked on rows "
                         "grouped by expert, counts from routing the workload's tokens")
     p.add_argument("--max-tokens", type=int, default=None, help="masked layout: rows per expert (default: max count)")
+    p.add_argument("--scale-fmt", choices=["f32", "ue8m0"], default="f32",
+                   help="block scales: fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)")
     p.add_argument("--weights", choices=["tiled", "nk"], default="tiled",
                    help="expert weight layout: tile-packed at load time (default) or the pages' [E, N, K]")
     return p.parse_args()
@@ -81,8 +83,9 @@ def describe(wl, world):
 
 
 def describe_weights(args):
+    fmt = ", scales rounded up to powers of two (ue8m0)" if args.scale_fmt == "ue8m0" else ", fp32 scales"
     return ("e4m3 128x128 blocks, tile-packed at load time (moe_fp8_block_pack_weights)"
-            if args.weights == "tiled" else "e4m3 128x128 blocks, [E, N, K] layout")
+            if args.weights == "tiled" else "e4m3 128x128 blocks, [E, N, K] layout") + fmt
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -273,8 +276,8 @@ def run_ours(args, wl):
     w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
     for e0 in range(0, E, 8):
         ex = range(e0, min(E, e0 + 8))
-        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex))
-        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex))
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), args.scale_fmt)
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), args.scale_fmt)
     if args.weights == "tiled":
         # load-time conversion into the kernels' tile-packed layout (untimed, like the quantisation)
         w13q = moe.moe_fp8_block_pack_weights(w13q)
@@ -289,7 +292,7 @@ def run_ours(args, wl):
 
     def step(events=None):
         moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
-                                  workspace=ws, events=events)
+                                  workspace=ws, events=events, scale_fmt=args.scale_fmt)
 
     def barrier():
         if dist:
@@ -373,7 +376,7 @@ def run_ours(args, wl):
             if i >= nbuf:
                 comp.wait_event(d2h_done[b])            # output buffer b was downloaded
             moe.moe_fp8_block_forward(hid_d[b], log_d[b], w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp,
-                                      out=out_d[b], workspace=ws)
+                                      out=out_d[b], workspace=ws, scale_fmt=args.scale_fmt)
             fwd_done[b].record(comp)
             with torch.cuda.stream(down):
                 down.wait_event(fwd_done[b])
@@ -481,15 +484,16 @@ def run_masked(args, wl):
     w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
     for e0 in range(0, E, 8):
         ex = range(e0, min(E, e0 + 8))
-        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex))
-        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex))
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), args.scale_fmt)
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), args.scale_fmt)
     w13p, w2p = (moe.moe_fp8_block_pack_weights(w13q), moe.moe_fp8_block_pack_weights(w2q)) \
         if args.weights == "tiled" else (w13q, w2q)
     out = torch.empty(E, M, H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(moe.moe_fp8_block_masked_workspace_size(E, M, H, I), dtype=torch.uint8, device=dev)
 
     def step():
-        moe.moe_fp8_block_forward_masked(hidden, counts, w13p, w13s, w2p, w2s, out=out, workspace=ws)
+        moe.moe_fp8_block_forward_masked(hidden, counts, w13p, w13s, w2p, w2s, out=out, workspace=ws,
+                                         scale_fmt=args.scale_fmt)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
