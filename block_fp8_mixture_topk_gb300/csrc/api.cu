@@ -333,6 +333,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
     GemmArgs g{};
+    g.a_box_rows = 128;
     g.A = A;
     g.a_scale = a_scale;
     g.as_row_stride = a_scale_row_stride;
@@ -461,6 +462,9 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     float* a2s = reinterpret_cast<float*>(ws + L.a2s);
     uint16_t* ypairs = reinterpret_cast<uint16_t*>(ws + L.y);
     const int64_t P = static_cast<int64_t>(T) * topk;
+    // an expert holds at most T rows: with T <= 32 only the first 32 rows of a tile can be
+    // real, so the GEMMs load 32-row activation boxes
+    const int a_box_rows = T <= 32 ? 32 : 128;
 
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
@@ -493,6 +497,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
         GemmArgs g{};
+        g.a_box_rows = a_box_rows;
         g.A = a1;
         g.a_scale = a1s;
         g.as_row_stride = 1;
@@ -521,6 +526,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (e == cudaSuccess) e = mark(4);
     if (e == cudaSuccess) {
         GemmArgs g{};
+        g.a_box_rows = a_box_rows;
         g.A = a2;
         g.a_scale = a2s;
         g.as_row_stride = 1;
@@ -600,6 +606,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     if (e == cudaSuccess) e = launch_group_quant(hidden, EM, H, H, a1, H, a1s, 1, L.rows, pos, 1, scale_fmt, s);
     if (e == cudaSuccess) {
         GemmArgs g{};
+        g.a_box_rows = max_tokens <= 32 ? 32 : 128;   // no expert has more rows than max_tokens
         g.A = a1;
         g.a_scale = a1s;
         g.as_row_stride = 1;
@@ -628,6 +635,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     if (e == cudaSuccess) {
         // one "pair" per input row: unit weight, written to the row's place in out
         GemmArgs g{};
+        g.a_box_rows = max_tokens <= 32 ? 32 : 128;   // no expert has more rows than max_tokens
         g.A = a2;
         g.a_scale = a2s;
         g.as_row_stride = 1;

@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     bdx = BK;
                     bdy = 0;
                 }
-                const uint32_t bytes = A_TILE + (t.has1 ? B_TILE : B_HALF);
+                // decode tiles (a_box_rows = 32): only the first 32 rows of A hold real rows;
+                // the MMA reads whatever rows 32..127 of the stage hold, for padding rows only
+                const uint32_t bytes = a.a_box_rows * BK + (t.has1 ? B_TILE : B_HALF);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
                         ok = false;
@@ -530,11 +532,12 @@ cudaError_t get_encoder() {
     return g_encode ? cudaSuccess : cudaErrorNotSupported;
 }
 
-// 2-D e4m3 matrix [rows, cols] (row stride = cols bytes), 128x128 boxes, 128-byte swizzle
-cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows) {
+// 2-D e4m3 matrix [rows, cols] (row stride = cols bytes), boxes of 128 bytes x box_rows rows,
+// 128-byte swizzle
+cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows, uint32_t box_rows = 128) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t elem[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box, elem,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -570,7 +573,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     const int64_t bound = args.max_tiles * NT;
     if (bound == 0) return cudaSuccess;
     CUtensorMap tmA, tmB;
-    cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows);
+    if (args.a_box_rows != 32 && args.a_box_rows != 128) return cudaErrorInvalidValue;
+    cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows, static_cast<uint32_t>(args.a_box_rows));
     if (err != cudaSuccess) return err;
     if (args.b_tiled)   // [E][N/128][K/128] blocks of 128 rows x 128 bytes, stacked
         err = make_map(&tmB, args.B, 128, static_cast<int64_t>(args.E) * args.N * (args.K / 128));

@@ -81,6 +81,7 @@ struct GemmArgs {
     const float* a_scale;
     int64_t as_row_stride, as_kb_stride;
     int64_t a_rows;
+    int a_box_rows;            // rows of A loaded per tile: 128, or 32 when no tile has real rows past 32
     const uint8_t* B;
     int b_tiled;               // B in the tile-packed layout (moe_fp8_block_pack_weights)
     const float* b_scale;

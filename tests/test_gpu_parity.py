@@ -586,6 +586,48 @@ def test_forward_all_tokens_to_one_expert():
     assert_output_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3_decode", 8), ("mixtral", None)])
+def test_forward_replays_from_a_cuda_graph(name, T):
+    """The whole layer captured once in a CUDA graph (its kernels linked by programmatic
+    dependent launch) and replayed on new inputs copied into the captured buffers: every
+    replay equals the eager forward on those inputs, bit for bit."""
+    wl = workload(name, T)
+    layer = Layer(wl)
+    rp, _ = routing_of(wl)
+    hid = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    log = torch.empty(wl.T, wl.E, dtype=torch.float32, device=DEV)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8,
+                     device=DEV)
+    hid.copy_(mi.hidden(wl).to(DEV))
+    log.copy_(mi.router_logits(wl).to(DEV))
+
+    def step():
+        moe.moe_fp8_block_forward(hid, log, layer.w13q, layer.w13s, layer.w2q, layer.w2s, wl.topk,
+                                  wl.renormalize, rp, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in range(3):
+        wl_s = wl.with_(number=wl.number + 500 + seed)
+        h, l = mi.hidden(wl_s).to(DEV), mi.router_logits(wl_s).to(DEV)
+        hid.copy_(h)
+        log.copy_(l)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        want = moe.moe_fp8_block_forward(h, l, layer.w13q, layer.w13s, layer.w2q, layer.w2s, wl.topk,
+                                         wl.renormalize, rp)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+
+
 def test_forward_zero_tokens_is_noop():
     wl = mi.WORKLOADS["tiny"]
     layer = Layer(wl)
