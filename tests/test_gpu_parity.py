@@ -573,6 +573,21 @@ def test_forward_sort_path_boundaries(T, H, I, E, topk):
     assert_output_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("name,T", [("dsv3_decode", 1), ("dsv3_decode", 2), ("mixtral", 1)])
+def test_forward_one_and_two_token_batches(name, T):
+    """One or two tokens (each expert's tile holds one or two real rows, 32-row activation
+    boxes, fewer GEMM items than SMs): every token matches the oracle."""
+    wl = workload(name, T)
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
+def test_forward_two_tokens_small_shape():
+    wl = mi.Workload("twotok", 81, 2, 256, 512, 6, 3)
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
 def test_forward_all_tokens_to_one_expert():
     """300 tokens, top-1, every token on expert 2: three tiles of one expert, the other experts empty."""
     wl = mi.Workload("skew", 77, 300, 256, 256, 4, 1)
@@ -586,7 +601,8 @@ def test_forward_all_tokens_to_one_expert():
     assert_output_close(out, ref["out"])
 
 
-@pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3_decode", 8), ("mixtral", None)])
+@pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3_decode", 8), ("mixtral", None), ("dsv3_decode", 1),
+                                    ("dsv3_decode", 2)])
 def test_forward_replays_from_a_cuda_graph(name, T):
     """The whole layer captured once in a CUDA graph (its kernels linked by programmatic
     dependent launch) and replayed on new inputs copied into the captured buffers: every
