@@ -109,3 +109,41 @@ def test_forward_rejects_bad_arguments_on_host():
     # workspace too small
     assert L.moe_fp8_block_forward(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.c_void_p(0x10000), 16, p,
                                    None) == -3
+
+
+def test_newer_entry_points_reject_bad_arguments_on_host():
+    """Options, scale formats, packing, the pair sum and the masked layout: argument errors are
+    returned before anything touches a device."""
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    big = ctypes.c_void_p(0x100000)
+    # forward options: unknown weight layout / scale format
+    for layout, fmt in [(7, 0), (0, 5)]:
+        opts = ops._ForwardOptions(layout, fmt)
+        assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                          1 << 30, p, None, None) == -1
+    # quantisers: unknown scale format
+    assert L.fp8_group_quant_ex(p, 4, 128, 128, p, p, 3, None) == -1
+    assert L.fp8_block_quant_weight_ex(p, 1, 128, 128, p, p, 3, None) == -1
+    # packing: N not a multiple of 128; in place; empty is a no-op
+    assert L.moe_fp8_block_pack_weights(p, 1, 100, 128, big, None) == -2
+    assert L.moe_fp8_block_pack_weights(big, 2, 128, 128, ctypes.c_void_p(0x100000 + 4096), None) == -1
+    assert L.moe_fp8_block_pack_weights(None, 0, 128, 128, None, None) == 0
+    # pair sum: H not a multiple of 8
+    assert L.moe_combine_pairs(p, p, 4, 2, 100, p, None) == -2
+    # grouped GEMM: unknown weight layout / scale format in the epilogue options
+    ep = ops._Epilogue(0, 1, p, None, None, 0, 0, None, None, 0, None, 4, 0)
+    assert L.fp8_block_grouped_gemm(p, p, 1, 1, 128, p, p, 256, 128, 1, p, p, p, 1, ctypes.byref(ep), None) == -1
+    ep = ops._Epilogue(0, 1, p, None, None, 0, 0, None, None, 0, None, 0, 9)
+    assert L.fp8_block_grouped_gemm(p, p, 1, 1, 128, p, p, 256, 128, 1, p, p, p, 1, ctypes.byref(ep), None) == -1
+    # masked layout
+    ws = moe.moe_fp8_block_masked_workspace_size(4, 16, 256, 256)
+    assert ws > 0
+    assert L.moe_fp8_block_forward_masked(p, p, p, p, p, p, 4, 16, 100, 256, None, big, ws, p, None) == -2
+    assert L.moe_fp8_block_forward_masked(p, p, p, p, p, p, 2048, 16, 256, 256, None, big, 1 << 40, p, None) == -2
+    assert L.moe_fp8_block_forward_masked(p, p, p, p, p, p, 4, 16, 256, 256, None, big, ws - 256, p, None) == -3
+    bad = ops._ForwardOptions(3, 0)
+    assert L.moe_fp8_block_forward_masked(p, p, p, p, p, p, 4, 16, 256, 256, ctypes.byref(bad), big, ws, p,
+                                          None) == -1
+    assert L.moe_fp8_block_forward_masked(None, None, None, None, None, None, 0, 16, 256, 256, None, None, 0, None,
+                                          None) == 0
