@@ -33,8 +33,14 @@ import torch  # noqa: E402
 import moe_inputs as mi  # noqa: E402
 
 FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
-PROFILE = os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md")
-GEMM_SOURCES = [os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc", f) for f in ("gemm.cu", "common.cuh")]
+CSRC = os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc")
+# ncu summary of each w13 kernel and the sources it was taken on: tile GEMM, decode-path GEMM
+PROFILES = {
+    False: (os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md"),
+            [os.path.join(CSRC, f) for f in ("gemm.cu", "common.cuh")]),
+    True: (os.path.join(ROOT, "profiles", "decode_w13_dsv3_decode.md"),
+           [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
+}
 
 
 def parse():
@@ -54,6 +60,9 @@ def parse():
     p.add_argument("--max-tokens", type=int, default=None, help="masked layout: rows per expert (default: max count)")
     p.add_argument("--scale-fmt", choices=["f32", "ue8m0"], default="f32",
                    help="block scales: fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)")
+    p.add_argument("--decode", choices=["auto", "off", "on"], default="auto",
+                   help="expert GEMMs of small steps: decode-path kernels for up to 8 tokens (auto), never, "
+                        "or whenever the step qualifies")
     p.add_argument("--weights", choices=["tiled", "nk"], default="tiled",
                    help="expert weight layout: tile-packed at load time (default) or the pages' [E, N, K]")
     return p.parse_args()
@@ -224,24 +233,27 @@ def run_reference(args, wl):
 
 
 # ----------------------------------------------------------------------------- ours (GPU)
-def gemm_source_sha():
+def gemm_source_sha(decode=False):
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in PROFILES[decode][1]:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(wl):
-    """dram bytes per launch of the w13 GEMM from the committed ncu summary, if it was taken
-    on the current kernel source for this workload; else None."""
-    if not os.path.exists(PROFILE):
+def profiled_traffic(wl, decode=False):
+    """dram bytes per launch of the w13 GEMM (tile or decode-path kernel) from the committed ncu
+    summary, if it was taken on the current kernel source for this workload; else None."""
+    path = PROFILES[decode][0]
+    if not os.path.exists(path):
         return None
     kv = {}
-    for line in open(PROFILE):
+    for line in open(path):
         if "=" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split("=", 1)
             kv[k.strip()] = v.strip().strip("`")
-    if kv.get("source_sha") != gemm_source_sha() or kv.get("workload") != wl.name:
+    if kv.get("source_sha") != gemm_source_sha(decode) or kv.get("workload") != wl.name:
+        return None
+    if "tokens" in kv and kv["tokens"] != str(wl.T):
         return None
     try:
         return float(kv["dram_bytes_per_launch_full"])
@@ -289,10 +301,11 @@ def run_ours(args, wl):
     ids, _ = moe.moe_route_topk(logits, wl.topk, wl.renormalize, rp)
     touched = int(torch.unique(ids).numel())
     P = wl.P
+    decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode)
 
     def step(events=None):
         moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
-                                  workspace=ws, events=events, scale_fmt=args.scale_fmt)
+                                  workspace=ws, events=events, scale_fmt=args.scale_fmt, decode=args.decode)
 
     def barrier():
         if dist:
@@ -376,7 +389,7 @@ def run_ours(args, wl):
             if i >= nbuf:
                 comp.wait_event(d2h_done[b])            # output buffer b was downloaded
             moe.moe_fp8_block_forward(hid_d[b], log_d[b], w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp,
-                                      out=out_d[b], workspace=ws, scale_fmt=args.scale_fmt)
+                                      out=out_d[b], workspace=ws, scale_fmt=args.scale_fmt, decode=args.decode)
             fwd_done[b].record(comp)
             with torch.cuda.stream(down):
                 down.wait_event(fwd_done[b])
@@ -424,10 +437,11 @@ def run_ours(args, wl):
         roof = {"bound": "hbm", "achieved": gemm_bytes / (g_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)"
+    roof["kernel"] = ("decode_gemm_kernel<silu> (w13 GEMM, decode path)" if decode
+                      else "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)")
     roof["algorithmic_bytes_per_launch"] = gemm_bytes
     roof["ms_per_launch"] = g_ms
-    roof["traffic"] = profiled_traffic(wl)
+    roof["traffic"] = profiled_traffic(wl, decode)
 
     line = {"metric": "block-FP8 fused-MoE tokens/s", "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -438,7 +452,7 @@ def run_ours(args, wl):
             "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
             "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,
             "ms_per_step_eager": eager_ms, "ms_per_step_graph": graph_ms, "launch": launch,
-            "experts_touched": touched, "weight_bytes_touched": touched * per_expert,
+            "experts_touched": touched, "weight_bytes_touched": touched * per_expert, "decode_path": decode,
             "stage_ms": stage_ms, "clocks": clk,
             "e2e": {"value": whole_job_rate(world, wl.T, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,

@@ -41,7 +41,8 @@ int device_state(DeviceState** out) {
         } else {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || route_init_device() != cudaSuccess ||
-                permute_init_device() != cudaSuccess || gemm_init_device() != cudaSuccess) {
+                permute_init_device() != cudaSuccess || gemm_init_device() != cudaSuccess ||
+                decode_init_device() != cudaSuccess) {
                 cudaGetLastError();
                 return MOE_ERR_CUDA;
             }
@@ -81,9 +82,29 @@ int64_t max_rows(int64_t P, int64_t E, int64_t bm) {
 }
 
 struct ForwardLayout {
-    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, y, total;
+    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, y, dh, dcnt, dtab,
+        total;
     int64_t rows, tiles;
+    int64_t dcnt_n;   // decode-path group counters (0: the step cannot take the decode path)
 };
+
+// Steps of up to this many tokens take the decode-path GEMMs by default (MOE_DECODE_AUTO); 0
+// while the tile GEMMs are as fast for every step size.
+constexpr int kDecodeAutoMaxTokens = 0;
+
+// Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
+// rows per expert), a sort small enough for the one-launch prologue (which writes the decode
+// path's tile records and zeroes its counters), an expert's w13 under 2^31 bytes (the
+// kernels' 32-bit row offsets) and tile records that fit a CTA's shared memory.
+bool decode_possible(int T, int H, int I, int topk) {
+    const int64_t P = static_cast<int64_t>(T) * topk;
+    return T > 0 && decode_cols(T) > 0 && P <= kSmallPairs && static_cast<int64_t>(2) * I * H < (int64_t(1) << 31) &&
+           static_cast<size_t>(P) <= decode_max_tiles();   // at most one tile per routed pair
+}
+bool use_decode(int T, int H, int I, int topk, int mode) {
+    if (!decode_possible(T, H, I, topk) || mode == MOE_DECODE_OFF) return false;
+    return mode == MOE_DECODE_ON || T <= kDecodeAutoMaxTokens;
+}
 
 ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     ForwardLayout L;
@@ -112,6 +133,12 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
     L.y = take(static_cast<size_t>(P) * H * 2);
+    // decode path: h = silu(gate) * up by pair [P, I] fp32, the per-(tile, group) counters and
+    // the tile records
+    L.dcnt_n = decode_possible(T, H, I, topk) ? L.tiles * (I / 128) : 0;
+    L.dh = take(L.dcnt_n ? static_cast<size_t>(P) * I * 4 : 0);
+    L.dcnt = take(static_cast<size_t>(L.dcnt_n) * 4);
+    L.dtab = take(L.dcnt_n ? static_cast<size_t>(L.tiles) * sizeof(DecodeTile) : 0);
     L.total = off;
     return L;
 }
@@ -396,6 +423,12 @@ int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
     return 1 + (P <= kSmallPairs ? 1 : 4) + 2 + 1;
 }
 
+int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode) {
+    if (T < 0 || H < 0 || I < 0 || topk < 1) return -1;
+    if (mode != MOE_DECODE_AUTO && mode != MOE_DECODE_OFF && mode != MOE_DECODE_ON) return -1;
+    return use_decode(T, H, I, topk, mode) ? 1 : 0;
+}
+
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk) {
     if (T < 0 || H < 0 || I < 0 || E < 1 || topk < 1) return 0;
     return forward_layout(T, H, I, E, topk).total;
@@ -413,7 +446,7 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
                                  const float* w13_scale, const uint8_t* w2, const float* w2_scale, int T, int H,
                                  int I, int E, int topk, int renormalize, const moe_routing_params* rp,
                                  void* workspace, size_t workspace_bytes, uint16_t* out, void* stream) {
-    const moe_forward_options opts{MOE_WEIGHTS_TILED, MOE_SCALE_F32};
+    const moe_forward_options opts{MOE_WEIGHTS_TILED, MOE_SCALE_F32, MOE_DECODE_AUTO};
     return moe_fp8_block_forward_ex(hidden, router_logits, w13, w13_scale, w2, w2_scale, T, H, I, E, topk,
                                     renormalize, rp, &opts, workspace, workspace_bytes, out, stream, nullptr);
 }
@@ -427,8 +460,11 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (rc != MOE_OK) return rc;
     const int weight_layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
     const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
+    const int decode_mode = opts ? opts->decode_path : MOE_DECODE_AUTO;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
     if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+    if (decode_mode != MOE_DECODE_AUTO && decode_mode != MOE_DECODE_OFF && decode_mode != MOE_DECODE_ON)
+        return MOE_ERR_INVALID_ARG;
     if (weight_layout == MOE_WEIGHTS_TILED &&
         static_cast<int64_t>(E) * 2 * I * (H / 128) >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -480,10 +516,15 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     // quantisation stage is then empty); larger ones by the three sort kernels and the
     // grid-wide quantiser
     const bool small = P <= kSmallPairs;
+    const bool decode = use_decode(T, H, I, topk, decode_mode);
+    int32_t* dcnt = reinterpret_cast<int32_t*>(ws + L.dcnt);
+    DecodeTile* dtab = reinterpret_cast<DecodeTile*>(ws + L.dtab);
+    DecodeSetup dsetup{};
+    if (decode) dsetup = DecodeSetup{dtab, wts, dcnt, static_cast<int>(L.dcnt_n)};
     if (e == cudaSuccess && small)
         e = launch_sort_quant_small(ids, static_cast<int>(P), E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                     reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
-                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, scale_fmt, s);
+                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, scale_fmt, dsetup, s);
     if (e == cudaSuccess && !small)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
@@ -495,7 +536,46 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (e == cudaSuccess && !small)
         e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, scale_fmt, s);
     if (e == cudaSuccess) e = mark(3);
-    if (e == cudaSuccess) {
+    if (decode) {
+        // up to 8 rows per expert: weight-streaming items of 32 weight rows (decode.cu); the
+        // requantised intermediate goes to the a2 / a2s regions at the padded rows, as in the
+        // tile path
+        DecodeGemmArgs d{};
+        d.w_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        d.E = E;
+        d.tiles = dtab;
+        d.num_tiles = ntiles;
+        d.max_tiles = static_cast<int>(L.tiles);
+        d.cols = decode_cols(T);
+        d.status = st->status;
+        DecodeGemmArgs d1 = d;
+        d1.W = w13;
+        d1.w_scale = w13_scale;
+        d1.N = 2 * I;
+        d1.K = H;
+        d1.act = a1;
+        d1.act_scale = a1s;
+        d1.rows = L.rows;
+        d1.h = reinterpret_cast<float*>(ws + L.dh);
+        d1.group_count = dcnt;
+        d1.out_q = a2;
+        d1.out_scale = a2s;
+        d1.scale_fmt = scale_fmt;
+        if (e == cudaSuccess) e = launch_decode_gemm(d1, true, st->num_sms, s);
+        if (e == cudaSuccess) e = mark(4);
+        DecodeGemmArgs d2 = d;
+        d2.W = w2;
+        d2.w_scale = w2_scale;
+        d2.N = H;
+        d2.K = I;
+        d2.act = a2;
+        d2.act_scale = a2s;
+        d2.rows = L.rows;
+        d2.y = ypairs;
+        if (e == cudaSuccess) e = launch_decode_gemm(d2, false, st->num_sms, s);
+        if (e == cudaSuccess) e = mark(5);
+    }
+    if (e == cudaSuccess && !decode) {
         GemmArgs g{};
         g.a_box_rows = a_box_rows;
         g.A = a1;
@@ -522,9 +602,9 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.os_kb_stride = L.rows;
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
+        if (e == cudaSuccess) e = mark(4);
     }
-    if (e == cudaSuccess) e = mark(4);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && !decode) {
         GemmArgs g{};
         g.a_box_rows = a_box_rows;
         g.A = a2;
@@ -550,8 +630,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.num_pairs = P;
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
+        if (e == cudaSuccess) e = mark(5);
     }
-    if (e == cudaSuccess) e = mark(5);
     if (e == cudaSuccess) e = launch_combine_pairs(ypairs, pos, T, topk, H, out, s);
     if (e == cudaSuccess) e = mark(6);
     return cuda_rc(e);

@@ -547,6 +547,40 @@ cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t
 
 }  // namespace
 
+cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
+                             const uint64_t* strides, const uint32_t* box) {
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], elem[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        elem[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<uint8_t*>(ptr),
+                          d, st, b, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_u8_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows, uint32_t box_cols,
+                          uint32_t box_rows, bool swizzle128) {
+    cudaError_t err = get_encoder();
+    if (err != cudaSuccess) return err;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box, elem,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t gemm_init_device() {
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;

@@ -42,13 +42,32 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
                                  int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
                                  int32_t* chunk_counts, uint32_t* status, cudaStream_t stream);
 
-// prologue.cu: expert sort + scattering quantisation of a small batch in one block
+// Per-expert-tile record of a decode step (at most kDecodeCols rows per expert, so one tile per
+// expert), written by the small-batch sort and read by the decode-path GEMMs: the tile's
+// expert, its first padded row, its routed rows and, for row j < cnt, the pair index and its
+// router weight (-1 and 0 from cnt on).
+constexpr int kDecodeCols = 8;
+struct DecodeTile {
+    int32_t e, poff, cnt, pad;
+    int32_t pair[kDecodeCols];
+    float weight[kDecodeCols];
+};
+// What the small-batch sort also writes for the decode path (tiles == nullptr: nothing).
+struct DecodeSetup {
+    DecodeTile* tiles;           // [max_tiles]
+    const float* topk_weights;   // [P]
+    int32_t* counters;           // zeroed: the w13 decode GEMM's group counters
+    int ncounters;
+};
+
+// prologue.cu: expert sort + scattering quantisation of a small batch in one launch, and the
+// decode path's tile records
 constexpr int kSmallPairs = 512;   // routed pairs the one-block path takes
 cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_m, int32_t* expert_offsets,
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream);
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec, cudaStream_t stream);
 
 // masked.cu: row maps and tile table of the masked batched layout [E, M, H] (Mp = M rounded
 // up to 128): row_map [E*Mp] (input row or -1), pos [E*M] (padded row or -1), ones [E*M]
@@ -104,6 +123,47 @@ struct GemmArgs {
     uint32_t* status;
 };
 cudaError_t gemm_init_device();
+// Tensor map of a 2-D byte matrix [rows, cols] (row stride = cols bytes), boxes of
+// box_cols x box_rows, with the 128-byte swizzle or none.
+cudaError_t encode_u8_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows, uint32_t box_cols,
+                          uint32_t box_rows, bool swizzle128);
+// Tensor map of a byte tensor of `rank` dimensions (dims[0] innermost; strides[i] = bytes between
+// consecutive indices of dimension i+1), boxes `box`, no swizzle.
+cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
+                             const uint64_t* strides, const uint32_t* box);
+
+// decode.cu: the two expert GEMMs of a step with at most 8 rows per expert, as weight-streaming
+// work items of 32 weight rows (see decode.cu)
+struct DecodeGemmArgs {
+    const uint8_t* W;          // expert weights, [E, N, K] or tile-packed
+    int w_tiled;
+    const float* w_scale;      // [E, N/128, K/128]
+    int N, K, E;
+    const uint8_t* act;        // activation codes [rows, K]: a tile's j-th row at padded row poff + j
+    const float* act_scale;    // their scales, [K/128][rows]
+    int64_t rows;
+    const DecodeTile* tiles;   // [max_tiles] (the small-batch sort's records)
+    const int32_t* num_tiles;
+    int max_tiles;
+    int cols;                  // the most routed rows an expert can hold, 1..8 (decode_cols: min(T, 8))
+    // w13 (SiLU): h [P, N/2] fp32 by pair, per-(tile, group) counters [max_tiles, N/256] (zero
+    // on entry), requantised codes [rows, N/2] and scales [N/256][rows] at the padded rows
+    float* h;
+    int32_t* group_count;
+    uint8_t* out_q;
+    float* out_scale;
+    int scale_fmt;
+    // w2: y [P, N] bf16 = router weight * C in pair order
+    uint16_t* y;
+    uint32_t* status;
+};
+// the most rows an expert holds in a step of T tokens, as the decode kernels take it (0: T too
+// large for them)
+int decode_cols(int T);
+// tile records a decode GEMM CTA can hold in shared memory
+size_t decode_max_tiles();
+cudaError_t decode_init_device();
+cudaError_t launch_decode_gemm(const DecodeGemmArgs& args, bool silu, int num_sms, cudaStream_t stream);
 
 // api.cu: once-per-device set-up; on MOE_OK, *status = the device status word's address
 int device_status_word(uint32_t** status);

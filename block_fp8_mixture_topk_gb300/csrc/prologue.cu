@@ -11,7 +11,10 @@
 // same, element for element: per-expert counts, exclusive scans, the stable order by
 // (expert, pair) -- a pair's rank is the number of earlier pairs with its expert,
 // counted, so no atomics -- the tile table, and the codes and scales.  In a decode step
-// this removes three launches and the gaps between them.
+// this removes three launches and the gaps between them.  For the decode-path GEMMs it also
+// writes one record per expert tile (expert, first row, rows, their pairs and router
+// weights), so that those kernels read everything about a tile in one load, and zeroes their
+// group counters.
 #include "kernels.cuh"
 
 namespace mfp8 {
@@ -23,7 +26,7 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles,
     uint32_t* status, const uint16_t* __restrict__ x, int T, int H, int topk, uint8_t* __restrict__ q,
-    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt) {
+    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec) {
     grid_dependency_wait();
     __shared__ int s_id[kSmallPairs];
     __shared__ int s_pos[kSmallPairs];
@@ -50,6 +53,8 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     const int off = block_exclusive_scan(total, warp_sums);
     const int poff = block_exclusive_scan(padded, warp_sums);
     const bool writer = blockIdx.x == 0;
+    if (writer)
+        for (int i = tid; i < dec.ncounters; i += blockDim.x) dec.counters[i] = 0;
     if (tid < E) s_poff[tid] = poff;
     if (writer && tid < E) {
         expert_offsets[tid] = off;
@@ -64,6 +69,18 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
             tile_row0[i] = i * block_m;
         }
         for (int r = poff + total; r < poff + padded; ++r) sorted_pair_ids[r] = -1;
+        if (dec.tiles && total > 0) {
+            // the decode path takes at most kDecodeCols rows per expert: one tile each
+            DecodeTile& dt = dec.tiles[poff / block_m];
+            dt.e = tid;
+            dt.poff = poff;
+            dt.cnt = total;
+            dt.pad = 0;
+            for (int j = total; j < kDecodeCols; ++j) {
+                dt.pair[j] = -1;
+                dt.weight[j] = 0.0f;
+            }
+        }
     }
     __syncthreads();
 
@@ -76,6 +93,11 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
             for (int o = 0; o < p; ++o) before += s_id[o] == id ? 1 : 0;
             r = s_poff[id] + before;
             if (writer) sorted_pair_ids[r] = p;
+            if (writer && dec.tiles && before < kDecodeCols) {
+                DecodeTile& dt = dec.tiles[s_poff[id] / block_m];
+                dt.pair[before] = p;
+                dt.weight[before] = dec.topk_weights[p];
+            }
         }
         if (writer) pos[p] = r;
         s_pos[p] = r;
@@ -121,14 +143,15 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream) {
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec,
+                                    cudaStream_t stream) {
     const int groups = T * (H / 128);
     int blocks = (groups + 63) / 64;
     if (blocks < 1) blocks = 1;
     if (blocks > 148) blocks = 148;
     return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
                       padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
-                      q, q_ld, s, s_rs, s_gs, scale_fmt);
+                      q, q_ld, s, s_rs, s_gs, scale_fmt, dec);
 }
 
 }  // namespace mfp8

@@ -46,7 +46,11 @@ class _Epilogue(ctypes.Structure):
 
 
 class _ForwardOptions(ctypes.Structure):
-    _fields_ = [("weight_layout", ctypes.c_int32), ("scale_fmt", ctypes.c_int32)]
+    _fields_ = [("weight_layout", ctypes.c_int32), ("scale_fmt", ctypes.c_int32), ("decode_path", ctypes.c_int32)]
+
+
+# MOE_DECODE_*: which kernels run the expert GEMMs of a small step
+DECODE_PATH = {"auto": 0, "off": 1, "on": 2}
 
 
 @dataclasses.dataclass
@@ -94,6 +98,7 @@ def lib():
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward_kernel_count": ([I, I, I, I, I], I),
+                "moe_fp8_block_decode_path": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P, P, P], I),
@@ -278,6 +283,14 @@ def moe_combine_pairs(y, pos, T, topk, out=None):
     return out
 
 
+def moe_fp8_block_decode_path(T, H, I, topk, decode="auto") -> bool:
+    """Whether a step of T tokens takes the decode-path GEMMs under `decode` (auto / off / on)."""
+    r = int(lib().moe_fp8_block_decode_path(T, H, I, topk, DECODE_PATH[decode]))
+    if r < 0:
+        raise ValueError(f"moe_fp8_block_decode_path({T}, {H}, {I}, {topk}, {decode!r})")
+    return bool(r)
+
+
 def moe_fp8_block_forward_kernel_count(T, H, I, E, topk) -> int:
     """Kernels one moe_fp8_block_forward launches for these sizes."""
     return int(lib().moe_fp8_block_forward_kernel_count(T, H, I, E, topk))
@@ -304,10 +317,11 @@ FORWARD_STAGES = ("route", "sort", "quant", "gemm_w13", "gemm_w2", "unpermute_su
 
 def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
                           routing: RoutingParams | None = None, out=None, workspace=None, events=None,
-                          scale_fmt="f32"):
+                          scale_fmt="f32", decode="auto"):
     """The whole layer: returns bf16 [T, H] (written into `out` when given).
 
     w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D).
+    decode: "auto", "off" or "on" -- the decode-path GEMMs for small steps (MOE_DECODE_*).
     events: optional list of 7 torch.cuda.Event recorded between the stages
     (FORWARD_STAGES) on the current stream, for per-stage timing."""
     _cuda(hidden, torch.bfloat16, "hidden")
@@ -326,7 +340,7 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     if workspace is None:
         workspace = _workspace(hidden.device, nbytes)
     rp = routing.to_c() if routing else None
-    opts = _ForwardOptions(layout, SCALE_FMT[scale_fmt])
+    opts = _ForwardOptions(layout, SCALE_FMT[scale_fmt], DECODE_PATH[decode])
     arr = None
     if events is not None:
         if len(events) != len(FORWARD_STAGES) + 1:
@@ -368,7 +382,7 @@ def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, o
         workspace = _workspace(hidden.device, nbytes)
     rc = lib().moe_fp8_block_forward_masked(_ptr(hidden), _ptr(counts), _ptr(w13), _ptr(w13_scale), _ptr(w2),
                                             _ptr(w2_scale), E, M, H, I, ctypes.byref(_ForwardOptions(layout,
-                                            SCALE_FMT[scale_fmt])), _ptr(workspace), workspace.numel(),
+                                            SCALE_FMT[scale_fmt], 0)), _ptr(workspace), workspace.numel(),
                                             _ptr(out), _stream())
     _check("moe_fp8_block_forward_masked", rc)
     return out

@@ -308,11 +308,33 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
                                  const moe_routing_params* rp, void* workspace, size_t workspace_bytes,
                                  uint16_t* out, void* stream);
 
-/* Options of the layer: the expert weights' layout and the scale format of the activations
- * and of the requantised intermediate (NULL options = MOE_WEIGHTS_NK, MOE_SCALE_F32). */
+/* ---- decode path ---------------------------------------------------------------------
+ * Which kernels run the two expert GEMMs of moe_fp8_block_forward_ex.  A step of at most 32
+ * tokens (T*topk <= 512) can take the decode-path GEMMs: work items of 32 weight rows of one
+ * expert over the whole K, streamed into registers and multiplied on the warp-level tensor
+ * core MMA, so that every SM streams weights even when only a few experts are touched (a
+ * one-token DeepSeek-V3-shaped step touches 8 experts: 1024 w13 items instead of 128
+ * 128x256 tiles).  Same operands, block scales and epilogues as the tile GEMMs; the sums run
+ * in another order, so results agree with the tile path to fp32 rounding, not bit for bit.
+ *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300 (currently
+ *                    the tile GEMMs for every size)
+ *   MOE_DECODE_OFF:  always the tile GEMMs
+ *   MOE_DECODE_ON:   the decode path whenever the step qualifies */
+#define MOE_DECODE_AUTO 0
+#define MOE_DECODE_OFF 1
+#define MOE_DECODE_ON 2
+/* 1 if a step of T tokens (hidden H, intermediate I, this top-k) takes the decode-path GEMMs
+ * under `mode`, 0 if it takes the tile GEMMs, -1 for a negative size, topk < 1 or an unknown
+ * mode.  Host only. */
+int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode);
+
+/* Options of the layer: the expert weights' layout, the scale format of the activations
+ * and of the requantised intermediate, and the GEMM kernels of small steps
+ * (NULL options = MOE_WEIGHTS_NK, MOE_SCALE_F32, MOE_DECODE_AUTO). */
 typedef struct moe_forward_options {
     int32_t weight_layout;            /* MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED */
     int32_t scale_fmt;                /* MOE_SCALE_F32 or MOE_SCALE_UE8M0 */
+    int32_t decode_path;              /* MOE_DECODE_AUTO, MOE_DECODE_OFF or MOE_DECODE_ON */
 } moe_forward_options;
 
 /* The same layer with options, optionally recording CUDA events between its stages for

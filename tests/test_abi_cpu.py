@@ -63,6 +63,22 @@ def test_host_only_queries():
     assert moe.moe_fp8_block_forward_kernel_count(-1, 7168, 2048, 256, 8) == -1
 
 
+def test_decode_path_selection():
+    """"on" takes the decode-path GEMMs for any step they can serve (at most 8 tokens, at most
+    512 routed pairs, an expert's w13 under 2^31 bytes), "off" never, "auto" never more than
+    "on"."""
+    dp = moe.moe_fp8_block_decode_path
+    assert dp(1, 7168, 2048, 8, "on") and dp(8, 7168, 2048, 8, "on")
+    assert not dp(9, 7168, 2048, 8) and not dp(4096, 7168, 2048, 8)
+    assert not dp(1, 7168, 2048, 8, "off")
+    assert dp(8, 256, 256, 32, "on") and not dp(9, 256, 256, 2, "on") and not dp(0, 256, 256, 8, "on")
+    assert not dp(1, 65536, 16384, 8, "on")
+    L = ops.lib()
+    assert L.moe_fp8_block_decode_path(1, 256, 256, 8, 3) == -1
+    assert L.moe_fp8_block_decode_path(-1, 256, 256, 8, 0) == -1
+    assert L.moe_fp8_block_decode_path(1, 256, 256, 0, 0) == -1
+
+
 @pytest.mark.parametrize("T,E,topk,rp,code", [
     (-1, 8, 2, None, -1),
     (4, 0, 1, None, -1),
@@ -117,9 +133,9 @@ def test_newer_entry_points_reject_bad_arguments_on_host():
     L = ops.lib()
     p = ctypes.c_void_p(0x1000)
     big = ctypes.c_void_p(0x100000)
-    # forward options: unknown weight layout / scale format
-    for layout, fmt in [(7, 0), (0, 5)]:
-        opts = ops._ForwardOptions(layout, fmt)
+    # forward options: unknown weight layout / scale format / decode-path mode
+    for layout, fmt, dec in [(7, 0, 0), (0, 5, 0), (0, 0, 3), (0, 0, -1)]:
+        opts = ops._ForwardOptions(layout, fmt, dec)
         assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
                                           1 << 30, p, None, None) == -1
     # quantisers: unknown scale format

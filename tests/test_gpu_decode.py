@@ -1,0 +1,115 @@
+"""The decode-path GEMMs (steps of up to 8 tokens): the whole layer against the oracle on
+every token, the same steps through the tile GEMMs, both weight layouts, both scale formats,
+and repeated calls on one workspace (the per-group completion counters start from zero on
+every call)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import block_fp8_mixture_topk_gb300 as moe
+from moe_testutil import Layer, assert_output_close, routing_of
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def workload(name, T):
+    return mi.WORKLOADS[name].with_tokens(T)
+
+
+def forward(layer, hidden, logits, rp, decode, packed=False, workspace=None):
+    wl = layer.wl
+    w13, w2 = layer.w13q, layer.w2q
+    if packed:
+        w13, w2 = moe.moe_fp8_block_pack_weights(w13), moe.moe_fp8_block_pack_weights(w2)
+    return moe.moe_fp8_block_forward(hidden, logits, w13, layer.w13s, w2, layer.w2s, wl.topk, wl.renormalize, rp,
+                                     scale_fmt=layer.scale_fmt, decode=decode, workspace=workspace)
+
+
+def oracle_out(layer, hidden, logits, okw):
+    wl = layer.wl
+    oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    w13q, w13s, w2q, w2s = layer.oracle_weights(set(oids.reshape(-1).tolist()))
+    fmt = oracle.SCALE_UE8M0 if layer.scale_fmt == "ue8m0" else oracle.SCALE_F32
+    return oracle.moe_forward(bits(hidden), logits.numpy(), w13q, w13s, w2q, w2s, wl.topk, wl.renormalize,
+                              scale_fmt=fmt, **okw)["out"]
+
+
+CASES = [
+    ("dsv3_decode", 1), ("dsv3_decode", 2), ("dsv3_decode", 3), ("dsv3_decode", 8),
+    ("mixtral", 1), ("mixtral", 8),      # 8 experts, top-2: up to 8 rows on one expert
+    ("tiny", 5), ("tiny", 8),            # 4 experts, top-2: experts with several rows
+]
+
+
+@pytest.mark.parametrize("name,T", CASES)
+def test_decode_path_matches_oracle_and_tile_path(name, T):
+    wl = workload(name, T)
+    assert moe.moe_fp8_block_decode_path(T, wl.H, wl.I, wl.topk, "on")
+    layer = Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    h, l = hidden.to(DEV), logits.to(DEV)
+    dec = forward(layer, h, l, rp, "on")
+    dec_packed = forward(layer, h, l, rp, "on", packed=True)
+    tile = forward(layer, h, l, rp, "off")
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(clear=True) == 0
+    # the two weight layouts read the same bytes in the same order
+    assert torch.equal(dec, dec_packed)
+    ref = oracle_out(layer, hidden, logits, okw)
+    assert_output_close(dec, ref)
+    assert_output_close(tile, ref)
+    # decode and tile paths differ only in the fp32 summation order
+    assert_output_close(dec, tile.float().cpu().double().numpy())
+
+
+@pytest.mark.parametrize("T,H,I,E,topk", [(1, 128, 128, 1, 1), (8, 128, 256, 1, 1), (6, 256, 128, 3, 3),
+                                          (4, 384, 384, 32, 32)])
+def test_decode_path_edge_shapes(T, H, I, E, topk):
+    """One expert and top-1 (a dense block-FP8 MLP), every token on the single expert (8 rows),
+    top-k equal to the number of experts, and K smaller than the eight warps' K blocks."""
+    wl = mi.Workload("dec_edge", 90 + T + E, T, H, I, E, topk)
+    layer = Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    out = forward(layer, hidden.to(DEV), logits.to(DEV), rp, "on")
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(clear=True) == 0
+    assert_output_close(out, oracle_out(layer, hidden, logits, okw))
+
+
+def test_decode_path_ue8m0_scales():
+    wl = workload("dsv3_decode", 4)
+    layer = Layer(wl, scale_fmt="ue8m0")
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    out = forward(layer, hidden.to(DEV), logits.to(DEV), rp, "on")
+    assert_output_close(out, oracle_out(layer, hidden, logits, okw))
+
+
+def test_decode_path_repeated_calls_on_one_workspace():
+    """Ten calls on one workspace, on changing inputs: each equals a call on a fresh workspace
+    (the group counters are zeroed by every call's sort and reset by the item that completes
+    a group)."""
+    wl = workload("dsv3_decode", 2)
+    layer = Layer(wl)
+    rp, _ = routing_of(wl)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8,
+                     device=DEV)
+    ws.fill_(0x7F)   # garbage in every counter before the first call
+    for seed in range(10):
+        wl_s = wl.with_(number=wl.number + 700 + seed)
+        h, l = mi.hidden(wl_s).to(DEV), mi.router_logits(wl_s).to(DEV)
+        got = forward(layer, h, l, rp, "on", workspace=ws)
+        fresh = torch.empty_like(ws)
+        want = forward(layer, h, l, rp, "on", workspace=fresh)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    assert moe.moe_get_device_status(clear=True) == 0
