@@ -88,9 +88,11 @@ struct ForwardLayout {
     int64_t dcnt_n;   // decode-path group counters (0: the step cannot take the decode path)
 };
 
-// Steps of up to this many tokens take the decode-path GEMMs by default (MOE_DECODE_AUTO); 0
-// while the tile GEMMs are as fast for every step size.
-constexpr int kDecodeAutoMaxTokens = 0;
+// Steps of up to this many tokens take the decode path by default (MOE_DECODE_AUTO).  Measured on
+// GB300 with the DeepSeek-V3-shaped layer (E=256, top-8, tile-packed weights, CUDA-graph replay):
+// one token 0.087 ms against 0.090 ms on the tile GEMMs; two tokens 0.143 against 0.141; four
+// and eight tokens slower (0.256 / 0.428 against 0.245 / 0.387).
+constexpr int kDecodeAutoMaxTokens = 1;
 
 // Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
 // rows per expert), a sort small enough for the one-launch prologue (which writes the decode
@@ -133,9 +135,8 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
     L.y = take(static_cast<size_t>(P) * H * 2);
-    // decode path: h = silu(gate) * up by pair [P, I] fp32, the per-(tile, group) counters and
-    // the tile records
-    L.dcnt_n = decode_possible(T, H, I, topk) ? L.tiles * (I / 128) : 0;
+    // decode path: h = silu(gate) * up by pair [P, I] fp32, the counters and the tile records
+    L.dcnt_n = decode_possible(T, H, I, topk) ? decode_counters(static_cast<int>(L.tiles), I) : 0;
     L.dh = take(L.dcnt_n ? static_cast<size_t>(P) * I * 4 : 0);
     L.dcnt = take(static_cast<size_t>(L.dcnt_n) * 4);
     L.dtab = take(L.dcnt_n ? static_cast<size_t>(L.tiles) * sizeof(DecodeTile) : 0);
@@ -420,6 +421,7 @@ int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
     if (T < 0 || H <= 0 || I <= 0 || E < 1 || topk < 1) return -1;
     if (T == 0) return 0;
     const int64_t P = static_cast<int64_t>(T) * topk;
+    if (use_decode(T, H, I, topk, MOE_DECODE_AUTO)) return 1 + 1 + 1 + 1;
     return 1 + (P <= kSmallPairs ? 1 : 4) + 2 + 1;
 }
 
@@ -537,42 +539,34 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, scale_fmt, s);
     if (e == cudaSuccess) e = mark(3);
     if (decode) {
-        // up to 8 rows per expert: weight-streaming items of 32 weight rows (decode.cu); the
+        // up to 8 rows per expert: both GEMMs in one weight-streaming launch (decode.cu); the
         // requantised intermediate goes to the a2 / a2s regions at the padded rows, as in the
-        // tile path
-        DecodeGemmArgs d{};
+        // tile path.  Its time is recorded as the w13 stage (the w2 stage is empty).
+        DecodeMlpArgs d{};
+        d.w13 = w13;
+        d.w13_scale = w13_scale;
+        d.w2 = w2;
+        d.w2_scale = w2_scale;
         d.w_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        d.H = H;
+        d.I = I;
         d.E = E;
+        d.a1 = a1;
+        d.a1s = a1s;
+        d.a2 = a2;
+        d.a2s = a2s;
+        d.rows = L.rows;
         d.tiles = dtab;
         d.num_tiles = ntiles;
         d.max_tiles = static_cast<int>(L.tiles);
         d.cols = decode_cols(T);
+        d.h = reinterpret_cast<float*>(ws + L.dh);
+        d.counters = dcnt;
+        d.scale_fmt = scale_fmt;
+        d.y = ypairs;
         d.status = st->status;
-        DecodeGemmArgs d1 = d;
-        d1.W = w13;
-        d1.w_scale = w13_scale;
-        d1.N = 2 * I;
-        d1.K = H;
-        d1.act = a1;
-        d1.act_scale = a1s;
-        d1.rows = L.rows;
-        d1.h = reinterpret_cast<float*>(ws + L.dh);
-        d1.group_count = dcnt;
-        d1.out_q = a2;
-        d1.out_scale = a2s;
-        d1.scale_fmt = scale_fmt;
-        if (e == cudaSuccess) e = launch_decode_gemm(d1, true, st->num_sms, s);
+        if (e == cudaSuccess) e = launch_decode_mlp(d, st->num_sms, s);
         if (e == cudaSuccess) e = mark(4);
-        DecodeGemmArgs d2 = d;
-        d2.W = w2;
-        d2.w_scale = w2_scale;
-        d2.N = H;
-        d2.K = I;
-        d2.act = a2;
-        d2.act_scale = a2s;
-        d2.rows = L.rows;
-        d2.y = ypairs;
-        if (e == cudaSuccess) e = launch_decode_gemm(d2, false, st->num_sms, s);
         if (e == cudaSuccess) e = mark(5);
     }
     if (e == cudaSuccess && !decode) {

@@ -1,35 +1,47 @@
-// Decode-regime expert GEMMs: the two grouped block-FP8 GEMMs of the layer when every
-// expert holds at most 8 routed rows (a decode step of up to 8 tokens).
+// Decode-regime expert MLP: both grouped block-FP8 GEMMs of the layer in one persistent
+// launch, for steps in which every expert holds at most 8 routed rows (up to 8 tokens).
 //
-// The same products as the tensor-core grouped GEMM (gemm.cu),
+// The same products as the tile GEMMs (gemm.cu),
 //   C[r, n] = sum_kb a_scale[r, kb] * w_scale[e, n/128, kb] * sum_{k in kb} A[r, k] * W[e, n, k],
 // with the "[num_experts, N, K]" weights in 128x128 blocks (page "Quantization and MoE
-// Optimizations", sections FusedMoE Class and Fp8Config), shaped for weight streaming.
-// With a few rows per expert the layer reads each touched expert's weights once and does
-// two flops per weight byte and row: its time is the weight bytes over HBM bandwidth, so
-// every SM has to stream weights for the whole kernel.  The 128-row tiles of the tile
-// GEMM give a one-token DeepSeek-V3-shaped step only 128 w13 work items (8 experts x 16
-// groups of 128 gate + 128 up rows) for 152 SMs, and a w13 tile cannot be split further
-// because its 1x128 requantisation group needs all 256 of its rows.
+// Optimizations", sections FusedMoE Class and Fp8Config), shaped for weight streaming.  With
+// a few rows per expert the layer reads each touched expert's weights once and does two
+// flops per weight byte and row: its time is the weight bytes over HBM bandwidth, so every
+// SM has to stream weights from the first to the last microsecond.  The 128-row tiles of
+// the tile GEMMs give a one-token DeepSeek-V3-shaped step only 128 w13 work items for 152
+// SMs (a w13 tile cannot be split further: its 1x128 requantisation groups need all 256 of
+// its gate and up rows), and the w2 launch cannot start streaming before the w13 launch has
+// drained.
 //
-// Here a work item is 32 weight rows of one expert over the whole K:
-//   w13: 16 gate rows [16u, 16u+16) and the matching 16 up rows [I+16u, ...)
-//   w2 : 32 rows [32u, 32u+32)
-// (a one-token DeepSeek-V3 step: 1024 w13 items and 1792 w2 items).  One persistent CTA
-// per SM takes every gridDim-th item.  Roles (416 threads):
-//   warp 0      producer: per group of 8 K blocks of an item, one TMA load of each 16-row
-//               weight tile over the 8 blocks (16 KB each) and one of the expert's 8
-//               activation rows over them (8 KB) into a 4-stage ring (40 KB a stage, 160 KB
-//               in flight), and the blocks' weight-block and activation scales by cp.async,
-//               all completing on the stage's mbarrier.  The ring runs on across items.
-//               (Boxes of one K block, 2 KB each, kept too few bytes in flight per SM.)
-//   warps 1..8  MMA warps: warp w takes K block w-1 of every stage; it reads its 16-byte
-//               pieces from shared memory, releases the stage, and runs the tensor cores'
+// Work items (tickets, taken in order from one counter by the CTAs' producers):
+//   first every w13 item: 16 gate rows [16u, 16u+16) and the matching 16 up rows [I+16u, ...)
+//   of one expert over the whole K = H;
+//   then every w2 item: 32 rows [32u, 32u+32) of one expert over K = I.
+// (A one-token DeepSeek-V3 step: 1024 w13 items, then 1792 w2 items.)  A w2 item needs its
+// expert's whole requantised intermediate: its producer streams the item's weights at once
+// but loads the activation rows only after the expert's I/128 groups are counted as done.
+// Tickets are taken in that order by running CTAs, so every w13 item a w2 item waits for is
+// held by a running CTA that waits for nothing: the waits end without any assumption about
+// how many CTAs are resident.  Dynamic tickets also balance the items over the SMs.
+//
+// Roles of a CTA (one per SM, 416 threads):
+//   warp 0      producer: per group of 16 K blocks of an item, TMA loads of its weight rows
+//               over the 16 blocks (w13: two boxes of 16 rows, 32 KB each; w2: one box of 32
+//               rows, 64 KB) and of the expert's activation rows over them (a box of 1, 2, 4
+//               or 8 rows, the fewest that hold the item's rows) into a ring of 2-3 stages, and
+//               the blocks' weight-block and activation scales by cp.async, all completing
+//               on the stage's mbarrier.  The ring runs on across items and across the two
+//               GEMMs.  (On GB300 an SM streams at the HBM share only with large boxes: a
+//               probe streaming 16 KB weight boxes lost 16% when each stage added a 1 KB box,
+//               none with 32 KB boxes; boxes of one K block, 2 KB each, or activation copies
+//               by cp.async were several times slower.)
+//   warps 1..8  MMA warps: warp w takes K blocks w-1 and w+7 of every stage; it reads its
+//               16-byte pieces from shared memory and runs the tensor cores'
 //               warp-level MMA (mma.sync m16n8k32 e4m3 x e4m3 -> fp32: 16 weight rows as the
-//               A operand, the 8 activation rows as B) and promotes the K block's product
-//               with its two scales into fp32 accumulators, as the tile GEMM does.  At the
-//               end of an item each warp stores its partial sums to one of three reduction
-//               buffers and goes on with the next item.
+//               A operand, up to 8 activation rows as B) and promotes the K block's product
+//               with its two scales into fp32 accumulators, as the tile GEMM does, then
+//               releases the stage.  At the end of an item each warp stores its partial sums
+//               to one of two reduction buffers and goes on with the next item.
 //   warps 9..12 epilogue: add the eight partial sums in warp order (deterministic) and
 //               finish the item while the MMA warps stream the next ones.
 // The k order inside an MMA is free as long as A and B agree: lane (g, t) gives bytes
@@ -38,14 +50,14 @@
 //
 // w13 epilogue: h = silu(gate) * up in fp32 for the item's 16 columns, stored to an fp32
 // buffer by routed pair.  The eight items of a 1x128 requantisation group count their
-// completion on a per-(expert tile, group) counter (release fence, then one atomic add);
-// the item that completes the group re-reads the group's 128 values and requantises them
-// (amax/448, e4m3 codes) into the expert's padded rows, the layout the w2 GEMM reads, as
-// the tile GEMM's fused epilogue does.  No item waits for another.  The counters are
-// zeroed by the expert sort of the same call.
+// completion on a per-(expert tile, group) counter (a barrier, then one acq_rel atomic add);
+// the item that completes the group re-reads the group's 128 values, requantises them
+// (amax/448, e4m3 codes) into the expert's padded rows, as the tile GEMM's fused epilogue
+// does, and counts the group on the tile's ready counter.  No w13 item waits for another.
 // w2 epilogue: bf16(router weight * C) to the pair's row of the [T*topk, H] buffer that
 // the k-way sum (moe_combine_pairs) reads, as the tile GEMM's pairs epilogue.
-// Every wait is bounded (mbar_wait); on expiry the CTA records MOE_STATUS_WAIT_TIMEOUT,
+// The counters and the ticket are zeroed by the expert sort of the same call.  Every wait
+// is bounded (mbar_wait, wait_count); on expiry the CTA records MOE_STATUS_WAIT_TIMEOUT,
 // lets its loads in flight land and exits.
 #include "kernels.cuh"
 
@@ -53,35 +65,47 @@ namespace mfp8 {
 
 namespace {
 
-constexpr int kCols = kDecodeCols;              // routed rows per expert: the MMA's 8 B columns
+constexpr int kCols = kDecodeCols;              // routed rows per expert at most: the MMA's 8 B columns
 constexpr int kMmaWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = (1 + kMmaWarps + kEpiWarps) * 32;
-constexpr int kStages = 4;
-constexpr int kGroupKB = 8;                     // K blocks per stage: one per MMA warp
-constexpr int kTileBytes = 16 * 128 * kGroupKB; // 16 weight rows over 8 K blocks
-constexpr int kActBytes = kCols * 128 * kGroupKB;   // 8 activation rows over 8 K blocks
-constexpr int kStageBytes = 2 * kTileBytes + kActBytes;
+constexpr int kMaxStages = 4;
+constexpr int kGroupKB = 16;                    // K blocks per stage: two per MMA warp
+constexpr int kTileBytes = 16 * 128 * kGroupKB; // 16 weight rows over 16 K blocks
+constexpr int kWeightBytes = 2 * kTileBytes;    // a stage's weights: 32 rows over 16 K blocks
 constexpr int kStageScales = 2 * kGroupKB + kCols * kGroupKB;   // [tile][kb] weight scales, [kb][row] activation scales
 constexpr int kGroupItems = 128 / 16;           // w13 items per 1x128 group of the intermediate
-constexpr int kRedBufs = 3;                     // items whose partial sums await the epilogue
+constexpr int kRedBufs = 2;                     // items whose partial sums await the epilogue
 
 struct Ctl {
-    uint64_t full[kStages];                     // a stage landed (1 + 32 arrivals, tx bytes)
-    uint64_t empty[kStages];                    // the MMA warps have read it (8 arrivals)
+    uint64_t full[kMaxStages];                  // a stage landed (1 + 32 arrivals, tx bytes)
+    uint64_t empty[kMaxStages];                 // the MMA warps have read it (8 arrivals)
     uint64_t red_full[kRedBufs];                // all MMA warps stored their partials (8 arrivals)
     uint64_t red_empty[kRedBufs];               // the epilogue has read them (4 arrivals)
     int abort_flag;
     int last;
-    float scl[kStages][kStageScales];
+    int stage_item[kMaxStages];                 // the stage's item (ticket), -1: no more work
+    int stage_grp[kMaxStages];                  // its group of K blocks
+    int stage_rows[kMaxStages];                 // activation rows it holds (1, 2, 4 or 8)
+    int red_item[kRedBufs];                     // the reduction buffer's item, -1: no more work
+    alignas(16) float scl[kMaxStages][kStageScales];
     alignas(16) float red[kRedBufs][kMmaWarps][2][32][4];
 };
-// ring, control block, then the step's tile records (max_tiles of them)
-constexpr size_t kSmemFixed = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl);
+// shared memory: alignment slack, the control block, the ring (stages x stage bytes: a stage's
+// weights, then its activation rows), the step's tile records
+constexpr size_t kCtlBytes = (sizeof(Ctl) + 1023) / 1024 * 1024;
 constexpr size_t kSmemLimit = 232448;
-static_assert(kSmemFixed + 64 * sizeof(DecodeTile) <= kSmemLimit, "shared memory per CTA exceeds the sm_103 limit");
-size_t smem_bytes(int max_tiles) { return kSmemFixed + static_cast<size_t>(max_tiles) * sizeof(DecodeTile); }
+// a stage holds up to `cols` activation rows in a box of the next power of two rows
+size_t stage_bytes(int cols) {
+    int r = 1;
+    while (r < cols) r <<= 1;
+    return (kWeightBytes + static_cast<size_t>(r) * 128 * kGroupKB + 1023) / 1024 * 1024;
+}
+size_t smem_bytes(int max_tiles, int stages, int cols) {
+    return 1024 + kCtlBytes + static_cast<size_t>(stages) * stage_bytes(cols) +
+           static_cast<size_t>(max_tiles) * sizeof(DecodeTile);
+}
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -101,29 +125,81 @@ __device__ __forceinline__ void epilogue_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
 }
 
-template <bool SILU>
+// The counters follow the release / acquire pattern of a CTA-wide barrier: the epilogue
+// threads' stores, a barrier among them, then one thread's atomic with release (or acq_rel)
+// semantics at GPU scope; the reader acquires, then a barrier among its threads.
+__device__ __forceinline__ int atom_add_acq_rel(int32_t* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release(int32_t* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded, like mbar_wait) until *p >= target, with acquire ordering.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort_flag, uint32_t* status) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        if (ld_acquire(p) >= target) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        __nanosleep(64);
+    }
+    *abort_flag = 1;
+    status_set(status, MOE_STATUS_WAIT_TIMEOUT);
+    return false;
+}
+
+// The two GEMMs' shapes: w13 (first) [2I, H], w2 (second) [H, I].
+struct Gemm {
+    int N, K, KB, GKB, NG, per_tile;
+};
+__device__ __forceinline__ Gemm gemm_of(const DecodeMlpArgs& a, bool second) {
+    Gemm g;
+    g.N = second ? a.H : 2 * a.I;
+    g.K = second ? a.I : a.H;
+    g.KB = g.K / 128;
+    g.GKB = g.KB < kGroupKB ? g.KB : kGroupKB;   // K blocks per stage (fewer only when K has fewer)
+    g.NG = (g.KB + g.GKB - 1) / g.GKB;           // stages per item
+    g.per_tile = g.N / 32;                       // items per expert tile
+    return g;
+}
+
+// Activation rows of a stage come in boxes of 1, 2, 4 or 8 rows (the fewest that hold the
+// item's rows): maps [gemm][log2 rows], gemm 0 = w13 (a1), 1 = w2 (a2).
+struct ActMaps {
+    CUtensorMap m[2][4];
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const DecodeGemmArgs a) {
+    decode_mlp_kernel(const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2,
+                      const __grid_constant__ ActMaps tmX, const DecodeMlpArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
-    uint8_t* ring = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    Ctl* ctl = reinterpret_cast<Ctl*>(ring + kStages * kStageBytes);
-    DecodeTile* tab = reinterpret_cast<DecodeTile*>(ctl + 1);
+    uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    Ctl* ctl = reinterpret_cast<Ctl*>(base);
+    uint8_t* ring = base + kCtlBytes;
+    const int S = a.stages;
+    const int SB = a.stage_bytes;
+    DecodeTile* tab = reinterpret_cast<DecodeTile*>(ring + static_cast<size_t>(S) * SB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KB = a.K / 128;
-    const int NB = a.N / 128;
-    // K blocks per stage (fewer than 8 only when K has fewer) and stages per item
-    const int GKB = KB < kGroupKB ? KB : kGroupKB;
-    const int NG = (KB + GKB - 1) / GKB;
-    // activation rows loaded per stage: the most rows an expert can hold (a.cols <= 8); the
-    // B columns past them hold stale shared memory and their results are never read
-    const uint32_t stage_tx = static_cast<uint32_t>((2 * 16 + a.cols) * 128 * GKB);
-    const int per_tile = a.N / 32;   // w13: (N/2)/16 items of 16 gate + 16 up rows; w2: N/32 items of 32 rows
+    const int I = a.I;
+    const int GPT = I / 128;                     // 1x128 groups of the intermediate per expert tile
+    int32_t* group_count = a.counters;           // [max_tiles][I/128]
+    int32_t* ready = a.counters + static_cast<int64_t>(a.max_tiles) * GPT;   // [max_tiles]
+    int32_t* ticket = ready + a.max_tiles;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1 + 32);
             mbar_init(smem_addr(&ctl->empty[s]), kMmaWarps);
         }
@@ -135,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmW);
-        tma_prefetch_map(&tmX);
+        tma_prefetch_map(&tmW13);
+        tma_prefetch_map(&tmW2);
     }
     // the set-up above overlaps the previous kernel's tail; its outputs are read from here on
     grid_dependency_wait();
@@ -150,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t ntiles = *a.num_tiles;
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
-    const int64_t total = ntiles * per_tile;
+    const Gemm G1 = gemm_of(a, false), G2 = gemm_of(a, true);
+    const int total1 = static_cast<int>(ntiles * G1.per_tile);
+    const int total = total1 + static_cast<int>(ntiles * G2.per_tile);
     volatile int* abort_flag = &ctl->abort_flag;
     __syncthreads();
 
@@ -158,56 +236,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ producer
         uint32_t q = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const int m = static_cast<int>(w / per_tile), u = static_cast<int>(w % per_tile);
+        // tickets are taken two items ahead: an atomic's round trip is longer than a w2 item's issue
+        int item = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(ticket, 1) : 0, 0);
+        int next = lane == 0 ? atomicAdd(ticket, 1) : 0;
+        while (ok) {
+            if (item >= total) {
+                // no more work: a stage that says so
+                const uint32_t stage = q % S, use = q / S;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->empty[stage]), (use & 1u) ^ 1u, abort_flag,
+                                                       a.status)))
+                    ok = false;
+                if (ok) {
+                    const uint32_t fb = smem_addr(&ctl->full[stage]);
+                    if (lane == 0) {
+                        ctl->stage_item[stage] = -1;
+                        mbar_arrive(fb);
+                    }
+                    cp_async_arrive(fb);
+                    ++q;
+                }
+                break;
+            }
+            const int next2 = lane == 0 ? atomicAdd(ticket, 1) : 0;
+            const bool second = item >= total1;
+            const Gemm& G = second ? G2 : G1;
+            const int w = second ? item - total1 : item;
+            const int m = w / G.per_tile, u = w - m * G.per_tile;
             // (a record with an expert out of range -- the sort writes none -- streams expert 0
             // and its item's output is dropped by the epilogue)
             const int e = (tab[m].e >= 0 && tab[m].e < a.E) ? tab[m].e : 0;
             const int poff = tab[m].poff;
-            const int row0 = SILU ? u * 16 : u * 32;
-            const int row1 = SILU ? a.N / 2 + u * 16 : u * 32 + 16;
-            const float* ws[2] = {a.w_scale + (static_cast<int64_t>(e) * NB + row0 / 128) * KB,
-                                  a.w_scale + (static_cast<int64_t>(e) * NB + row1 / 128) * KB};
-            for (int grp = 0; grp < NG; ++grp, ++q) {
-                const uint32_t stage = q % kStages, use = q / kStages;
+            const int row0 = second ? u * 32 : u * 16;
+            const int row1 = second ? u * 32 + 16 : I + u * 16;
+            const int NB = G.N / 128;
+            const CUtensorMap* tmW = second ? &tmW2 : &tmW13;
+            const float* wsc = second ? a.w2_scale : a.w13_scale;
+            const float* ws[2] = {wsc + (static_cast<int64_t>(e) * NB + row0 / 128) * G.KB,
+                                  wsc + (static_cast<int64_t>(e) * NB + row1 / 128) * G.KB};
+            const float* xsc = second ? a.a2s : a.a1s;
+            // activation rows: the item's rows rounded up to a power of two (zero-row records of
+            // invalid tiles load one row)
+            int cnt = tab[m].cnt;
+            cnt = cnt < 1 ? 1 : (cnt > a.cols ? a.cols : cnt);
+            const int lg = cnt <= 1 ? 0 : cnt <= 2 ? 1 : cnt <= 4 ? 2 : 3;
+            const CUtensorMap* tmA = &tmX.m[second ? 1 : 0][lg];
+            // bytes per stage: weights (w13: two 16-row boxes; w2: one 32-row box) + activations
+            const uint32_t stage_tx = static_cast<uint32_t>((32 + (1 << lg)) * 128 * G.GKB);
+            for (int grp = 0; grp < G.NG; ++grp, ++q) {
+                const uint32_t stage = q % S, use = q / S;
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->empty[stage]), (use & 1u) ^ 1u, abort_flag,
                                                        a.status))) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = smem_addr(&ctl->full[stage]);
-                const uint32_t dst = smem_addr(ring + stage * kStageBytes);
-                const int kb0 = grp * GKB;
+                uint8_t* st = ring + static_cast<size_t>(stage) * SB;
+                const uint32_t dst = smem_addr(st);
+                const int kb0 = grp * G.GKB;
                 if (lane == 0) {
+                    ctl->stage_item[stage] = item;
+                    ctl->stage_grp[stage] = grp;
+                    ctl->stage_rows[stage] = 1 << lg;
                     // K blocks past K are out of the tensor: zero-filled (and counted), and skipped
                     // by the MMA warps
                     mbar_arrive_expect_tx(fb, stage_tx);
-                    if (a.w_tiled) {   // [E*N/128][K/128][128 rows][128 bytes]: box 16 rows x 8 K blocks
-                        tma_load_4d(dst, &tmW, 0, row0 % 128, kb0, e * NB + row0 / 128, fb);
-                        tma_load_4d(dst + kTileBytes, &tmW, 0, row1 % 128, kb0, e * NB + row1 / 128, fb);
-                    } else {           // [E*N rows][K/128][128 bytes]: box 8 K blocks x 16 rows
-                        tma_load_3d(dst, &tmW, 0, kb0, e * a.N + row0, fb);
-                        tma_load_3d(dst + kTileBytes, &tmW, 0, kb0, e * a.N + row1, fb);
+                    // the item's weight rows over the stage's K blocks: w2 one box of 32 rows, w13
+                    // a box of its 16 gate rows and one of its 16 up rows (I rows apart)
+                    if (second) {
+                        if (a.w_tiled)
+                            tma_load_4d(dst, tmW, 0, row0 % 128, kb0, e * NB + row0 / 128, fb);
+                        else
+                            tma_load_3d(dst, tmW, 0, kb0, e * G.N + row0, fb);
+                    } else if (a.w_tiled) {
+                        tma_load_4d(dst, tmW, 0, row0 % 128, kb0, e * NB + row0 / 128, fb);
+                        tma_load_4d(dst + kTileBytes, tmW, 0, row1 % 128, kb0, e * NB + row1 / 128, fb);
+                    } else {
+                        tma_load_3d(dst, tmW, 0, kb0, e * G.N + row0, fb);
+                        tma_load_3d(dst + kTileBytes, tmW, 0, kb0, e * G.N + row1, fb);
                     }
-                    tma_load_3d(dst + 2 * kTileBytes, &tmX, 0, kb0, poff, fb);
                 }
-                for (int i = lane; i < kStageScales; i += 32) {
-                    const int kbi = i < 2 * kGroupKB ? (i % kGroupKB) : (i - 2 * kGroupKB) / kCols;
-                    const int kb = kb0 + kbi;
-                    if (kbi >= GKB || kb >= KB) continue;
-                    const float* src = i < 2 * kGroupKB
-                                           ? ws[i / kGroupKB] + kb
-                                           : a.act_scale + static_cast<int64_t>(kb) * a.rows + poff +
-                                                 (i - 2 * kGroupKB) % kCols;
-                    cp_async_4(smem_addr(&ctl->scl[stage][i]), src);
+                bool got = true;
+                if (second && grp == 0 && tab[m].pad == 0) {
+                    // the expert's requantised intermediate is complete once its I/128 groups are
+                    // counted; every lane acquires it before its loads of the activations, once
+                    // per tile (the record's spare field remembers it)
+                    got = lane == 0 ? wait_count(ready + m, GPT, abort_flag, a.status) : true;
+                    got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+                    if (got) got = ld_acquire(ready + m) >= GPT;
+                    got = __all_sync(0xffffffffu, got);
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __syncwarp();
+                    if (got && lane == 0) tab[m].pad = 1;
+                    __syncwarp();
+                }
+                // the activation rows of the stage's K blocks (after a failed wait the load still
+                // goes out, so that the stage's phase completes and the drain below can wait for
+                // it; the status word marks the outputs invalid)
+                if (lane == 0) tma_load_3d(dst + kWeightBytes, tmA, 0, kb0, poff, fb);
+                {
+                    // weight-block scales (read-only here: 4-byte copies through L1), lane = tile * 16 + kbi
+                    const int kbi = lane % kGroupKB, kb = kb0 + kbi;
+                    if (kbi < G.GKB && kb < G.KB)
+                        cp_async_4(smem_addr(&ctl->scl[stage][lane]), ws[lane / kGroupKB] + kb);
+                }
+                {
+                    // activation scales of a K block's 8 rows, two 16-byte copies that bypass L1 (the
+                    // w13 items of other SMs write the intermediate's scales during the kernel)
+                    const int kbi = lane >> 1, c = lane & 1, kb = kb0 + kbi;
+                    if (kbi < G.GKB && kb < G.KB)
+                        cp_async_16(smem_addr(&ctl->scl[stage][2 * kGroupKB + kbi * kCols + 4 * c]),
+                                    xsc + static_cast<int64_t>(kb) * a.rows + poff + 4 * c);
                 }
                 cp_async_arrive(fb);
+                if (!got) {
+                    ok = false;
+                    ++q;
+                    break;
+                }
             }
+            item = __shfl_sync(0xffffffffu, next, 0);
+            next = next2;
         }
         if (!ok) {
             // let every stage load already issued land before the CTA exits
-            for (uint32_t s = 0; s < kStages && lane == 0; ++s) {
-                const uint32_t n_s = (q + kStages - 1 - s) / kStages;
+            for (uint32_t s = 0; s < static_cast<uint32_t>(S) && lane == 0; ++s) {
+                const uint32_t n_s = (q + S - 1 - s) / S;
                 if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
             }
         }
@@ -216,90 +369,133 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ MMA warps
         const int cw = warp - 1;
         const int g = lane >> 2, t = lane & 3;
-        uint32_t q0 = 0, iter = 0;
-        bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            float acc[2][4];
+        uint32_t q = 0, iter = 0;
+        float acc[2][4];
 #pragma unroll
-            for (int tile = 0; tile < 2; ++tile)
+        for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[tile][i] = 0.0f;
-            for (int grp = 0; grp < NG; ++grp) {
-                const uint32_t q = q0 + grp;
-                const uint32_t stage = q % kStages;
-                if (!mbar_wait(smem_addr(&ctl->full[stage]), (q / kStages) & 1u, abort_flag, a.status)) {
-                    ok = false;
+            for (int i = 0; i < 4; ++i) acc[tile][i] = 0.0f;
+        while (true) {
+            const uint32_t stage = q % S;
+            if (!mbar_wait(smem_addr(&ctl->full[stage]), (q / S) & 1u, abort_flag, a.status)) break;
+            ++q;
+            const int item = ctl->stage_item[stage];
+            if (item < 0) {
+                // no more work: pass that on to the epilogue
+                const uint32_t buf = iter % kRedBufs, use = iter / kRedBufs;
+                if (use > 0 && !mbar_wait(smem_addr(&ctl->red_empty[buf]), (use - 1) & 1u, abort_flag, a.status))
                     break;
-                }
-                const int kb = grp * GKB + cw;   // this warp's K block of the stage
-                const uint8_t* st = ring + stage * kStageBytes;
-                uint4 wv[2][2][2], xv[2];
-                float ws[2] = {0.0f, 0.0f}, xa = 0.0f, xb = 0.0f;
-                const bool live = cw < GKB && kb < KB;
-                if (live) {
+                if (cw == 0 && lane == 0) ctl->red_item[buf] = -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[buf]));
+                break;
+            }
+            const int grp = ctl->stage_grp[stage];
+            const bool second = item >= total1;
+            const Gemm& G = second ? G2 : G1;
+            const uint8_t* st = ring + static_cast<size_t>(stage) * SB;
+            const int xr = ctl->stage_rows[stage];
+            // this warp's K blocks of the stage: cw and cw + 8
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int kbi = cw + 8 * half, kb = grp * G.GKB + kbi;
+                if (kbi >= G.GKB || kb >= G.KB) continue;
+                uint4 wv[2][2][2], xv[2];   // [tile][row g / g+8][K half c], [K half c]
+                // 128-byte rows of the stage's weight boxes, tile-packed with the 128-byte swizzle:
+                //   w2: [K block][32 rows]       w13: gate box, up box, each [K block][16 rows]
+                // [E, N, K] without swizzle:
+                //   w2: [32 rows][K block]       w13: gate box, up box, each [16 rows][K block]
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int r16 = g + 8 * hr;   // row within the 16-row tile
+                        int box, srow;   // the box's offset in the stage, the row within the box
+                        if (second) {
+                            box = 0;
+                            srow = a.w_tiled ? kbi * 32 + 16 * tile + r16 : (16 * tile + r16) * G.GKB + kbi;
+                        } else {
+                            box = tile * kTileBytes;
+                            srow = a.w_tiled ? kbi * 16 + r16 : r16 * G.GKB + kbi;
+                        }
+                        const int x = a.w_tiled ? (r16 & 7) : 0;   // == srow & 7 when tiled
+                        const uint8_t* rp = st + box + srow * 128;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            wv[tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
+                    }
+                // the stage holds xr activation rows: B columns past them are zero (their results
+                // are never read)
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    xv[c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWeightBytes + (g * G.GKB + kbi) * 128 +
+                                                                     64 * c + 16 * t)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                const float ws[2] = {ctl->scl[stage][kbi], ctl->scl[stage][kGroupKB + kbi]};
+                const float xa = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
+                const float xb = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                // four independent chains (tile, K half c) of two MMAs each
+                float f[2][2][4];
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) f[tile][c][i] = 0.0f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            // tile-packed boxes are [K block][row][128 B], [E, N, K] boxes [row][K block][128 B]
-                            const int row = g + 8 * hr;
-                            const int off = a.w_tiled ? (cw * 16 + row) * 128 : (row * GKB + cw) * 128;
-#pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                wv[tile][hr][c] =
-                                    *reinterpret_cast<const uint4*>(st + tile * kTileBytes + off + 64 * c + 16 * t);
-                        }
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        xv[c] = *reinterpret_cast<const uint4*>(st + 2 * kTileBytes + (g * GKB + cw) * 128 +
-                                                                64 * c + 16 * t);
-                    ws[0] = ctl->scl[stage][cw];
-                    ws[1] = ctl->scl[stage][kGroupKB + cw];
-                    xa = ctl->scl[stage][2 * kGroupKB + cw * kCols + 2 * t];
-                    xb = ctl->scl[stage][2 * kGroupKB + cw * kCols + 2 * t + 1];
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
-                if (!live) continue;
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    float f[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            mma_16x8x32(f, word(wv[tile][0][c], 2 * h), word(wv[tile][1][c], 2 * h),
+                        for (int c = 0; c < 2; ++c)
+                            mma_16x8x32(f[tile][c], word(wv[tile][0][c], 2 * h), word(wv[tile][1][c], 2 * h),
                                         word(wv[tile][0][c], 2 * h + 1), word(wv[tile][1][c], 2 * h + 1),
                                         word(xv[c], 2 * h), word(xv[c], 2 * h + 1));
-                    // accumulator (row g / g+8, column 2t / 2t+1): the weight block's scale
-                    // times the column's activation scale
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    // accumulator (row g / g+8, column 2t / 2t+1): the weight block's scale times the
+                    // column's activation scale
                     const float s0 = ws[tile] * xa, s1 = ws[tile] * xb;
-                    acc[tile][0] = fmaf(f[0], s0, acc[tile][0]);
-                    acc[tile][1] = fmaf(f[1], s1, acc[tile][1]);
-                    acc[tile][2] = fmaf(f[2], s0, acc[tile][2]);
-                    acc[tile][3] = fmaf(f[3], s1, acc[tile][3]);
+                    acc[tile][0] = fmaf(f[tile][0][0] + f[tile][1][0], s0, acc[tile][0]);
+                    acc[tile][1] = fmaf(f[tile][0][1] + f[tile][1][1], s1, acc[tile][1]);
+                    acc[tile][2] = fmaf(f[tile][0][2] + f[tile][1][2], s0, acc[tile][2]);
+                    acc[tile][3] = fmaf(f[tile][0][3] + f[tile][1][3], s1, acc[tile][3]);
                 }
             }
-            if (!ok) break;
-            const uint32_t buf = iter % kRedBufs, use = iter / kRedBufs;
-            if (use > 0 && !mbar_wait(smem_addr(&ctl->red_empty[buf]), (use - 1) & 1u, abort_flag, a.status))
-                break;
-#pragma unroll
-            for (int tile = 0; tile < 2; ++tile)
-                *reinterpret_cast<float4*>(&ctl->red[buf][cw][tile][lane][0]) =
-                    make_float4(acc[tile][0], acc[tile][1], acc[tile][2], acc[tile][3]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[buf]));
-            q0 += NG;
-            ++iter;
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+            if (grp == G.NG - 1) {
+                // the item's last stage: partial sums to a reduction buffer
+                const uint32_t buf = iter % kRedBufs, use = iter / kRedBufs;
+                if (use > 0 && !mbar_wait(smem_addr(&ctl->red_empty[buf]), (use - 1) & 1u, abort_flag, a.status))
+                    break;
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    *reinterpret_cast<float4*>(&ctl->red[buf][cw][tile][lane][0]) =
+                        make_float4(acc[tile][0], acc[tile][1], acc[tile][2], acc[tile][3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[tile][i] = 0.0f;
+                }
+                if (cw == 0 && lane == 0) ctl->red_item[buf] = item;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[buf]));
+                ++iter;
+            }
         }
     } else {
         // ------------------------------------------------------------------ epilogue warps
         const int et = threadIdx.x - kFirstEpiWarp * 32;   // 0..127
         const int ew = warp - kFirstEpiWarp;
         uint32_t iter = 0;
-        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const int m = static_cast<int>(w / per_tile), u = static_cast<int>(w % per_tile);
+        while (true) {
+            const uint32_t buf = iter % kRedBufs;
+            if (!mbar_wait(smem_addr(&ctl->red_full[buf]), (iter / kRedBufs) & 1u, abort_flag, a.status)) break;
+            const int item = ctl->red_item[buf];
+            if (item < 0) break;
+            const bool second = item >= total1;
+            const Gemm& G = second ? G2 : G1;
+            const int w = second ? item - total1 : item;
+            const int m = w / G.per_tile, u = w - m * G.per_tile;
             const DecodeTile& tl = tab[m];
             const bool valid = tl.e >= 0 && tl.e < a.E;
             const int poff = tl.poff;
@@ -311,12 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cnt = cnt > a.cols ? a.cols : cnt;
             }
             // this thread's outputs: w13 (row r of 16, column j); w2 (row r of 32, columns j, j+4)
-            const int r = SILU ? (et & 15) : (et & 31);
-            const int j = SILU ? (et >> 4) : (et >> 5);
-            const int pair0 = j < cnt ? tl.pair[j] : -1;
-            const int pair1 = (!SILU && j + 4 < cnt) ? tl.pair[j + 4] : -1;
-            const uint32_t buf = iter % kRedBufs;
-            if (!mbar_wait(smem_addr(&ctl->red_full[buf]), (iter / kRedBufs) & 1u, abort_flag, a.status)) break;
+            const int r = second ? (et & 31) : (et & 15);
+            const int j = second ? (et >> 5) : (et >> 4);
             // partial sums of (row rr of a 16-row tile, column jj): lane (rr % 8) * 4 + jj / 2,
             // register (rr >= 8 ? 2 : 0) + (jj & 1), added in warp order
             auto total_of = [&](int tile, int rr, int jj) {
@@ -327,62 +519,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return s;
             };
             float v0, v1;
-            if (SILU) {
-                v0 = total_of(0, r, j);    // gate
-                v1 = total_of(1, r, j);    // up
-            } else {
+            if (second) {
                 v0 = total_of(r >> 4, r & 15, j);
                 v1 = total_of(r >> 4, r & 15, j + 4);
+            } else {
+                v0 = total_of(0, r, j);    // gate
+                v1 = total_of(1, r, j);    // up
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl->red_empty[buf]));
             ++iter;
 
-            if (SILU) {
-                const int I = a.N / 2;
-                if (pair0 >= 0) {
-                    // silu(g) * up = g * up / (1 + e^-g), as the tile GEMM's epilogue
-                    a.h[static_cast<int64_t>(pair0) * I + u * 16 + r] = __fdividef(v0 * v1, 1.0f + __expf(-v0));
-                }
-                // the item that completes a 1x128 group requantises it
-                __threadfence();
-                epilogue_barrier();
-                const int grp = u / kGroupItems;
-                if (et == 0) {
-                    int32_t* counter = a.group_count + static_cast<int64_t>(m) * (I / 128) + grp;
-                    const int done = atomicAdd(counter, 1);
-                    const int last = done == kGroupItems - 1;
-                    if (last) *counter = 0;
-                    ctl->last = last;
-                }
-                epilogue_barrier();
-                const int last = ctl->last;
-                epilogue_barrier();   // ctl->last is rewritten by the next item
-                if (!last) continue;
-                __threadfence();
-                for (int jj = ew; jj < cnt; jj += kEpiWarps) {
-                    const int64_t p = tl.pair[jj];
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.h + p * I + grp * 128 + lane * 4));
-                    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                    const float sc = group_scale_fmt(amax, a.scale_fmt);
-                    const float rsc = __frcp_rn(sc);
-                    const uint32_t lo = e4m3x2(div_by_scale(v.x, sc, rsc), div_by_scale(v.y, sc, rsc));
-                    const uint32_t hi = e4m3x2(div_by_scale(v.z, sc, rsc), div_by_scale(v.w, sc, rsc));
-                    const int64_t row = poff + jj;
-                    *reinterpret_cast<uint32_t*>(a.out_q + row * I + grp * 128 + lane * 4) = lo | (hi << 16);
-                    if (lane == 0) a.out_scale[static_cast<int64_t>(grp) * a.rows + row] = sc;
-                }
-            } else {
+            if (second) {
                 // consecutive threads take consecutive rows of one pair's output row
-                if (pair0 >= 0)
-                    a.y[static_cast<int64_t>(pair0) * a.N + u * 32 + r] =
+                if (j < cnt)
+                    a.y[static_cast<int64_t>(tl.pair[j]) * a.H + u * 32 + r] =
                         static_cast<uint16_t>(bf16x2(tl.weight[j] * v0, 0.0f) & 0xFFFFu);
-                if (pair1 >= 0)
-                    a.y[static_cast<int64_t>(pair1) * a.N + u * 32 + r] =
+                if (j + 4 < cnt)
+                    a.y[static_cast<int64_t>(tl.pair[j + 4]) * a.H + u * 32 + r] =
                         static_cast<uint16_t>(bf16x2(tl.weight[j + 4] * v1, 0.0f) & 0xFFFFu);
+                continue;
             }
+            if (j < cnt) {
+                // silu(g) * up = g * up / (1 + e^-g), as the tile GEMM's epilogue
+                a.h[static_cast<int64_t>(tl.pair[j]) * I + u * 16 + r] = __fdividef(v0 * v1, 1.0f + __expf(-v0));
+            }
+            // the item that completes a 1x128 group requantises it
+            epilogue_barrier();
+            const int grp = u / kGroupItems;
+            if (et == 0) {
+                int32_t* counter = group_count + static_cast<int64_t>(m) * GPT + grp;
+                ctl->last = atom_add_acq_rel(counter, 1) == kGroupItems - 1;
+            }
+            epilogue_barrier();
+            const int last = ctl->last;
+            epilogue_barrier();   // ctl->last is rewritten by the next item
+            if (!last) continue;
+            for (int jj = ew; jj < cnt; jj += kEpiWarps) {
+                const int64_t p = tl.pair[jj];
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.h + p * I + grp * 128 + lane * 4));
+                float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sc = group_scale_fmt(amax, a.scale_fmt);
+                const float rsc = __frcp_rn(sc);
+                const uint32_t lo = e4m3x2(div_by_scale(v.x, sc, rsc), div_by_scale(v.y, sc, rsc));
+                const uint32_t hi = e4m3x2(div_by_scale(v.z, sc, rsc), div_by_scale(v.w, sc, rsc));
+                const int64_t row = poff + jj;
+                *reinterpret_cast<uint32_t*>(a.a2 + row * I + grp * 128 + lane * 4) = lo | (hi << 16);
+                if (lane == 0) a.a2s[static_cast<int64_t>(grp) * a.rows + row] = sc;
+            }
+            // count the group on the tile: its w2 items may load it once all I/128 are counted
+            epilogue_barrier();
+            if (et == 0) red_add_release(ready + m, 1);
         }
     }
 }
@@ -391,53 +580,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int decode_cols(int T) { return T >= 1 && T <= kCols ? T : 0; }
 
-cudaError_t decode_init_device() {
-    cudaError_t err = cudaFuncSetAttribute(decode_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemLimit));
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(decode_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kSmemLimit));
-    return err;
+size_t decode_max_tiles() {
+    // room for two stages of 8 activation rows
+    return (kSmemLimit - smem_bytes(0, 2, kCols)) / sizeof(DecodeTile);
 }
 
-cudaError_t launch_decode_gemm(const DecodeGemmArgs& a, bool silu, int num_sms, cudaStream_t stream) {
-    if (a.max_tiles <= 0) return cudaSuccess;
-    if (a.cols < 1 || a.cols > kCols || a.N % 128 != 0 || a.K % 128 != 0 || (silu && a.N % 256 != 0))
-        return cudaErrorInvalidValue;
-    const size_t smem = smem_bytes(a.max_tiles);
-    if (smem > kSmemLimit) return cudaErrorInvalidValue;
-    CUtensorMap tmW, tmX;
-    const uint64_t KB = static_cast<uint64_t>(a.K / 128);
-    const uint32_t GKB = static_cast<uint32_t>(KB < kGroupKB ? KB : kGroupKB);   // K blocks per box
-    const uint64_t E = static_cast<uint64_t>(a.E), N = static_cast<uint64_t>(a.N), K = static_cast<uint64_t>(a.K);
-    cudaError_t err;
-    if (a.w_tiled) {
-        // [E*N/128 blocks][K/128][128 rows][128 bytes]
-        const uint64_t dims[4] = {128, 128, KB, E * (N / 128)};
+int64_t decode_counters(int max_tiles, int I) { return static_cast<int64_t>(max_tiles) * (I / 128 + 1) + 1; }
+
+cudaError_t decode_init_device() {
+    return cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemLimit));
+}
+
+namespace {
+
+// Weight boxes of `rows` rows x GKB K blocks.  Tile-packed weights [E*N/128 blocks][K/128][128
+// rows][128 bytes] get the 128-byte swizzle: in shared memory the rows of a box are consecutive,
+// so lanes reading the same 16 bytes of 8 consecutive rows hit 8 different bank groups.  The
+// pages' [E*N rows][K/128][128 bytes] get none.
+cudaError_t weight_map(CUtensorMap* map, const uint8_t* w, bool tiled, int E, int N, int K, uint32_t rows) {
+    const uint64_t KB = static_cast<uint64_t>(K / 128);
+    const uint32_t GKB = static_cast<uint32_t>(KB < kGroupKB ? KB : kGroupKB);
+    if (tiled) {
+        const uint64_t dims[4] = {128, 128, KB, static_cast<uint64_t>(E) * (N / 128)};
         const uint64_t strides[3] = {128, 128 * 128, KB * 128 * 128};
-        const uint32_t box[4] = {128, 16, GKB, 1};
-        err = encode_u8_map_nd(&tmW, a.W, 4, dims, strides, box);
-    } else {
-        // [E*N rows][K/128][128 bytes]
-        const uint64_t dims[3] = {128, KB, E * N};
-        const uint64_t strides[2] = {128, K};
-        const uint32_t box[3] = {128, GKB, 16};
-        err = encode_u8_map_nd(&tmW, a.W, 3, dims, strides, box);
+        const uint32_t box[4] = {128, rows, GKB, 1};
+        return encode_u8_map_nd(map, w, 4, dims, strides, box, true);
     }
-    if (err == cudaSuccess) {
-        // activations [rows][K/128][128 bytes]
-        const uint64_t dims[3] = {128, KB, static_cast<uint64_t>(a.rows)};
-        const uint64_t strides[2] = {128, K};
-        const uint32_t box[3] = {128, GKB, static_cast<uint32_t>(a.cols)};
-        err = encode_u8_map_nd(&tmX, a.act, 3, dims, strides, box);
+    const uint64_t dims[3] = {128, KB, static_cast<uint64_t>(E) * N};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(K)};
+    const uint32_t box[3] = {128, GKB, rows};
+    return encode_u8_map_nd(map, w, 3, dims, strides, box, false);
+}
+
+// activations [rows][K/128][128 bytes]: boxes of `r` rows x GKB K blocks
+cudaError_t act_map(CUtensorMap* map, const uint8_t* x, int64_t rows, int K, uint32_t r) {
+    const uint64_t KB = static_cast<uint64_t>(K / 128);
+    const uint32_t GKB = static_cast<uint32_t>(KB < kGroupKB ? KB : kGroupKB);
+    const uint64_t dims[3] = {128, KB, static_cast<uint64_t>(rows)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(K)};
+    const uint32_t box[3] = {128, GKB, r};
+    return encode_u8_map_nd(map, x, 3, dims, strides, box, false);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mlp(const DecodeMlpArgs& args, int num_sms, cudaStream_t stream) {
+    if (args.max_tiles <= 0) return cudaSuccess;
+    if (args.cols < 1 || args.cols > kCols || args.H % 128 != 0 || args.I % 128 != 0) return cudaErrorInvalidValue;
+    DecodeMlpArgs a = args;
+    // as many ring stages as fit next to the control block and the tile records
+    a.stage_bytes = static_cast<int>(stage_bytes(a.cols));
+    const size_t fixed = smem_bytes(a.max_tiles, 0, a.cols);
+    if (fixed + 2 * static_cast<size_t>(a.stage_bytes) > kSmemLimit) return cudaErrorInvalidValue;
+    a.stages = static_cast<int>((kSmemLimit - fixed) / a.stage_bytes);
+    if (a.stages > kMaxStages) a.stages = kMaxStages;
+    const size_t smem = smem_bytes(a.max_tiles, a.stages, a.cols);
+    CUtensorMap tmW13, tmW2;
+    cudaError_t err = weight_map(&tmW13, a.w13, a.w_tiled != 0, a.E, 2 * a.I, a.H, 16);
+    if (err == cudaSuccess) err = weight_map(&tmW2, a.w2, a.w_tiled != 0, a.E, a.H, a.I, 32);
+    ActMaps tmX;
+    for (int lg = 0; lg < 4 && err == cudaSuccess; ++lg) {
+        err = act_map(&tmX.m[0][lg], a.a1, a.rows, a.H, 1u << lg);
+        if (err == cudaSuccess) err = act_map(&tmX.m[1][lg], a.a2, a.rows, a.I, 1u << lg);
     }
     if (err != cudaSuccess) return err;
-    const int64_t items = static_cast<int64_t>(a.max_tiles) * (a.N / 32);
+    const int64_t items = static_cast<int64_t>(a.max_tiles) * (2 * a.I / 32 + a.H / 32);
     const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
-    if (silu) return launch_pdl(decode_gemm_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, tmW, tmX, a);
-    return launch_pdl(decode_gemm_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, tmW, tmX, a);
+    return launch_pdl(decode_mlp_kernel, dim3(grid), dim3(kThreads), smem, stream, tmW13, tmW2, tmX, a);
 }
-
-size_t decode_max_tiles() { return (kSmemLimit - kSmemFixed) / sizeof(DecodeTile); }
 
 }  // namespace mfp8

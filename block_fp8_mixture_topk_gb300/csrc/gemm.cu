@@ -548,7 +548,7 @@ cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t
 }  // namespace
 
 cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
-                             const uint64_t* strides, const uint32_t* box) {
+                             const uint64_t* strides, const uint32_t* box, bool swizzle128) {
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
     if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
@@ -561,7 +561,8 @@ cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, con
         if (i + 1 < rank) st[i] = strides[i];
     }
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<uint8_t*>(ptr),
-                          d, st, b, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          d, st, b, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

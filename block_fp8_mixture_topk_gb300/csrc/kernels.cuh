@@ -48,7 +48,7 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
 // router weight (-1 and 0 from cnt on).
 constexpr int kDecodeCols = 8;
 struct DecodeTile {
-    int32_t e, poff, cnt, pad;
+    int32_t e, poff, cnt, pad;   // pad: zero (the decode kernel marks tiles it has seen ready in its own copy)
     int32_t pair[kDecodeCols];
     float weight[kDecodeCols];
 };
@@ -56,7 +56,7 @@ struct DecodeTile {
 struct DecodeSetup {
     DecodeTile* tiles;           // [max_tiles]
     const float* topk_weights;   // [P]
-    int32_t* counters;           // zeroed: the w13 decode GEMM's group counters
+    int32_t* counters;           // zeroed: the decode kernel's counters
     int ncounters;
 };
 
@@ -128,42 +128,46 @@ cudaError_t gemm_init_device();
 cudaError_t encode_u8_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows, uint32_t box_cols,
                           uint32_t box_rows, bool swizzle128);
 // Tensor map of a byte tensor of `rank` dimensions (dims[0] innermost; strides[i] = bytes between
-// consecutive indices of dimension i+1), boxes `box`, no swizzle.
+// consecutive indices of dimension i+1), boxes `box`, with the 128-byte swizzle (box[0] = 128,
+// destinations 1024-byte aligned: 16-byte chunk c of the 128-byte row at shared address A lands
+// at chunk c ^ ((A / 128) % 8)) or none.
 cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
-                             const uint64_t* strides, const uint32_t* box);
+                             const uint64_t* strides, const uint32_t* box, bool swizzle128);
 
-// decode.cu: the two expert GEMMs of a step with at most 8 rows per expert, as weight-streaming
-// work items of 32 weight rows (see decode.cu)
-struct DecodeGemmArgs {
-    const uint8_t* W;          // expert weights, [E, N, K] or tile-packed
+// decode.cu: both expert GEMMs of a step with at most 8 rows per expert in one persistent
+// launch, as weight-streaming work items of 32 weight rows (see decode.cu)
+struct DecodeMlpArgs {
+    const uint8_t* w13;        // [E, 2I, H] or tile-packed
+    const float* w13_scale;    // [E, 2I/128, H/128]
+    const uint8_t* w2;         // [E, H, I] or tile-packed
+    const float* w2_scale;     // [E, H/128, I/128]
     int w_tiled;
-    const float* w_scale;      // [E, N/128, K/128]
-    int N, K, E;
-    const uint8_t* act;        // activation codes [rows, K]: a tile's j-th row at padded row poff + j
-    const float* act_scale;    // their scales, [K/128][rows]
+    int H, I, E;
+    const uint8_t* a1;         // activation codes [rows, H]: a tile's j-th row at padded row poff + j
+    const float* a1s;          // their scales [H/128][rows]
+    uint8_t* a2;               // requantised intermediate [rows, I] at the same rows (written here)
+    float* a2s;                // its scales [I/128][rows]
     int64_t rows;
     const DecodeTile* tiles;   // [max_tiles] (the small-batch sort's records)
     const int32_t* num_tiles;
     int max_tiles;
-    int cols;                  // the most routed rows an expert can hold, 1..8 (decode_cols: min(T, 8))
-    // w13 (SiLU): h [P, N/2] fp32 by pair, per-(tile, group) counters [max_tiles, N/256] (zero
-    // on entry), requantised codes [rows, N/2] and scales [N/256][rows] at the padded rows
-    float* h;
-    int32_t* group_count;
-    uint8_t* out_q;
-    float* out_scale;
+    int cols;                  // the most routed rows an expert can hold, 1..8 (decode_cols: T)
+    float* h;                  // h = silu(gate) * up [P, I] fp32 by pair
+    int32_t* counters;         // decode_counters(max_tiles, I) ints, zero on entry
     int scale_fmt;
-    // w2: y [P, N] bf16 = router weight * C in pair order
-    uint16_t* y;
+    uint16_t* y;               // [P, H] bf16 = router weight * C2 in pair order
     uint32_t* status;
+    int stages, stage_bytes;   // ring geometry (set by launch_decode_mlp)
 };
-// the most rows an expert holds in a step of T tokens, as the decode kernels take it (0: T too
-// large for them)
+// the most rows an expert holds in a step of T tokens, as the decode kernel takes it (0: T too
+// large for it)
 int decode_cols(int T);
-// tile records a decode GEMM CTA can hold in shared memory
+// tile records a decode CTA can hold in shared memory
 size_t decode_max_tiles();
+// ints of the decode kernel's counters: per-(tile, group) counts, per-tile ready counts, the ticket
+int64_t decode_counters(int max_tiles, int I);
 cudaError_t decode_init_device();
-cudaError_t launch_decode_gemm(const DecodeGemmArgs& args, bool silu, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode_mlp(const DecodeMlpArgs& args, int num_sms, cudaStream_t stream);
 
 // api.cu: once-per-device set-up; on MOE_OK, *status = the device status word's address
 int device_status_word(uint32_t** status);

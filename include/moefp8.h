@@ -289,8 +289,8 @@ int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, in
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
 /* Number of kernels one moe_fp8_block_forward launches for these sizes (host only):
  * routing, the expert sort and quantisation (one kernel for up to 512 routed pairs,
- * four otherwise), the two grouped GEMMs and the weighted sum; 0 when T == 0, -1 for
- * invalid sizes. */
+ * four otherwise), the two grouped GEMMs (one kernel on the decode path) and the weighted
+ * sum, under MOE_DECODE_AUTO; 0 when T == 0, -1 for invalid sizes. */
 int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk);
 int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const uint8_t* w13, const float* w13_scale,
@@ -309,15 +309,17 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
                                  uint16_t* out, void* stream);
 
 /* ---- decode path ---------------------------------------------------------------------
- * Which kernels run the two expert GEMMs of moe_fp8_block_forward_ex.  A step of at most 32
- * tokens (T*topk <= 512) can take the decode-path GEMMs: work items of 32 weight rows of one
- * expert over the whole K, streamed into registers and multiplied on the warp-level tensor
- * core MMA, so that every SM streams weights even when only a few experts are touched (a
- * one-token DeepSeek-V3-shaped step touches 8 experts: 1024 w13 items instead of 128
- * 128x256 tiles).  Same operands, block scales and epilogues as the tile GEMMs; the sums run
- * in another order, so results agree with the tile path to fp32 rounding, not bit for bit.
- *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300 (currently
- *                    the tile GEMMs for every size)
+ * Which kernels run the two expert GEMMs of moe_fp8_block_forward_ex.  A step of at most 8
+ * tokens (T*topk <= 512, 2*I*H < 2^31) can take the decode path: both GEMMs in one persistent
+ * kernel whose work items are 32 weight rows of one expert over the whole K, streamed by TMA
+ * and multiplied on the warp-level tensor core MMA, so that every SM streams weights even
+ * when only a few experts are touched (a one-token DeepSeek-V3-shaped step touches 8 experts:
+ * 1024 w13 items instead of 128 tiles of 128 x 256) and the w2 weights stream while the last
+ * w13 items finish.  Same operands, block scales and epilogues as the tile GEMMs; the sums
+ * run in another order, so results agree with the tile path to fp32 rounding, not bit for
+ * bit.  With events, its time is recorded as the w13 GEMM stage and the w2 stage is empty.
+ *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300: the decode
+ *                    path for one-token steps, the tile GEMMs otherwise
  *   MOE_DECODE_OFF:  always the tile GEMMs
  *   MOE_DECODE_ON:   the decode path whenever the step qualifies */
 #define MOE_DECODE_AUTO 0

@@ -113,3 +113,46 @@ def test_decode_path_repeated_calls_on_one_workspace():
         torch.cuda.synchronize()
         assert torch.equal(got, want)
     assert moe.moe_get_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_path_replays_from_a_cuda_graph(T):
+    """The decode path captured once in a CUDA graph and replayed on new inputs: the counters
+    and the ticket are zeroed inside every replay, and each replay equals an eager call."""
+    wl = workload("dsv3_decode", T)
+    layer = Layer(wl)
+    rp, _ = routing_of(wl)
+    w13p, w2p = moe.moe_fp8_block_pack_weights(layer.w13q), moe.moe_fp8_block_pack_weights(layer.w2q)
+    hid = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    log = torch.empty(wl.T, wl.E, dtype=torch.float32, device=DEV)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8,
+                     device=DEV)
+    hid.copy_(mi.hidden(wl).to(DEV))
+    log.copy_(mi.router_logits(wl).to(DEV))
+
+    def step():
+        moe.moe_fp8_block_forward(hid, log, w13p, layer.w13s, w2p, layer.w2s, wl.topk, wl.renormalize, rp,
+                                  out=out, workspace=ws, decode="on")
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in range(3):
+        wl_s = wl.with_(number=wl.number + 900 + seed)
+        h, l = mi.hidden(wl_s).to(DEV), mi.router_logits(wl_s).to(DEV)
+        hid.copy_(h)
+        log.copy_(l)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        want = moe.moe_fp8_block_forward(h, l, w13p, layer.w13s, w2p, layer.w2s, wl.topk, wl.renormalize, rp,
+                                         decode="on")
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    assert moe.moe_get_device_status(clear=True) == 0
