@@ -302,9 +302,10 @@ def run_ours(args, wl):
     touched = int(torch.unique(ids).numel())
     P = wl.P
     decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode)
-    # kernels per step: route, sort + quantisation, then both GEMMs in one kernel (decode path)
-    # or the counted sequence, then the weighted sum
-    launches_per_step = 4 if decode else moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
+    # kernels per step (the decode path's one GEMM kernel in place of two)
+    launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
+    if decode != moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk):
+        launches_per_step += -1 if decode else 1
 
     def step(events=None):
         moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
