@@ -89,10 +89,10 @@ struct ForwardLayout {
 };
 
 // Steps of up to this many tokens take the decode path by default (MOE_DECODE_AUTO).  Measured on
-// GB300 with the DeepSeek-V3-shaped layer (E=256, top-8, tile-packed weights, CUDA-graph replay):
-// one token 0.087 ms against 0.090 ms on the tile GEMMs; two tokens 0.143 against 0.141; four
-// and eight tokens slower (0.256 / 0.428 against 0.245 / 0.387).
-constexpr int kDecodeAutoMaxTokens = 1;
+// GB300 with the DeepSeek-V3-shaped layer (E=256, top-8, tile-packed weights, CUDA-graph replay),
+// ms per step, decode path against the tile GEMMs: one token 0.085 / 0.090, two 0.140 / 0.141,
+// four 0.249 / 0.245, eight 0.421 / 0.387.
+constexpr int kDecodeAutoMaxTokens = 2;
 
 // Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
 // rows per expert), a sort small enough for the one-launch prologue (which writes the decode

@@ -24,7 +24,7 @@
 // held by a running CTA that waits for nothing: the waits end without any assumption about
 // how many CTAs are resident.  Dynamic tickets also balance the items over the SMs.
 //
-// Roles of a CTA (one per SM, 416 threads):
+// Roles of a CTA (one per SM, 384 threads):
 //   warp 0      producer: per group of 16 K blocks of an item, TMA loads of its weight rows
 //               over the 16 blocks (w13: two boxes of 16 rows, 32 KB each; w2: one box of 32
 //               rows, 64 KB) and of the expert's activation rows over them (a box of 1, 2, 4
@@ -36,13 +36,13 @@
 //               none with 32 KB boxes; boxes of one K block, 2 KB each, or activation copies
 //               by cp.async were several times slower.)
 //   warps 1..8  MMA warps: warp w takes K blocks w-1 and w+7 of every stage; it reads its
-//               16-byte pieces from shared memory and runs the tensor cores'
-//               warp-level MMA (mma.sync m16n8k32 e4m3 x e4m3 -> fp32: 16 weight rows as the
-//               A operand, up to 8 activation rows as B) and promotes the K block's product
-//               with its two scales into fp32 accumulators, as the tile GEMM does, then
-//               releases the stage.  At the end of an item each warp stores its partial sums
+//               16-byte pieces from shared memory into registers, releases the stage, and
+//               runs the tensor cores' warp-level MMA (mma.sync m16n8k32 e4m3 x e4m3 -> fp32:
+//               16 weight rows as the A operand, up to 8 activation rows as B) and promotes
+//               the K block's product with its two scales into fp32 accumulators, as the tile
+//               GEMM does.  At the end of an item each warp stores its partial sums
 //               to one of two reduction buffers and goes on with the next item.
-//   warps 9..12 epilogue: add the eight partial sums in warp order (deterministic) and
+//   warps 9..11 epilogue: add the eight partial sums in warp order (deterministic) and
 //               finish the item while the MMA warps stream the next ones.
 // The k order inside an MMA is free as long as A and B agree: lane (g, t) gives bytes
 // 16t..16t+7 (and 64+16t..) of weight rows g and g+8 and of activation row g to one MMA
@@ -67,7 +67,7 @@ namespace {
 
 constexpr int kCols = kDecodeCols;              // routed rows per expert at most: the MMA's 8 B columns
 constexpr int kMmaWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 3;
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreads = (1 + kMmaWarps + kEpiWarps) * 32;
 constexpr int kMaxStages = 4;
@@ -395,12 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Gemm& G = second ? G2 : G1;
             const uint8_t* st = ring + static_cast<size_t>(stage) * SB;
             const int xr = ctl->stage_rows[stage];
-            // this warp's K blocks of the stage: cw and cw + 8
+            // this warp's K blocks of the stage, cw and cw + 8: both into registers, the stage
+            // released, then their MMAs
+            uint4 wv[2][2][2][2], xv[2][2];   // [half][tile][row g / g+8][K half c], [half][K half c]
+            float ws[2][2], xa[2], xb[2];
+            bool live[2];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int kbi = cw + 8 * half, kb = grp * G.GKB + kbi;
-                if (kbi >= G.GKB || kb >= G.KB) continue;
-                uint4 wv[2][2][2], xv[2];   // [tile][row g / g+8][K half c], [K half c]
+                live[half] = kbi < G.GKB && kb < G.KB;
+                if (!live[half]) continue;
                 // 128-byte rows of the stage's weight boxes, tile-packed with the 128-byte swizzle:
                 //   w2: [K block][32 rows]       w13: gate box, up box, each [K block][16 rows]
                 // [E, N, K] without swizzle:
@@ -422,18 +426,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint8_t* rp = st + box + srow * 128;
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
-                            wv[tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
+                            wv[half][tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
                     }
                 // the stage holds xr activation rows: B columns past them are zero (their results
                 // are never read)
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
-                    xv[c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWeightBytes + (g * G.GKB + kbi) * 128 +
-                                                                     64 * c + 16 * t)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-                const float ws[2] = {ctl->scl[stage][kbi], ctl->scl[stage][kGroupKB + kbi]};
-                const float xa = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
-                const float xb = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                    xv[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWeightBytes +
+                                                                           (g * G.GKB + kbi) * 128 + 64 * c + 16 * t)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                ws[half][0] = ctl->scl[stage][kbi];
+                ws[half][1] = ctl->scl[stage][kGroupKB + kbi];
+                xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
+                xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                if (!live[half]) continue;
                 // four independent chains (tile, K half c) of two MMAs each
                 float f[2][2][4];
 #pragma unroll
@@ -448,22 +459,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
-                            mma_16x8x32(f[tile][c], word(wv[tile][0][c], 2 * h), word(wv[tile][1][c], 2 * h),
-                                        word(wv[tile][0][c], 2 * h + 1), word(wv[tile][1][c], 2 * h + 1),
-                                        word(xv[c], 2 * h), word(xv[c], 2 * h + 1));
+                            mma_16x8x32(f[tile][c], word(wv[half][tile][0][c], 2 * h),
+                                        word(wv[half][tile][1][c], 2 * h), word(wv[half][tile][0][c], 2 * h + 1),
+                                        word(wv[half][tile][1][c], 2 * h + 1), word(xv[half][c], 2 * h),
+                                        word(xv[half][c], 2 * h + 1));
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile) {
                     // accumulator (row g / g+8, column 2t / 2t+1): the weight block's scale times the
                     // column's activation scale
-                    const float s0 = ws[tile] * xa, s1 = ws[tile] * xb;
+                    const float s0 = ws[half][tile] * xa[half], s1 = ws[half][tile] * xb[half];
                     acc[tile][0] = fmaf(f[tile][0][0] + f[tile][1][0], s0, acc[tile][0]);
                     acc[tile][1] = fmaf(f[tile][0][1] + f[tile][1][1], s1, acc[tile][1]);
                     acc[tile][2] = fmaf(f[tile][0][2] + f[tile][1][2], s0, acc[tile][2]);
                     acc[tile][3] = fmaf(f[tile][0][3] + f[tile][1][3], s1, acc[tile][3]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
             if (grp == G.NG - 1) {
                 // the item's last stage: partial sums to a reduction buffer
                 const uint32_t buf = iter % kRedBufs, use = iter / kRedBufs;
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------ epilogue warps
-        const int et = threadIdx.x - kFirstEpiWarp * 32;   // 0..127
+        const int et = threadIdx.x - kFirstEpiWarp * 32;   // 0..95
         const int ew = warp - kFirstEpiWarp;
         uint32_t iter = 0;
         while (true) {
@@ -506,9 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                 cnt = cnt > a.cols ? a.cols : cnt;
             }
-            // this thread's outputs: w13 (row r of 16, column j); w2 (row r of 32, columns j, j+4)
-            const int r = second ? (et & 31) : (et & 15);
-            const int j = second ? (et >> 5) : (et >> 4);
             // partial sums of (row rr of a 16-row tile, column jj): lane (rr % 8) * 4 + jj / 2,
             // register (rr >= 8 ? 2 : 0) + (jj & 1), added in warp order
             auto total_of = [&](int tile, int rr, int jj) {
@@ -518,32 +525,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cw = 0; cw < kMmaWarps; ++cw) s += ctl->red[buf][cw][tile][l][c];
                 return s;
             };
-            float v0, v1;
-            if (second) {
-                v0 = total_of(r >> 4, r & 15, j);
-                v1 = total_of(r >> 4, r & 15, j + 4);
-            } else {
-                v0 = total_of(0, r, j);    // gate
-                v1 = total_of(1, r, j);    // up
+            // the item's outputs, consecutive threads on consecutive rows of one column: w2 32 rows
+            // x 8 columns (bf16(router weight * C) to the pair's row of y), w13 16 rows x 8 columns
+            // (h = silu(gate) * up by pair; silu(g) * up = g * up / (1 + e^-g), as the tile GEMM)
+            const int rows = second ? 32 : 16;
+            for (int idx = et; idx < rows * kCols; idx += kEpiWarps * 32) {
+                const int r = idx % rows, j = idx / rows;
+                if (j >= cnt) continue;
+                if (second) {
+                    const float v = total_of(r >> 4, r & 15, j);
+                    a.y[static_cast<int64_t>(tl.pair[j]) * a.H + u * 32 + r] =
+                        static_cast<uint16_t>(bf16x2(tl.weight[j] * v, 0.0f) & 0xFFFFu);
+                } else {
+                    const float gate = total_of(0, r, j), up = total_of(1, r, j);
+                    a.h[static_cast<int64_t>(tl.pair[j]) * I + u * 16 + r] =
+                        __fdividef(gate * up, 1.0f + __expf(-gate));
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl->red_empty[buf]));
             ++iter;
-
-            if (second) {
-                // consecutive threads take consecutive rows of one pair's output row
-                if (j < cnt)
-                    a.y[static_cast<int64_t>(tl.pair[j]) * a.H + u * 32 + r] =
-                        static_cast<uint16_t>(bf16x2(tl.weight[j] * v0, 0.0f) & 0xFFFFu);
-                if (j + 4 < cnt)
-                    a.y[static_cast<int64_t>(tl.pair[j + 4]) * a.H + u * 32 + r] =
-                        static_cast<uint16_t>(bf16x2(tl.weight[j + 4] * v1, 0.0f) & 0xFFFFu);
-                continue;
-            }
-            if (j < cnt) {
-                // silu(g) * up = g * up / (1 + e^-g), as the tile GEMM's epilogue
-                a.h[static_cast<int64_t>(tl.pair[j]) * I + u * 16 + r] = __fdividef(v0 * v1, 1.0f + __expf(-v0));
-            }
+            if (second) continue;
             // the item that completes a 1x128 group requantises it
             epilogue_barrier();
             const int grp = u / kGroupItems;

@@ -319,7 +319,7 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
  * run in another order, so results agree with the tile path to fp32 rounding, not bit for
  * bit.  With events, its time is recorded as the w13 GEMM stage and the w2 stage is empty.
  *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300: the decode
- *                    path for one-token steps, the tile GEMMs otherwise
+ *                    path for steps of one or two tokens, the tile GEMMs otherwise
  *   MOE_DECODE_OFF:  always the tile GEMMs
  *   MOE_DECODE_ON:   the decode path whenever the step qualifies */
 #define MOE_DECODE_AUTO 0

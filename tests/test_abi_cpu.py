@@ -56,7 +56,8 @@ def test_host_only_queries():
     assert ws >= rows * 7168 + rows * 2048 + 32768 * 7168 * 2
     assert moe.moe_fp8_block_workspace_size(16, 256, 256, 4, 2) > 0
     # route + sort/quantise (one kernel up to 512 pairs, four above) + two GEMMs + weighted sum
-    assert moe.moe_fp8_block_forward_kernel_count(2, 7168, 2048, 256, 8) == 5
+    assert moe.moe_fp8_block_forward_kernel_count(2, 7168, 2048, 256, 8) == 4
+    assert moe.moe_fp8_block_forward_kernel_count(3, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(64, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(65, 7168, 2048, 256, 8) == 8
     assert moe.moe_fp8_block_forward_kernel_count(0, 7168, 2048, 256, 8) == 0
@@ -69,7 +70,7 @@ def test_decode_path_selection():
     "on"."""
     dp = moe.moe_fp8_block_decode_path
     assert dp(1, 7168, 2048, 8, "on") and dp(8, 7168, 2048, 8, "on")
-    assert dp(1, 7168, 2048, 8) and not dp(2, 7168, 2048, 8)
+    assert dp(1, 7168, 2048, 8) and dp(2, 7168, 2048, 8) and not dp(3, 7168, 2048, 8)
     assert not dp(9, 7168, 2048, 8) and not dp(4096, 7168, 2048, 8)
     # route + sort/quantise + both GEMMs in one kernel + weighted sum
     assert moe.moe_fp8_block_forward_kernel_count(1, 7168, 2048, 256, 8) == 4
