@@ -122,16 +122,17 @@ def test_route_limits(E, topk, scoring):
     assert ids.cpu()[0].tolist() == list(range(topk))
 
 
+@pytest.mark.parametrize("T", [300, 40])
 @pytest.mark.parametrize("E,n_group,topk_group,topk", [
     (96, 4, 2, 6),      # 24-expert groups over 6 lanes: the shared-memory kernel
     (72, 6, 3, 5),      # 12-expert groups over 3 lanes: the shared-memory kernel
     (48, 3, 2, 5),      # 16-expert groups over 8 lanes: the register kernel
     (160, 5, 3, 8),     # 32-expert groups over 4 lanes, 20 of 32 lanes used: the register kernel
     (512, 16, 5, 12),   # 32-expert groups over 2 lanes: the register kernel
+    (1024, 32, 7, 32),  # the most experts, groups and choices
 ])
-def test_route_grouped_shapes_bit_exact(E, n_group, topk_group, topk):
+def test_route_grouped_shapes_bit_exact(E, n_group, topk_group, topk, T):
     g = torch.Generator().manual_seed(E + n_group)
-    T = 300
     logits = torch.randn(T, E, generator=g)
     logits[0] = 0.25                                  # all ties: lowest groups, lowest indices
     bias = torch.randn(E, generator=g) * 0.01
@@ -143,12 +144,13 @@ def test_route_grouped_shapes_bit_exact(E, n_group, topk_group, topk):
     np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T", [512, 64])
 @pytest.mark.parametrize("n_group,topk_group,with_bias", [(1, 1, False), (8, 4, True), (4, 2, False)])
-def test_route_near_ties_fall_back_to_exact_scores(n_group, topk_group, with_bias):
+def test_route_near_ties_fall_back_to_exact_scores(n_group, topk_group, with_bias, T):
     """Logits a few fp32 ulps apart make the fp32 sigmoids too close to decide: the kernel must
     repeat those tokens on the exact (fp64-evaluated) scores and still match the oracle bit-exactly."""
     g = torch.Generator().manual_seed(n_group * 10 + topk_group)
-    T, E, k = 512, 64, 6
+    E, k = 64, 6
     logits = (0.5 + torch.randint(0, 6, (T, E), generator=g).float() * 2.0 ** -22).float()
     logits[T // 2:] = torch.randn(T - T // 2, E, generator=g)       # ordinary rows take the fast path
     bias = (torch.randint(0, 3, (E,), generator=g).float() * 2.0 ** -24) if with_bias else None
