@@ -93,6 +93,9 @@ struct ForwardLayout {
 // ms per step, decode path against the tile GEMMs: one token 0.085 / 0.090, two 0.140 / 0.141,
 // four 0.249 / 0.245, eight 0.421 / 0.387.
 constexpr int kDecodeAutoMaxTokens = 2;
+// the w13 GEMM visits an expert's few tiles column by column when one expert's w13 has at least
+// this many bytes (see GemmArgs::padded_offsets)
+constexpr int64_t kColumnOrderMinExpertBytes = int64_t(16) << 20;
 
 // Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
 // rows per expert), a sort small enough for the one-launch prologue (which writes the decode
@@ -587,6 +590,11 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.tile_row0 = tile_r;
         g.num_tiles = ntiles;
         g.max_tiles = L.tiles;
+        // column-by-column order for experts of a few tiles, where one expert's w13 is too large
+        // to stay in L2 while a tile sweeps its columns (Mixtral-like 117 MB, DeepSeek-V3-like
+        // 29 MB); experts of a few MB gain nothing from it and lost ~2% in measurement
+        if (static_cast<int64_t>(2) * I * H >= kColumnOrderMinExpertBytes)
+            g.padded_offsets = reinterpret_cast<const int32_t*>(ws + L.poff);
         g.epi = MOE_EPI_SILU_MUL_QUANT;
         g.scale_fmt = scale_fmt;
         g.sorted_pair_ids = sorted;

@@ -64,6 +64,8 @@ struct RegSplit {
 };
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 constexpr int SR = 8;                  // slots of the scale ring (K blocks in flight)
+constexpr int ITEMS = 256;             // work items of a CTA whose tile and column are cached in shared memory
+constexpr int PAIR_TILES = 4;          // experts with at most this many tiles take their tiles column by column
 constexpr int SCL = 132;               // floats per slot: 128 row scales, 2 weight-block scales, pad
 
 struct SmemCtl {
@@ -80,6 +82,8 @@ struct SmemCtl {
     float amax_x[2][2][BM];            // [tile parity][column half][row]
     alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
     alignas(16) float scl[SR][SCL];    // scale ring: a_scale of the tile's 128 rows, then the two weight scales
+    int item_m[ITEMS];                 // the CTA's work items (see item_of), in its visiting order
+    int item_n[ITEMS];
 };
 constexpr int STAGE_ROW = 20;          // floats per staged row (80 B: conflict-free 16-byte slots)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
@@ -94,13 +98,42 @@ struct Tile {
     bool ok;
 };
 
-// Work item w -> (tile m = w / NT, column block n = w % NT): consecutive CTAs take
-// the column blocks of one tile, so its A rows are shared in L2.
+// Work item w -> (tile m, column block n).  Without expert offsets: m = w / NT, n = w % NT, so
+// consecutive CTAs take the column blocks of one tile and share its A rows in L2.  With them,
+// the items of an expert whose rows fill c <= PAIR_TILES tiles (its items are w in [f*NT,
+// (f+c)*NT) either way, f its first tile) go column by column: n = l / c, m = f + l % c for
+// l = w - f*NT, so that its c tiles read each weight block one after the other and the block
+// is still in L2 for the second (an expert with 129-256 rows otherwise streamed its weights
+// twice when N is large); experts with more tiles keep the tile-by-tile order.
+__device__ __forceinline__ void item_of(const GemmArgs& a, int64_t w, int NT, int& m, int& n) {
+    const int64_t mt = w / NT;
+    m = static_cast<int>(mt);
+    n = static_cast<int>(w - mt * NT);
+    if (!a.padded_offsets) return;
+    const int e = a.tile_expert[mt];
+    if (e < 0 || e >= a.E) return;
+    const int f = a.padded_offsets[e] / BM;
+    const int c = (a.padded_offsets[e + 1] - a.padded_offsets[e]) / BM;
+    if (c < 2 || c > PAIR_TILES || mt < f || mt >= f + c) return;
+    const int64_t l = w - static_cast<int64_t>(f) * NT;
+    n = static_cast<int>(l / c);
+    m = f + static_cast<int>(l - static_cast<int64_t>(n) * c);
+}
+
 template <int EPI>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int64_t w, int NT) {
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const SmemCtl* ctl, int64_t k, int64_t w, int NT) {
     Tile t;
-    const int64_t m = w / NT;
-    t.n = static_cast<int>(w - m * NT);
+    int m, n;
+    if constexpr (EPI != MOE_EPI_SILU_MUL_QUANT) {
+        m = static_cast<int>(w / NT);
+        n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
+    } else if (k < ITEMS) {
+        m = ctl->item_m[k];
+        n = ctl->item_n[k];
+    } else {
+        item_of(a, w, NT, m, n);
+    }
+    t.n = n;
     t.e = a.tile_expert[m];
     t.row0 = a.tile_row0[m];
     t.ok = t.e >= 0 && t.e < a.E && t.row0 >= 0 && t.row0 + BM <= a.a_rows;
@@ -166,6 +199,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const int64_t total = ntiles * NT;
+    // the w13 GEMM's work items of this CTA (w = blockIdx.x + k * gridDim.x), their tiles and
+    // columns looked up once; the w2 GEMM keeps the tile-by-tile order (its column blocks of one
+    // expert run in the same wave for the shapes served, and it gained nothing measurable)
+    if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
+        for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
+            const int64_t w = blockIdx.x + k * gridDim.x;
+            if (w >= total) break;
+            int m, n;
+            item_of(a, w, NT, m, n);
+            ctl->item_m[k] = m;
+            ctl->item_n[k] = n;
+        }
+        __syncthreads();
+    }
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     if (warp < FIRST_EPI_WARP) {
@@ -178,8 +225,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, issued = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                const Tile t = decode_tile<EPI>(a, w, NT);
+            int64_t k = 0;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+                const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) {
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
@@ -238,8 +286,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int NBn = a.N / 128;
         uint32_t q = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Tile t = decode_tile<EPI>(a, w, NT);
+        int64_t k = 0;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int nb0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? t.n : t.bcol0 / 128;
             const int nb1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? NBn / 2 + t.n : (t.has1 ? nb0 + 1 : nb0);
@@ -277,8 +326,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, buf = 0, bphase = 0;
             bool ok = true;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                const Tile t = decode_tile<EPI>(a, w, NT);
+            int64_t k = 0;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+                const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) continue;
                 const uint32_t idesc = t.has1 ? idesc_full : idesc_half;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -320,8 +370,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
         uint32_t buf = 0, bphase = 0, tile_iter = 0, q = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Tile t = decode_tile<EPI>(a, w, NT);
+        int64_t k = 0;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int64_t grow = t.row0 + row;
             // rows whose sorted pair id is -1 are padding: a warp with no real row skips the

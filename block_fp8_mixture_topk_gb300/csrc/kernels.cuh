@@ -109,6 +109,11 @@ struct GemmArgs {
     const int32_t* tile_row0;
     const int32_t* num_tiles;
     int64_t max_tiles;
+    // optional [E + 1] padded row offsets of a tile table whose tiles are the experts' padded rows
+    // in order (tile m = rows [128m, 128m + 128)): lets the SiLU-epilogue GEMM visit an expert's
+    // few tiles column by column (see item_of in gemm.cu); nullptr, and the other epilogues, keep
+    // the tile-by-tile order
+    const int32_t* padded_offsets;
     int epi;
     float* out_f32;
     uint8_t* out_q;
