@@ -11,7 +11,9 @@ source.  bf16 tensors are passed as ``uint16`` arrays holding the bf16 bits.
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` except the
 bytes of the requantised intermediate (SiLU(gate)*up): those depend on fp32
-rounding order and are compared only within +-1 e4m3 code.
+rounding order and are compared only within +-1 e4m3 code.  The NVFP4 block
+step (block scale = e4m3(max|x| / 6), code = e2m1(x / scale)) is a reading of
+the pages, which name scaled_fp4_quant without its arithmetic.
 """
 from __future__ import annotations
 
@@ -61,6 +63,12 @@ def _load():
             lib.orc_route.restype = I
             lib.orc_permute.argtypes = [P, L, I, P, P, P]
             lib.orc_experts.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P, I]
+            lib.orc_experts_nvfp4.argtypes = [P, P, P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P, I]
+            lib.orc_e2m1_value.argtypes = [I]
+            lib.orc_e2m1_value.restype = ctypes.c_double
+            lib.orc_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.orc_e2m1_encode.restype = ctypes.c_uint8
+            lib.orc_quant_nvfp4_bf16.argtypes = [P, L, L, L, P, P, P]
             lib.orc_combine.argtypes = [P, P, P, P, L, L, I, P]
             lib.orc_num_threads.restype = I
             _lib = lib
@@ -148,6 +156,34 @@ def quant_1x128_f32(x: np.ndarray, scale_fmt: int = SCALE_F32):
     return q, s
 
 
+def e2m1_values() -> np.ndarray:
+    """fp64 value of each of the 16 e2m1 (fp4) codes."""
+    lib = _load()
+    return np.array([lib.orc_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """fp32 values -> e2m1 codes (nearest, ties to even, saturating at +-6), one per uint8."""
+    x = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.orc_e2m1_encode(float(v)) for v in x.reshape(-1)], dtype=np.uint8).reshape(x.shape)
+
+
+def quant_nvfp4_bf16(w_bits: np.ndarray):
+    """NVFP4 quantisation of stacked expert weights (page "vllm.model_executor.layers.quantization.
+    online.nvfp4", _quantize_moe_weight_to_nvfp4): bf16 bits [E, N, K] (K % 16 == 0) ->
+    (codes [E, N, K/2] u8, element 2i in the low nibble; block scales [E, N, K/16] u8 (e4m3 bits);
+    global scales [E] f32 = 1 / ((6 * 448) / amax))."""
+    w_bits = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    E, N, K = w_bits.shape
+    assert K % 16 == 0
+    q = np.zeros((E, N, K // 2), dtype=np.uint8)
+    sf = np.zeros((E, N, K // 16), dtype=np.uint8)
+    gs = np.zeros(E, dtype=np.float32)
+    _load().orc_quant_nvfp4_bf16(_ptr(w_bits), E, N, K, _ptr(q), _ptr(sf), _ptr(gs))
+    return q, sf, gs
+
+
 def quant_128x128_bf16(w_bits: np.ndarray, scale_fmt: int = SCALE_F32):
     """128x128 block quantisation of stacked bf16 weights [E,N,K]: (codes [E,N,K], scales [E,N/128,K/128])."""
     w = np.ascontiguousarray(w_bits, dtype=np.uint16)
@@ -204,12 +240,57 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
     Returns a dict with ids, weights, offsets, sorted, pos, a1q, a1s, a2q, a2s
     (by sorted row), c2 (by sorted row), out (fp64 [T,H]) and out_bf16 bits.
     """
+    E, N1, H2 = w13.shape
+    assert N1 % 256 == 0
+    I = N1 // 2
+    assert w2.shape == (E, H2, I)
+    w13c = np.ascontiguousarray(w13, dtype=np.uint8)
+    w2c = np.ascontiguousarray(w2, dtype=np.uint8)
+    w13s = np.ascontiguousarray(w13_scale, dtype=np.float32)
+    w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
+
+    def experts(a1q, a1s, offsets, sorted_, need, T, H, topk_, a2q, a2s, c1, c2):
+        _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
+                            _ptr(offsets), _ptr(sorted_), _ptr(need), T, H, I, E, topk_,
+                            _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2), scale_fmt)
+
+    return _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring, bias, n_group,
+                         topk_group, routed_scaling, tokens, want_c1, scale_fmt)
+
+
+def moe_forward_nvfp4(hidden_bits, logits, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, topk, renormalize=True,
+                      scoring=SOFTMAX, bias=None, n_group=1, topk_group=1, routed_scaling=1.0,
+                      tokens=None, want_c1=False, scale_fmt=SCALE_F32):
+    """The whole layer with NVFP4 expert weights (page "vllm.model_executor.layers.quantization.
+    online.nvfp4", _quantize_moe_weight_to_nvfp4): the same routing, activation quantisation,
+    SiLU(gate)*up requantisation and combine as ``moe_forward``; the weight values are
+    code * block scale * global scale.
+
+    w13 [E,2I,H/2] u8 (two fp4 codes per byte), w13_sf [E,2I,H/16] u8 (e4m3 bits), w13_gs [E] f32;
+    w2 [E,H,I/2], w2_sf [E,H,I/16], w2_gs [E].  Returns the same dict as ``moe_forward``.
+    """
+    E, N1, H2h = w13.shape
+    assert N1 % 256 == 0
+    I = N1 // 2
+    H = 2 * H2h
+    assert w13_sf.shape == (E, N1, H // 16) and w2.shape == (E, H, I // 2) and w2_sf.shape == (E, H, I // 16)
+    c = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w13, w13_sf, w2, w2_sf)]
+    g = [np.ascontiguousarray(a, dtype=np.float32).reshape(E) for a in (w13_gs, w2_gs)]
+
+    def experts(a1q, a1s, offsets, sorted_, need, T, H_, topk_, a2q, a2s, c1, c2):
+        _load().orc_experts_nvfp4(_ptr(a1q), _ptr(a1s), _ptr(c[0]), _ptr(c[1]), _ptr(g[0]), _ptr(c[2]),
+                                  _ptr(c[3]), _ptr(g[1]), _ptr(offsets), _ptr(sorted_), _ptr(need), T, H_, I,
+                                  E, topk_, _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2), scale_fmt)
+
+    return _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring, bias, n_group,
+                         topk_group, routed_scaling, tokens, want_c1, scale_fmt)
+
+
+def _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring, bias, n_group, topk_group,
+                  routed_scaling, tokens, want_c1, scale_fmt):
     hidden_bits = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
     T, H = hidden_bits.shape
-    E, N1, H2 = w13.shape
-    assert H2 == H and N1 % 256 == 0
-    I = N1 // 2
-    assert w2.shape == (E, H, I)
+    N1 = 2 * I
     ids, wts = route(logits, topk, renormalize, scoring, bias, n_group, topk_group, routed_scaling)
     offsets, sorted_, pos = permute(ids, E)
     a1q, a1s = quant_1x128_bf16(hidden_bits, scale_fmt)
@@ -223,13 +304,7 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
     a2s = np.zeros((P, I // 128), dtype=np.float32)
     c1 = np.full((P, N1), np.nan) if want_c1 else None
     c2 = np.full((P, H), np.nan)
-    w13c = np.ascontiguousarray(w13, dtype=np.uint8)
-    w2c = np.ascontiguousarray(w2, dtype=np.uint8)
-    w13s = np.ascontiguousarray(w13_scale, dtype=np.float32)
-    w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
-    _load().orc_experts(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
-                        _ptr(offsets), _ptr(sorted_), _ptr(need), T, H, I, E, topk,
-                        _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2), scale_fmt)
+    experts(a1q, a1s, offsets, sorted_, need, T, H, topk, a2q, a2s, c1, c2)
     out = np.full((T, H), np.nan)
     _load().orc_combine(_ptr(c2), _ptr(wts), _ptr(pos), _ptr(need), T, H, topk, _ptr(out))
     out_bf16 = np.zeros((T, H), dtype=np.uint16)

@@ -22,7 +22,8 @@
  *    only steers selection; group score = sum of the two largest biased scores;
  *  - ties in every top-k resolve to the lower index;
  *  - w13 rows [0, I) are the gate projection, rows [I, 2I) the up projection;
- *  - the intermediate SiLU(gate)*up is requantised from fp32 values.
+ *  - the intermediate SiLU(gate)*up is requantised from fp32 values;
+ *  - NVFP4 block step: block scale = e4m3(max|x| / 6), code = e2m1(x / block scale).
  *
  * Parity pins: every function here is checked by tests against closed forms,
  * exhaustive enumeration, brute force on tiny inputs or an independent
@@ -215,6 +216,84 @@ void orc_quant_128x128_bf16(const uint16_t* w, long E, long N, long K, uint8_t* 
 }
 
 /* ------------------------------------------------------------------------- */
+/* e2m1 (fp4) format ("FLOAT4_E2M1_MAX" = 6, [NVFP4] _quantize_moe_weight_to_nvfp4):
+ * 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no infinities or NaN.
+ * Normal (e > 0): (1 + m/2) * 2^(e-1); subnormal (e = 0): m/2.  Two codes per byte in the
+ * packed [.., K/2] tensors: element 2i in the low nibble, 2i + 1 in the high nibble. */
+double orc_e2m1_value(int code) {
+    int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Round an fp32 value to the nearest e2m1 value, ties to the even code, saturating at +-6;
+ * the sign bit follows the input's (a negative value that rounds to zero gives -0). */
+uint8_t orc_e2m1_encode(float xf) {
+    double x = (double)xf;
+    int neg = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    int c;
+    if (isnan(x)) {
+        c = 0;                                   /* e2m1 has no NaN; not produced by the quantiser */
+    } else if (a >= 6.0) {
+        c = 7;
+    } else {
+        /* codes 0..7 hold the non-negative values in increasing order */
+        c = 0;
+        while (c < 7 && orc_e2m1_value(c + 1) <= a) ++c;
+        if (orc_e2m1_value(c) != a) {
+            double below = a - orc_e2m1_value(c), above = orc_e2m1_value(c + 1) - a;
+            if (above < below || (above == below && (c & 1))) ++c;   /* tie: even mantissa */
+        }
+    }
+    return (uint8_t)(c | (neg ? 8 : 0));
+}
+
+/* NVFP4 quantisation of stacked expert weights [E, N, K] as [NVFP4]
+ * _quantize_moe_weight_to_nvfp4 states it: per expert, amax over the whole [N, K] (floored at
+ * 1e-8), global_scale = (FLOAT4_E2M1_MAX * FLOAT8_E4M3_MAX) / amax, the weights multiplied by it
+ * in fp32 and rounded back to bf16; those quantised in blocks of 16 along K with one FP8 (e4m3)
+ * scale per block; stored: fp4 codes [E, N, K/2], block scales [E, N, K/16] and the per-expert
+ * global scale 1 / global_scale [E].  The block step (scaled_fp4_quant with a unit global scale)
+ * is not printed on the pages; its reading here, as for the FP8 groups: block scale =
+ * e4m3(max|x| / 6), code = e2m1(x / block scale) (fp32 divisions; a zero scale gives code 0). */
+void orc_quant_nvfp4_bf16(const uint16_t* w, long E, long N, long K, uint8_t* q, uint8_t* sf, float* gs2) {
+    e4m3_build();
+    long KB16 = K / 16;
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < E; ++e) {
+        float amax = 0.0f;
+        for (long i = 0; i < N * K; ++i) {
+            float a = fabsf(bf16_to_f32(w[e * N * K + i]));
+            if (a > amax) amax = a;
+        }
+        if (amax < 1e-8f) amax = 1e-8f;
+        float gsc = (6.0f * 448.0f) / amax;             /* fp32 IEEE division */
+        gs2[e] = 1.0f / gsc;
+        for (long n = 0; n < N; ++n) {
+            for (long b = 0; b < KB16; ++b) {
+                float v[16];
+                float vmax = 0.0f;
+                for (int i = 0; i < 16; ++i) {
+                    long idx = (e * N + n) * K + b * 16 + i;
+                    uint16_t bits = orc_bf16_from_f64((double)(bf16_to_f32(w[idx]) * gsc));   /* fp32 product -> bf16 */
+                    v[i] = bf16_to_f32(bits);
+                    if (fabsf(v[i]) > vmax) vmax = fabsf(v[i]);
+                }
+                uint8_t s = orc_e4m3_encode(vmax / 6.0f);
+                float sv = (float)e4m3_val[s];
+                sf[(e * N + n) * KB16 + b] = s;
+                for (int i = 0; i < 16; i += 2) {
+                    uint8_t lo = sv == 0.0f ? 0 : orc_e2m1_encode(v[i] / sv);
+                    uint8_t hi = sv == 0.0f ? 0 : orc_e2m1_encode(v[i + 1] / sv);
+                    q[((e * N + n) * K + b * 16 + i) / 2] = (uint8_t)((lo & 15) | ((hi & 15) << 4));
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Top-k routing ("router — top-K router", [QMO] FusedMoE Class; "fused grouped
  * top-K routing", [QMO] Key Environment Variables).
  *
@@ -370,13 +449,16 @@ void orc_permute(const int32_t* ids, long P, int E, int32_t* offsets, int32_t* s
  * others are left untouched), so large configurations can be sampled.
  *
  * a2q: [P, I], a2s: [P, I/128], c1: [P, 2I] (may be NULL), c2: [P, H] fp64,
- * each indexed by sorted row. */
-void orc_experts(const uint8_t* a1q, const float* a1s,
-                 const uint8_t* w13, const float* w13s, const uint8_t* w2, const float* w2s,
-                 const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
-                 long T, long H, long I, int E, int topk,
-                 uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
-    (void)T;
+ * each indexed by sorted row.  With NVFP4 weights (orc_experts_nvfp4) only the
+ * weight values change: code(w) * block scale * global scale, see dequant_nvfp4. */
+
+/* dequantised weights of expert e: which 0 = w13 as [2I][H], 1 = w2 as [H][I], in fp64 */
+typedef void (*dequant_fn)(const void* ctx, int e, int which, long N1, long H, long I, double* wdq);
+
+static void experts_core(const uint8_t* a1q, const float* a1s, dequant_fn dq, const void* ctx,
+                         const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
+                         long H, long I, int E, int topk, uint8_t* a2q, float* a2s, double* c1, double* c2,
+                         int fmt) {
     e4m3_build();
     long N1 = 2 * I, HB = H / 128, IB = I / 128;
     double* wdq = (double*)malloc(sizeof(double) * (size_t)(N1 * H > H * I ? N1 * H : H * I));
@@ -385,12 +467,7 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
         long nrows = 0;
         for (long r = r0; r < r1; ++r) if (need[sorted[r] / topk]) nrows++;
         if (nrows == 0) continue;
-        /* dequantised w13[e] */
-#pragma omp parallel for schedule(static)
-        for (long n = 0; n < N1; ++n)
-            for (long h = 0; h < H; ++h)
-                wdq[n * H + h] = e4m3_val[w13[((long)e * N1 + n) * H + h]] *
-                                 (double)w13s[((long)e * (N1 / 128) + n / 128) * HB + h / 128];
+        dq(ctx, e, 0, N1, H, I, wdq);
 #pragma omp parallel for schedule(dynamic, 1)
         for (long r = r0; r < r1; ++r) {
             long p = sorted[r], t = p / topk;
@@ -413,12 +490,7 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
             orc_quant_1x128_f32(h1, 1, I, a2q + r * I, a2s + r * IB, fmt);
             free(a); free(g); free(h1);
         }
-        /* dequantised w2[e] */
-#pragma omp parallel for schedule(static)
-        for (long n = 0; n < H; ++n)
-            for (long i = 0; i < I; ++i)
-                wdq[n * I + i] = e4m3_val[w2[((long)e * H + n) * I + i]] *
-                                 (double)w2s[((long)e * HB + n / 128) * IB + i / 128];
+        dq(ctx, e, 1, N1, H, I, wdq);
 #pragma omp parallel for schedule(dynamic, 1)
         for (long r = r0; r < r1; ++r) {
             long p = sorted[r], t = p / topk;
@@ -435,6 +507,75 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
         }
     }
     free(wdq);
+}
+
+/* 128x128-block FP8 weights: code value times its block's fp32 scale */
+struct fp8_weights {
+    const uint8_t *w13, *w2;
+    const float *w13s, *w2s;
+};
+
+static void dequant_fp8(const void* ctx, int e, int which, long N1, long H, long I, double* wdq) {
+    const struct fp8_weights* W = (const struct fp8_weights*)ctx;
+    long HB = H / 128, IB = I / 128;
+    if (which == 0) {
+#pragma omp parallel for schedule(static)
+        for (long n = 0; n < N1; ++n)
+            for (long h = 0; h < H; ++h)
+                wdq[n * H + h] = e4m3_val[W->w13[((long)e * N1 + n) * H + h]] *
+                                 (double)W->w13s[((long)e * (N1 / 128) + n / 128) * HB + h / 128];
+    } else {
+#pragma omp parallel for schedule(static)
+        for (long n = 0; n < H; ++n)
+            for (long i = 0; i < I; ++i)
+                wdq[n * I + i] = e4m3_val[W->w2[((long)e * H + n) * I + i]] *
+                                 (double)W->w2s[((long)e * HB + n / 128) * IB + i / 128];
+    }
+}
+
+/* NVFP4 weights ([NVFP4] _quantize_moe_weight_to_nvfp4): code value times its 16-block's e4m3
+ * scale times the expert's global scale (the products are exact in fp64) */
+struct nvfp4_weights {
+    const uint8_t *w13, *w2, *w13sf, *w2sf;
+    const float *w13gs, *w2gs;
+};
+
+static void dequant_nvfp4(const void* ctx, int e, int which, long N1, long H, long I, double* wdq) {
+    const struct nvfp4_weights* W = (const struct nvfp4_weights*)ctx;
+    long N = which == 0 ? N1 : H, K = which == 0 ? H : I;
+    const uint8_t* q = which == 0 ? W->w13 : W->w2;
+    const uint8_t* sf = which == 0 ? W->w13sf : W->w2sf;
+    double gs = (double)(which == 0 ? W->w13gs : W->w2gs)[e];
+#pragma omp parallel for schedule(static)
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k) {
+            long i = ((long)e * N + n) * K + k;
+            int code = (q[i / 2] >> (4 * (k & 1))) & 15;
+            wdq[n * K + k] = orc_e2m1_value(code) * e4m3_val[sf[i / 16]] * gs;
+        }
+}
+
+void orc_experts(const uint8_t* a1q, const float* a1s,
+                 const uint8_t* w13, const float* w13s, const uint8_t* w2, const float* w2s,
+                 const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
+                 long T, long H, long I, int E, int topk,
+                 uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
+    (void)T;
+    struct fp8_weights W = {w13, w2, w13s, w2s};
+    experts_core(a1q, a1s, dequant_fp8, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt);
+}
+
+/* The same expert MLP with NVFP4 weights: codes [E, N, K/2], block scales [E, N, K/16] (e4m3),
+ * global scales [E] (fp32) for w13 and w2. */
+void orc_experts_nvfp4(const uint8_t* a1q, const float* a1s,
+                       const uint8_t* w13, const uint8_t* w13sf, const float* w13gs,
+                       const uint8_t* w2, const uint8_t* w2sf, const float* w2gs,
+                       const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
+                       long T, long H, long I, int E, int topk,
+                       uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
+    (void)T;
+    struct nvfp4_weights W = {w13, w2, w13sf, w2sf, w13gs, w2gs};
+    experts_core(a1q, a1s, dequant_nvfp4, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt);
 }
 
 /* Weighted unpermute-sum ("gathers results", [QMO] Modular Kernel Architecture;
