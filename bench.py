@@ -36,10 +36,12 @@ FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
 CSRC = os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc")
 # ncu summary of each w13 kernel and the sources it was taken on: tile GEMM, decode-path GEMM
 PROFILES = {
-    False: (os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md"),
-            [os.path.join(CSRC, f) for f in ("gemm.cu", "common.cuh")]),
-    True: (os.path.join(ROOT, "profiles", "decode_mlp_dsv3_decode.md"),
-           [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
+    "tile": (os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md"),
+             [os.path.join(CSRC, f) for f in ("gemm.cu", "common.cuh")]),
+    "decode": (os.path.join(ROOT, "profiles", "decode_mlp_dsv3_decode.md"),
+               [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
+    "nvfp4": (os.path.join(ROOT, "profiles", "decode_mlp_nvfp4_dsv3_decode.md"),
+              [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
 }
 
 
@@ -63,8 +65,9 @@ def parse():
     p.add_argument("--decode", choices=["auto", "off", "on"], default="auto",
                    help="expert GEMMs of small steps: decode-path kernels for up to 8 tokens (auto), never, "
                         "or whenever the step qualifies")
-    p.add_argument("--weights", choices=["tiled", "nk"], default="tiled",
-                   help="expert weight layout: tile-packed at load time (default) or the pages' [E, N, K]")
+    p.add_argument("--weights", choices=["tiled", "nk", "nvfp4"], default="tiled",
+                   help="expert weights: e4m3 tile-packed at load time (default), e4m3 in the pages' [E, N, K], "
+                        "or NVFP4 (e2m1 codes with e4m3 16-blocks and a global scale, packed; decode-path kernel)")
     return p.parse_args()
 
 
@@ -93,8 +96,21 @@ def describe(wl, world):
 
 def describe_weights(args):
     fmt = ", scales rounded up to powers of two (ue8m0)" if args.scale_fmt == "ue8m0" else ", fp32 scales"
+    if args.weights == "nvfp4":
+        return ("NVFP4: e2m1 codes, e4m3 scale per 16 along K, fp32 global scale per expert, packed at load "
+                "time (moe_nvfp4_pack_weights); activations e4m3 1x128 groups" + fmt)
     return ("e4m3 128x128 blocks, tile-packed at load time (moe_fp8_block_pack_weights)"
             if args.weights == "tiled" else "e4m3 128x128 blocks, [E, N, K] layout") + fmt
+
+
+def expert_weight_bytes(wl, nvfp4=False):
+    """Bytes one expert's w13 and w2 occupy (codes and scales): (w13, both)."""
+    H, I = wl.H, wl.I
+    if nvfp4:
+        w13 = 2 * I * H // 2 + 2 * I * H // 16 + 4
+        return w13, w13 + H * I // 2 + H * I // 16 + 4
+    w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+    return w13, 3 * H * I + ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -170,11 +186,13 @@ def whole_job_rate(world, units_per_rank, ms):
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
-def oracle_inputs(wl, tokens, device):
+def oracle_inputs(wl, tokens, device, nvfp4=False):
     """CPU copies of the workload's inputs and the oracle's own quantisation of the experts
     the sampled tokens use (untimed preparation)."""
     import numpy as np
     import oracle
+    if nvfp4:
+        return oracle_inputs_nvfp4(wl, tokens, device)
     hidden, logits = mi.hidden(wl, device), mi.router_logits(wl, device)
     bias = mi.expert_bias(wl, device)
     okw = dict(scoring=wl.scoring, bias=None if bias is None else bias.cpu().numpy(), n_group=wl.n_group,
@@ -195,20 +213,41 @@ def oracle_inputs(wl, tokens, device):
     return args, okw, len(experts)
 
 
+def oracle_inputs_nvfp4(wl, tokens, device):
+    import numpy as np
+    import oracle
+    hidden, logits = mi.hidden(wl, device), mi.router_logits(wl, device)
+    bias = mi.expert_bias(wl, device)
+    okw = dict(scoring=wl.scoring, bias=None if bias is None else bias.cpu().numpy(), n_group=wl.n_group,
+               topk_group=wl.topk_group, routed_scaling=wl.routed_scaling)
+    ids, _ = oracle.route(logits.cpu().numpy(), wl.topk, wl.renormalize, **okw)
+    experts = sorted(set(ids[tokens].reshape(-1).tolist()))
+    E, H, I = wl.E, wl.H, wl.I
+    w = [np.zeros((E, 2 * I, H // 2), np.uint8), np.zeros((E, 2 * I, H // 16), np.uint8), np.ones(E, np.float32),
+         np.zeros((E, H, I // 2), np.uint8), np.zeros((E, H, I // 16), np.uint8), np.ones(E, np.float32)]
+    for e in experts:
+        for i, t in ((0, mi.w13_bf16(wl, device, [e])), (3, mi.w2_bf16(wl, device, [e]))):
+            q, sf, gs = oracle.quant_nvfp4_bf16(mi.bf16_bits(t))
+            w[i][e], w[i + 1][e], w[i + 2][e] = q[0], sf[0], gs[0]
+    args = (mi.bf16_bits(hidden), logits.cpu().numpy(), *w, wl.topk, wl.renormalize)
+    return args, okw, len(experts)
+
+
 def default_sample(wl):
     return max(1, min(wl.T, 2 if wl.E * wl.H * wl.I > 1e9 else 16))
 
 
-def time_oracle(wl, n_tokens, device, runs=1, warmup=0):
+def time_oracle(wl, n_tokens, device, runs=1, warmup=0, nvfp4=False):
     import oracle
     tokens = list(range(n_tokens))
-    args, okw, n_exp = oracle_inputs(wl, tokens, device)
+    args, okw, n_exp = oracle_inputs(wl, tokens, device, nvfp4)
+    layer = oracle.moe_forward_nvfp4 if nvfp4 else oracle.moe_forward
     for _ in range(warmup):
-        oracle.moe_forward(*args, tokens=tokens, **okw)
+        layer(*args, tokens=tokens, **okw)
     times = []
     for _ in range(runs):
         t0 = time.perf_counter()
-        oracle.moe_forward(*args, tokens=tokens, **okw)
+        layer(*args, tokens=tokens, **okw)
         times.append(time.perf_counter() - t0)
     sample = (f"first {n_tokens} of {wl.T} tokens ({n_tokens * wl.topk} routed pairs over {n_exp} experts); "
               f"routing, sort and quantisation of all {wl.T} tokens included")
@@ -219,7 +258,8 @@ def run_reference(args, wl):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     n = args.cpu_sample or default_sample(wl)
-    times, sample, cores = time_oracle(wl, n, "cpu", runs=args.steps, warmup=args.warmup)
+    times, sample, cores = time_oracle(wl, n, "cpu", runs=args.steps, warmup=args.warmup,
+                                       nvfp4=args.weights == "nvfp4")
     ms = 1000.0 * sum(times) / len(times)
     value = n / (ms / 1000.0)
     line = {"impl": "reference", "metric": "block-FP8 fused-MoE tokens/s", "value": value, "unit": "tokens/s",
@@ -233,17 +273,18 @@ def run_reference(args, wl):
 
 
 # ----------------------------------------------------------------------------- ours (GPU)
-def gemm_source_sha(decode=False):
+def gemm_source_sha(mode="tile"):
     h = hashlib.sha256()
-    for f in PROFILES[decode][1]:
+    for f in PROFILES[mode][1]:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(wl, decode=False):
-    """dram bytes per launch of the w13 GEMM (tile or decode-path kernel) from the committed ncu
-    summary, if it was taken on the current kernel source for this workload; else None."""
-    path = PROFILES[decode][0]
+def profiled_traffic(wl, mode="tile"):
+    """dram bytes per launch of the w13 GEMM (tile GEMM, decode-path kernel, or the decode-path
+    kernel on NVFP4 weights) from the committed ncu summary, if it was taken on the current kernel
+    source for this workload; else None."""
+    path = PROFILES[mode][0]
     if not os.path.exists(path):
         return None
     kv = {}
@@ -251,7 +292,7 @@ def profiled_traffic(wl, decode=False):
         if "=" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split("=", 1)
             kv[k.strip()] = v.strip().strip("`")
-    if kv.get("source_sha") != gemm_source_sha(decode) or kv.get("workload") != wl.name:
+    if kv.get("source_sha") != gemm_source_sha(mode) or kv.get("workload") != wl.name:
         return None
     if "tokens" in kv and kv["tokens"] != str(wl.T):
         return None
@@ -282,14 +323,34 @@ def run_ours(args, wl):
     rp = (moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling, bias)
           if wl.scoring == mi.SIGMOID else moe.RoutingParams("softmax", 1, 1, wl.routed_scaling))
     E, H, I = wl.E, wl.H, wl.I
-    w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
-    w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
-    w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
-    w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
-    for e0 in range(0, E, 8):
-        ex = range(e0, min(E, e0 + 8))
-        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), args.scale_fmt)
-        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), args.scale_fmt)
+    nvfp4 = args.weights == "nvfp4"
+    if nvfp4:
+        # NVFP4: quantised and packed at load time, a few experts at a time (untimed)
+        unit = 16 * 64 + 16 * 8
+        w13q = torch.empty(E, 2 * I // 16, H // 128, unit, dtype=torch.uint8, device=dev)
+        w2q = torch.empty(E, H // 16, I // 128, unit, dtype=torch.uint8, device=dev)
+        w13s = torch.empty(E, dtype=torch.float32, device=dev)
+        w2s = torch.empty(E, dtype=torch.float32, device=dev)
+        for e0 in range(0, E, 8):
+            ex = range(e0, min(E, e0 + 8))
+            n = len(ex)
+            q, sf, w13s[e0:e0 + n] = moe.moe_nvfp4_quant_weight(mi.w13_bf16(wl, dev, ex))
+            w13q[e0:e0 + n] = moe.moe_nvfp4_pack_weights(q, sf)
+            q, sf, w2s[e0:e0 + n] = moe.moe_nvfp4_quant_weight(mi.w2_bf16(wl, dev, ex))
+            w2q[e0:e0 + n] = moe.moe_nvfp4_pack_weights(q, sf)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    else:
+        w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+        for e0 in range(0, E, 8):
+            ex = range(e0, min(E, e0 + 8))
+            w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex),
+                                                                                        args.scale_fmt)
+            w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex),
+                                                                                      args.scale_fmt)
     if args.weights == "tiled":
         # load-time conversion into the kernels' tile-packed layout (untimed, like the quantisation)
         w13q = moe.moe_fp8_block_pack_weights(w13q)
@@ -306,6 +367,12 @@ def run_ours(args, wl):
     launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
     if decode != moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk):
         launches_per_step += -1 if decode else 1
+    if nvfp4:
+        if args.decode == "off":
+            raise SystemExit("NVFP4 weights run on the decode-path kernel: --decode off does not apply")
+        # route, sort + quantise, the decode kernel, the weighted sum, per 8 tokens
+        decode = True
+        launches_per_step = 4 * ((wl.T + 7) // 8)
 
     def step(events=None):
         moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
@@ -424,8 +491,7 @@ def run_ours(args, wl):
     pk = peaks()
     tokens_s = whole_job_rate(world, wl.T, ms)
     flops = wl.flops()
-    per_expert_w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
-    per_expert = 3 * H * I + ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128)) * 4
+    per_expert_w13, per_expert = expert_weight_bytes(wl, nvfp4)
     layer_bytes = touched * per_expert + wl.T * H * 2 * 2 + wl.T * E * 4
     # algorithmic bytes of one w13 GEMM launch: touched experts' w13 + scales, the sorted activation
     # rows and scales read once, the requantised intermediate and its scales written once
@@ -448,16 +514,18 @@ def run_ours(args, wl):
         roof = {"bound": "hbm", "achieved": gemm_bytes / (g_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = ("decode_mlp_kernel (both GEMMs, decode path)" if decode
+    roof["kernel"] = ("decode_mlp_kernel<nvfp4> (both GEMMs, decode path, NVFP4 weights)" if nvfp4
+                      else "decode_mlp_kernel (both GEMMs, decode path)" if decode
                       else "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)")
     roof["algorithmic_bytes_per_launch"] = gemm_bytes
     roof["ms_per_launch"] = g_ms
-    roof["traffic"] = profiled_traffic(wl, decode)
+    roof["traffic"] = profiled_traffic(wl, "nvfp4" if nvfp4 else "decode" if decode else "tile")
 
     line = {"metric": "block-FP8 fused-MoE tokens/s", "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-            "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e4m3 (f16 MMA)" if nvfp4 else "e4m3",
+            "data": ("synthetic (seeded; weights N(0,0.02) quantised to NVFP4)" if nvfp4 else
+                     "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)"),
             "config": describe(wl, world), "weights_layout": describe_weights(args),
             "tflops": world * flops / (ms / 1e3) / 1e12,
             "pct_fp8_peak": world * flops / (ms / 1e3) / 1e12 / fp8_peak,
@@ -472,7 +540,7 @@ def run_ours(args, wl):
             "roofline": roof}
     if world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or default_sample(wl)
-        times, sample, cores = time_oracle(wl, n, dev, runs=1)
+        times, sample, cores = time_oracle(wl, n, dev, runs=1, nvfp4=nvfp4)
         line["cpu_baseline"] = {"value": n / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     print(json.dumps(line), flush=True)
@@ -489,6 +557,8 @@ def run_masked(args, wl):
     import block_fp8_mixture_topk_gb300 as moe
     import oracle
 
+    if args.weights == "nvfp4":
+        raise SystemExit("the masked layout takes FP8 weights (--weights tiled or nk)")
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     E, H, I = wl.E, wl.H, wl.I

@@ -26,6 +26,10 @@ from .ops import (  # noqa: F401
     moe_get_device_status,
     moe_max_padded_rows,
     moe_max_tiles,
+    moe_nvfp4_forward,
+    moe_nvfp4_pack_weights,
+    moe_nvfp4_packed_bytes,
+    moe_nvfp4_quant_weight,
     moe_route_topk,
     moe_unpermute_sum,
 )

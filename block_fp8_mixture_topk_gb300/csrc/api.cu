@@ -323,6 +323,39 @@ int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* p
     return cuda_rc(launch_pack_weights(w, E, N, K, packed, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* block_scale,
+                           float* global_scale, void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (K % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (static_cast<int64_t>(E) * N * (K / 16) >= (int64_t(1) << 39)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!w || !q || !block_scale || !global_scale || !aligned(w, 16) || !aligned(q, 8) || !aligned(global_scale, 4))
+        return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_nvfp4_quant_weight(w, E, N, K, q, block_scale, global_scale,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_nvfp4_packed_bytes(int E, int N, int K) {
+    if (E < 0 || N < 0 || K < 0 || N % 16 != 0 || K % 128 != 0) return 0;
+    return nvfp4_packed_bytes(E, N, K);
+}
+
+int moe_nvfp4_pack_weights(const uint8_t* q, const uint8_t* block_scale, int E, int N, int K, uint8_t* packed,
+                           void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (N % 16 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (!q || !block_scale || !packed || !aligned(q, 16) || !aligned(block_scale, 8) || !aligned(packed, 16))
+        return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_nvfp4_pack(q, block_scale, E, N, K, packed, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_scale_row_stride,
                            int64_t a_scale_kb_stride, int64_t a_rows, const uint8_t* B, const float* b_scale, int N,
                            int K, int E, const int32_t* tile_expert, const int32_t* tile_row0,
@@ -466,10 +499,34 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     const int weight_layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
     const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
     const int decode_mode = opts ? opts->decode_path : MOE_DECODE_AUTO;
-    if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
+    if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED && weight_layout != MOE_WEIGHTS_NVFP4)
+        return MOE_ERR_INVALID_ARG;
     if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
     if (decode_mode != MOE_DECODE_AUTO && decode_mode != MOE_DECODE_OFF && decode_mode != MOE_DECODE_ON)
         return MOE_ERR_INVALID_ARG;
+    const bool fp4 = weight_layout == MOE_WEIGHTS_NVFP4;
+    if (fp4 && T > kDecodeCols) {
+        // NVFP4 weights run on the decode-path kernel only: steps of more tokens go through it
+        // kDecodeCols tokens at a time (every token's rows are independent)
+        if (H % 128 != 0 || I % 128 != 0 || !hidden || !router_logits || !out) return MOE_ERR_UNSUPPORTED_SHAPE;
+        // stage events: the chunks' kernels interleave, so the whole step is recorded as the w13
+        // stage (events 0-3 before the first chunk, 4-6 after the last)
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        for (int i = 0; events && i < 4; ++i)
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) != cudaSuccess) return MOE_ERR_CUDA;
+        for (int t0 = 0; t0 < T; t0 += kDecodeCols) {
+            const int n = T - t0 < kDecodeCols ? T - t0 : kDecodeCols;
+            rc = moe_fp8_block_forward_ex(hidden + static_cast<int64_t>(t0) * H,
+                                          router_logits + static_cast<int64_t>(t0) * E, w13, w13_scale, w2,
+                                          w2_scale, n, H, I, E, topk, renormalize, rp, opts, workspace,
+                                          workspace_bytes, out + static_cast<int64_t>(t0) * H, stream, nullptr);
+            if (rc != MOE_OK) return rc;
+        }
+        for (int i = 4; events && i < MOE_FORWARD_NUM_EVENTS; ++i)
+            if (cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (fp4 && decode_mode == MOE_DECODE_OFF) return MOE_ERR_INVALID_ARG;
     if (weight_layout == MOE_WEIGHTS_TILED &&
         static_cast<int64_t>(E) * 2 * I * (H / 128) >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -521,7 +578,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     // quantisation stage is then empty); larger ones by the three sort kernels and the
     // grid-wide quantiser
     const bool small = P <= kSmallPairs;
-    const bool decode = use_decode(T, H, I, topk, decode_mode);
+    if (fp4 && !decode_possible(T, H, I, topk)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const bool decode = fp4 || use_decode(T, H, I, topk, decode_mode);
     int32_t* dcnt = reinterpret_cast<int32_t*>(ws + L.dcnt);
     DecodeTile* dtab = reinterpret_cast<DecodeTile*>(ws + L.dtab);
     DecodeSetup dsetup{};
@@ -551,6 +609,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         d.w2 = w2;
         d.w2_scale = w2_scale;
         d.w_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        d.w_fp4 = fp4;
         d.H = H;
         d.I = I;
         d.E = E;

@@ -74,6 +74,9 @@ constexpr int kMaxStages = 4;
 constexpr int kGroupKB = 16;                    // K blocks per stage: two per MMA warp
 constexpr int kTileBytes = 16 * 128 * kGroupKB; // 16 weight rows over 16 K blocks
 constexpr int kWeightBytes = 2 * kTileBytes;    // a stage's weights: 32 rows over 16 K blocks
+// NVFP4 weights: a 16-row slab over 16 K blocks is 16 packed units (codes and block scales)
+constexpr int kTileBytes4 = kFp4UnitBytes * kGroupKB;
+constexpr int kWeightBytes4 = 2 * kTileBytes4;
 constexpr int kStageScales = 2 * kGroupKB + kCols * kGroupKB;   // [tile][kb] weight scales, [kb][row] activation scales
 constexpr int kGroupItems = 128 / 16;           // w13 items per 1x128 group of the intermediate
 constexpr int kRedBufs = 2;                     // items whose partial sums await the epilogue
@@ -97,13 +100,13 @@ struct Ctl {
 constexpr size_t kCtlBytes = (sizeof(Ctl) + 1023) / 1024 * 1024;
 constexpr size_t kSmemLimit = 232448;
 // a stage holds up to `cols` activation rows in a box of the next power of two rows
-size_t stage_bytes(int cols) {
+size_t stage_bytes(int cols, bool fp4 = false) {
     int r = 1;
     while (r < cols) r <<= 1;
-    return (kWeightBytes + static_cast<size_t>(r) * 128 * kGroupKB + 1023) / 1024 * 1024;
+    return ((fp4 ? kWeightBytes4 : kWeightBytes) + static_cast<size_t>(r) * 128 * kGroupKB + 1023) / 1024 * 1024;
 }
-size_t smem_bytes(int max_tiles, int stages, int cols) {
-    return 1024 + kCtlBytes + static_cast<size_t>(stages) * stage_bytes(cols) +
+size_t smem_bytes(int max_tiles, int stages, int cols, bool fp4 = false) {
+    return 1024 + kCtlBytes + static_cast<size_t>(stages) * stage_bytes(cols, fp4) +
            static_cast<size_t>(max_tiles) * sizeof(DecodeTile);
 }
 
@@ -119,6 +122,34 @@ __device__ __forceinline__ void mma_16x8x32(float* d, uint32_t a0, uint32_t a1, 
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d += A(16x16, f16) * B(16x8, f16), fp32 accumulators
+__device__ __forceinline__ void mma_16x8x16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                            uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// the two e2m1 codes of byte (v >> shift) as f16x2 (low nibble in the low half); exact
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t v, int shift) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(v >> shift));
+    return r;
+}
+// the two e4m3 codes of the 16 bits (v >> shift) as f16x2 (low byte in the low half); exact
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v, int shift) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v >> shift));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 __device__ __forceinline__ void epilogue_barrier() {
@@ -179,9 +210,14 @@ struct ActMaps {
     CUtensorMap m[2][4];
 };
 
+// FP4: NVFP4 weights (nvfp4.cu's packed units); the MMA warps expand each code times its block
+// scale to f16 (exact: at most 6 significant bits, |w| <= 6 * 448) and the activation codes to
+// f16 (exact), and run f16 MMAs; the expert's 1 / global_scale joins the promotion's scale.
+template <bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mlp_kernel(const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2,
                       const __grid_constant__ ActMaps tmX, const DecodeMlpArgs a) {
+    constexpr int kWB = FP4 ? kWeightBytes4 : kWeightBytes;   // a stage's weight bytes: activations follow
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -280,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             cnt = cnt < 1 ? 1 : (cnt > a.cols ? a.cols : cnt);
             const int lg = cnt <= 1 ? 0 : cnt <= 2 ? 1 : cnt <= 4 ? 2 : 3;
             const CUtensorMap* tmA = &tmX.m[second ? 1 : 0][lg];
-            // bytes per stage: weights (w13: two 16-row boxes; w2: one 32-row box) + activations
-            const uint32_t stage_tx = static_cast<uint32_t>((32 + (1 << lg)) * 128 * G.GKB);
+            // bytes per stage: weights (w13: two 16-row boxes; w2: one 32-row box; NVFP4: two 16-row
+            // slabs of packed units) + activations
+            const uint32_t stage_tx = FP4 ? static_cast<uint32_t>((2 * kFp4UnitBytes + (1 << lg) * 128) * G.GKB)
+                                          : static_cast<uint32_t>((32 + (1 << lg)) * 128 * G.GKB);
             for (int grp = 0; grp < G.NG; ++grp, ++q) {
                 const uint32_t stage = q % S, use = q / S;
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->empty[stage]), (use & 1u) ^ 1u, abort_flag,
@@ -302,7 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, stage_tx);
                     // the item's weight rows over the stage's K blocks: w2 one box of 32 rows, w13
                     // a box of its 16 gate rows and one of its 16 up rows (I rows apart)
-                    if (second) {
+                    if constexpr (FP4) {
+                        // slabs of 16 rows: w2 rows [32u, 32u + 32), w13 gate [16u, ...) and up [I + 16u, ...)
+                        const int slab0 = e * (G.N / 16) + row0 / 16, slab1 = e * (G.N / 16) + row1 / 16;
+                        tma_load_4d(dst, tmW, 0, 0, kb0, slab0, fb);
+                        tma_load_4d(dst + kTileBytes4, tmW, 0, 0, kb0, slab1, fb);
+                    } else if (second) {
                         if (a.w_tiled)
                             tma_load_4d(dst, tmW, 0, row0 % 128, kb0, e * NB + row0 / 128, fb);
                         else
@@ -332,8 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the activation rows of the stage's K blocks (after a failed wait the load still
                 // goes out, so that the stage's phase completes and the drain below can wait for
                 // it; the status word marks the outputs invalid)
-                if (lane == 0) tma_load_3d(dst + kWeightBytes, tmA, 0, kb0, poff, fb);
-                {
+                if (lane == 0) tma_load_3d(dst + kWB, tmA, 0, kb0, poff, fb);
+                if constexpr (FP4) {
+                    // the expert's 1 / global_scale (the block scales came with the codes)
+                    if (lane == 0) cp_async_4(smem_addr(&ctl->scl[stage][0]), wsc + e);
+                } else {
                     // weight-block scales (read-only here: 4-byte copies through L1), lane = tile * 16 + kbi
                     const int kbi = lane % kGroupKB, kb = kb0 + kbi;
                     if (kbi < G.GKB && kb < G.KB)
@@ -395,83 +441,164 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Gemm& G = second ? G2 : G1;
             const uint8_t* st = ring + static_cast<size_t>(stage) * SB;
             const int xr = ctl->stage_rows[stage];
-            // this warp's K blocks of the stage, cw and cw + 8: both into registers, the stage
-            // released, then their MMAs
-            uint4 wv[2][2][2][2], xv[2][2];   // [half][tile][row g / g+8][K half c], [half][K half c]
-            float ws[2][2], xa[2], xb[2];
-            bool live[2];
+            if constexpr (FP4) {
+                // this warp's K blocks of the stage, cw and cw + 8.  Lane (g, t) feeds K positions
+                // [32t, 32t + 32) of a block (any K order works when A and B agree): MMA j takes
+                // positions 32t + 4j + {0, 1} (A/B registers 0) and + {2, 3} (registers 1), i.e.
+                // code bytes 2j and 2j + 1 of the lane's 16 and activation bytes 4j .. 4j + 3 of its
+                // 32; positions below 32t + 16 use block scale 2t, the others 2t + 1.
+                uint4 cv[2][2][2], xq[2][2];   // [half][tile][row g / g+8] codes, [half][16-byte half] activations
+                uint32_t sv[2][2][2];          // [half][tile][row] the two block scales' bytes
+                float xa[2], xb[2];
+                bool live[2];
+                const float gsc = ctl->scl[stage][0];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int kbi = cw + 8 * half, kb = grp * G.GKB + kbi;
-                live[half] = kbi < G.GKB && kb < G.KB;
-                if (!live[half]) continue;
-                // 128-byte rows of the stage's weight boxes, tile-packed with the 128-byte swizzle:
-                //   w2: [K block][32 rows]       w13: gate box, up box, each [K block][16 rows]
-                // [E, N, K] without swizzle:
-                //   w2: [32 rows][K block]       w13: gate box, up box, each [16 rows][K block]
+                for (int half = 0; half < 2; ++half) {
+                    const int kbi = cw + 8 * half, kb = grp * G.GKB + kbi;
+                    live[half] = kbi < G.GKB && kb < G.KB;
+                    if (!live[half]) continue;
 #pragma unroll
-                for (int tile = 0; tile < 2; ++tile)
+                    for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int r16 = g + 8 * hr;   // row within the 16-row tile
-                        int box, srow;   // the box's offset in the stage, the row within the box
-                        if (second) {
-                            box = 0;
-                            srow = a.w_tiled ? kbi * 32 + 16 * tile + r16 : (16 * tile + r16) * G.GKB + kbi;
-                        } else {
-                            box = tile * kTileBytes;
-                            srow = a.w_tiled ? kbi * 16 + r16 : r16 * G.GKB + kbi;
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const uint8_t* up = st + tile * kTileBytes4 + kbi * kFp4UnitBytes;
+                            const int r16 = g + 8 * hr;
+                            cv[half][tile][hr] = *reinterpret_cast<const uint4*>(up + r16 * 64 + 16 * t);
+                            sv[half][tile][hr] = *reinterpret_cast<const uint16_t*>(up + 16 * 64 + r16 * 8 + 2 * t);
                         }
-                        const int x = a.w_tiled ? (r16 & 7) : 0;   // == srow & 7 when tiled
-                        const uint8_t* rp = st + box + srow * 128;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            wv[half][tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
-                    }
-                // the stage holds xr activation rows: B columns past them are zero (their results
-                // are never read)
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    xv[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWeightBytes +
-                                                                           (g * G.GKB + kbi) * 128 + 64 * c + 16 * t)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-                ws[half][0] = ctl->scl[stage][kbi];
-                ws[half][1] = ctl->scl[stage][kGroupKB + kbi];
-                xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
-                xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                if (!live[half]) continue;
-                // four independent chains (tile, K half c) of two MMAs each
-                float f[2][2][4];
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
+                        xq[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWB + (g * G.GKB + kbi) * 128 +
+                                                                               32 * t + 16 * c)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
+                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) f[tile][c][i] = 0.0f;
+                for (int half = 0; half < 2; ++half) {
+                    if (!live[half]) continue;
+                    uint32_t s2[2][2][2];   // [tile][row][block 2t / 2t+1] the scale in both f16 halves
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                    for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const uint32_t sc = e4m3x2_f16x2(sv[half][tile][hr], 0);
+                            s2[tile][hr][0] = __byte_perm(sc, 0u, 0x1010);
+                            s2[tile][hr][1] = __byte_perm(sc, 0u, 0x3232);
+                        }
+                    float f[2][2][4];   // [tile][chain: j even / odd]
 #pragma unroll
                     for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
-                            mma_16x8x32(f[tile][c], word(wv[half][tile][0][c], 2 * h),
-                                        word(wv[half][tile][1][c], 2 * h), word(wv[half][tile][0][c], 2 * h + 1),
-                                        word(wv[half][tile][1][c], 2 * h + 1), word(xv[half][c], 2 * h),
-                                        word(xv[half][c], 2 * h + 1));
 #pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    // accumulator (row g / g+8, column 2t / 2t+1): the weight block's scale times the
-                    // column's activation scale
-                    const float s0 = ws[half][tile] * xa[half], s1 = ws[half][tile] * xb[half];
-                    acc[tile][0] = fmaf(f[tile][0][0] + f[tile][1][0], s0, acc[tile][0]);
-                    acc[tile][1] = fmaf(f[tile][0][1] + f[tile][1][1], s1, acc[tile][1]);
-                    acc[tile][2] = fmaf(f[tile][0][2] + f[tile][1][2], s0, acc[tile][2]);
-                    acc[tile][3] = fmaf(f[tile][0][3] + f[tile][1][3], s1, acc[tile][3]);
+                            for (int i = 0; i < 4; ++i) f[tile][c][i] = 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t xw = word(xq[half][j >> 2], j & 3);
+                        const uint32_t b0 = e4m3x2_f16x2(xw, 0), b1 = e4m3x2_f16x2(xw, 16);
+                        const int sh = 16 * (j & 1), blk = j >> 2;
+#pragma unroll
+                        for (int tile = 0; tile < 2; ++tile) {
+                            const uint32_t w0 = word(cv[half][tile][0], j >> 1), w1 = word(cv[half][tile][1], j >> 1);
+                            mma_16x8x16(f[tile][j & 1], hmul2(e2m1x2_f16x2(w0, sh), s2[tile][0][blk]),
+                                        hmul2(e2m1x2_f16x2(w1, sh), s2[tile][1][blk]),
+                                        hmul2(e2m1x2_f16x2(w0, sh + 8), s2[tile][0][blk]),
+                                        hmul2(e2m1x2_f16x2(w1, sh + 8), s2[tile][1][blk]), b0, b1);
+                        }
+                    }
+                    // accumulator (row g / g+8, column 2t / 2t+1): the expert's 1 / global_scale times
+                    // the column's activation scale
+                    const float s0 = gsc * xa[half], s1 = gsc * xb[half];
+#pragma unroll
+                    for (int tile = 0; tile < 2; ++tile) {
+                        acc[tile][0] = fmaf(f[tile][0][0] + f[tile][1][0], s0, acc[tile][0]);
+                        acc[tile][1] = fmaf(f[tile][0][1] + f[tile][1][1], s1, acc[tile][1]);
+                        acc[tile][2] = fmaf(f[tile][0][2] + f[tile][1][2], s0, acc[tile][2]);
+                        acc[tile][3] = fmaf(f[tile][0][3] + f[tile][1][3], s1, acc[tile][3]);
+                    }
+                }
+            } else {
+                // this warp's K blocks of the stage, cw and cw + 8: both into registers, the stage
+                // released, then their MMAs
+                uint4 wv[2][2][2][2], xv[2][2];   // [half][tile][row g / g+8][K half c], [half][K half c]
+                float ws[2][2], xa[2], xb[2];
+                bool live[2];
+    #pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int kbi = cw + 8 * half, kb = grp * G.GKB + kbi;
+                    live[half] = kbi < G.GKB && kb < G.KB;
+                    if (!live[half]) continue;
+                    // 128-byte rows of the stage's weight boxes, tile-packed with the 128-byte swizzle:
+                    //   w2: [K block][32 rows]       w13: gate box, up box, each [K block][16 rows]
+                    // [E, N, K] without swizzle:
+                    //   w2: [32 rows][K block]       w13: gate box, up box, each [16 rows][K block]
+    #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile)
+    #pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int r16 = g + 8 * hr;   // row within the 16-row tile
+                            int box, srow;   // the box's offset in the stage, the row within the box
+                            if (second) {
+                                box = 0;
+                                srow = a.w_tiled ? kbi * 32 + 16 * tile + r16 : (16 * tile + r16) * G.GKB + kbi;
+                            } else {
+                                box = tile * kTileBytes;
+                                srow = a.w_tiled ? kbi * 16 + r16 : r16 * G.GKB + kbi;
+                            }
+                            const int x = a.w_tiled ? (r16 & 7) : 0;   // == srow & 7 when tiled
+                            const uint8_t* rp = st + box + srow * 128;
+    #pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                wv[half][tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
+                        }
+                    // the stage holds xr activation rows: B columns past them are zero (their results
+                    // are never read)
+    #pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        xv[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWB +
+                                                                               (g * G.GKB + kbi) * 128 + 64 * c + 16 * t)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                    ws[half][0] = ctl->scl[stage][kbi];
+                    ws[half][1] = ctl->scl[stage][kGroupKB + kbi];
+                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
+                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
+    #pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    if (!live[half]) continue;
+                    // four independent chains (tile, K half c) of two MMAs each
+                    float f[2][2][4];
+    #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile)
+    #pragma unroll
+                        for (int c = 0; c < 2; ++c)
+    #pragma unroll
+                            for (int i = 0; i < 4; ++i) f[tile][c][i] = 0.0f;
+    #pragma unroll
+                    for (int h = 0; h < 2; ++h)
+    #pragma unroll
+                        for (int tile = 0; tile < 2; ++tile)
+    #pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                mma_16x8x32(f[tile][c], word(wv[half][tile][0][c], 2 * h),
+                                            word(wv[half][tile][1][c], 2 * h), word(wv[half][tile][0][c], 2 * h + 1),
+                                            word(wv[half][tile][1][c], 2 * h + 1), word(xv[half][c], 2 * h),
+                                            word(xv[half][c], 2 * h + 1));
+    #pragma unroll
+                    for (int tile = 0; tile < 2; ++tile) {
+                        // accumulator (row g / g+8, column 2t / 2t+1): the weight block's scale times the
+                        // column's activation scale
+                        const float s0 = ws[half][tile] * xa[half], s1 = ws[half][tile] * xb[half];
+                        acc[tile][0] = fmaf(f[tile][0][0] + f[tile][1][0], s0, acc[tile][0]);
+                        acc[tile][1] = fmaf(f[tile][0][1] + f[tile][1][1], s1, acc[tile][1]);
+                        acc[tile][2] = fmaf(f[tile][0][2] + f[tile][1][2], s0, acc[tile][2]);
+                        acc[tile][3] = fmaf(f[tile][0][3] + f[tile][1][3], s1, acc[tile][3]);
+                    }
                 }
             }
             if (grp == G.NG - 1) {
@@ -590,8 +717,12 @@ size_t decode_max_tiles() {
 int64_t decode_counters(int max_tiles, int I) { return static_cast<int64_t>(max_tiles) * (I / 128 + 1) + 1; }
 
 cudaError_t decode_init_device() {
-    return cudaFuncSetAttribute(decode_mlp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemLimit));
+    cudaError_t e = cudaFuncSetAttribute(decode_mlp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemLimit));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_mlp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemLimit));
+    return e;
 }
 
 namespace {
@@ -615,6 +746,19 @@ cudaError_t weight_map(CUtensorMap* map, const uint8_t* w, bool tiled, int E, in
     return encode_u8_map_nd(map, w, 3, dims, strides, box, false);
 }
 
+// NVFP4-packed weights [E*N/16 slabs][K/128][9][128 bytes] (nvfp4.cu's units): boxes of one slab
+// x GKB K blocks, one contiguous run; in shared memory each unit's 16 rows of 64 code bytes are
+// consecutive, so the 8 lanes of a quarter-warp (two rows, four 16-byte pieces) read 128
+// consecutive bytes
+cudaError_t fp4_weight_map(CUtensorMap* map, const uint8_t* w, int E, int N, int K) {
+    const uint64_t KB = static_cast<uint64_t>(K / 128);
+    const uint32_t GKB = static_cast<uint32_t>(KB < kGroupKB ? KB : kGroupKB);
+    const uint64_t dims[4] = {128, kFp4UnitBytes / 128, KB, static_cast<uint64_t>(E) * (N / 16)};
+    const uint64_t strides[3] = {128, kFp4UnitBytes, KB * kFp4UnitBytes};
+    const uint32_t box[4] = {128, kFp4UnitBytes / 128, GKB, 1};
+    return encode_u8_map_nd(map, w, 4, dims, strides, box, false);
+}
+
 // activations [rows][K/128][128 bytes]: boxes of `r` rows x GKB K blocks
 cudaError_t act_map(CUtensorMap* map, const uint8_t* x, int64_t rows, int K, uint32_t r) {
     const uint64_t KB = static_cast<uint64_t>(K / 128);
@@ -632,15 +776,22 @@ cudaError_t launch_decode_mlp(const DecodeMlpArgs& args, int num_sms, cudaStream
     if (args.cols < 1 || args.cols > kCols || args.H % 128 != 0 || args.I % 128 != 0) return cudaErrorInvalidValue;
     DecodeMlpArgs a = args;
     // as many ring stages as fit next to the control block and the tile records
-    a.stage_bytes = static_cast<int>(stage_bytes(a.cols));
-    const size_t fixed = smem_bytes(a.max_tiles, 0, a.cols);
+    const bool fp4 = a.w_fp4 != 0;
+    a.stage_bytes = static_cast<int>(stage_bytes(a.cols, fp4));
+    const size_t fixed = smem_bytes(a.max_tiles, 0, a.cols, fp4);
     if (fixed + 2 * static_cast<size_t>(a.stage_bytes) > kSmemLimit) return cudaErrorInvalidValue;
     a.stages = static_cast<int>((kSmemLimit - fixed) / a.stage_bytes);
     if (a.stages > kMaxStages) a.stages = kMaxStages;
-    const size_t smem = smem_bytes(a.max_tiles, a.stages, a.cols);
+    const size_t smem = smem_bytes(a.max_tiles, a.stages, a.cols, fp4);
     CUtensorMap tmW13, tmW2;
-    cudaError_t err = weight_map(&tmW13, a.w13, a.w_tiled != 0, a.E, 2 * a.I, a.H, 16);
-    if (err == cudaSuccess) err = weight_map(&tmW2, a.w2, a.w_tiled != 0, a.E, a.H, a.I, 32);
+    cudaError_t err;
+    if (fp4) {
+        err = fp4_weight_map(&tmW13, a.w13, a.E, 2 * a.I, a.H);
+        if (err == cudaSuccess) err = fp4_weight_map(&tmW2, a.w2, a.E, a.H, a.I);
+    } else {
+        err = weight_map(&tmW13, a.w13, a.w_tiled != 0, a.E, 2 * a.I, a.H, 16);
+        if (err == cudaSuccess) err = weight_map(&tmW2, a.w2, a.w_tiled != 0, a.E, a.H, a.I, 32);
+    }
     ActMaps tmX;
     for (int lg = 0; lg < 4 && err == cudaSuccess; ++lg) {
         err = act_map(&tmX.m[0][lg], a.a1, a.rows, a.H, 1u << lg);
@@ -649,7 +800,8 @@ cudaError_t launch_decode_mlp(const DecodeMlpArgs& args, int num_sms, cudaStream
     if (err != cudaSuccess) return err;
     const int64_t items = static_cast<int64_t>(a.max_tiles) * (2 * a.I / 32 + a.H / 32);
     const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
-    return launch_pdl(decode_mlp_kernel, dim3(grid), dim3(kThreads), smem, stream, tmW13, tmW2, tmX, a);
+    if (fp4) return launch_pdl(decode_mlp_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, tmW13, tmW2, tmX, a);
+    return launch_pdl(decode_mlp_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, tmW13, tmW2, tmX, a);
 }
 
 }  // namespace mfp8

@@ -94,6 +94,16 @@ cudaError_t launch_unpermute_sum(const float* y, int64_t y_rows, const int32_t* 
 cudaError_t launch_combine_pairs(const uint16_t* y, const int32_t* pos, int64_t T, int topk, int H, uint16_t* out,
                                  cudaStream_t stream);
 
+// nvfp4.cu: NVFP4 expert weights (codes [E, N, K/2], e4m3 block scales [E, N, K/16], per-expert
+// 1 / global_scale [E]) and their packed form for the decode kernel: [E][N/16][K/128] units of
+// kFp4UnitBytes = 16 rows x 64 code bytes, then 16 rows x 8 scale bytes
+constexpr int kFp4UnitBytes = 16 * 64 + 16 * 8;
+cudaError_t launch_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* sf, float* gs,
+                                      cudaStream_t stream);
+size_t nvfp4_packed_bytes(int E, int N, int K);
+cudaError_t launch_nvfp4_pack(const uint8_t* q, const uint8_t* sf, int E, int N, int K, uint8_t* packed,
+                              cudaStream_t stream);
+
 // gemm.cu
 struct GemmArgs {
     const uint8_t* A;
@@ -142,11 +152,12 @@ cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, con
 // decode.cu: both expert GEMMs of a step with at most 8 rows per expert in one persistent
 // launch, as weight-streaming work items of 32 weight rows (see decode.cu)
 struct DecodeMlpArgs {
-    const uint8_t* w13;        // [E, 2I, H] or tile-packed
-    const float* w13_scale;    // [E, 2I/128, H/128]
-    const uint8_t* w2;         // [E, H, I] or tile-packed
-    const float* w2_scale;     // [E, H/128, I/128]
+    const uint8_t* w13;        // [E, 2I, H] or tile-packed (w_fp4: NVFP4-packed)
+    const float* w13_scale;    // [E, 2I/128, H/128] (w_fp4: the per-expert 1 / global_scale [E])
+    const uint8_t* w2;         // [E, H, I] or tile-packed (w_fp4: NVFP4-packed)
+    const float* w2_scale;     // [E, H/128, I/128] (w_fp4: [E])
     int w_tiled;
+    int w_fp4;                 // NVFP4 weights in the packed layout of nvfp4.cu
     int H, I, E;
     const uint8_t* a1;         // activation codes [rows, H]: a tile's j-th row at padded row poff + j
     const float* a1s;          // their scales [H/128][rows]

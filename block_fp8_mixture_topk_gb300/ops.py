@@ -16,7 +16,8 @@ import torch
 from . import build as _build
 
 MOE_BLOCK_M = 128
-MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED = 0, 1
+MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED, MOE_WEIGHTS_NVFP4 = 0, 1, 2
+NVFP4_UNIT_BYTES = 16 * 64 + 16 * 8   # one 16-row slab x one 128-wide K block: codes, then block scales
 SCALE_FMT = {"f32": 0, "ue8m0": 1}      # fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)
 SCORING = {"softmax": 0, "sigmoid": 1}
 EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
@@ -103,6 +104,9 @@ def lib():
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P, P, P], I),
                 "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
+                "moe_nvfp4_quant_weight": ([P, I, I, I, P, P, P, P], I),
+                "moe_nvfp4_packed_bytes": ([I, I, I], SZ),
+                "moe_nvfp4_pack_weights": ([P, P, I, I, I, P, P], I),
                 "moe_fp8_block_masked_workspace_size": ([I, I, I, I], SZ),
                 "moe_fp8_block_forward_masked": ([P, P, P, P, P, P, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
@@ -234,10 +238,46 @@ def moe_fp8_block_pack_weights(w):
     return packed
 
 
+def moe_nvfp4_quant_weight(w):
+    """NVFP4 quantisation of bf16 expert weights [E, N, K] (page "vllm.model_executor.layers.
+    quantization.online.nvfp4", _quantize_moe_weight_to_nvfp4): returns (codes uint8 [E, N, K/2],
+    two e2m1 per byte, element 2i in the low nibble; block scales uint8 [E, N, K/16], e4m3 bits;
+    global scales fp32 [E], the factor that dequantises)."""
+    _cuda(w, torch.bfloat16, "w")
+    E, N, K = w.shape
+    q = torch.empty(E, N, K // 2, dtype=torch.uint8, device=w.device)
+    sf = torch.empty(E, N, K // 16, dtype=torch.uint8, device=w.device)
+    gs = torch.empty(E, dtype=torch.float32, device=w.device)
+    _check("moe_nvfp4_quant_weight",
+           lib().moe_nvfp4_quant_weight(_ptr(w), E, N, K, _ptr(q), _ptr(sf), _ptr(gs), _stream()))
+    return q, sf, gs
+
+
+def moe_nvfp4_pack_weights(q, block_scale):
+    """NVFP4 codes [E, N, K/2] and block scales [E, N, K/16] -> the packed layout the forward
+    reads (MOE_WEIGHTS_NVFP4): uint8 [E, N/16, K/128, 1152] (load-time, once)."""
+    q = _cuda(q, torch.uint8, "q")
+    block_scale = _codes(_cuda(block_scale, None, "block_scale"))
+    E, N, K2 = q.shape
+    K = 2 * K2
+    if block_scale.shape != (E, N, K // 16):
+        raise ValueError("block_scale must be [E, N, K/16]")
+    packed = torch.empty(E, N // 16, K // 128, NVFP4_UNIT_BYTES, dtype=torch.uint8, device=q.device)
+    _check("moe_nvfp4_pack_weights",
+           lib().moe_nvfp4_pack_weights(_ptr(q), _ptr(block_scale), E, N, K, _ptr(packed), _stream()))
+    return packed
+
+
+def moe_nvfp4_packed_bytes(E, N, K) -> int:
+    return int(lib().moe_nvfp4_packed_bytes(E, N, K))
+
+
 def _weight_shape(w):
-    """(E, N, K, layout) of expert weights in either layout."""
+    """(E, N, K, layout) of expert weights in any of the layouts."""
     if w.dim() == 5:
         return w.shape[0], w.shape[1] * 128, w.shape[2] * 128, MOE_WEIGHTS_TILED
+    if w.dim() == 4 and w.shape[3] == NVFP4_UNIT_BYTES:
+        return w.shape[0], w.shape[1] * 16, w.shape[2] * 128, MOE_WEIGHTS_NVFP4
     E, N, K = w.shape
     return E, N, K, MOE_WEIGHTS_NK
 
@@ -320,7 +360,8 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
                           scale_fmt="f32", decode="auto"):
     """The whole layer: returns bf16 [T, H] (written into `out` when given).
 
-    w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D).
+    w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D), or
+    NVFP4-packed (moe_nvfp4_pack_weights, 4-D) with w13_scale / w2_scale the global scales [E].
     decode: "auto", "off" or "on" -- the decode-path GEMMs for small steps (MOE_DECODE_*).
     events: optional list of 7 torch.cuda.Event recorded between the stages
     (FORWARD_STAGES) on the current stream, for per-stage timing."""
@@ -355,6 +396,16 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
                                         workspace.numel(), _ptr(out), _stream(), arr)
     _check("moe_fp8_block_forward", rc)
     return out
+
+
+def moe_nvfp4_forward(hidden, router_logits, w13, w13_global_scale, w2, w2_global_scale, topk, renormalize=True,
+                      routing: RoutingParams | None = None, out=None, workspace=None, events=None, scale_fmt="f32"):
+    """The layer on NVFP4 expert weights (moe_nvfp4_pack_weights outputs and their global scales
+    [E]); activations and the intermediate in FP8 1x128 groups (scale_fmt)."""
+    if _weight_shape(w13)[3] != MOE_WEIGHTS_NVFP4 or _weight_shape(w2)[3] != MOE_WEIGHTS_NVFP4:
+        raise ValueError("w13 and w2 must be NVFP4-packed (moe_nvfp4_pack_weights)")
+    return moe_fp8_block_forward(hidden, router_logits, w13, w13_global_scale, w2, w2_global_scale, topk,
+                                 renormalize, routing, out, workspace, events, scale_fmt, "on")
 
 
 def moe_fp8_block_masked_workspace_size(E, max_tokens, H, I) -> int:

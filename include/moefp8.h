@@ -171,7 +171,33 @@ int fp8_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, f
  * multiples of 128, E*N*K/128 < 2^31. */
 #define MOE_WEIGHTS_NK 0      /* [E, N, K] row-major, the pages' layout */
 #define MOE_WEIGHTS_TILED 1   /* moe_fp8_block_pack_weights output */
+#define MOE_WEIGHTS_NVFP4 2   /* NVFP4 weights, moe_nvfp4_pack_weights output */
 int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* packed, void* stream);
+
+/* NVFP4 expert weights (page "vllm.model_executor.layers.quantization.online.nvfp4",
+ * _quantize_moe_weight_to_nvfp4; load time).  Per expert: amax over the whole [N, K] weight,
+ * floored at 1e-8; global_scale = (FLOAT4_E2M1_MAX * FLOAT8_E4M3_MAX) / amax = 2688 / amax; the
+ * weights times global_scale rounded back to bf16 are quantised in blocks of 16 along K with
+ * one e4m3 scale per block: block scale = e4m3(max|x| / 6), code = e2m1(x / block scale)
+ * (nearest, ties to even, saturating at +-6; the pages name scaled_fp4_quant's inputs, not its
+ * arithmetic, and this is the FP8 groups' rule with e2m1's maximum).
+ *   w            bf16 [E, N, K], device, 16-byte aligned; K a multiple of 16
+ *   q            uint8 [E, N, K/2]: two e2m1 codes per byte, element 2i in the low nibble
+ *   block_scale  uint8 [E, N, K/16]: e4m3fn bits
+ *   global_scale fp32 [E]: 1 / global_scale, the factor that dequantises
+ * Dequantised weight = e2m1(code) * block_scale * global_scale[e].  Three launches on `stream`
+ * (amax, quantise, global scales); global_scale serves as the amax scratch until the last. */
+int moe_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* block_scale,
+                           float* global_scale, void* stream);
+/* Bytes of the packed NVFP4 layout of an [E, N, K] weight (N % 16 == 0, K % 128 == 0; else 0):
+ * [E][N/16][K/128] units of 1152 bytes, each the 16 rows x 64 code bytes of one 16-row slab over
+ * one 128-wide K block followed by their 16 rows x 8 block-scale bytes. */
+size_t moe_nvfp4_packed_bytes(int E, int N, int K);
+/* Load-time conversion of moe_nvfp4_quant_weight's codes and block scales into that layout (the
+ * one the forward reads with MOE_WEIGHTS_NVFP4).  q: 16-byte aligned, block_scale: 8-byte
+ * aligned, packed: 16-byte aligned, moe_nvfp4_packed_bytes(E, N, K) bytes, not overlapping. */
+int moe_nvfp4_pack_weights(const uint8_t* q, const uint8_t* block_scale, int E, int N, int K, uint8_t* packed,
+                           void* stream);
 
 /* ---- scale formats ------------------------------------------------------------------
  * Every 1x128 group and 128x128 block scale is max(amax, 1e-8)/448 in fp32 (MOE_SCALE_F32),
@@ -332,9 +358,15 @@ int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode);
 
 /* Options of the layer: the expert weights' layout, the scale format of the activations
  * and of the requantised intermediate, and the GEMM kernels of small steps
- * (NULL options = MOE_WEIGHTS_NK, MOE_SCALE_F32, MOE_DECODE_AUTO). */
+ * (NULL options = MOE_WEIGHTS_NK, MOE_SCALE_F32, MOE_DECODE_AUTO).
+ * MOE_WEIGHTS_NVFP4: w13 / w2 are moe_nvfp4_pack_weights outputs and w13_scale / w2_scale the
+ * per-expert global scales [E] (moe_nvfp4_quant_weight); activations and the intermediate keep
+ * their FP8 1x128 groups.  Both GEMMs then run on the decode-path kernel (decode_path
+ * MOE_DECODE_OFF is rejected with MOE_ERR_INVALID_ARG), a step of more than 8 tokens 8 tokens
+ * at a time (4 launches each); moe_fp8_block_workspace_size(T, ...) still suffices.  Shapes the
+ * decode kernel cannot take give MOE_ERR_UNSUPPORTED_SHAPE. */
 typedef struct moe_forward_options {
-    int32_t weight_layout;            /* MOE_WEIGHTS_NK or MOE_WEIGHTS_TILED */
+    int32_t weight_layout;            /* MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED or MOE_WEIGHTS_NVFP4 */
     int32_t scale_fmt;                /* MOE_SCALE_F32 or MOE_SCALE_UE8M0 */
     int32_t decode_path;              /* MOE_DECODE_AUTO, MOE_DECODE_OFF or MOE_DECODE_ON */
 } moe_forward_options;

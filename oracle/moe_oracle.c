@@ -260,9 +260,9 @@ uint8_t orc_e2m1_encode(float xf) {
 void orc_quant_nvfp4_bf16(const uint16_t* w, long E, long N, long K, uint8_t* q, uint8_t* sf, float* gs2) {
     e4m3_build();
     long KB16 = K / 16;
-#pragma omp parallel for schedule(static)
     for (long e = 0; e < E; ++e) {
         float amax = 0.0f;
+#pragma omp parallel for reduction(max : amax) schedule(static)
         for (long i = 0; i < N * K; ++i) {
             float a = fabsf(bf16_to_f32(w[e * N * K + i]));
             if (a > amax) amax = a;
@@ -270,6 +270,7 @@ void orc_quant_nvfp4_bf16(const uint16_t* w, long E, long N, long K, uint8_t* q,
         if (amax < 1e-8f) amax = 1e-8f;
         float gsc = (6.0f * 448.0f) / amax;             /* fp32 IEEE division */
         gs2[e] = 1.0f / gsc;
+#pragma omp parallel for schedule(static)
         for (long n = 0; n < N; ++n) {
             for (long b = 0; b < KB16; ++b) {
                 float v[16];

@@ -167,3 +167,27 @@ def test_newer_entry_points_reject_bad_arguments_on_host():
                                           None) == -1
     assert L.moe_fp8_block_forward_masked(None, None, None, None, None, None, 0, 16, 256, 256, None, None, 0, None,
                                           None) == 0
+
+
+def test_nvfp4_entry_points_reject_bad_arguments_on_host():
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    big = ctypes.c_void_p(0x100000)
+    # packed layout: [E][N/16][K/128] units of 16 x 64 code bytes + 16 x 8 scale bytes
+    assert moe.moe_nvfp4_packed_bytes(2, 256, 512) == 2 * 16 * 4 * 1152
+    assert moe.moe_nvfp4_packed_bytes(2, 250, 512) == 0
+    assert moe.moe_nvfp4_packed_bytes(2, 256, 200) == 0
+    # K not a multiple of 16 (quantiser) or 128 (packing); N not a multiple of 16; empty is a no-op
+    assert L.moe_nvfp4_quant_weight(p, 1, 128, 120, p, p, p, None) == -2
+    assert L.moe_nvfp4_quant_weight(None, 0, 128, 128, None, None, None, None) == 0
+    assert L.moe_nvfp4_pack_weights(p, p, 1, 100, 128, big, None) == -2
+    assert L.moe_nvfp4_pack_weights(p, p, 1, 128, 64, big, None) == -2
+    assert L.moe_nvfp4_pack_weights(None, None, 0, 128, 128, None, None) == 0
+    # NVFP4 weights run on the decode-path kernel: turning it off is an argument error
+    opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 1)
+    assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                      1 << 30, p, None, None) == -1
+    # an expert MLP the decode kernel cannot take (top-k above 64 gives more than 512 pairs)
+    opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 0)
+    assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 8, 256, 256, 128, 65, 1, None, ctypes.byref(opts), big,
+                                      1 << 40, p, None, None) == -2
