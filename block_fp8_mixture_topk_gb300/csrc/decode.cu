@@ -134,17 +134,21 @@ __device__ __forceinline__ void mma_16x8x16(float* d, uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// the two e2m1 codes of byte (v >> shift) as f16x2 (low nibble in the low half); exact
-__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t v, int shift) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(v >> shift));
-    return r;
+// the four bytes of w, each two e2m1 codes (low nibble first), as four f16x2 (byte i -> r[i],
+// low nibble in the low half); exact
+__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t* r) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(w));
 }
-// the two e4m3 codes of the 16 bits (v >> shift) as f16x2 (low byte in the low half); exact
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v, int shift) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v >> shift));
-    return r;
+// the four e4m3 codes of w as two f16x2 (bytes 0, 1 -> lo; 2, 3 -> hi); exact
+__device__ __forceinline__ void e4m3x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, h0;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     uint32_t r;
@@ -484,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
                         for (int hr = 0; hr < 2; ++hr) {
-                            const uint32_t sc = e4m3x2_f16x2(sv[half][tile][hr], 0);
+                            uint32_t sc, unused;
+                            e4m3x4_f16x2(sv[half][tile][hr], sc, unused);
                             s2[tile][hr][0] = __byte_perm(sc, 0u, 0x1010);
                             s2[tile][hr][1] = __byte_perm(sc, 0u, 0x3232);
                         }
@@ -496,17 +501,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) f[tile][c][i] = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t xw = word(xq[half][j >> 2], j & 3);
-                        const uint32_t b0 = e4m3x2_f16x2(xw, 0), b1 = e4m3x2_f16x2(xw, 16);
-                        const int sh = 16 * (j & 1), blk = j >> 2;
+                    for (int jw = 0; jw < 4; ++jw) {
+                        // code word jw of each row holds MMAs 2jw and 2jw + 1 (two bytes each)
+                        uint32_t r[2][2][4];   // [tile][row] the word's four bytes as f16x2
 #pragma unroll
-                        for (int tile = 0; tile < 2; ++tile) {
-                            const uint32_t w0 = word(cv[half][tile][0], j >> 1), w1 = word(cv[half][tile][1], j >> 1);
-                            mma_16x8x16(f[tile][j & 1], hmul2(e2m1x2_f16x2(w0, sh), s2[tile][0][blk]),
-                                        hmul2(e2m1x2_f16x2(w1, sh), s2[tile][1][blk]),
-                                        hmul2(e2m1x2_f16x2(w0, sh + 8), s2[tile][0][blk]),
-                                        hmul2(e2m1x2_f16x2(w1, sh + 8), s2[tile][1][blk]), b0, b1);
+                        for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                            for (int hr = 0; hr < 2; ++hr) e2m1x8_f16x2(word(cv[half][tile][hr], jw), r[tile][hr]);
+                        const int blk = jw >> 1;
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int j = 2 * jw + jj;
+                            uint32_t b0, b1;
+                            e4m3x4_f16x2(word(xq[half][j >> 2], j & 3), b0, b1);
+#pragma unroll
+                            for (int tile = 0; tile < 2; ++tile)
+                                mma_16x8x16(f[tile][jj], hmul2(r[tile][0][2 * jj], s2[tile][0][blk]),
+                                            hmul2(r[tile][1][2 * jj], s2[tile][1][blk]),
+                                            hmul2(r[tile][0][2 * jj + 1], s2[tile][0][blk]),
+                                            hmul2(r[tile][1][2 * jj + 1], s2[tile][1][blk]), b0, b1);
                         }
                     }
                     // accumulator (row g / g+8, column 2t / 2t+1): the expert's 1 / global_scale times
