@@ -31,5 +31,6 @@ from .ops import (  # noqa: F401
     moe_nvfp4_packed_bytes,
     moe_nvfp4_quant_weight,
     moe_route_topk,
+    moe_selftest_bounded_wait,
     moe_unpermute_sum,
 )

@@ -338,6 +338,13 @@ int moe_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, u
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int moe_selftest_bounded_wait(int expire, void* stream) {
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_bounded_wait_check(expire, st->status, static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_nvfp4_packed_bytes(int E, int N, int K) {
     if (E < 0 || N < 0 || K < 0 || N % 16 != 0 || K % 128 != 0) return 0;
     return nvfp4_packed_bytes(E, N, K);

@@ -104,6 +104,9 @@ size_t nvfp4_packed_bytes(int E, int N, int K);
 cudaError_t launch_nvfp4_pack(const uint8_t* q, const uint8_t* sf, int E, int N, int K, uint8_t* packed,
                               cudaStream_t stream);
 
+// selftest.cu: one bounded pipeline wait that expires (expire != 0) or completes at once
+cudaError_t launch_bounded_wait_check(int expire, uint32_t* status, cudaStream_t stream);
+
 // gemm.cu
 struct GemmArgs {
     const uint8_t* A;

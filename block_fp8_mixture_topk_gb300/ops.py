@@ -112,6 +112,7 @@ def lib():
                 "moe_unpermute_sum": ([P, I64, P, I, I, I, P, P], I),
                 "moe_combine_pairs": ([P, P, I, I, I, P, P], I),
                 "moe_get_device_status": ([P, I], I),
+                "moe_selftest_bounded_wait": ([I, P], I),
                 "moe_error_string": ([I], ctypes.c_char_p),
                 "moe_device_supported": ([], I),
             }
@@ -437,6 +438,12 @@ def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, o
                                             _ptr(out), _stream())
     _check("moe_fp8_block_forward_masked", rc)
     return out
+
+
+def moe_selftest_bounded_wait(expire=True):
+    """Make one pipeline wait expire (about 2 s, MOE_STATUS_WAIT_TIMEOUT) or complete at once;
+    read the outcome with moe_get_device_status."""
+    _check("moe_selftest_bounded_wait", lib().moe_selftest_bounded_wait(int(bool(expire)), _stream()))
 
 
 def moe_get_device_status(clear=False) -> int:

@@ -411,6 +411,13 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts,
 /* Reads (and with clear != 0, resets) the device status word of the current
  * device into *status (host).  Synchronises the device. */
 int moe_get_device_status(uint32_t* status, int clear);
+/* Failure-detection check of the pipelines' bounded wait (every mbarrier wait of the GEMM and
+ * decode kernels gives up after 2 s of device time, sets MOE_STATUS_WAIT_TIMEOUT in the status
+ * word and lets its kernel return).  expire != 0: one such wait on a phase that nothing completes
+ * runs out (about 2 s) and sets MOE_STATUS_WAIT_TIMEOUT; expire == 0: the phase is completed
+ * first and the wait returns at once.  Nothing faults; the context stays usable.  Asynchronous
+ * on `stream`; read the result with moe_get_device_status. */
+int moe_selftest_bounded_wait(int expire, void* stream);
 /* Human-readable name of a MOE_* return code. */
 const char* moe_error_string(int code);
 /* 1 if the current device can run these kernels (compute capability 10.3). */

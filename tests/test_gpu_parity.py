@@ -584,6 +584,16 @@ def test_forward_one_and_two_token_batches(name, T):
     assert_output_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("T,E,topk", [(640, 4, 1), (300, 2, 2), (900, 4, 2)])
+def test_forward_column_order_experts_all_tokens(T, E, topk):
+    """Experts whose w13 is 16 MB or more (H=2048, I=4096) with 129-512 rows, the case where the
+    w13 GEMM visits an expert's two to four tiles column by column: every token matches."""
+    wl = mi.Workload("colorder", 90 + T + E, T, 2048, 4096, E, topk)
+    assert 2 * wl.I * wl.H >= 16 << 20
+    out, ref = run_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
 def test_forward_two_tokens_small_shape():
     wl = mi.Workload("twotok", 81, 2, 256, 512, 6, 3)
     out, ref = run_layer(wl)
