@@ -82,8 +82,10 @@ struct SmemCtl {
     float amax_x[2][2][BM];            // [tile parity][column half][row]
     alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
     alignas(16) float scl[SR][SCL];    // scale ring: a_scale of the tile's 128 rows, then the two weight scales
-    int item_m[ITEMS];                 // the CTA's work items (see item_of), in its visiting order
-    int item_n[ITEMS];
+    int item_m[ITEMS];                 // the CTA's work items (see item_of), in its visiting order:
+    int item_n[ITEMS];                 // tile, column block,
+    int item_e[ITEMS];                 // the tile's expert
+    int item_r0[ITEMS];                // and first row
 };
 constexpr int STAGE_ROW = 20;          // floats per staged row (80 B: conflict-free 16-byte slots)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
@@ -123,19 +125,23 @@ __device__ __forceinline__ void item_of(const GemmArgs& a, int64_t w, int NT, in
 template <int EPI>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const SmemCtl* ctl, int64_t k, int64_t w, int NT) {
     Tile t;
-    int m, n;
-    if constexpr (EPI != MOE_EPI_SILU_MUL_QUANT) {
-        m = static_cast<int>(w / NT);
-        n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
-    } else if (k < ITEMS) {
-        m = ctl->item_m[k];
-        n = ctl->item_n[k];
+    if (k < ITEMS) {
+        // cached at the kernel's start: no global load at an item boundary
+        t.n = ctl->item_n[k];
+        t.e = ctl->item_e[k];
+        t.row0 = ctl->item_r0[k];
     } else {
-        item_of(a, w, NT, m, n);
+        int m, n;
+        if constexpr (EPI != MOE_EPI_SILU_MUL_QUANT) {
+            m = static_cast<int>(w / NT);
+            n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
+        } else {
+            item_of(a, w, NT, m, n);
+        }
+        t.n = n;
+        t.e = a.tile_expert[m];
+        t.row0 = a.tile_row0[m];
     }
-    t.n = n;
-    t.e = a.tile_expert[m];
-    t.row0 = a.tile_row0[m];
     t.ok = t.e >= 0 && t.e < a.E && t.row0 >= 0 && t.row0 + BM <= a.a_rows;
     if (EPI == MOE_EPI_SILU_MUL_QUANT) {
         t.bcol0 = t.n * 128;
@@ -199,20 +205,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const int64_t total = ntiles * NT;
-    // the w13 GEMM's work items of this CTA (w = blockIdx.x + k * gridDim.x), their tiles and
-    // columns looked up once; the w2 GEMM keeps the tile-by-tile order (its column blocks of one
-    // expert run in the same wave for the shapes served, and it gained nothing measurable)
-    if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
-        for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
-            const int64_t w = blockIdx.x + k * gridDim.x;
-            if (w >= total) break;
-            int m, n;
+    // this CTA's first ITEMS work items (w = blockIdx.x + k * gridDim.x): tile, column block,
+    // expert and first row looked up once, so that no role waits on a global load when it starts
+    // an item.  Only the w13 GEMM reorders (item_of); the w2 GEMM keeps the tile-by-tile order
+    // (its column blocks of one expert run in the same wave for the shapes served, and the
+    // reorder gained nothing measurable there).
+    for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
+        const int64_t w = blockIdx.x + k * gridDim.x;
+        if (w >= total) break;
+        int m, n;
+        if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
             item_of(a, w, NT, m, n);
-            ctl->item_m[k] = m;
-            ctl->item_n[k] = n;
+        } else {
+            m = static_cast<int>(w / NT);
+            n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
         }
-        __syncthreads();
+        ctl->item_m[k] = m;
+        ctl->item_n[k] = n;
+        ctl->item_e[k] = a.tile_expert[m];
+        ctl->item_r0[k] = a.tile_row0[m];
     }
+    __syncthreads();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     if (warp < FIRST_EPI_WARP) {
