@@ -239,6 +239,67 @@ __device__ int select_experts_reg(const float (&sel)[V], uint32_t live, int E, i
     int my_id = -1;
     float prev = 0.0f;
     const int rounds = check ? topk + 1 : topk;
+    if constexpr (V <= 16) {
+        // Each lane sorts its live candidates (value descending, expert index ascending) once;
+        // a round is then one warp-wide unsigned max over the lanes' heads (values mapped to
+        // order-preserving keys; -0 counted as +0, 0 = no candidate), a ballot for the lowest lane
+        // holding it (lanes hold consecutive experts, so the lowest lane has the lowest index
+        // among equal values), and the winning lane dropping its head: the same winners, in the
+        // same order, as the argmax rounds below.
+        uint32_t key[V];
+        int ix[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            const uint32_t b = __float_as_uint(sel[v] + 0.0f);
+            key[v] = ((live >> v) & 1u) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+            ix[v] = v;
+        }
+#pragma unroll
+        for (int k = 2; k <= V; k <<= 1)
+#pragma unroll
+            for (int jj = k >> 1; jj > 0; jj >>= 1)
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    const int l = i ^ jj;
+                    if (l <= i) continue;
+                    // first / second: the pair's required order ((i & k) == 0: i before l)
+                    const int f = (i & k) == 0 ? i : l, g2 = (i & k) == 0 ? l : i;
+                    const bool ok = key[f] > key[g2] || (key[f] == key[g2] && ix[f] < ix[g2]);
+                    if (!ok) {
+                        const uint32_t tk = key[i];
+                        key[i] = key[l];
+                        key[l] = tk;
+                        const int ti = ix[i];
+                        ix[i] = ix[l];
+                        ix[l] = ti;
+                    }
+                }
+        for (int j = 0; j < rounds; ++j) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+            if (m == 0u) break;   // fewer candidates than rounds (only the extra round)
+            const int wl = __ffs(__ballot_sync(0xffffffffu, key[0] == m)) - 1;
+            const int widx = wl * V + __shfl_sync(0xffffffffu, ix[0], wl);
+            const float wv = __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
+            if (check && j > 0) {
+                const float bound = 0x1p-19f + 0x1p-20f * fmaxf(fabsf(prev), fabsf(wv));
+                if (prev - wv <= bound) close = true;
+            }
+            prev = wv;
+            if (j < topk) {
+                if (lane == wl) {
+#pragma unroll
+                    for (int v = 0; v + 1 < V; ++v) {
+                        key[v] = key[v + 1];
+                        ix[v] = ix[v + 1];
+                    }
+                    key[V - 1] = 0u;
+                }
+                if (lane == j) my_id = widx;
+            }
+        }
+        if (thin) *thin = close;
+        return my_id;
+    }
     for (int j = 0; j < rounds; ++j) {
         Cand c{0.0f, INT32_MAX};
 #pragma unroll
