@@ -265,7 +265,8 @@ def run_reference(args, wl):
     line = {"impl": "reference", "metric": "block-FP8 fused-MoE tokens/s", "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)",
+            "data": ("synthetic (seeded; weights N(0,0.02) quantised to NVFP4)" if args.weights == "nvfp4" else
+                     "synthetic (seeded; weights N(0,0.02) quantised to 128x128 e4m3 blocks)"),
             "config": describe(wl, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
