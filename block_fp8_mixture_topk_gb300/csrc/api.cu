@@ -515,7 +515,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (fp4 && T > kDecodeCols) {
         // NVFP4 weights run on the decode-path kernel only: steps of more tokens go through it
         // kDecodeCols tokens at a time (every token's rows are independent)
-        if (H % 128 != 0 || I % 128 != 0 || !hidden || !router_logits || !out) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (H <= 0 || I <= 0 || !hidden || !router_logits || !out) return MOE_ERR_INVALID_ARG;
+        if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
         // stage events: the chunks' kernels interleave, so the whole step is recorded as the w13
         // stage (events 0-3 before the first chunk, 4-6 after the last)
         cudaStream_t s = static_cast<cudaStream_t>(stream);

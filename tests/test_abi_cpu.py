@@ -187,6 +187,11 @@ def test_nvfp4_entry_points_reject_bad_arguments_on_host():
     opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 1)
     assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
                                       1 << 30, p, None, None) == -1
+    # more than 8 tokens run 8 at a time: argument errors still come back before any launch
+    assert L.moe_fp8_block_forward_ex(None, p, p, p, p, p, 20, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                      1 << 30, p, None, None) == -1
+    assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 20, 200, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                      1 << 30, p, None, None) == -2
     # an expert MLP the decode kernel cannot take (top-k above 64 gives more than 512 pairs)
     opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 0)
     assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 8, 256, 256, 128, 65, 1, None, ctypes.byref(opts), big,
