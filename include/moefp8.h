@@ -316,7 +316,9 @@ size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
 /* Number of kernels one moe_fp8_block_forward launches for these sizes (host only):
  * routing, the expert sort and quantisation (one kernel for up to 512 routed pairs,
  * four otherwise), the two grouped GEMMs (one kernel on the decode path) and the weighted
- * sum, under MOE_DECODE_AUTO; 0 when T == 0, -1 for invalid sizes. */
+ * sum, under MOE_DECODE_AUTO; 0 when T == 0, -1 for invalid sizes.  (With MOE_WEIGHTS_NVFP4
+ * a forward launches 4 kernels per 8 tokens: routing, sort and quantisation, the decode
+ * kernel, the weighted sum.) */
 int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk);
 int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const uint8_t* w13, const float* w13_scale,
