@@ -187,3 +187,16 @@ def test_nvfp4_routed_layer_brute_force_per_token():
     rel = np.linalg.norm(r["out"] - ref) / np.linalg.norm(ref)
     assert rel < 1e-9, rel
     assert np.array_equal(r["out_bf16"], oracle.bf16_from_f64(r["out"]))
+
+
+def test_nvfp4_sampled_tokens_match_full_run():
+    rng = np.random.default_rng(35)
+    T, H, I, E, k = 9, 128, 256, 3, 2
+    hid = bf16_bits(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    q13, s13, g13 = oracle.quant_nvfp4_bf16(bf16_bits(rng.standard_normal((E, 2 * I, H)) * 0.02))
+    q2, s2, g2 = oracle.quant_nvfp4_bf16(bf16_bits(rng.standard_normal((E, H, I)) * 0.02))
+    full = oracle.moe_forward_nvfp4(hid, logits, q13, s13, g13, q2, s2, g2, k)
+    part = oracle.moe_forward_nvfp4(hid, logits, q13, s13, g13, q2, s2, g2, k, tokens=[1, 8])
+    assert np.array_equal(part["out"][[1, 8]], full["out"][[1, 8]])
+    assert np.all(np.isnan(part["out"][[0, 2, 7]]))
