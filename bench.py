@@ -103,6 +103,12 @@ def describe_weights(args):
             if args.weights == "tiled" else "e4m3 128x128 blocks, [E, N, K] layout") + fmt
 
 
+def touched_per_pass(ids, tokens_per_pass):
+    """Experts touched, summed over passes of `tokens_per_pass` consecutive tokens (ids [T, k])."""
+    return sum(int(torch.unique(ids[t0:t0 + tokens_per_pass]).numel())
+               for t0 in range(0, ids.shape[0], tokens_per_pass))
+
+
 def expert_weight_bytes(wl, nvfp4=False):
     """Bytes one expert's w13 and w2 occupy (codes and scales): (w13, both)."""
     H, I = wl.H, wl.I
@@ -362,6 +368,9 @@ def run_ours(args, wl):
     ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, H, I, E, wl.topk), dtype=torch.uint8, device=dev)
     ids, _ = moe.moe_route_topk(logits, wl.topk, wl.renormalize, rp)
     touched = int(torch.unique(ids).numel())
+    # NVFP4 steps of more than 8 tokens run 8 tokens at a time: each pass streams the experts
+    # its own tokens touch
+    touched_streamed = touched_per_pass(ids, 8) if args.weights == "nvfp4" else touched
     P = wl.P
     decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode)
     # kernels per step (the decode path's one GEMM kernel in place of two)
@@ -503,7 +512,8 @@ def run_ours(args, wl):
         # the decode path runs both GEMMs in one kernel (timed as the w13 stage): both GEMMs'
         # weights, the activation rows read, the intermediate written and read once, the
         # weighted bf16 rows written
-        gemm_bytes = (touched * per_expert + P * (H + H // 128 * 4) + 2 * P * (I + I // 128 * 4) + P * H * 2)
+        gemm_bytes = (touched_streamed * per_expert + P * (H + H // 128 * 4) + 2 * P * (I + I // 128 * 4) +
+                      P * H * 2)
         gemm_flops = 6 * P * H * I
         g_ms = stage_ms["gemm_w13"] + stage_ms["gemm_w2"]
     fp8_peak = pk["bf16"] * FP8_OVER_BF16
