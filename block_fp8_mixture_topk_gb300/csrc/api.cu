@@ -517,6 +517,17 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         // kDecodeCols tokens at a time (every token's rows are independent)
         if (H <= 0 || I <= 0 || !hidden || !router_logits || !out) return MOE_ERR_INVALID_ARG;
         if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+        // every check a pass of kDecodeCols tokens makes, before anything is enqueued (the last,
+        // shorter pass needs no more than a full one)
+        if (decode_mode == MOE_DECODE_OFF) return MOE_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) || static_cast<int64_t>(E) * H >= (int64_t(1) << 31))
+            return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (!decode_possible(kDecodeCols, H, I, topk)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (!w13 || !w13_scale || !w2 || !w2_scale || !workspace) return MOE_ERR_INVALID_ARG;
+        if (!aligned(hidden, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
+            !aligned(workspace, 256))
+            return MOE_ERR_INVALID_ARG;
+        if (workspace_bytes < forward_layout(kDecodeCols, H, I, E, topk).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
         // stage events: the chunks' kernels interleave, so the whole step is recorded as the w13
         // stage (events 0-3 before the first chunk, 4-6 after the last)
         cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -238,7 +238,9 @@ def moe_forward(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renorma
     w13_scale [E,2I/128,H/128] f32, w2 [E,H,I] u8, w2_scale [E,H/128,I/128] f32.
     ``tokens``: optional iterable of token indices to compute (others stay NaN).
     Returns a dict with ids, weights, offsets, sorted, pos, a1q, a1s, a2q, a2s
-    (by sorted row), c2 (by sorted row), out (fp64 [T,H]) and out_bf16 bits.
+    (by sorted row), c2 (by sorted row), out (fp64 [T,H]) and out_bf16 bits.  With
+    ``tokens`` given, a2q, a2s, c1 and c2 hold only the rows of those tokens' pairs, and
+    ``rows`` gives the sorted-row index of each (without, ``rows`` = all P rows).
     """
     E, N1, H2 = w13.shape
     assert N1 % 256 == 0
@@ -298,21 +300,35 @@ def _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring
     need = np.zeros(T, dtype=np.uint8)
     if tokens is None:
         need[:] = 1
+        rows = np.arange(P, dtype=np.int64)
+        r_offsets, r_sorted, r_pos = offsets, sorted_, pos
     else:
         need[np.asarray(list(tokens), dtype=np.int64)] = 1
-    a2q = np.zeros((P, I), dtype=np.uint8)
-    a2s = np.zeros((P, I // 128), dtype=np.float32)
-    c1 = np.full((P, N1), np.nan) if want_c1 else None
-    c2 = np.full((P, H), np.nan)
-    experts(a1q, a1s, offsets, sorted_, need, T, H, topk, a2q, a2s, c1, c2)
+        # only the sorted rows of the chosen tokens' pairs are held (in sorted order): every row is
+        # computed on its own, so leaving the others out changes no value, and a sample of a large
+        # step needs no [P, H] buffer
+        rows = np.nonzero(need[sorted_ // topk])[0]
+        expert_of_row = np.repeat(np.arange(E), np.diff(offsets))
+        r_offsets = np.zeros(E + 1, dtype=np.int32)
+        r_offsets[1:] = np.cumsum(np.bincount(expert_of_row[rows], minlength=E))
+        r_sorted = np.ascontiguousarray(sorted_[rows], dtype=np.int32)
+        r_pos = np.zeros(P, dtype=np.int32)
+        r_pos[r_sorted] = np.arange(rows.size, dtype=np.int32)
+    R = max(int(rows.size), 1)
+    a2q = np.zeros((R, I), dtype=np.uint8)
+    a2s = np.zeros((R, I // 128), dtype=np.float32)
+    c1 = np.full((R, N1), np.nan) if want_c1 else None
+    c2 = np.full((R, H), np.nan)
+    experts(a1q, a1s, r_offsets, r_sorted, need, T, H, topk, a2q, a2s, c1, c2)
     out = np.full((T, H), np.nan)
-    _load().orc_combine(_ptr(c2), _ptr(wts), _ptr(pos), _ptr(need), T, H, topk, _ptr(out))
+    _load().orc_combine(_ptr(c2), _ptr(wts), _ptr(r_pos), _ptr(need), T, H, topk, _ptr(out))
     out_bf16 = np.zeros((T, H), dtype=np.uint16)
-    rows = np.nonzero(need)[0]
-    if rows.size:
-        out_bf16[rows] = bf16_from_f64(out[rows])
+    toks = np.nonzero(need)[0]
+    if toks.size:
+        out_bf16[toks] = bf16_from_f64(out[toks])
+    # a2q, a2s, c1, c2 are indexed like `rows` (sorted-row indices; all P rows when tokens is None)
     return dict(ids=ids, weights=wts, offsets=offsets, sorted=sorted_, pos=pos, a1q=a1q, a1s=a1s,
-                a2q=a2q, a2s=a2s, c1=c1, c2=c2, out=out, out_bf16=out_bf16, need=need)
+                a2q=a2q, a2s=a2s, c1=c1, c2=c2, rows=rows, out=out, out_bf16=out_bf16, need=need)
 
 
 # --------------------------------------------------------------------------- masked batched layout

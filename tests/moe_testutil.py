@@ -90,3 +90,46 @@ def unpadded_rows(padded_offsets: np.ndarray, offsets: np.ndarray):
         n = offsets[e + 1] - offsets[e]
         out[offsets[e]:offsets[e + 1]] = padded_offsets[e] + np.arange(n)
     return out
+
+
+def check_sort(perm, ids_np, E, block_m=128):
+    """The GPU's expert sort (outputs of moe_align_permute or its no-workspace variant) against
+    the oracle's stable sort of the same ids, bit for bit: offsets, padded offsets, the pair of
+    every real row, -1 in every padding row, the unpermute map and the tile table."""
+    off, sorted_, pos = oracle.permute(ids_np, E)
+    counts = np.diff(off)
+    padded = (counts + block_m - 1) // block_m * block_m
+    poff = np.concatenate([[0], np.cumsum(padded)])
+    assert np.array_equal(perm["expert_offsets"].cpu().numpy(), off)
+    assert np.array_equal(perm["padded_offsets"].cpu().numpy(), poff)
+    rows = unpadded_rows(poff, off)
+    sp = perm["sorted_pair_ids"].cpu().numpy()
+    assert np.array_equal(sp[rows], sorted_)
+    pad = np.ones(poff[-1], dtype=bool)
+    pad[rows] = False
+    assert np.all(sp[:poff[-1]][pad] == -1)
+    assert np.array_equal(perm["pos"].cpu().numpy()[:ids_np.size], rows[pos])
+    nt = int(perm["num_tiles"].item())
+    assert nt == poff[-1] // block_m
+    te = perm["tile_expert"].cpu().numpy()[:nt]
+    tr = perm["tile_row0"].cpu().numpy()[:nt]
+    assert np.array_equal(tr, np.arange(nt) * block_m)
+    assert np.array_equal(te, np.searchsorted(poff, tr, side="right") - 1)
+
+
+def tile_sample_tokens(oids: np.ndarray, E: int, block_m: int = 128, extra=()):
+    """Tokens that cover every expert tile of a routed step: for each padded tile of
+    block_m rows, the token owning its last real row, and for each expert the token owning its
+    first row (rows in the sort's order: by expert, pairs p = t*topk + j ascending).  `extra`
+    tokens are added.  Returns a sorted list."""
+    topk = oids.shape[1]
+    off, sorted_, _ = oracle.permute(oids, E)
+    toks = set(int(t) for t in extra)
+    for e in range(E):
+        n = int(off[e + 1] - off[e])
+        if n == 0:
+            continue
+        toks.add(int(sorted_[off[e]]) // topk)
+        for last in range(block_m - 1, n + block_m - 1, block_m):
+            toks.add(int(sorted_[off[e] + min(last, n - 1)]) // topk)
+    return sorted(toks)

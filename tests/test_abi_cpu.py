@@ -192,6 +192,16 @@ def test_nvfp4_entry_points_reject_bad_arguments_on_host():
                                       1 << 30, p, None, None) == -1
     assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 20, 200, 256, 4, 2, 1, None, ctypes.byref(opts), big,
                                       1 << 30, p, None, None) == -2
+    # ... including the weights, the workspace and its size, checked before the first stage event is
+    # recorded (the fake event handles below would fail if they were recorded)
+    opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 0)
+    events = (ctypes.c_void_p * 7)(*([0x40] * 7))
+    assert L.moe_fp8_block_forward_ex(p, p, None, p, p, p, 20, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                      1 << 30, p, None, events) == -1
+    assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 20, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                      256, p, None, events) == -3
+    assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 20, 256, 256, 4, 2, 1, None, ctypes.byref(opts),
+                                      ctypes.c_void_p(0x100010), 1 << 30, p, None, events) == -1
     # an expert MLP the decode kernel cannot take (top-k above 64 gives more than 512 pairs)
     opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 0)
     assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 8, 256, 256, 128, 65, 1, None, ctypes.byref(opts), big,

@@ -128,6 +128,26 @@ def test_nvfp4_layer_matches_oracle(name, T):
     assert_output_close(out, ref)
 
 
+@pytest.mark.parametrize("T", [32, 128])
+def test_nvfp4_dsv3_decode_steps_in_passes_of_eight(T):
+    """DeepSeek-V3-shaped decode steps of 32 and 128 tokens on NVFP4 weights (grouped sigmoid
+    routing with bias and routed scaling): the forward runs them eight tokens at a time.  Sampled
+    tokens from the first, a middle and the last pass of eight against the oracle."""
+    wl = mi.WORKLOADS["dsv3_decode"].with_tokens(T)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    tokens = sorted(set([0, 7, 8, T // 2 + 3, T - 9, T - 1]))
+    layer = Fp4Layer(wl)
+    out = layer.forward(hidden.to(DEV), logits.to(DEV), rp)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(clear=True) == 0
+    w = layer.oracle_weights(set(oids[tokens].reshape(-1).tolist()))
+    ref = oracle.moe_forward_nvfp4(bits(hidden), logits.numpy(), w["q13"], w["s13"], w["g13"], w["q2"], w["s2"],
+                                   w["g2"], wl.topk, wl.renormalize, tokens=tokens, **okw)["out"]
+    assert_output_close(out, ref, rows=tokens)
+
+
 @pytest.mark.parametrize("T,H,I,E,topk", [(1, 128, 128, 1, 1), (8, 128, 256, 1, 1), (6, 256, 128, 3, 3)])
 def test_nvfp4_edge_shapes(T, H, I, E, topk):
     """One expert and top-1 (a dense NVFP4 MLP), every token on the single expert, top-k equal to

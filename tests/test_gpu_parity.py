@@ -13,7 +13,7 @@ import torch
 import moe_inputs as mi
 import oracle
 import block_fp8_mixture_topk_gb300 as moe
-from moe_testutil import Layer, assert_output_close, routing_of, unpadded_rows
+from moe_testutil import Layer, assert_output_close, check_sort, routing_of, tile_sample_tokens, unpadded_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -170,28 +170,6 @@ def test_route_without_renormalize():
         oids, ow = oracle.route(logits.numpy(), 6, False, scoring=sc, routed_scaling=1.5)
         assert np.array_equal(ids.cpu().numpy(), oids)
         np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6, atol=1e-7)
-
-
-def check_sort(perm, ids_np, E, block_m=128):
-    off, sorted_, pos = oracle.permute(ids_np, E)
-    counts = np.diff(off)
-    padded = (counts + block_m - 1) // block_m * block_m
-    poff = np.concatenate([[0], np.cumsum(padded)])
-    assert np.array_equal(perm["expert_offsets"].cpu().numpy(), off)
-    assert np.array_equal(perm["padded_offsets"].cpu().numpy(), poff)
-    rows = unpadded_rows(poff, off)
-    sp = perm["sorted_pair_ids"].cpu().numpy()
-    assert np.array_equal(sp[rows], sorted_)
-    pad = np.ones(poff[-1], dtype=bool)
-    pad[rows] = False
-    assert np.all(sp[:poff[-1]][pad] == -1)
-    assert np.array_equal(perm["pos"].cpu().numpy()[:ids_np.size], rows[pos])
-    nt = int(perm["num_tiles"].item())
-    assert nt == poff[-1] // block_m
-    te = perm["tile_expert"].cpu().numpy()[:nt]
-    tr = perm["tile_row0"].cpu().numpy()[:nt]
-    assert np.array_equal(tr, np.arange(nt) * block_m)
-    assert np.array_equal(te, np.searchsorted(poff, tr, side="right") - 1)
 
 
 @pytest.mark.parametrize("name,T", ROUTE_CASES)
@@ -541,10 +519,61 @@ def test_forward_tiny_all_tokens():
 
 
 @pytest.mark.parametrize("name", ["mixtral", "dsv3", "qwen3_skew"])
-def test_forward_full_size_sampled_tokens(name):
+def test_forward_full_size_every_tile_sampled(name):
+    """The full-size layer against the oracle on a sample that reaches every expert tile of both
+    GEMMs: for each 128-row tile the token owning its last real row, and for each expert the token
+    owning its first row (DeepSeek-V3 shape: every touched expert; Qwen3 Zipf shape: every tile
+    of the hot experts)."""
     wl = mi.WORKLOADS[name]
-    tokens = [0, 1, wl.T // 2, wl.T - 1]
+    _, okw = routing_of(wl)
+    oids, _ = oracle.route(mi.router_logits(wl).numpy(), wl.topk, wl.renormalize, **okw)
+    tokens = tile_sample_tokens(oids, wl.E, extra=[0, 1, wl.T // 2, wl.T - 1])
     out, ref = run_layer(wl, tokens)
+    assert_output_close(out, ref["out"], rows=tokens)
+
+
+def test_forward_more_items_than_a_cta_caches():
+    """Both grouped GEMMs with more than 256 work items per CTA on every SM (a CTA caches its first
+    256 items' tile, column block, expert and first row in shared memory and looks up later ones
+    in global memory).  H=4096, I=2048: 16 column blocks per tile in each GEMM; 50000 tokens, top-8
+    over 32 experts: about 3150 tiles, so the items of tiles from 16 x (SM count) on come after a
+    CTA's 256th.  Experts 28-31 hold exactly 300 rows each (three tiles, a w13 of 16 MB: the w13
+    GEMM visits their tiles column by column) and sit in the last tiles.  Tokens whose rows lie
+    past the cached items are compared with the oracle."""
+    T, H, I, E, topk = 50000, 4096, 2048, 32, 8
+    wl = mi.Workload("items", 95, T, H, I, E, topk)
+    logits = mi.router_logits(wl)
+    small = torch.arange(E - 4, E)
+    logits[:, small] -= 1000.0                 # experts 28-31 never chosen ...
+    chosen = torch.arange(0, T, T // 300)[:300]
+    logits[chosen.unsqueeze(1), small.unsqueeze(0)] += 2000.0   # ... except by these 300 tokens
+    layer = Layer(wl)
+    rp, _ = routing_of(wl)
+    out = layer.forward(mi.hidden(wl).to(DEV), logits.to(DEV), rp)
+    oids, _ = oracle.route(logits.numpy(), topk, True)
+    counts = np.bincount(oids.reshape(-1), minlength=E)
+    assert np.all(counts[E - 4:] == 300)
+    tiles_per_expert = (counts + 127) // 128
+    first_tile = np.concatenate([[0], np.cumsum(tiles_per_expert)])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cached_tiles = 256 * sms // 16             # tiles whose items are among the CTAs' first 256
+    assert first_tile[-1] > cached_tiles + 400
+    # tokens with rows in the uncached tiles: every tile's last real row past the cache, thinned,
+    # plus the small experts' first and last rows
+    off, sorted_, _ = oracle.permute(oids, E)
+    toks = set()
+    for e in range(E):
+        n = int(counts[e])
+        for i in range(0, n, 128):
+            tile = first_tile[e] + i // 128
+            last = min(i + 127, n - 1)
+            if tile >= cached_tiles and (e >= E - 4 or tile % 16 == 0):
+                toks.add(int(sorted_[off[e] + last]) // topk)
+        if e >= E - 4:
+            toks.add(int(sorted_[off[e]]) // topk)
+    tokens = sorted(toks)
+    w13q, w13s, w2q, w2s = layer.oracle_weights(set(oids[tokens].reshape(-1).tolist()))
+    ref = oracle.moe_forward(bits(mi.hidden(wl)), logits.numpy(), w13q, w13s, w2q, w2s, topk, True, tokens=tokens)
     assert_output_close(out, ref["out"], rows=tokens)
 
 

@@ -2,9 +2,10 @@
 device memory when they call (its scratch is a fixed array inside the library).
 
 Both entry points are called through the C ABI on the same routed ids and every
-output must be identical (the sort is integer work: bit-exact).  Two calls in a
-row, of different sizes, check that what the shared array keeps from the first
-call does not leak into the second.  This file is collected last so that a run
+output must be identical (the sort is integer work: bit-exact), and the
+no-allocation sort must equal the oracle's stable sort of the same ids.  Two calls
+in a row, of different sizes, check that what the shared array keeps from the
+first call does not leak into the second.  This file is collected last so that a run
 stopping at the first failure has run everything else first.
 """
 import ctypes
@@ -14,6 +15,7 @@ import torch
 
 import block_fp8_mixture_topk_gb300 as moe
 from block_fp8_mixture_topk_gb300 import ops
+from moe_testutil import check_sort
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -72,6 +74,25 @@ def test_noalloc_sort_matches_workspace_sort_on_two_calls_in_a_row():
         got = sort_noalloc(ids, E)
         torch.cuda.synchronize()
         assert_same_sort(want, got, T, k)
+        check_sort(got, ids.cpu().numpy(), E)
+    assert moe.moe_get_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("T,k,E,block_m", [
+    (8192, 32, 1024, 128),    # 256 chunks x 1024 experts: exactly the whole scratch
+    (3000, 4, 1024, 64),      # the largest expert count, 64-row tiles
+    (5000, 6, 64, 1),         # one-row "tiles"
+    (700, 3, 96, 1000),       # tiles of 1000 rows
+])
+def test_noalloc_sort_equals_the_oracle(T, k, E, block_m):
+    """Expert counts up to the library's maximum (1024) and tile sizes other than 128, against the
+    oracle's stable sort, bit for bit."""
+    moe.moe_get_device_status(clear=True)
+    assert -(-T * k // 1024) * E <= SCRATCH_INTS
+    ids = routed_ids(T, k, E, T + E + block_m)
+    got = sort_noalloc(ids, E, block_m)
+    torch.cuda.synchronize()
+    check_sort(got, ids.cpu().numpy(), E, block_m)
     assert moe.moe_get_device_status(clear=True) == 0
 
 
