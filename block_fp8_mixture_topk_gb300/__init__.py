@@ -21,6 +21,7 @@ from .ops import (  # noqa: F401
     moe_fp8_block_masked_workspace_size,
     moe_fp8_block_forward_kernel_count,
     moe_fp8_block_decode_path,
+    moe_fp8_block_pack_scales,
     moe_fp8_block_pack_weights,
     moe_fp8_block_workspace_size,
     moe_get_device_status,
@@ -30,6 +31,7 @@ from .ops import (  # noqa: F401
     moe_nvfp4_pack_weights,
     moe_nvfp4_packed_bytes,
     moe_nvfp4_quant_weight,
+    moe_packed_scale_bytes,
     moe_route_topk,
     moe_selftest_bounded_wait,
     moe_unpermute_sum,

@@ -81,9 +81,14 @@ int64_t max_rows(int64_t P, int64_t E, int64_t bm) {
     return P + busy * (bm - 1);
 }
 
+// bytes of the packed UE8M0 scale tiles of a [rows, K] operand (common.cuh, packed_sf_offset)
+int64_t packed_sf_bytes(int64_t rows, int K) {
+    return (rows + 127) / 128 * ((K / 128 + 3) / 4) * kSfTileBytes;
+}
+
 struct ForwardLayout {
-    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, y, dh, dcnt, dtab,
-        total;
+    size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, a1sf, a2sf, y, dh,
+        dcnt, dtab, total;
     int64_t rows, tiles;
     int64_t dcnt_n;   // decode-path group counters (0: the step cannot take the decode path)
 };
@@ -137,6 +142,9 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
+    // packed UE8M0 scale tiles of A1 and A2 (MOE_SCALE_UE8M0_PACKED)
+    L.a1sf = take(packed_sf_bytes(L.rows, H));
+    L.a2sf = take(packed_sf_bytes(L.rows, I));
     L.y = take(static_cast<size_t>(P) * H * 2);
     // decode path: h = silu(gate) * up by pair [P, I] fp32, the counters and the tile records
     L.dcnt_n = decode_possible(T, H, I, topk) ? decode_counters(static_cast<int>(L.tiles), I) : 0;
@@ -148,7 +156,7 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
 }
 
 struct MaskedLayout {
-    size_t row_map, pos, ones, tile_e, tile_r, ntiles, a1, a1s, a2, a2s, total;
+    size_t row_map, pos, ones, tile_e, tile_r, ntiles, a1, a1s, a2, a2s, a1sf, a2sf, total;
     int64_t Mp, rows, tiles;
 };
 
@@ -174,8 +182,14 @@ MaskedLayout masked_layout(int E, int M, int H, int I) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
+    L.a1sf = take(packed_sf_bytes(L.rows, H));
+    L.a2sf = take(packed_sf_bytes(L.rows, I));
     L.total = off;
     return L;
+}
+
+inline bool known_scale_fmt(int f) {
+    return f == MOE_SCALE_F32 || f == MOE_SCALE_UE8M0 || f == MOE_SCALE_UE8M0_PACKED;
 }
 
 }  // namespace
@@ -278,14 +292,18 @@ int fp8_group_quant(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, f
 int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, int scale_fmt,
                        void* stream) {
     if (rows < 0 || cols < 0 || ld < cols) return MOE_ERR_INVALID_ARG;
-    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+    if (!known_scale_fmt(scale_fmt)) return MOE_ERR_INVALID_ARG;
     if (cols % 128 != 0 || ld % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0 || cols == 0) return MOE_OK;
     if (!x || !q || !s) return MOE_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(q, 8) || !aligned(s, 4)) return MOE_ERR_INVALID_ARG;
+    const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    if (!aligned(x, 16) || !aligned(q, 8) || (!packed && !aligned(s, 4))) return MOE_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
+    if (packed)
+        return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, nullptr, 0, 0, nullptr, 1, MOE_SCALE_UE8M0,
+                                          static_cast<cudaStream_t>(stream), reinterpret_cast<uint8_t*>(s)));
     return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, s, cols / 128, 1, nullptr, 1, scale_fmt,
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -321,6 +339,22 @@ int moe_fp8_block_pack_weights(const uint8_t* w, int E, int N, int K, uint8_t* p
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
     return cuda_rc(launch_pack_weights(w, E, N, K, packed, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_packed_scale_bytes(int64_t rows, int K) {
+    if (rows < 0 || K < 0 || K % 128 != 0) return 0;
+    return static_cast<size_t>(packed_sf_bytes(rows, K));
+}
+
+int moe_fp8_block_pack_scales(const float* s, int E, int N, int K, uint8_t* out, void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (!s || !out || !aligned(s, 4) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_pack_scales(s, E, N, K, out, st->status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* block_scale,
@@ -376,7 +410,14 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     if (!A || !a_scale || !B || !b_scale || !tile_expert || !tile_row0 || !num_tiles) return MOE_ERR_INVALID_ARG;
     if (!aligned(A, 16) || !aligned(B, 16)) return MOE_ERR_INVALID_ARG;
     if (ep->b_layout != MOE_WEIGHTS_NK && ep->b_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
-    if (ep->scale_fmt != MOE_SCALE_F32 && ep->scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+    if (!known_scale_fmt(ep->scale_fmt)) return MOE_ERR_INVALID_ARG;
+    const bool packed = ep->scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    if (packed) {
+        if (ep->kind != MOE_EPI_STORE_F32 && ep->kind != MOE_EPI_SILU_MUL_QUANT &&
+            ep->kind != MOE_EPI_WEIGHTED_PAIRS_BF16)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned(a_scale, 16) || !aligned(b_scale, 16)) return MOE_ERR_INVALID_ARG;
+    }
     if (ep->b_layout == MOE_WEIGHTS_TILED && static_cast<int64_t>(E) * N * (K / 128) >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     switch (ep->kind) {
@@ -431,7 +472,13 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.num_pairs = ep->num_pairs;
     g.out_bf16 = ep->out_bf16;
     g.b_tiled = ep->b_layout == MOE_WEIGHTS_TILED;
-    g.scale_fmt = ep->scale_fmt;
+    g.scale_fmt = packed ? MOE_SCALE_UE8M0 : ep->scale_fmt;
+    if (packed) {
+        g.sf_packed = 1;
+        g.a_sf = reinterpret_cast<const uint8_t*>(a_scale);
+        g.b_sf = reinterpret_cast<const uint8_t*>(b_scale);
+        g.out_sf = reinterpret_cast<uint8_t*>(ep->out_scale);
+    }
     g.status = st->status;
     return cuda_rc(launch_grouped_gemm(g, st->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -508,10 +555,14 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     const int decode_mode = opts ? opts->decode_path : MOE_DECODE_AUTO;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED && weight_layout != MOE_WEIGHTS_NVFP4)
         return MOE_ERR_INVALID_ARG;
-    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+    if (!known_scale_fmt(scale_fmt)) return MOE_ERR_INVALID_ARG;
     if (decode_mode != MOE_DECODE_AUTO && decode_mode != MOE_DECODE_OFF && decode_mode != MOE_DECODE_ON)
         return MOE_ERR_INVALID_ARG;
     const bool fp4 = weight_layout == MOE_WEIGHTS_NVFP4;
+    // packed UE8M0 scales: both GEMMs on the block-scaled MMA (tile kernels only)
+    const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    if (packed && (fp4 || decode_mode == MOE_DECODE_ON)) return MOE_ERR_INVALID_ARG;
+    if (packed && (!aligned(w13_scale, 16) || !aligned(w2_scale, 16))) return MOE_ERR_INVALID_ARG;
     if (fp4 && T > kDecodeCols) {
         // NVFP4 weights run on the decode-path kernel only: steps of more tokens go through it
         // kDecodeCols tokens at a time (every token's rows are independent)
@@ -598,7 +649,9 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     // grid-wide quantiser
     const bool small = P <= kSmallPairs;
     if (fp4 && !decode_possible(T, H, I, topk)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    const bool decode = fp4 || use_decode(T, H, I, topk, decode_mode);
+    const bool decode = fp4 || (!packed && use_decode(T, H, I, topk, decode_mode));
+    uint8_t* a1sf = packed ? ws + L.a1sf : nullptr;
+    uint8_t* a2sf = ws + L.a2sf;
     int32_t* dcnt = reinterpret_cast<int32_t*>(ws + L.dcnt);
     DecodeTile* dtab = reinterpret_cast<DecodeTile*>(ws + L.dtab);
     DecodeSetup dsetup{};
@@ -606,7 +659,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     if (e == cudaSuccess && small)
         e = launch_sort_quant_small(ids, static_cast<int>(P), E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                     reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
-                                    st->status, hidden, T, H, topk, a1, H, a1s, 1, L.rows, scale_fmt, dsetup, s);
+                                    st->status, hidden, T, H, topk, a1, H, packed ? nullptr : a1s, 1, L.rows,
+                                    scale_fmt, dsetup, s, a1sf);
     if (e == cudaSuccess && !small)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
@@ -616,7 +670,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     // ([H/128][rows]) for the GEMM's per-row reads
     if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess && !small)
-        e = launch_group_quant(hidden, T, H, H, a1, H, a1s, 1, L.rows, pos, topk, scale_fmt, s);
+        e = launch_group_quant(hidden, T, H, H, a1, H, packed ? nullptr : a1s, 1, L.rows, pos, topk, scale_fmt, s,
+                               a1sf);
     if (e == cudaSuccess) e = mark(3);
     if (decode) {
         // up to 8 rows per expert: both GEMMs in one weight-streaming launch (decode.cu); the
@@ -680,6 +735,12 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.out_scale = a2s;
         g.os_row_stride = 1;
         g.os_kb_stride = L.rows;
+        if (packed) {
+            g.sf_packed = 1;
+            g.a_sf = a1sf;
+            g.b_sf = reinterpret_cast<const uint8_t*>(w13_scale);
+            g.out_sf = a2sf;
+        }
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
         if (e == cudaSuccess) e = mark(4);
@@ -708,6 +769,11 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.topk_weights = wts;
         g.topk = topk;
         g.num_pairs = P;
+        if (packed) {
+            g.sf_packed = 1;
+            g.a_sf = a2sf;
+            g.b_sf = reinterpret_cast<const uint8_t*>(w2_scale);
+        }
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
         if (e == cudaSuccess) e = mark(5);
@@ -731,7 +797,9 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     const int weight_layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
     const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
-    if (scale_fmt != MOE_SCALE_F32 && scale_fmt != MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+    if (!known_scale_fmt(scale_fmt)) return MOE_ERR_INVALID_ARG;
+    const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    if (packed && (!aligned(w13_scale, 16) || !aligned(w2_scale, 16))) return MOE_ERR_INVALID_ARG;
     if (H % 128 != 0 || I % 128 != 0 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (E == 0 || max_tokens == 0) return MOE_OK;
     const MaskedLayout L = masked_layout(E, max_tokens, H, I);
@@ -760,10 +828,14 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     float* a2s = reinterpret_cast<float*>(ws + L.a2s);
     const int64_t EM = static_cast<int64_t>(E) * max_tokens;
 
+    uint8_t* a1sf = packed ? ws + L.a1sf : nullptr;
+    uint8_t* a2sf = ws + L.a2sf;
     cudaError_t e = launch_masked_map(counts, E, max_tokens, static_cast<int>(L.Mp), row_map, pos, ones, tile_e,
                                       tile_r, ntiles, st->status, s);
-    // valid rows quantised into their padded rows; scales transposed ([H/128][rows])
-    if (e == cudaSuccess) e = launch_group_quant(hidden, EM, H, H, a1, H, a1s, 1, L.rows, pos, 1, scale_fmt, s);
+    // valid rows quantised into their padded rows; scales transposed ([H/128][rows]), or packed
+    if (e == cudaSuccess)
+        e = launch_group_quant(hidden, EM, H, H, a1, H, packed ? nullptr : a1s, 1, L.rows, pos, 1, scale_fmt, s,
+                               a1sf);
     if (e == cudaSuccess) {
         GemmArgs g{};
         g.a_box_rows = max_tokens <= 32 ? 32 : 128;   // no expert has more rows than max_tokens
@@ -789,6 +861,12 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
         g.out_scale = a2s;
         g.os_row_stride = 1;
         g.os_kb_stride = L.rows;
+        if (packed) {
+            g.sf_packed = 1;
+            g.a_sf = a1sf;
+            g.b_sf = reinterpret_cast<const uint8_t*>(w13_scale);
+            g.out_sf = a2sf;
+        }
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
     }
@@ -817,6 +895,11 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
         g.topk_weights = ones;
         g.topk = 1;
         g.num_pairs = EM;
+        if (packed) {
+            g.sf_packed = 1;
+            g.a_sf = a2sf;
+            g.b_sf = reinterpret_cast<const uint8_t*>(w2_scale);
+        }
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);
     }

@@ -170,6 +170,79 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
            | (static_cast<uint32_t>(m >> 4) << 24);      // M / 16
 }
 
+// ---------------------------------------------------------------- block-scaled MMA (UE8M0)
+// Packed UE8M0 scale factors ("UE8M0: packed UE8M0, 4 values per int32, Blackwell", page
+// "Quantization and MoE Optimizations", section DeepGEMM Scale Formats).  The scales of 128 rows
+// (or 128 weight columns) over 4 consecutive 128-wide K blocks form one 512-byte tile: 32 lines of
+// 16 bytes, line l holding rows l, l+32, l+64, l+96 as four 32-bit words, byte b of a word the
+// scale of K block 4q + b.  A tile goes to tensor memory as it is (tcgen05.cp 32x128b, copied to
+// all four lane quarters): 4 columns, where row m's word sits in column m / 32 of every quarter,
+// the layout the block-scaled MMA reads.
+constexpr int kSfTileBytes = 512;
+
+// Byte offset of (row r, K block kb) in a packed array of such tiles, tiles ordered
+// [row / 128][kb / 4] with kb4 = ceil(K blocks / 4) tiles per 128 rows.
+__host__ __device__ __forceinline__ int64_t packed_sf_offset(int64_t r, int kb, int kb4) {
+    return ((r >> 7) * kb4 + (kb >> 2)) * kSfTileBytes + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+// UE8M0 byte of a power-of-two fp32 scale: its biased exponent (value 2^(byte - 127)).
+__device__ __forceinline__ uint8_t ue8m0_byte(float s) {
+    return static_cast<uint8_t>((__float_as_uint(s) >> 23) & 0xFFu);
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte tile stored row after row (no swizzle): the
+// source of tcgen05.cp 32x128b (8-row groups 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sf_tile(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);   // start address
+    d |= static_cast<uint64_t>(128 >> 4) << 16;           // leading byte offset (one 16-byte column: unused)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;           // stride byte offset: 8 rows x 16 B
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version (sm_100 family)
+    return d;                                             // swizzle field 0: none
+}
+
+// Copy a 512-byte scale-factor tile from shared memory into 4 tensor-memory columns of all four
+// lane quarters (issued by one thread; ordered before the MMAs this thread issues after it).
+__device__ __forceinline__ void tmem_copy_sf_tile(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of a block-scaled kind::mxf8f6f4 MMA: A and B e4m3, both K-major,
+// UE8M0 scale factors, fp32 accumulator, M = m, N = n; sf_id picks the byte of each 32-bit
+// scale word (here: which of the 4 packed K blocks).
+__host__ __device__ constexpr uint32_t idesc_e4m3_ue8m0(int m, int n, int sf_id) {
+    return (static_cast<uint32_t>(sf_id & 3) << 4)          // B scale-factor byte
+           | (0u << 7) | (0u << 10)                         // A, B format: e4m3
+           | (static_cast<uint32_t>(n >> 3) << 17)          // N / 8
+           | (1u << 23)                                     // scale-factor format: UE8M0
+           | (static_cast<uint32_t>(m >> 4) << 24)          // M / 16
+           | (static_cast<uint32_t>(sf_id & 3) << 29);      // A scale-factor byte
+}
+
+// D[tmem] (+)= (A * sfA)[smem] * (B * sfB)[smem]^T, 128 x N x 32 e4m3 with one UE8M0 scale per
+// row of A and per column of B for these 32 K (scale factors in tensor memory), issued by one thread.
+__device__ __forceinline__ void mma_e4m3_block_scaled(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                      uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// 1-D bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) into shared memory,
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, 128 x N x 32 e4m3, issued by one thread.
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {

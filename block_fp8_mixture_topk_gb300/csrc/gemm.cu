@@ -82,8 +82,7 @@ struct SmemCtl {
     float amax_x[2][2][BM];            // [tile parity][column half][row]
     alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
     alignas(16) float scl[SR][SCL];    // scale ring: a_scale of the tile's 128 rows, then the two weight scales
-    int item_m[ITEMS];                 // the CTA's work items (see item_of), in its visiting order:
-    int item_n[ITEMS];                 // tile, column block,
+    int item_n[ITEMS];                 // the CTA's work items (see item_of), in its visiting order: column block,
     int item_e[ITEMS];                 // the tile's expert
     int item_r0[ITEMS];                // and first row
 };
@@ -122,8 +121,8 @@ __device__ __forceinline__ void item_of(const GemmArgs& a, int64_t w, int NT, in
     m = f + static_cast<int>(l - static_cast<int64_t>(n) * c);
 }
 
-template <int EPI>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const SmemCtl* ctl, int64_t k, int64_t w, int NT) {
+template <int EPI, class Ctl>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, int64_t k, int64_t w, int NT) {
     Tile t;
     if (k < ITEMS) {
         // cached at the kernel's start: no global load at an item boundary
@@ -143,6 +142,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const SmemCtl* ct
         t.row0 = a.tile_row0[m];
     }
     t.ok = t.e >= 0 && t.e < a.E && t.row0 >= 0 && t.row0 + BM <= a.a_rows;
+    // the packed scale-factor tiles of A cover rows 128q .. 128q + 127
+    if (a.sf_packed && (t.row0 & (BM - 1))) t.ok = false;
     if (EPI == MOE_EPI_SILU_MUL_QUANT) {
         t.bcol0 = t.n * 128;
         t.bcol1 = a.N / 2 + t.n * 128;
@@ -153,6 +154,169 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const SmemCtl* ct
         t.has1 = t.bcol1 < a.N;
     }
     return t;
+}
+
+// This CTA's first ITEMS work items (w = blockIdx.x + k * gridDim.x): tile, column block, expert
+// and first row looked up once (all threads, one round of global loads), so that no role waits on
+// a global load when it starts an item.  Only the w13 GEMM reorders (item_of); the w2 GEMM keeps the
+// tile-by-tile order (its column blocks of one expert run in the same wave for the shapes served,
+// and the reorder gained nothing measurable there).
+template <int EPI, class Ctl>
+__device__ __forceinline__ void fill_item_cache(const GemmArgs& a, Ctl* ctl, int64_t total, int NT) {
+    for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
+        const int64_t w = blockIdx.x + k * gridDim.x;
+        if (w >= total) break;
+        int m, n;
+        if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
+            item_of(a, w, NT, m, n);
+        } else {
+            m = static_cast<int>(w / NT);
+            n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
+        }
+        ctl->item_n[k] = n;
+        ctl->item_e[k] = a.tile_expert[m];
+        ctl->item_r0[k] = a.tile_row0[m];
+    }
+}
+
+// The epilogue of one finished work item, run by each of the 8 epilogue warps on its share:
+// acc holds the warp's 32 rows (TMEM lane quarter sp, row = sp * 32 + lane) by 128 columns
+// (silu: gate columns g*64 .. +63 in acc[0, 64) and the matching up columns in acc[64, 128);
+// otherwise columns g*128 .. +127 of the tile).  SiLU(gate)*up with 1x128 requantisation (the
+// group amax exchanged between the two column halves through shared memory; with sf_packed the
+// scale goes out as its UE8M0 byte in packed tiles), or the router-weighted / plain row stores.
+// Returns false if the amax exchange's wait gave up.
+template <int EPI, class Ctl>
+__device__ __forceinline__ bool finish_item(const GemmArgs& a, Ctl* ctl, const Tile& t, float* acc, int warp, int lane,
+                                            int g, int row, int64_t grow, bool active, uint32_t tile_iter,
+                                            volatile int* abort_flag) {
+    const int sp = warp & 3;
+    if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            // silu(g) * u = g * u / (1 + e^-g); its fp32 rounding is not part of the
+            // definition (the requantised bytes are compared within one code)
+            const float gate = acc[j];
+            const float h = __fdividef(gate * acc[64 + j], 1.0f + __expf(-gate));
+            acc[j] = h;
+            amax = fmaxf(amax, fabsf(h));
+        }
+        const uint32_t par = tile_iter & 1u;
+        ctl->amax_x[par][g][row] = amax;
+        mbar_arrive(smem_addr(&ctl->amax_bar[par]));
+        if (!mbar_wait(smem_addr(&ctl->amax_bar[par]), (tile_iter >> 1) & 1u, abort_flag, a.status)) return false;
+        amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
+        const float sc = group_scale_fmt(amax, a.sf_packed ? MOE_SCALE_UE8M0 : a.scale_fmt);
+        const float rsc = __frcp_rn(sc);
+        uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float* h = acc + c * 16 + j * 4;
+                const uint32_t lo = e4m3x2(div_by_scale(h[0], sc, rsc), div_by_scale(h[1], sc, rsc));
+                const uint32_t hi = e4m3x2(div_by_scale(h[2], sc, rsc), div_by_scale(h[3], sc, rsc));
+                wv[j] = lo | (hi << 16);
+            }
+            dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        if (g == 0) {
+            if (a.sf_packed)
+                a.out_sf[packed_sf_offset(grow, t.n, (a.N / 256 + 3) / 4)] = ue8m0_byte(sc);
+            else
+                a.out_scale[grow * a.os_row_stride + static_cast<int64_t>(t.n) * a.os_kb_stride] = sc;
+        }
+    } else if (EPI == MOE_EPI_WEIGHTED_SCATTER) {
+        if (active) {
+            const int32_t pair = a.sorted_pair_ids[grow];
+            if (pair >= 0 && pair < a.num_pairs) {
+                const int64_t tok = pair / a.topk;
+                const float wgt = a.topk_weights[pair];
+                float* dst = a.out_f32 + tok * a.N + t.bcol0 + g * 128;
+#pragma unroll
+                for (int j = 0; j < 128; j += 4)
+                    atomicAdd(reinterpret_cast<float4*>(dst + j),
+                              make_float4(wgt * acc[j], wgt * acc[j + 1], wgt * acc[j + 2], wgt * acc[j + 3]));
+            }
+        }
+    } else if (EPI == MOE_EPI_WEIGHTED_PAIRS_BF16) {
+        // bf16 rows (times the router weight) to out_bf16[pair], through a per-warp
+        // staging buffer of 32 rows x 32 columns (64 B per row, 16-byte chunks swizzled
+        // by row so that both the row-wise writes and the column-wise reads are free
+        // of bank conflicts): each store instruction covers 8 rows x 64 contiguous bytes
+        if (active) {
+            const int32_t pair = a.sorted_pair_ids[grow];
+            const bool keep = pair >= 0 && pair < a.num_pairs;
+            const float wgt = keep ? a.topk_weights[pair] : 0.0f;
+            const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+            uint32_t* stg = reinterpret_cast<uint32_t*>(ctl->stage[warp - FIRST_EPI_WARP]);
+            const int r_out = lane >> 2, q_out = lane & 3;
+            uint16_t* dst[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t p = __shfl_sync(0xffffffffu, pair, i * 8 + r_out);
+                dst[i] = a.out_bf16 + p * a.N + t.bcol0 + g * 128 + q_out * 8;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float* v = acc + c * 32 + q * 8;
+                    const int slot = q ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4*>(stg + lane * 16 + slot * 4) =
+                        make_uint4(bf16x2(wgt * v[0], wgt * v[1]), bf16x2(wgt * v[2], wgt * v[3]),
+                                   bf16x2(wgt * v[4], wgt * v[5]), bf16x2(wgt * v[6], wgt * v[7]));
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i * 8 + r_out;
+                    const int slot = q_out ^ ((r >> 1) & 3);
+                    const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 16 + slot * 4);
+                    if ((keep_mask >> r) & 1u) *reinterpret_cast<uint4*>(dst[i] + c * 32) = v;
+                }
+                __syncwarp();
+            }
+        }
+    } else {
+        // fp32 rows (times the router weight for the rows epilogue) written through a
+        // per-warp staging buffer, 16 columns at a time, so that each store instruction
+        // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
+        if (active) {
+            bool keep = true;
+            float wgt = 1.0f;
+            if (EPI == MOE_EPI_WEIGHTED_ROWS) {
+                const int32_t pair = a.sorted_pair_ids[grow];
+                keep = pair >= 0 && pair < a.num_pairs;
+                wgt = keep ? a.topk_weights[pair] : 0.0f;
+            }
+            const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+            float* stg = ctl->stage[warp - FIRST_EPI_WARP];
+            const int r_out = lane >> 2, q_out = lane & 3;
+            float* gbase = a.out_f32 + (t.row0 + sp * 32) * a.N + t.bcol0 + g * 128 + q_out * 4;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float* v = acc + c * 16 + q * 4;
+                    *reinterpret_cast<float4*>(stg + lane * STAGE_ROW + q * 4) =
+                        make_float4(wgt * v[0], wgt * v[1], wgt * v[2], wgt * v[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = i * 8 + r_out;
+                    const float4 v = *reinterpret_cast<const float4*>(stg + r * STAGE_ROW + q_out * 4);
+                    if ((keep_mask >> r) & 1u)
+                        *reinterpret_cast<float4*>(gbase + static_cast<int64_t>(r) * a.N + c * 16) = v;
+                }
+                __syncwarp();
+            }
+        }
+    }
+    return true;
 }
 
 template <int EPI>
@@ -205,26 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const int64_t total = ntiles * NT;
-    // this CTA's first ITEMS work items (w = blockIdx.x + k * gridDim.x): tile, column block,
-    // expert and first row looked up once, so that no role waits on a global load when it starts
-    // an item.  Only the w13 GEMM reorders (item_of); the w2 GEMM keeps the tile-by-tile order
-    // (its column blocks of one expert run in the same wave for the shapes served, and the
-    // reorder gained nothing measurable there).
-    for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
-        const int64_t w = blockIdx.x + k * gridDim.x;
-        if (w >= total) break;
-        int m, n;
-        if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
-            item_of(a, w, NT, m, n);
-        } else {
-            m = static_cast<int>(w / NT);
-            n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
-        }
-        ctl->item_m[k] = m;
-        ctl->item_n[k] = n;
-        ctl->item_e[k] = a.tile_expert[m];
-        ctl->item_r0[k] = a.tile_row0[m];
-    }
+    fill_item_cache<EPI>(a, ctl, total, NT);
     __syncthreads();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -439,129 +584,276 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++q;
             }
             if (!ok) break;
+            if (!finish_item<EPI>(a, ctl, t, acc, warp, lane, g, row, grow, active, tile_iter, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++tile_iter;
+        }
+    }
 
-            if (EPI == MOE_EPI_SILU_MUL_QUANT) {
-                float amax = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    // silu(g) * u = g * u / (1 + e^-g); its fp32 rounding is not part of the
-                    // definition (the requantised bytes are compared within one code)
-                    const float gate = acc[j];
-                    const float h = __fdividef(gate * acc[64 + j], 1.0f + __expf(-gate));
-                    acc[j] = h;
-                    amax = fmaxf(amax, fabsf(h));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ block-scaled variant
+// With packed UE8M0 scales ("UE8M0: packed UE8M0, 4 values per int32, Blackwell", page
+// "Quantization and MoE Optimizations", section DeepGEMM Scale Formats) every scale is a power of
+// two, so the tensor cores apply them: tcgen05.mma kind::mxf8f6f4.block_scale multiplies each
+// product by the UE8M0 scales of its row of A and its column of B for that K range, and the whole K
+// loop accumulates in one TMEM accumulator with no promotion step.  A 128-wide K block is four MMAs
+// of K = 32 that all use the K block's scale byte (the 128-wide groups and 128x128 blocks span 4
+// scale vectors of 32 each: the same value).  Scale-factor tiles (512 bytes, common.cuh) come with
+// the stage of every fourth K block (one TMA bulk copy for A's 128 rows, one for each of B's 128-
+// column blocks) and are copied into tensor memory by the MMA thread before its MMAs (tcgen05.cp).
+//
+// Tensor memory: columns 0..255 hold the accumulator of the current item; 4 slots of 16 columns
+// from column 256 hold scale factors (A: 4 columns, B: 8 columns).  A slot is reused 4 scale loads
+// later: the stage that brings the new tiles was refilled only after the MMAs of the K block 4
+// stages back completed, and each load covers at least one K block, so the MMAs reading the slot's
+// old contents are complete.  With one accumulator the epilogue first moves its share into
+// registers and frees the accumulator at once; the next item's MMAs run while it finishes the
+// previous item from registers.
+constexpr int SF_STAGE = 3 * kSfTileBytes;   // per stage: A's tile, then B's two
+constexpr uint32_t TMEM_SF = 256;
+constexpr int SF_SLOTS = 4;
+
+struct SmemCtlBs {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull;                    // the accumulator holds a finished item
+    uint64_t tempty;                   // the epilogue warps have moved it to registers (8 arrivals)
+    uint64_t amax_bar[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    float amax_x[2][2][BM];
+    alignas(16) float stage[NUM_EPI_WARPS][32 * 20];
+    int item_n[ITEMS];
+    int item_e[ITEMS];
+    int item_r0[ITEMS];
+};
+constexpr size_t SMEM_BYTES_BS = 1024 + STAGES * (A_TILE + B_TILE + SF_STAGE) + sizeof(SmemCtlBs);
+static_assert(SMEM_BYTES_BS <= 232448, "shared memory per CTA exceeds the sm_103 limit");
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* smA = base;
+    uint8_t* smB = base + STAGES * A_TILE;
+    uint8_t* smSF = smB + STAGES * B_TILE;
+    SmemCtlBs* ctl = reinterpret_cast<SmemCtlBs*>(smSF + STAGES * SF_STAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NT = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 256 : (a.N + 255) / 256;
+    const int KB = a.K / BK;
+    const int KB4 = (KB + 3) / 4;   // scale-factor tiles per 128 rows of A or per 128 columns of B
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        mbar_init(smem_addr(&ctl->tfull), 1);
+        mbar_init(smem_addr(&ctl->tempty), NUM_EPI_WARPS);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_addr(&ctl->amax_bar[b]), NUM_EPI_WARPS * 32);
+        mbar_init(smem_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    grid_dependency_wait();
+    int64_t ntiles = *a.num_tiles;
+    if (ntiles < 0) ntiles = 0;
+    if (ntiles > a.max_tiles) ntiles = a.max_tiles;
+    const int64_t total = ntiles * NT;
+    fill_item_cache<EPI>(a, ctl, total, NT);
+    __syncthreads();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int* abort_flag = &ctl->abort_flag;
+    if (warp < FIRST_EPI_WARP) {
+      regs_decrease<RegSplit<EPI>::control>();
+      if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok = true;
+            int64_t k = 0;
+            const int NBn = a.N / 128;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+                const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
+                if (!t.ok) {
+                    status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+                    continue;
                 }
-                const uint32_t par = tile_iter & 1u;
-                ctl->amax_x[par][g][row] = amax;
-                mbar_arrive(smem_addr(&ctl->amax_bar[par]));
-                if (!mbar_wait(smem_addr(&ctl->amax_bar[par]), (tile_iter >> 1) & 1u, abort_flag, a.status)) {
+                int32_t by0, by1, bdx, bdy;
+                if (a.b_tiled) {
+                    by0 = ((t.e * (a.N / 128) + t.bcol0 / 128) * KB) * 128;
+                    by1 = ((t.e * (a.N / 128) + t.bcol1 / 128) * KB) * 128;
+                    bdx = 0;
+                    bdy = 128;
+                } else {
+                    by0 = t.e * a.N + t.bcol0;
+                    by1 = t.e * a.N + t.bcol1;
+                    bdx = BK;
+                    bdy = 0;
+                }
+                const uint8_t* sfa = a.a_sf + (t.row0 >> 7) * KB4 * kSfTileBytes;
+                const uint8_t* sfb0 = a.b_sf + (static_cast<int64_t>(t.e) * NBn + t.bcol0 / 128) * KB4 * kSfTileBytes;
+                const uint8_t* sfb1 = a.b_sf + (static_cast<int64_t>(t.e) * NBn + t.bcol1 / 128) * KB4 * kSfTileBytes;
+                const uint32_t bytes = a.a_box_rows * BK + (t.has1 ? B_TILE : B_HALF);
+                const uint32_t sf_bytes = (t.has1 ? 3 : 2) * kSfTileBytes;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_addr(&ctl->full[stage]);
+                    const bool load_sf = (kb & 3) == 0;
+                    mbar_arrive_expect_tx(fb, bytes + (load_sf ? sf_bytes : 0u));
+                    tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
+                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
+                    if (t.has1)
+                        tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * bdx, by1 + kb * bdy, fb);
+                    if (load_sf) {
+                        const uint32_t dst = smem_addr(smSF + stage * SF_STAGE);
+                        const int64_t q = (kb >> 2) * kSfTileBytes;
+                        bulk_load(dst, sfa + q, kSfTileBytes, fb);
+                        bulk_load(dst + kSfTileBytes, sfb0 + q, kSfTileBytes, fb);
+                        if (t.has1) bulk_load(dst + 2 * kSfTileBytes, sfb1 + q, kSfTileBytes, fb);
+                    }
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < STAGES; ++s) {
+                    const uint32_t n_s = (issued + STAGES - 1 - s) / STAGES;
+                    if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
+                }
+            }
+        }
+      } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0, items = 0, sf_loads = 0;
+            bool ok = true;
+            int64_t k = 0;
+            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+                const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
+                if (!t.ok) continue;
+                const int n = t.has1 ? 256 : 128;
+                // the accumulator is free once the epilogue warps moved the previous item out
+                if (!mbar_wait(smem_addr(&ctl->tempty), (items & 1u) ^ 1u, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
-                amax = fmaxf(ctl->amax_x[par][0][row], ctl->amax_x[par][1][row]);
-                const float sc = group_scale_fmt(amax, a.scale_fmt);
-                const float rsc = __frcp_rn(sc);
-                uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float* h = acc + c * 16 + j * 4;
-                        const uint32_t lo = e4m3x2(div_by_scale(h[0], sc, rsc), div_by_scale(h[1], sc, rsc));
-                        const uint32_t hi = e4m3x2(div_by_scale(h[2], sc, rsc), div_by_scale(h[3], sc, rsc));
-                        wv[j] = lo | (hi << 16);
+                tc_fence_after();
+                uint32_t sfa_t = 0, sfb_t = 0;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
                     }
-                    dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    tc_fence_after();
+                    if ((kb & 3) == 0) {
+                        const uint32_t col = TMEM_SF + (sf_loads % SF_SLOTS) * 16;
+                        const uint32_t src = smem_addr(smSF + stage * SF_STAGE);
+                        sfa_t = tmem + col;
+                        sfb_t = tmem + col + 4;
+                        tmem_copy_sf_tile(sfa_t, smem_desc_sf_tile(src));
+                        tmem_copy_sf_tile(sfb_t, smem_desc_sf_tile(src + kSfTileBytes));
+                        if (t.has1) tmem_copy_sf_tile(sfb_t + 4, smem_desc_sf_tile(src + 2 * kSfTileBytes));
+                        ++sf_loads;
+                    }
+                    const uint32_t idesc = idesc_e4m3_ue8m0(BM, n, kb & 3);
+                    const uint32_t a0 = smem_addr(smA + stage * A_TILE);
+                    const uint32_t b0 = smem_addr(smB + stage * B_TILE);
+#pragma unroll
+                    for (int s = 0; s < BK / 32; ++s)
+                        mma_e4m3_block_scaled(tmem, smem_desc_k128_sw128(a0 + s * 32), smem_desc_k128_sw128(b0 + s * 32),
+                                              idesc, sfa_t, sfb_t, (kb | s) != 0 ? 1u : 0u);
+                    mma_commit(smem_addr(&ctl->empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                if (g == 0) a.out_scale[grow * a.os_row_stride + static_cast<int64_t>(t.n) * a.os_kb_stride] = sc;
-            } else if (EPI == MOE_EPI_WEIGHTED_SCATTER) {
-                if (active) {
-                    const int32_t pair = a.sorted_pair_ids[grow];
-                    if (pair >= 0 && pair < a.num_pairs) {
-                        const int64_t tok = pair / a.topk;
-                        const float wgt = a.topk_weights[pair];
-                        float* dst = a.out_f32 + tok * a.N + t.bcol0 + g * 128;
+                if (!ok) break;
+                mma_commit(smem_addr(&ctl->tfull));
+                ++items;
+            }
+            if (!ok) {
+                mma_commit(smem_addr(&ctl->drain));
+                mbar_wait(smem_addr(&ctl->drain), 0, nullptr, a.status);
+            }
+        }
+      }
+    } else {
+        regs_increase<RegSplit<EPI>::epilogue>();
+        // ---------------------------------------------------------------- epilogue
+        const int g = (warp - FIRST_EPI_WARP) >> 2;   // column half
+        const int sp = warp & 3;                      // TMEM lane quarter
+        const int row = sp * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        uint32_t tile_iter = 0;
+        bool ok = true;
+        int64_t k = 0;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
+            if (!t.ok) continue;
+            const int64_t grow = t.row0 + row;
+            const bool row_real = a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0;
+            const bool warp_live = __any_sync(0xffffffffu, row_real);
+            const bool active = ((EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1) && warp_live;
+            float acc[128];
+            if (!mbar_wait(smem_addr(&ctl->tfull), tile_iter & 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (active) {
+                // silu: gate columns g*64 .. +63 -> acc[0, 64), up columns 128 + g*64 .. -> acc[64, 128)
 #pragma unroll
-                        for (int j = 0; j < 128; j += 4)
-                            atomicAdd(reinterpret_cast<float4*>(dst + j),
-                                      make_float4(wgt * acc[j], wgt * acc[j + 1], wgt * acc[j + 2], wgt * acc[j + 3]));
-                    }
-                }
-            } else if (EPI == MOE_EPI_WEIGHTED_PAIRS_BF16) {
-                // bf16 rows (times the router weight) to out_bf16[pair], through a per-warp
-                // staging buffer of 32 rows x 32 columns (64 B per row, 16-byte chunks swizzled
-                // by row so that both the row-wise writes and the column-wise reads are free
-                // of bank conflicts): each store instruction covers 8 rows x 64 contiguous bytes
-                if (active) {
-                    const int32_t pair = a.sorted_pair_ids[grow];
-                    const bool keep = pair >= 0 && pair < a.num_pairs;
-                    const float wgt = keep ? a.topk_weights[pair] : 0.0f;
-                    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
-                    uint32_t* stg = reinterpret_cast<uint32_t*>(ctl->stage[warp - FIRST_EPI_WARP]);
-                    const int r_out = lane >> 2, q_out = lane & 3;
-                    uint16_t* dst[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int64_t p = __shfl_sync(0xffffffffu, pair, i * 8 + r_out);
-                        dst[i] = a.out_bf16 + p * a.N + t.bcol0 + g * 128 + q_out * 8;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float* v = acc + c * 32 + q * 8;
-                            const int slot = q ^ ((lane >> 1) & 3);
-                            *reinterpret_cast<uint4*>(stg + lane * 16 + slot * 4) =
-                                make_uint4(bf16x2(wgt * v[0], wgt * v[1]), bf16x2(wgt * v[2], wgt * v[3]),
-                                           bf16x2(wgt * v[4], wgt * v[5]), bf16x2(wgt * v[6], wgt * v[7]));
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = i * 8 + r_out;
-                            const int slot = q_out ^ ((r >> 1) & 3);
-                            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 16 + slot * 4);
-                            if ((keep_mask >> r) & 1u) *reinterpret_cast<uint4*>(dst[i] + c * 32) = v;
-                        }
-                        __syncwarp();
-                    }
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t c0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? lane_base + r * 128 + g * 64
+                                                                        : lane_base + g * 128 + r * 64;
+                    tmem_ld32x2(c0, c0 + 32, acc + r * 64, acc + r * 64 + 32);
                 }
             } else {
-                // fp32 rows (times the router weight for the rows epilogue) written through a
-                // per-warp staging buffer, 16 columns at a time, so that each store instruction
-                // covers 8 rows x 64 contiguous bytes instead of 32 rows x 16 bytes
-                if (active) {
-                    bool keep = true;
-                    float wgt = 1.0f;
-                    if (EPI == MOE_EPI_WEIGHTED_ROWS) {
-                        const int32_t pair = a.sorted_pair_ids[grow];
-                        keep = pair >= 0 && pair < a.num_pairs;
-                        wgt = keep ? a.topk_weights[pair] : 0.0f;
-                    }
-                    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
-                    float* stg = ctl->stage[warp - FIRST_EPI_WARP];
-                    const int r_out = lane >> 2, q_out = lane & 3;
-                    float* gbase = a.out_f32 + (t.row0 + sp * 32) * a.N + t.bcol0 + g * 128 + q_out * 4;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float* v = acc + c * 16 + q * 4;
-                            *reinterpret_cast<float4*>(stg + lane * STAGE_ROW + q * 4) =
-                                make_float4(wgt * v[0], wgt * v[1], wgt * v[2], wgt * v[3]);
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = i * 8 + r_out;
-                            const float4 v = *reinterpret_cast<const float4*>(stg + r * STAGE_ROW + q_out * 4);
-                            if ((keep_mask >> r) & 1u)
-                                *reinterpret_cast<float4*>(gbase + static_cast<int64_t>(r) * a.N + c * 16) = v;
-                        }
-                        __syncwarp();
-                    }
-                }
+                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty));
+            if (!finish_item<EPI>(a, ctl, t, acc, warp, lane, g, row, grow, active, tile_iter, abort_flag)) {
+                ok = false;
+                break;
             }
             ++tile_iter;
         }
@@ -664,6 +956,16 @@ cudaError_t gemm_init_device() {
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const int bytes_bs = static_cast<int>(SMEM_BYTES_BS);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_bs_kernel<MOE_EPI_STORE_F32>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_bs);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_bs_kernel<MOE_EPI_SILU_MUL_QUANT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_bs);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_bs_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_bs);
     return err;
 }
 
@@ -681,6 +983,21 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
         err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(bound < num_sms ? bound : num_sms);
+    if (args.sf_packed) {
+        switch (args.epi) {
+            case MOE_EPI_STORE_F32:
+                return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_STORE_F32>, dim3(grid), dim3(NUM_THREADS),
+                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+            case MOE_EPI_SILU_MUL_QUANT:
+                return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_SILU_MUL_QUANT>, dim3(grid), dim3(NUM_THREADS),
+                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+            case MOE_EPI_WEIGHTED_PAIRS_BF16:
+                return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>, dim3(grid), dim3(NUM_THREADS),
+                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+            default:
+                return cudaErrorInvalidValue;
+        }
+    }
     switch (args.epi) {
         case MOE_EPI_STORE_F32:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_STORE_F32>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,

@@ -67,7 +67,8 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec, cudaStream_t stream);
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec, cudaStream_t stream,
+                                    uint8_t* sf = nullptr);
 
 // masked.cu: row maps and tile table of the masked batched layout [E, M, H] (Mp = M rounded
 // up to 128): row_map [E*Mp] (input row or -1), pos [E*M] (padded row or -1), ones [E*M]
@@ -79,9 +80,16 @@ cudaError_t launch_masked_map(const int32_t* counts, int E, int M, int Mp, int32
 // 1x128 group quantisation of bf16 rows.  Row r of x goes to output row r, or
 // (when pos != null) to output rows pos[r*topk + j], j < topk, skipping -1.
 // Scale of (output row o, group g) is stored at s[o*s_row_stride + g*s_group_stride].
+// s may be null (no fp32 scales); sf != null: the scales (then rounded up to powers of two,
+// MOE_SCALE_UE8M0) also go out as UE8M0 bytes in packed scale-factor tiles (packed_sf_offset,
+// ceil(cols/512) tiles per 128 output rows).
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, int scale_fmt, cudaStream_t stream);
+                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf = nullptr);
+// [E, N/128, K/128] power-of-two block scales -> [E][N/128][ceil(K/512)] scale-factor tiles (out
+// 16-byte aligned); a scale that is not a positive power of two sets MOE_STATUS_BAD_SCALE
+cudaError_t launch_pack_scales(const float* s, int E, int N, int K, uint8_t* out, uint32_t* status,
+                               cudaStream_t stream);
 cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
                                       cudaStream_t stream);
 // [E, N, K] e4m3 -> [E][N/128][K/128][128][128] (each 128x128 block contiguous)
@@ -138,6 +146,15 @@ struct GemmArgs {
     int64_t num_pairs;
     uint16_t* out_bf16;
     int scale_fmt;             // MOE_SCALE_*: the SiLU epilogue's requantisation scales
+    // packed UE8M0 scale factors (sf_packed != 0): the block-scaled kernel, with scale-factor tiles
+    // (common.cuh, packed_sf_offset) instead of fp32 scales.  a_sf: A's, ceil(K/512) tiles per 128
+    // rows (tiles start at row 0: tile_row0 must be a multiple of 128); b_sf: B's, [E][N/128]
+    // [ceil(K/512)] tiles; out_sf: the SiLU epilogue's requantisation scales, ceil(N/1024) tiles
+    // per 128 rows.  a_scale, b_scale and out_scale are then unused.
+    int sf_packed;
+    const uint8_t* a_sf;
+    const uint8_t* b_sf;
+    uint8_t* out_sf;
     uint32_t* status;
 };
 cudaError_t gemm_init_device();

@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles,
     uint32_t* status, const uint16_t* __restrict__ x, int T, int H, int topk, uint8_t* __restrict__ q,
-    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec) {
+    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec,
+    uint8_t* __restrict__ sf, int sf_kb4) {
     grid_dependency_wait();
     __shared__ int s_id[kSmallPairs];
     __shared__ int s_pos[kSmallPairs];
@@ -131,7 +132,10 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
                 const int64_t o = s_pos[t * topk + j];
                 if (o < 0) continue;
                 *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
-                if (sub == 0) s[o * s_rs + g * s_gs] = sc;
+                if (sub == 0) {
+                    if (s) s[o * s_rs + g * s_gs] = sc;
+                    if (sf) sf[packed_sf_offset(o, g, sf_kb4)] = ue8m0_byte(sc);
+                }
             }
         }
     }
@@ -144,14 +148,14 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
                                     int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, uint8_t* sf) {
     const int groups = T * (H / 128);
     int blocks = (groups + 63) / 64;
     if (blocks < 1) blocks = 1;
     if (blocks > 148) blocks = 148;
     return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
                       padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
-                      q, q_ld, s, s_rs, s_gs, scale_fmt, dec);
+                      q, q_ld, s, s_rs, s_gs, sf ? MOE_SCALE_UE8M0 : scale_fmt, dec, sf, (H / 128 + 3) / 4);
 }
 
 }  // namespace mfp8

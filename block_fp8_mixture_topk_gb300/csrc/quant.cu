@@ -30,7 +30,8 @@ namespace {
 __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __restrict__ x, int64_t rows, int cols,
                                                           int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
                                                           float* __restrict__ s, int64_t s_rs, int64_t s_gs,
-                                                          const int32_t* __restrict__ pos, int topk, int scale_fmt) {
+                                                          const int32_t* __restrict__ pos, int topk, int scale_fmt,
+                                                          uint8_t* __restrict__ sf, int sf_kb4) {
     grid_dependency_wait();
     const int G = cols / 128;
     const int64_t total = rows * G;
@@ -62,11 +63,17 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
                     const int64_t o = pos[r * topk + j];
                     if (o < 0) continue;
                     *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
-                    if (sub == 0) s[o * s_rs + g * s_gs] = sc;
+                    if (sub == 0) {
+                        if (s) s[o * s_rs + g * s_gs] = sc;
+                        if (sf) sf[packed_sf_offset(o, g, sf_kb4)] = ue8m0_byte(sc);
+                    }
                 }
             } else {
                 *reinterpret_cast<uint2*>(q + r * q_ld + g * 128 + sub * 8) = code;
-                if (sub == 0) s[r * s_rs + g * s_gs] = sc;
+                if (sub == 0) {
+                    if (s) s[r * s_rs + g * s_gs] = sc;
+                    if (sf) sf[packed_sf_offset(r, g, sf_kb4)] = ue8m0_byte(sc);
+                }
             }
         }
     }
@@ -112,6 +119,38 @@ __global__ void __launch_bounds__(256) block_quant_weight_kernel(const uint16_t*
         reinterpret_cast<uint4*>(q + off)[i] = make_uint4(out[2 * i].x, out[2 * i].y, out[2 * i + 1].x,
                                                           out[2 * i + 1].y);
     if (threadIdx.x == 0) s[(static_cast<int64_t>(e) * NB + nb) * KB + kb] = sc;
+}
+
+// Load-time packing of 128x128 block scales [E, N/128, K/128] (powers of two) into the
+// scale-factor tiles of the block-scaled GEMM: [E][N/128][ceil(K/512)] tiles, each line of a tile
+// holding the 4 K blocks' bytes once per 32-row quarter (a block's scale is the scale of all its
+// 128 rows).  One thread per 16-byte line; K blocks past the end get byte 127 (scale 1).  A scale
+// that is not a positive power of two sets MOE_STATUS_BAD_SCALE (its byte is then its exponent).
+__global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ s, int64_t nblocks, int KB,
+                                                          uint4* __restrict__ out, uint32_t* status) {
+    grid_dependency_wait();
+    const int KB4 = (KB + 3) / 4;
+    const int64_t lines = nblocks * KB4 * 32;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < lines;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t tile = i >> 5;
+        const int64_t blk = tile / KB4;
+        const int q = static_cast<int>(tile - blk * KB4);
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int kb = q * 4 + b;
+            uint32_t byte = 127u;
+            if (kb < KB) {
+                const float v = s[blk * KB + kb];
+                const uint32_t bits = __float_as_uint(v);
+                if ((bits & 0x007FFFFFu) || !(v > 0.0f) || bits >= 0x7F800000u) status_set(status, MOE_STATUS_BAD_SCALE);
+                byte = (bits >> 23) & 0xFFu;
+            }
+            word |= byte << (8 * b);
+        }
+        out[i] = make_uint4(word, word, word, word);
+    }
 }
 
 // out[t] = bf16(sum_j y[pos[t*topk + j]]): thread = 4 consecutive columns of one token,
@@ -220,11 +259,24 @@ int grid_for(int64_t work_items, int per_block) {
 
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, int scale_fmt, cudaStream_t stream) {
+                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf) {
     const int64_t groups = rows * (cols / 128);
     if (groups == 0) return cudaSuccess;
+    const int sf_kb4 = (cols / 128 + 3) / 4;
     return launch_pdl(group_quant_kernel, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, rows, cols, ld, q,
-                      q_ld, s, s_row_stride, s_group_stride, pos, topk, scale_fmt);
+                      q_ld, s, s_row_stride, s_group_stride, pos, topk, sf ? MOE_SCALE_UE8M0 : scale_fmt, sf, sf_kb4);
+}
+
+cudaError_t launch_pack_scales(const float* s, int E, int N, int K, uint8_t* out, uint32_t* status,
+                               cudaStream_t stream) {
+    const int64_t nblocks = static_cast<int64_t>(E) * (N / 128);
+    const int KB = K / 128;
+    const int64_t lines = nblocks * ((KB + 3) / 4) * 32;
+    if (lines == 0) return cudaSuccess;
+    int64_t blocks = (lines + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    return launch_pdl(pack_scales_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, s, nblocks, KB,
+                      reinterpret_cast<uint4*>(out), status);
 }
 
 cudaError_t launch_block_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,

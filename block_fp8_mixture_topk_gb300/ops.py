@@ -18,7 +18,9 @@ from . import build as _build
 MOE_BLOCK_M = 128
 MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED, MOE_WEIGHTS_NVFP4 = 0, 1, 2
 NVFP4_UNIT_BYTES = 16 * 64 + 16 * 8   # one 16-row slab x one 128-wide K block: codes, then block scales
-SCALE_FMT = {"f32": 0, "ue8m0": 1}      # fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)
+# fp32 amax/448; that scale rounded up to a power of two (FLOAT32_CEIL_UE8M0); the same UE8M0 scales in
+# the packed scale-factor tiles of the block-scaled MMA (MOE_SCALE_UE8M0_PACKED)
+SCALE_FMT = {"f32": 0, "ue8m0": 1, "ue8m0_packed": 2}
 SCORING = {"softmax": 0, "sigmoid": 1}
 EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
 
@@ -104,6 +106,8 @@ def lib():
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P, P, P], I),
                 "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
+                "moe_packed_scale_bytes": ([I64, I], SZ),
+                "moe_fp8_block_pack_scales": ([P, I, I, I, P, P], I),
                 "moe_nvfp4_quant_weight": ([P, I, I, I, P, P, P, P], I),
                 "moe_nvfp4_packed_bytes": ([I, I, I], SZ),
                 "moe_nvfp4_pack_weights": ([P, P, I, I, I, P, P], I),
@@ -206,13 +210,22 @@ def moe_align_permute(topk_ids, num_experts, block_m=MOE_BLOCK_M):
     return out
 
 
+def moe_packed_scale_bytes(rows, K) -> int:
+    """Bytes of the packed UE8M0 scale tiles of a [rows, K] operand."""
+    return int(lib().moe_packed_scale_bytes(rows, K))
+
+
 def fp8_group_quant(x, scale_fmt="f32"):
     """1x128 group quantisation of bf16 [rows, cols]: returns (codes uint8, scales fp32 [rows, cols/128]).
-    scale_fmt: "f32" (amax/448) or "ue8m0" (rounded up to a power of two)."""
+    scale_fmt: "f32" (amax/448), "ue8m0" (rounded up to a power of two) or "ue8m0_packed" (the same
+    scales as packed UE8M0 tiles: a uint8 tensor of moe_packed_scale_bytes(rows, cols) bytes)."""
     _cuda(x, torch.bfloat16, "x")
     rows, cols = x.shape
     q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
-    s = torch.empty(rows, max(cols // 128, 1), dtype=torch.float32, device=x.device)
+    if scale_fmt == "ue8m0_packed":
+        s = torch.zeros(max(moe_packed_scale_bytes(rows, cols), 16), dtype=torch.uint8, device=x.device)
+    else:
+        s = torch.empty(rows, max(cols // 128, 1), dtype=torch.float32, device=x.device)
     rc = lib().fp8_group_quant_ex(_ptr(x), rows, cols, cols, _ptr(q), _ptr(s), SCALE_FMT[scale_fmt], _stream())
     _check("fp8_group_quant", rc)
     return q, s
@@ -227,6 +240,17 @@ def fp8_block_quant_weight(w, scale_fmt="f32"):
     rc = lib().fp8_block_quant_weight_ex(_ptr(w), E, N, K, _ptr(q), _ptr(s), SCALE_FMT[scale_fmt], _stream())
     _check("fp8_block_quant_weight", rc)
     return q, s
+
+
+def moe_fp8_block_pack_scales(s):
+    """UE8M0 (power-of-two) block scales fp32 [E, N/128, K/128] -> the packed scale tiles of the
+    block-scaled GEMMs, uint8 [E, N/128, ceil(K/512), 512] (load-time, once)."""
+    _cuda(s, torch.float32, "s")
+    E, NB, KB = s.shape
+    out = torch.empty(E, NB, (KB + 3) // 4, 512, dtype=torch.uint8, device=s.device)
+    _check("moe_fp8_block_pack_scales", lib().moe_fp8_block_pack_scales(_ptr(s), E, NB * 128, KB * 128, _ptr(out),
+                                                                          _stream()))
+    return out
 
 
 def moe_fp8_block_pack_weights(w):
@@ -363,14 +387,17 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
 
     w13 / w2 in the pages' layout [E, N, K] or tile-packed (moe_fp8_block_pack_weights, 5-D), or
     NVFP4-packed (moe_nvfp4_pack_weights, 4-D) with w13_scale / w2_scale the global scales [E].
+    scale_fmt "ue8m0_packed": w13_scale / w2_scale are moe_fp8_block_pack_scales outputs and both
+    GEMMs run on the block-scaled MMA.
     decode: "auto", "off" or "on" -- the decode-path GEMMs for small steps (MOE_DECODE_*).
     events: optional list of 7 torch.cuda.Event recorded between the stages
     (FORWARD_STAGES) on the current stream, for per-stage timing."""
     _cuda(hidden, torch.bfloat16, "hidden")
     _cuda(router_logits, torch.float32, "router_logits")
     w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
-    _cuda(w13_scale, torch.float32, "w13_scale")
-    _cuda(w2_scale, torch.float32, "w2_scale")
+    sdt = torch.uint8 if scale_fmt == "ue8m0_packed" else torch.float32
+    _cuda(w13_scale, sdt, "w13_scale")
+    _cuda(w2_scale, sdt, "w2_scale")
     T, H = hidden.shape
     E, N1, _, layout = _weight_shape(w13)
     if _weight_shape(w2)[3] != layout:
@@ -420,8 +447,9 @@ def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, o
     _cuda(hidden, torch.bfloat16, "hidden")
     _cuda(counts, torch.int32, "counts")
     w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
-    _cuda(w13_scale, torch.float32, "w13_scale")
-    _cuda(w2_scale, torch.float32, "w2_scale")
+    sdt = torch.uint8 if scale_fmt == "ue8m0_packed" else torch.float32
+    _cuda(w13_scale, sdt, "w13_scale")
+    _cuda(w2_scale, sdt, "w2_scale")
     E, M, H = hidden.shape
     _, N1, _, layout = _weight_shape(w13)
     if _weight_shape(w2)[3] != layout:

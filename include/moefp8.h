@@ -51,6 +51,7 @@ extern "C" {
 #define MOE_STATUS_WAIT_TIMEOUT 0x1u      /* a pipeline wait gave up; outputs invalid */
 #define MOE_STATUS_BAD_EXPERT_ID 0x2u     /* a routed id was outside [0, E); pair dropped */
 #define MOE_STATUS_BAD_COUNT 0x4u         /* a masked-layout count was outside [0, max_tokens]; clamped */
+#define MOE_STATUS_BAD_SCALE 0x8u         /* a scale packed as UE8M0 was not a positive power of two */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024
@@ -208,7 +209,35 @@ int moe_nvfp4_pack_weights(const uint8_t* q, const uint8_t* block_scale, int E, 
  * the requantised intermediate are scaled, and should match the weights'. */
 #define MOE_SCALE_F32 0
 #define MOE_SCALE_UE8M0 1
-/* fp8_group_quant / fp8_block_quant_weight with a scale format. */
+/* MOE_SCALE_UE8M0_PACKED: the UE8M0 scales stored as 8-bit exponents (value 2^(byte - 127)) in the
+ * packed layout the tensor cores read ("UE8M0: packed UE8M0 (4 values per int32) (Blackwell)",
+ * page "Quantization and MoE Optimizations", section DeepGEMM Scale Formats).  With it the GEMMs
+ * run on the block-scaled MMA (tcgen05.mma kind::mxf8f6f4.block_scale): the tensor cores apply
+ * the scales and accumulate the whole K loop, with no per-K-block promotion.  The numbers are those
+ * of MOE_SCALE_UE8M0 (the same scales; only the fp32 summation order differs).
+ *
+ * Packed layout of the scales of a [rows, K] operand (1x128 groups of activations, or a weight's
+ * 128x128 blocks repeated over their 128 rows): 512-byte tiles ordered [ceil(rows/128)][ceil(K/512)];
+ * the byte of (row r, K block kb = k/128) is at
+ *     ((r / 128) * ceil(K/512) + kb / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4
+ * i.e. a tile is 32 lines of 16 bytes, line l holding rows l, l+32, l+64, l+96 as four 32-bit
+ * words, each word the scales of 4 consecutive K blocks (byte b = K block 4q + b).  Weights: one
+ * set of tiles per expert, [E][N/128][ceil(K/512)] tiles (moe_fp8_block_pack_scales). */
+#define MOE_SCALE_UE8M0_PACKED 2
+/* Bytes of the packed scale tiles of a [rows, K] operand: ceil(rows/128) * ceil(K/512) * 512
+ * (0 for negative sizes or K not a multiple of 128). */
+size_t moe_packed_scale_bytes(int64_t rows, int K);
+/* Load-time packing of UE8M0 weight block scales s [E, N/128, K/128] (fp32 powers of two, e.g.
+ * fp8_block_quant_weight_ex with MOE_SCALE_UE8M0) into the packed layout: out, device,
+ * moe_packed_scale_bytes(E * N, K) bytes, 16-byte aligned; K blocks past K in a tile get byte 127.
+ * A scale that is not a positive power of two sets MOE_STATUS_BAD_SCALE (device status word; its
+ * byte is then its exponent, not a rounding of it).  N and K multiples of 128. */
+int moe_fp8_block_pack_scales(const float* s, int E, int N, int K, uint8_t* out, void* stream);
+/* fp8_group_quant / fp8_block_quant_weight with a scale format.  fp8_group_quant_ex with
+ * MOE_SCALE_UE8M0_PACKED writes the UE8M0 scales as packed tiles: s is then a byte array of
+ * moe_packed_scale_bytes(rows, cols) (passed as float*), rows past `rows` in the last tile left as
+ * they are.  fp8_block_quant_weight_ex takes MOE_SCALE_F32 or MOE_SCALE_UE8M0 (pack its scales
+ * with moe_fp8_block_pack_scales). */
 int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, int scale_fmt,
                        void* stream);
 int fp8_block_quant_weight_ex(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,
@@ -251,7 +280,15 @@ int fp8_block_quant_weight_ex(const uint16_t* w, int E, int N, int K, uint8_t* q
  * computed and its output rows are left unspecified (the scatter and rows
  * epilogues always require it and skip padding rows).
  * Otherwise rows of a tile past its expert's count are computed from whatever
- * A holds there and belong to no pair. */
+ * A holds there and belong to no pair.
+ * Scale format (epilogue scale_fmt): MOE_SCALE_F32 / MOE_SCALE_UE8M0: fp32 scales as above, the
+ * format only deciding the SiLU epilogue's requantisation scales.  MOE_SCALE_UE8M0_PACKED: the
+ * block-scaled MMA; a_scale is A's packed scale tiles (a byte array of
+ * moe_packed_scale_bytes(a_rows, K), strides ignored), b_scale the weights' packed tiles
+ * (moe_fp8_block_pack_scales), every tile_row0 a multiple of 128 (other tiles are skipped and set
+ * MOE_STATUS_BAD_EXPERT_ID), the SiLU epilogue writes out_scale as packed tiles of
+ * moe_packed_scale_bytes(a_rows, N/2) bytes, and only MOE_EPI_STORE_F32, MOE_EPI_SILU_MUL_QUANT and
+ * MOE_EPI_WEIGHTED_PAIRS_BF16 are available. */
 #define MOE_EPI_STORE_F32 0
 #define MOE_EPI_SILU_MUL_QUANT 1
 #define MOE_EPI_WEIGHTED_SCATTER 2
@@ -366,10 +403,14 @@ int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode);
  * their FP8 1x128 groups.  Both GEMMs then run on the decode-path kernel (decode_path
  * MOE_DECODE_OFF is rejected with MOE_ERR_INVALID_ARG), a step of more than 8 tokens 8 tokens
  * at a time (4 launches each); moe_fp8_block_workspace_size(T, ...) still suffices.  Shapes the
- * decode kernel cannot take give MOE_ERR_UNSUPPORTED_SHAPE. */
+ * decode kernel cannot take give MOE_ERR_UNSUPPORTED_SHAPE.
+ * MOE_SCALE_UE8M0_PACKED: w13_scale / w2_scale are the packed UE8M0 weight scales
+ * (moe_fp8_block_pack_scales outputs, passed as const float*) and both GEMMs run on the block-scaled
+ * MMA; the decode-path kernel does not take them (MOE_DECODE_AUTO then takes the tile GEMMs,
+ * MOE_DECODE_ON and MOE_WEIGHTS_NVFP4 are rejected with MOE_ERR_INVALID_ARG). */
 typedef struct moe_forward_options {
     int32_t weight_layout;            /* MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED or MOE_WEIGHTS_NVFP4 */
-    int32_t scale_fmt;                /* MOE_SCALE_F32 or MOE_SCALE_UE8M0 */
+    int32_t scale_fmt;                /* MOE_SCALE_F32, MOE_SCALE_UE8M0 or MOE_SCALE_UE8M0_PACKED */
     int32_t decode_path;              /* MOE_DECODE_AUTO, MOE_DECODE_OFF or MOE_DECODE_ON */
 } moe_forward_options;
 
