@@ -60,8 +60,9 @@ def parse():
                    help="routed: the whole layer (default); masked: moe_fp8_block_forward_masked on rows "
                         "grouped by expert, counts from routing the workload's tokens")
     p.add_argument("--max-tokens", type=int, default=None, help="masked layout: rows per expert (default: max count)")
-    p.add_argument("--scale-fmt", choices=["f32", "ue8m0"], default="f32",
-                   help="block scales: fp32 amax/448, or rounded up to a power of two (FLOAT32_CEIL_UE8M0)")
+    p.add_argument("--scale-fmt", choices=["f32", "ue8m0", "ue8m0_packed"], default="f32",
+                   help="block scales: fp32 amax/448, rounded up to a power of two (FLOAT32_CEIL_UE8M0), or those "
+                        "UE8M0 scales packed for the block-scaled tensor-core MMA (the tile GEMMs only)")
     p.add_argument("--decode", choices=["auto", "off", "on"], default="auto",
                    help="expert GEMMs of small steps: decode-path kernels for up to 8 tokens (auto), never, "
                         "or whenever the step qualifies")
@@ -95,7 +96,9 @@ def describe(wl, world):
 
 
 def describe_weights(args):
-    fmt = ", scales rounded up to powers of two (ue8m0)" if args.scale_fmt == "ue8m0" else ", fp32 scales"
+    fmt = {"ue8m0": ", scales rounded up to powers of two (ue8m0)",
+           "ue8m0_packed": ", UE8M0 scales packed for the block-scaled MMA (ue8m0_packed)"}.get(args.scale_fmt,
+                                                                                                 ", fp32 scales")
     if args.weights == "nvfp4":
         return ("NVFP4: e2m1 codes, e4m3 scale per 16 along K, fp32 global scale per expert, packed at load "
                 "time (moe_nvfp4_pack_weights); activations e4m3 1x128 groups" + fmt)
@@ -109,9 +112,13 @@ def touched_per_pass(ids, tokens_per_pass):
                for t0 in range(0, ids.shape[0], tokens_per_pass))
 
 
-def expert_weight_bytes(wl, nvfp4=False):
+def expert_weight_bytes(wl, nvfp4=False, packed_scales=False):
     """Bytes one expert's w13 and w2 occupy (codes and scales): (w13, both)."""
     H, I = wl.H, wl.I
+    if packed_scales:
+        # UE8M0 scale tiles: 512 bytes per 128 weight rows and 4 K blocks
+        w13 = 2 * I * H + (2 * I // 128) * -(-H // 512) * 512
+        return w13, w13 + H * I + (H // 128) * -(-I // 512) * 512
     if nvfp4:
         w13 = 2 * I * H // 2 + 2 * I * H // 16 + 4
         return w13, w13 + H * I // 2 + H * I // 16 + 4
@@ -352,12 +359,15 @@ def run_ours(args, wl):
         w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
         w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
         w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+        wfmt = "ue8m0" if args.scale_fmt == "ue8m0_packed" else args.scale_fmt
         for e0 in range(0, E, 8):
             ex = range(e0, min(E, e0 + 8))
             w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex),
-                                                                                        args.scale_fmt)
-            w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex),
-                                                                                      args.scale_fmt)
+                                                                                        wfmt)
+            w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), wfmt)
+        if args.scale_fmt == "ue8m0_packed":
+            # load-time packing of the UE8M0 block scales for the block-scaled MMA (untimed)
+            w13s, w2s = moe.moe_fp8_block_pack_scales(w13s), moe.moe_fp8_block_pack_scales(w2s)
     if args.weights == "tiled":
         # load-time conversion into the kernels' tile-packed layout (untimed, like the quantisation)
         w13q = moe.moe_fp8_block_pack_weights(w13q)
@@ -372,7 +382,10 @@ def run_ours(args, wl):
     # its own tokens touch
     touched_streamed = touched_per_pass(ids, 8) if args.weights == "nvfp4" else touched
     P = wl.P
-    decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode)
+    packed_scales = args.scale_fmt == "ue8m0_packed"
+    if packed_scales and (nvfp4 or args.decode == "on"):
+        raise SystemExit("--scale-fmt ue8m0_packed runs on the tile GEMMs: not with NVFP4 weights or --decode on")
+    decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode) and not packed_scales
     # kernels per step (the decode path's one GEMM kernel in place of two)
     launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
     if decode != moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk):
@@ -501,7 +514,7 @@ def run_ours(args, wl):
     pk = peaks()
     tokens_s = whole_job_rate(world, wl.T, ms)
     flops = wl.flops()
-    per_expert_w13, per_expert = expert_weight_bytes(wl, nvfp4)
+    per_expert_w13, per_expert = expert_weight_bytes(wl, nvfp4, packed_scales)
     layer_bytes = touched * per_expert + wl.T * H * 2 * 2 + wl.T * E * 4
     # algorithmic bytes of one w13 GEMM launch: touched experts' w13 + scales, the sorted activation
     # rows and scales read once, the requantised intermediate and its scales written once
@@ -527,10 +540,12 @@ def run_ours(args, wl):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = ("decode_mlp_kernel<nvfp4> (both GEMMs, decode path, NVFP4 weights)" if nvfp4
                       else "decode_mlp_kernel (both GEMMs, decode path)" if decode
+                      else "grouped_gemm_bs_kernel<silu_mul_quant> (w13 GEMM, block-scaled MMA)" if packed_scales
                       else "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)")
     roof["algorithmic_bytes_per_launch"] = gemm_bytes
     roof["ms_per_launch"] = g_ms
-    roof["traffic"] = profiled_traffic(wl, "nvfp4" if nvfp4 else "decode" if decode else "tile")
+    roof["traffic"] = None if packed_scales else profiled_traffic(wl, "nvfp4" if nvfp4 else "decode" if decode
+                                                                  else "tile")
 
     line = {"metric": "block-FP8 fused-MoE tokens/s", "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -588,10 +603,13 @@ def run_masked(args, wl):
     w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
     w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
     w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+    wfmt = "ue8m0" if args.scale_fmt == "ue8m0_packed" else args.scale_fmt
     for e0 in range(0, E, 8):
         ex = range(e0, min(E, e0 + 8))
-        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), args.scale_fmt)
-        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), args.scale_fmt)
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), wfmt)
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), wfmt)
+    if args.scale_fmt == "ue8m0_packed":
+        w13s, w2s = moe.moe_fp8_block_pack_scales(w13s), moe.moe_fp8_block_pack_scales(w2s)
     w13p, w2p = (moe.moe_fp8_block_pack_weights(w13q), moe.moe_fp8_block_pack_weights(w2q)) \
         if args.weights == "tiled" else (w13q, w2q)
     out = torch.empty(E, M, H, dtype=torch.bfloat16, device=dev)

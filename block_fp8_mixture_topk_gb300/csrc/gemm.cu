@@ -156,6 +156,29 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, i
     return t;
 }
 
+// Both 128-row weight bands of a work item for K block kb in one 32 KB TMA box (rows bcol0 .. +127
+// land first, rows bcol1 .. +127 16 KB later, as two 128-row boxes would put them): an SM streams
+// many more bytes per second with fewer, larger boxes (a probe with every SM streaming L2-resident
+// tiles: 79 GB/s per SM with three 16 KB boxes per stage, 125 GB/s with two 32 KB boxes).  The box
+// steps from one band to the other with its outermost dimension (map: make_pair_map).
+//   silu:   gate band n and up band N/256 + n of expert e
+//   others: bands 2n and 2n + 1
+template <int EPI>
+__device__ __forceinline__ void load_b_pair(uint32_t dst, const CUtensorMap* m, const GemmArgs& a, const Tile& t,
+                                            int kb, uint32_t bar) {
+    if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
+        if (a.b_tiled)
+            tma_load_5d(dst, m, 0, 0, kb, t.n, 2 * t.e, bar);
+        else
+            tma_load_4d(dst, m, kb * BK, 0, t.n, 2 * t.e, bar);
+    } else {
+        if (a.b_tiled)
+            tma_load_4d(dst, m, 0, 0, kb, t.e * (a.N / 128) + 2 * t.n, bar);
+        else
+            tma_load_2d(dst, m, kb * BK, t.e * a.N + t.n * 256, bar);
+    }
+}
+
 // This CTA's first ITEMS work items (w = blockIdx.x + k * gridDim.x): tile, column block, expert
 // and first row looked up once (all threads, one round of global loads), so that no role waits on
 // a global load when it starts an item.  Only the w13 GEMM reorders (item_of); the w2 GEMM keeps the
@@ -322,7 +345,7 @@ __device__ __forceinline__ bool finish_item(const GemmArgs& a, Ctl* ctl, const T
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs a) {
+                        const __grid_constant__ CUtensorMap tmB2, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -355,6 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmB2);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
@@ -393,15 +417,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // weight tile coordinates: [E*N, K] rows in the pages' layout (x advances along
                 // K), or one 128-row block per 128 map rows in the tile-packed layout (each
                 // 128x128 block a contiguous 16 KB, consecutive K blocks adjacent: y advances)
-                int32_t by0, by1, bdx, bdy;
+                int32_t by0, bdx, bdy;
                 if (a.b_tiled) {
                     by0 = ((t.e * (a.N / 128) + t.bcol0 / 128) * KB) * 128;
-                    by1 = ((t.e * (a.N / 128) + t.bcol1 / 128) * KB) * 128;
                     bdx = 0;
                     bdy = 128;
                 } else {
                     by0 = t.e * a.N + t.bcol0;
-                    by1 = t.e * a.N + t.bcol1;
                     bdx = BK;
                     bdy = 0;
                 }
@@ -416,9 +438,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t fb = smem_addr(&ctl->full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
-                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
                     if (t.has1)
-                        tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * bdx, by1 + kb * bdy, fb);
+                        load_b_pair<EPI>(smem_addr(smB + stage * B_TILE), &tmB2, a, t, kb, fb);
+                    else
+                        tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -644,7 +667,7 @@ static_assert(SMEM_BYTES_BS <= 232448, "shared memory per CTA exceeds the sm_103
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                           const GemmArgs a) {
+                           const __grid_constant__ CUtensorMap tmB2, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -673,6 +696,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmB2);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
@@ -706,15 +730,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
                 }
-                int32_t by0, by1, bdx, bdy;
+                int32_t by0, bdx, bdy;
                 if (a.b_tiled) {
                     by0 = ((t.e * (a.N / 128) + t.bcol0 / 128) * KB) * 128;
-                    by1 = ((t.e * (a.N / 128) + t.bcol1 / 128) * KB) * 128;
                     bdx = 0;
                     bdy = 128;
                 } else {
                     by0 = t.e * a.N + t.bcol0;
-                    by1 = t.e * a.N + t.bcol1;
                     bdx = BK;
                     bdy = 0;
                 }
@@ -732,9 +754,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const bool load_sf = (kb & 3) == 0;
                     mbar_arrive_expect_tx(fb, bytes + (load_sf ? sf_bytes : 0u));
                     tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
-                    tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
                     if (t.has1)
-                        tma_load_2d(smem_addr(smB + stage * B_TILE + B_HALF), &tmB, kb * bdx, by1 + kb * bdy, fb);
+                        load_b_pair<EPI>(smem_addr(smB + stage * B_TILE), &tmB2, a, t, kb, fb);
+                    else
+                        tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
                     if (load_sf) {
                         const uint32_t dst = smem_addr(smSF + stage * SF_STAGE);
                         const int64_t q = (kb >> 2) * kSfTileBytes;
@@ -904,6 +927,44 @@ cudaError_t make_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t
 }  // namespace
 
 cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
+                             const uint64_t* strides, const uint32_t* box, bool swizzle128);
+
+namespace {
+
+// Map of the 32 KB boxes of load_b_pair: both 128-row bands of an item for one K block.
+cudaError_t make_pair_map(CUtensorMap* map, const GemmArgs& g) {
+    const uint64_t KB = g.K / 128, E = g.E, N = g.N, K = g.K;
+    if (g.epi == MOE_EPI_SILU_MUL_QUANT) {
+        const uint64_t NBh = N / 256;   // bands per half (gate / up)
+        if (g.b_tiled) {
+            // [E][2][NBh][KB][128 rows][128 B]: the outermost index is 2e + half
+            const uint64_t dims[5] = {128, 128, KB, NBh, 2 * E};
+            const uint64_t strides[4] = {128, 16384, KB * 16384, NBh * KB * 16384};
+            const uint32_t box[5] = {128, 128, 1, 1, 2};
+            return encode_u8_map_nd(map, g.B, 5, dims, strides, box, true);
+        }
+        // rows e*2I + half*I + j*128 + r of [E*N, K]
+        const uint64_t dims[4] = {K, 128, NBh, 2 * E};
+        const uint64_t strides[3] = {K, 128 * K, (N / 2) * K};
+        const uint32_t box[4] = {128, 128, 1, 2};
+        return encode_u8_map_nd(map, g.B, 4, dims, strides, box, true);
+    }
+    if (g.b_tiled) {
+        // [E*N/128 bands][KB][128 rows][128 B]
+        const uint64_t dims[4] = {128, 128, KB, E * (N / 128)};
+        const uint64_t strides[3] = {128, 16384, KB * 16384};
+        const uint32_t box[4] = {128, 128, 1, 2};
+        return encode_u8_map_nd(map, g.B, 4, dims, strides, box, true);
+    }
+    const uint64_t dims[2] = {K, E * N};
+    const uint64_t strides[1] = {K};
+    const uint32_t box[2] = {128, 256};
+    return encode_u8_map_nd(map, g.B, 2, dims, strides, box, true);
+}
+
+}  // namespace
+
+cudaError_t encode_u8_map_nd(CUtensorMap* map, const uint8_t* ptr, int rank, const uint64_t* dims,
                              const uint64_t* strides, const uint32_t* box, bool swizzle128) {
     cudaError_t err = get_encoder();
     if (err != cudaSuccess) return err;
@@ -982,18 +1043,22 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     else
         err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
     if (err != cudaSuccess) return err;
+    // (with N = 128 no item has two bands: the pair map is never read)
+    CUtensorMap tmB2 = tmB;
+    if (args.N >= 256) err = make_pair_map(&tmB2, args);
+    if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(bound < num_sms ? bound : num_sms);
     if (args.sf_packed) {
         switch (args.epi) {
             case MOE_EPI_STORE_F32:
                 return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_STORE_F32>, dim3(grid), dim3(NUM_THREADS),
-                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+                                  SMEM_BYTES_BS, stream, tmA, tmB, tmB2, args);
             case MOE_EPI_SILU_MUL_QUANT:
                 return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_SILU_MUL_QUANT>, dim3(grid), dim3(NUM_THREADS),
-                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+                                  SMEM_BYTES_BS, stream, tmA, tmB, tmB2, args);
             case MOE_EPI_WEIGHTED_PAIRS_BF16:
                 return launch_pdl(grouped_gemm_bs_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>, dim3(grid), dim3(NUM_THREADS),
-                                  SMEM_BYTES_BS, stream, tmA, tmB, args);
+                                  SMEM_BYTES_BS, stream, tmA, tmB, tmB2, args);
             default:
                 return cudaErrorInvalidValue;
         }
@@ -1001,23 +1066,23 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     switch (args.epi) {
         case MOE_EPI_STORE_F32:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_STORE_F32>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
-                             tmB, args);
+                             tmB, tmB2, args);
             break;
         case MOE_EPI_SILU_MUL_QUANT:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_SILU_MUL_QUANT>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
-                             tmB, args);
+                             tmB, tmB2, args);
             break;
         case MOE_EPI_WEIGHTED_SCATTER:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_SCATTER>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
-                             tmB, args);
+                             tmB, tmB2, args);
             break;
         case MOE_EPI_WEIGHTED_ROWS:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_ROWS>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
-                             tmB, args);
+                             tmB, tmB2, args);
             break;
         case MOE_EPI_WEIGHTED_PAIRS_BF16:
             err = launch_pdl(grouped_gemm_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA,
-                             tmB, args);
+                             tmB, tmB2, args);
             break;
         default:
             return cudaErrorInvalidValue;
