@@ -58,6 +58,9 @@ def _load():
             lib.orc_bf16_from_f64.restype = ctypes.c_uint16
             lib.orc_quant_1x128_f32.argtypes = [P, L, L, P, P, I]
             lib.orc_quant_1x128_bf16.argtypes = [P, L, L, P, P, I]
+            lib.orc_quant_1xg_f32.argtypes = [P, L, L, I, P, P, I]
+            lib.orc_quant_1xg_bf16.argtypes = [P, L, L, I, P, P, I]
+            lib.orc_experts_mxfp8.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, I, I, P, P, P, P]
             lib.orc_quant_128x128_bf16.argtypes = [P, L, L, L, P, P, I]
             lib.orc_route.argtypes = [P, P, L, I, I, I, I, I, I, ctypes.c_double, P, P]
             lib.orc_route.restype = I
@@ -154,6 +157,41 @@ def quant_1x128_f32(x: np.ndarray, scale_fmt: int = SCALE_F32):
     s = np.empty((R, C // 128), dtype=np.float32)
     _load().orc_quant_1x128_f32(_ptr(x), R, C, _ptr(q), _ptr(s), scale_fmt)
     return q, s
+
+
+def quant_1x32_bf16(x_bits: np.ndarray):
+    """MXFP8 activation quantisation ("MXFP8 (block [1, 32])", page "vllm.model_executor.layers.
+    fused_moe.oracle.fp8", make_fp8_moe_quant_config): groups of 32 along each bf16 row, scale
+    max(amax, 1e-8)/448 rounded up to a power of two (UE8M0).  Returns (codes [R, C] u8,
+    scales [R, C/32] f32, each a power of two)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((R, C // 32), dtype=np.float32)
+    _load().orc_quant_1xg_bf16(_ptr(x), R, C, 32, _ptr(q), _ptr(s), SCALE_UE8M0)
+    return q, s
+
+
+def quant_1x32_f32(x: np.ndarray):
+    """The same 1x32 UE8M0 quantisation of fp32 rows."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, C = x.shape
+    assert C % 32 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((R, C // 32), dtype=np.float32)
+    _load().orc_quant_1xg_f32(_ptr(x), R, C, 32, _ptr(q), _ptr(s), SCALE_UE8M0)
+    return q, s
+
+
+def quant_mxfp8_weight_bf16(w_bits: np.ndarray):
+    """MXFP8 expert weights [E, N, K] (bf16 bits): 1x32 blocks along K with UE8M0 scales ("e8m0
+    group-32 scales", _humming_fp8_weight_schema).  Returns (codes [E, N, K], scales [E, N, K/32]
+    f32 powers of two)."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    E, N, K = w.shape
+    q, s = quant_1x32_bf16(w.reshape(E * N, K))
+    return q.reshape(E, N, K), s.reshape(E, N, K // 32)
 
 
 def e2m1_values() -> np.ndarray:
@@ -288,14 +326,40 @@ def moe_forward_nvfp4(hidden_bits, logits, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs
                          topk_group, routed_scaling, tokens, want_c1, scale_fmt)
 
 
+def moe_forward_mxfp8(hidden_bits, logits, w13, w13_scale, w2, w2_scale, topk, renormalize=True,
+                      scoring=SOFTMAX, bias=None, n_group=1, topk_group=1, routed_scaling=1.0,
+                      tokens=None, want_c1=False):
+    """The whole layer in MXFP8 ("MXFP8 (block [1, 32])", page "vllm.model_executor.layers.
+    fused_moe.oracle.fp8", make_fp8_moe_quant_config): activations and the requantised
+    intermediate in 1x32 groups with UE8M0 scales, weights w13 [E,2I,H] / w2 [E,H,I] e4m3 with
+    w13_scale [E,2I,H/32] / w2_scale [E,H,I/32] (fp32 powers of two).  Same routing, sort, SiLU
+    and combine as ``moe_forward``; a1s / a2s in the result are [.., H/32] / [.., I/32]."""
+    E, N1, H2 = w13.shape
+    assert N1 % 256 == 0
+    I = N1 // 2
+    assert w2.shape == (E, H2, I) and w13_scale.shape == (E, N1, H2 // 32) and w2_scale.shape == (E, H2, I // 32)
+    w13c = np.ascontiguousarray(w13, dtype=np.uint8)
+    w2c = np.ascontiguousarray(w2, dtype=np.uint8)
+    w13s = np.ascontiguousarray(w13_scale, dtype=np.float32)
+    w2s = np.ascontiguousarray(w2_scale, dtype=np.float32)
+
+    def experts(a1q, a1s, offsets, sorted_, need, T, H, topk_, a2q, a2s, c1, c2):
+        _load().orc_experts_mxfp8(_ptr(a1q), _ptr(a1s), _ptr(w13c), _ptr(w13s), _ptr(w2c), _ptr(w2s),
+                                  _ptr(offsets), _ptr(sorted_), _ptr(need), T, H, I, E, topk_,
+                                  _ptr(a2q), _ptr(a2s), _ptr(c1), _ptr(c2))
+
+    return _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring, bias, n_group,
+                         topk_group, routed_scaling, tokens, want_c1, SCALE_UE8M0, group=32)
+
+
 def _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring, bias, n_group, topk_group,
-                  routed_scaling, tokens, want_c1, scale_fmt):
+                  routed_scaling, tokens, want_c1, scale_fmt, group=128):
     hidden_bits = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
     T, H = hidden_bits.shape
     N1 = 2 * I
     ids, wts = route(logits, topk, renormalize, scoring, bias, n_group, topk_group, routed_scaling)
     offsets, sorted_, pos = permute(ids, E)
-    a1q, a1s = quant_1x128_bf16(hidden_bits, scale_fmt)
+    a1q, a1s = quant_1x32_bf16(hidden_bits) if group == 32 else quant_1x128_bf16(hidden_bits, scale_fmt)
     P = T * topk
     need = np.zeros(T, dtype=np.uint8)
     if tokens is None:
@@ -316,7 +380,7 @@ def _routed_layer(experts, hidden_bits, logits, E, I, topk, renormalize, scoring
         r_pos[r_sorted] = np.arange(rows.size, dtype=np.int32)
     R = max(int(rows.size), 1)
     a2q = np.zeros((R, I), dtype=np.uint8)
-    a2s = np.zeros((R, I // 128), dtype=np.float32)
+    a2s = np.zeros((R, I // group), dtype=np.float32)
     c1 = np.full((R, N1), np.nan) if want_c1 else None
     c2 = np.full((R, H), np.nan)
     experts(a1q, a1s, r_offsets, r_sorted, need, T, H, topk, a2q, a2s, c1, c2)

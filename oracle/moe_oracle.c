@@ -23,7 +23,9 @@
  *  - ties in every top-k resolve to the lower index;
  *  - w13 rows [0, I) are the gate projection, rows [I, 2I) the up projection;
  *  - the intermediate SiLU(gate)*up is requantised from fp32 values;
- *  - NVFP4 block step: block scale = e4m3(max|x| / 6), code = e2m1(x / block scale).
+ *  - NVFP4 block step: block scale = e4m3(max|x| / 6), code = e2m1(x / block scale);
+ *  - MXFP8 (block [1, 32], UE8M0 scales): the same group rule on groups of 32 along the
+ *    contiguous dimension, each scale rounded up to a power of two.
  *
  * Parity pins: every function here is checked by tests against closed forms,
  * exhaustive enumeration, brute force on tiny inputs or an independent
@@ -148,43 +150,52 @@ static float group_scale(float amax, int fmt) {
     return fmt == 1 ? ceil_pow2(t) : t;
 }
 
-/* x: fp32 [rows, cols] (cols % 128 == 0) -> q [rows, cols], s [rows, cols/128] */
-void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
-    long G = cols / 128;
+/* x: fp32 [rows, cols] (cols % gs == 0) -> q [rows, cols], s [rows, cols/gs]: groups of gs
+ * values along a row (gs = 128: the layer's activation groups; gs = 32: MXFP8's [1, 32] blocks) */
+void orc_quant_1xg_f32(const float* x, long rows, long cols, int gs, uint8_t* q, float* s, int fmt) {
+    long G = cols / gs;
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
         for (long g = 0; g < G; ++g) {
-            const float* xg = x + r * cols + g * 128;
+            const float* xg = x + r * cols + g * gs;
             float amax = 0.0f;
-            for (int i = 0; i < 128; ++i) {
+            for (int i = 0; i < gs; ++i) {
                 float a = fabsf(xg[i]);
                 if (a > amax) amax = a;
             }
             float sc = group_scale(amax, fmt);
             s[r * G + g] = sc;
-            for (int i = 0; i < 128; ++i) q[r * cols + g * 128 + i] = orc_e4m3_encode(xg[i] / sc);
+            for (int i = 0; i < gs; ++i) q[r * cols + g * gs + i] = orc_e4m3_encode(xg[i] / sc);
         }
     }
 }
 
-/* bf16 input version of the 1x128 activation quantiser */
-void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
-    long G = cols / 128;
+/* bf16 input version */
+void orc_quant_1xg_bf16(const uint16_t* x, long rows, long cols, int gs, uint8_t* q, float* s, int fmt) {
+    long G = cols / gs;
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
         float row[128];
         for (long g = 0; g < G; ++g) {
             float amax = 0.0f;
-            for (int i = 0; i < 128; ++i) {
-                row[i] = bf16_to_f32(x[r * cols + g * 128 + i]);
+            for (int i = 0; i < gs; ++i) {
+                row[i] = bf16_to_f32(x[r * cols + g * gs + i]);
                 float a = fabsf(row[i]);
                 if (a > amax) amax = a;
             }
             float sc = group_scale(amax, fmt);
             s[r * G + g] = sc;
-            for (int i = 0; i < 128; ++i) q[r * cols + g * 128 + i] = orc_e4m3_encode(row[i] / sc);
+            for (int i = 0; i < gs; ++i) q[r * cols + g * gs + i] = orc_e4m3_encode(row[i] / sc);
         }
     }
+}
+
+void orc_quant_1x128_f32(const float* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
+    orc_quant_1xg_f32(x, rows, cols, 128, q, s, fmt);
+}
+
+void orc_quant_1x128_bf16(const uint16_t* x, long rows, long cols, uint8_t* q, float* s, int fmt) {
+    orc_quant_1xg_bf16(x, rows, cols, 128, q, s, fmt);
 }
 
 /* 128x128 block weight quantisation of stacked expert weights [E, N, K]
@@ -459,9 +470,9 @@ typedef void (*dequant_fn)(const void* ctx, int e, int which, long N1, long H, l
 static void experts_core(const uint8_t* a1q, const float* a1s, dequant_fn dq, const void* ctx,
                          const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
                          long H, long I, int E, int topk, uint8_t* a2q, float* a2s, double* c1, double* c2,
-                         int fmt) {
+                         int fmt, int ga) {
     e4m3_build();
-    long N1 = 2 * I, HB = H / 128, IB = I / 128;
+    long N1 = 2 * I, HB = H / ga, IB = I / ga;   /* activation groups of ga values (128, or 32 for MXFP8) */
     double* wdq = (double*)malloc(sizeof(double) * (size_t)(N1 * H > H * I ? N1 * H : H * I));
     for (int e = 0; e < E; ++e) {
         long r0 = offsets[e], r1 = offsets[e + 1];
@@ -476,7 +487,7 @@ static void experts_core(const uint8_t* a1q, const float* a1s, dequant_fn dq, co
             double* a = (double*)malloc(sizeof(double) * (size_t)H);
             double* g = (double*)malloc(sizeof(double) * (size_t)N1);
             float* h1 = (float*)malloc(sizeof(float) * (size_t)I);
-            for (long h = 0; h < H; ++h) a[h] = e4m3_val[a1q[t * H + h]] * (double)a1s[t * HB + h / 128];
+            for (long h = 0; h < H; ++h) a[h] = e4m3_val[a1q[t * H + h]] * (double)a1s[t * HB + h / ga];
             for (long n = 0; n < N1; ++n) {
                 double acc = 0.0;
                 const double* wr = wdq + n * H;
@@ -488,7 +499,7 @@ static void experts_core(const uint8_t* a1q, const float* a1s, dequant_fn dq, co
                 double gate = g[i], up = g[I + i];
                 h1[i] = (float)(gate / (1.0 + exp(-gate)) * up);
             }
-            orc_quant_1x128_f32(h1, 1, I, a2q + r * I, a2s + r * IB, fmt);
+            orc_quant_1xg_f32(h1, 1, I, ga, a2q + r * I, a2s + r * IB, fmt);
             free(a); free(g); free(h1);
         }
         dq(ctx, e, 1, N1, H, I, wdq);
@@ -497,7 +508,7 @@ static void experts_core(const uint8_t* a1q, const float* a1s, dequant_fn dq, co
             long p = sorted[r], t = p / topk;
             if (!need[t]) continue;
             double* a2 = (double*)malloc(sizeof(double) * (size_t)I);
-            for (long i = 0; i < I; ++i) a2[i] = e4m3_val[a2q[r * I + i]] * (double)a2s[r * IB + i / 128];
+            for (long i = 0; i < I; ++i) a2[i] = e4m3_val[a2q[r * I + i]] * (double)a2s[r * IB + i / ga];
             for (long n = 0; n < H; ++n) {
                 double acc = 0.0;
                 const double* wr = wdq + n * I;
@@ -563,7 +574,7 @@ void orc_experts(const uint8_t* a1q, const float* a1s,
                  uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
     (void)T;
     struct fp8_weights W = {w13, w2, w13s, w2s};
-    experts_core(a1q, a1s, dequant_fp8, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt);
+    experts_core(a1q, a1s, dequant_fp8, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt, 128);
 }
 
 /* The same expert MLP with NVFP4 weights: codes [E, N, K/2], block scales [E, N, K/16] (e4m3),
@@ -576,7 +587,40 @@ void orc_experts_nvfp4(const uint8_t* a1q, const float* a1s,
                        uint8_t* a2q, float* a2s, double* c1, double* c2, int fmt) {
     (void)T;
     struct nvfp4_weights W = {w13, w2, w13sf, w2sf, w13gs, w2gs};
-    experts_core(a1q, a1s, dequant_nvfp4, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt);
+    experts_core(a1q, a1s, dequant_nvfp4, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, fmt, 128);
+}
+
+/* MXFP8 weights ("MXFP8 (block [1, 32])", [FP8O] make_fp8_moe_quant_config; "e8m0 group-32
+ * scales", [FP8O] _humming_fp8_weight_schema): code value times the UE8M0 scale of its row's
+ * 32-wide K group, w13s [E, 2I, H/32] and w2s [E, H, I/32] (the scales as fp32 powers of two) */
+struct mxfp8_weights {
+    const uint8_t *w13, *w2;
+    const float *w13s, *w2s;
+};
+
+static void dequant_mxfp8(const void* ctx, int e, int which, long N1, long H, long I, double* wdq) {
+    const struct mxfp8_weights* W = (const struct mxfp8_weights*)ctx;
+    long N = which == 0 ? N1 : H, K = which == 0 ? H : I;
+    const uint8_t* q = which == 0 ? W->w13 : W->w2;
+    const float* sc = which == 0 ? W->w13s : W->w2s;
+#pragma omp parallel for schedule(static)
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < K; ++k) {
+            long i = ((long)e * N + n) * K + k;
+            wdq[n * K + k] = e4m3_val[q[i]] * (double)sc[((long)e * N + n) * (K / 32) + k / 32];
+        }
+}
+
+/* The expert MLP in MXFP8: activations and the requantised intermediate in 1x32 groups with UE8M0
+ * scales (a1s [T, H/32], a2s [P, I/32]), MXFP8 weights as above. */
+void orc_experts_mxfp8(const uint8_t* a1q, const float* a1s,
+                       const uint8_t* w13, const float* w13s, const uint8_t* w2, const float* w2s,
+                       const int32_t* offsets, const int32_t* sorted, const unsigned char* need,
+                       long T, long H, long I, int E, int topk,
+                       uint8_t* a2q, float* a2s, double* c1, double* c2) {
+    (void)T;
+    struct mxfp8_weights W = {w13, w2, w13s, w2s};
+    experts_core(a1q, a1s, dequant_mxfp8, &W, offsets, sorted, need, H, I, E, topk, a2q, a2s, c1, c2, 1, 32);
 }
 
 /* Weighted unpermute-sum ("gathers results", [QMO] Modular Kernel Architecture;
