@@ -27,6 +27,9 @@ from .ops import (  # noqa: F401
     moe_get_device_status,
     moe_max_padded_rows,
     moe_max_tiles,
+    moe_mxfp8_pack_scales,
+    moe_mxfp8_packed_scale_bytes,
+    moe_mxfp8_quant_weight,
     moe_nvfp4_forward,
     moe_nvfp4_pack_weights,
     moe_nvfp4_packed_bytes,

@@ -81,10 +81,12 @@ int64_t max_rows(int64_t P, int64_t E, int64_t bm) {
     return P + busy * (bm - 1);
 }
 
-// bytes of the packed UE8M0 scale tiles of a [rows, K] operand (common.cuh, packed_sf_offset)
+// bytes of the packed UE8M0 scale tiles of a [rows, K] operand (common.cuh, packed_sf_offset):
+// one tile per 128 rows and 4 K blocks, or (MXFP8) per 128 rows and K block
 int64_t packed_sf_bytes(int64_t rows, int K) {
     return (rows + 127) / 128 * ((K / 128 + 3) / 4) * kSfTileBytes;
 }
+int64_t mx_sf_bytes(int64_t rows, int K) { return (rows + 127) / 128 * (K / 128) * kSfTileBytes; }
 
 struct ForwardLayout {
     size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, a1sf, a2sf, y, dh,
@@ -142,9 +144,9 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
-    // packed UE8M0 scale tiles of A1 and A2 (MOE_SCALE_UE8M0_PACKED)
-    L.a1sf = take(packed_sf_bytes(L.rows, H));
-    L.a2sf = take(packed_sf_bytes(L.rows, I));
+    // packed scale tiles of A1 and A2 (MOE_SCALE_UE8M0_PACKED, MOE_SCALE_MXFP8: the larger)
+    L.a1sf = take(mx_sf_bytes(L.rows, H));
+    L.a2sf = take(mx_sf_bytes(L.rows, I));
     L.y = take(static_cast<size_t>(P) * H * 2);
     // decode path: h = silu(gate) * up by pair [P, I] fp32, the counters and the tile records
     L.dcnt_n = decode_possible(T, H, I, topk) ? decode_counters(static_cast<int>(L.tiles), I) : 0;
@@ -182,15 +184,17 @@ MaskedLayout masked_layout(int E, int M, int H, int I) {
     L.a1s = take(static_cast<size_t>(H / 128) * L.rows * 4);
     L.a2 = take(L.rows * I);
     L.a2s = take(static_cast<size_t>(I / 128) * L.rows * 4);
-    L.a1sf = take(packed_sf_bytes(L.rows, H));
-    L.a2sf = take(packed_sf_bytes(L.rows, I));
+    L.a1sf = take(mx_sf_bytes(L.rows, H));
+    L.a2sf = take(mx_sf_bytes(L.rows, I));
     L.total = off;
     return L;
 }
 
 inline bool known_scale_fmt(int f) {
-    return f == MOE_SCALE_F32 || f == MOE_SCALE_UE8M0 || f == MOE_SCALE_UE8M0_PACKED;
+    return f == MOE_SCALE_F32 || f == MOE_SCALE_UE8M0 || f == MOE_SCALE_UE8M0_PACKED || f == MOE_SCALE_MXFP8;
 }
+// formats whose GEMMs run on the block-scaled MMA: 1 = packed UE8M0, 2 = MXFP8, 0 = neither
+inline int sf_mode(int f) { return f == MOE_SCALE_UE8M0_PACKED ? 1 : f == MOE_SCALE_MXFP8 ? 2 : 0; }
 
 }  // namespace
 
@@ -297,10 +301,14 @@ int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q
     if (rows == 0 || cols == 0) return MOE_OK;
     if (!x || !q || !s) return MOE_ERR_INVALID_ARG;
     const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
-    if (!aligned(x, 16) || !aligned(q, 8) || (!packed && !aligned(s, 4))) return MOE_ERR_INVALID_ARG;
+    const bool mx = scale_fmt == MOE_SCALE_MXFP8;
+    if (!aligned(x, 16) || !aligned(q, 8) || (!packed && !mx && !aligned(s, 4))) return MOE_ERR_INVALID_ARG;
     DeviceState* st = nullptr;
     int rc = device_state(&st);
     if (rc != MOE_OK) return rc;
+    if (mx)
+        return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, nullptr, 0, 0, nullptr, 1, MOE_SCALE_MXFP8,
+                                          static_cast<cudaStream_t>(stream), nullptr, reinterpret_cast<uint8_t*>(s)));
     if (packed)
         return cuda_rc(launch_group_quant(x, rows, cols, ld, q, cols, nullptr, 0, 0, nullptr, 1, MOE_SCALE_UE8M0,
                                           static_cast<cudaStream_t>(stream), reinterpret_cast<uint8_t*>(s)));
@@ -357,6 +365,35 @@ int moe_fp8_block_pack_scales(const float* s, int E, int N, int K, uint8_t* out,
     return cuda_rc(launch_pack_scales(s, E, N, K, out, st->status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_mxfp8_packed_scale_bytes(int64_t rows, int K) {
+    if (rows < 0 || K < 0 || K % 128 != 0) return 0;
+    return static_cast<size_t>(mx_sf_bytes(rows, K));
+}
+
+int moe_mxfp8_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* s, void* stream) {
+    if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (E == 0 || N == 0 || K == 0) return MOE_OK;
+    if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    const int64_t rows = static_cast<int64_t>(E) * N;
+    return cuda_rc(launch_group_quant(w, rows, K, K, q, K, nullptr, 0, 0, nullptr, 1, MOE_SCALE_MXFP8,
+                                      static_cast<cudaStream_t>(stream), nullptr, s));
+}
+
+int moe_mxfp8_pack_scales(const uint8_t* s, int64_t rows, int K, uint8_t* out, void* stream) {
+    if (rows < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if (K % 128 != 0 || rows % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || K == 0) return MOE_OK;
+    if (!s || !out || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return cuda_rc(launch_pack_scale_bytes(s, rows, K / 32, out, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_nvfp4_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* block_scale,
                            float* global_scale, void* stream) {
     if (E < 0 || N < 0 || K < 0) return MOE_ERR_INVALID_ARG;
@@ -411,7 +448,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     if (!aligned(A, 16) || !aligned(B, 16)) return MOE_ERR_INVALID_ARG;
     if (ep->b_layout != MOE_WEIGHTS_NK && ep->b_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
     if (!known_scale_fmt(ep->scale_fmt)) return MOE_ERR_INVALID_ARG;
-    const bool packed = ep->scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    const bool packed = sf_mode(ep->scale_fmt) != 0;
     if (packed) {
         if (ep->kind != MOE_EPI_STORE_F32 && ep->kind != MOE_EPI_SILU_MUL_QUANT &&
             ep->kind != MOE_EPI_WEIGHTED_PAIRS_BF16)
@@ -474,7 +511,7 @@ int fp8_block_grouped_gemm(const uint8_t* A, const float* a_scale, int64_t a_sca
     g.b_tiled = ep->b_layout == MOE_WEIGHTS_TILED;
     g.scale_fmt = packed ? MOE_SCALE_UE8M0 : ep->scale_fmt;
     if (packed) {
-        g.sf_packed = 1;
+        g.sf_packed = sf_mode(ep->scale_fmt);
         g.a_sf = reinterpret_cast<const uint8_t*>(a_scale);
         g.b_sf = reinterpret_cast<const uint8_t*>(b_scale);
         g.out_sf = reinterpret_cast<uint8_t*>(ep->out_scale);
@@ -560,7 +597,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         return MOE_ERR_INVALID_ARG;
     const bool fp4 = weight_layout == MOE_WEIGHTS_NVFP4;
     // packed UE8M0 scales: both GEMMs on the block-scaled MMA (tile kernels only)
-    const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    const int sfm = sf_mode(scale_fmt);
+    const bool packed = sfm != 0;
     if (packed && (fp4 || decode_mode == MOE_DECODE_ON)) return MOE_ERR_INVALID_ARG;
     if (packed && (!aligned(w13_scale, 16) || !aligned(w2_scale, 16))) return MOE_ERR_INVALID_ARG;
     if (fp4 && T > kDecodeCols) {
@@ -736,7 +774,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.os_row_stride = 1;
         g.os_kb_stride = L.rows;
         if (packed) {
-            g.sf_packed = 1;
+            g.sf_packed = sfm;
             g.a_sf = a1sf;
             g.b_sf = reinterpret_cast<const uint8_t*>(w13_scale);
             g.out_sf = a2sf;
@@ -770,7 +808,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.topk = topk;
         g.num_pairs = P;
         if (packed) {
-            g.sf_packed = 1;
+            g.sf_packed = sfm;
             g.a_sf = a2sf;
             g.b_sf = reinterpret_cast<const uint8_t*>(w2_scale);
         }
@@ -798,7 +836,8 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
     const int scale_fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
     if (weight_layout != MOE_WEIGHTS_NK && weight_layout != MOE_WEIGHTS_TILED) return MOE_ERR_INVALID_ARG;
     if (!known_scale_fmt(scale_fmt)) return MOE_ERR_INVALID_ARG;
-    const bool packed = scale_fmt == MOE_SCALE_UE8M0_PACKED;
+    const int sfm = sf_mode(scale_fmt);
+    const bool packed = sfm != 0;
     if (packed && (!aligned(w13_scale, 16) || !aligned(w2_scale, 16))) return MOE_ERR_INVALID_ARG;
     if (H % 128 != 0 || I % 128 != 0 || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (E == 0 || max_tokens == 0) return MOE_OK;
@@ -862,7 +901,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
         g.os_row_stride = 1;
         g.os_kb_stride = L.rows;
         if (packed) {
-            g.sf_packed = 1;
+            g.sf_packed = sfm;
             g.a_sf = a1sf;
             g.b_sf = reinterpret_cast<const uint8_t*>(w13_scale);
             g.out_sf = a2sf;
@@ -896,7 +935,7 @@ int moe_fp8_block_forward_masked(const uint16_t* hidden, const int32_t* counts, 
         g.topk = 1;
         g.num_pairs = EM;
         if (packed) {
-            g.sf_packed = 1;
+            g.sf_packed = sfm;
             g.a_sf = a2sf;
             g.b_sf = reinterpret_cast<const uint8_t*>(w2_scale);
         }

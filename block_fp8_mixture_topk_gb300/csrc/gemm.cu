@@ -214,7 +214,36 @@ __device__ __forceinline__ bool finish_item(const GemmArgs& a, Ctl* ctl, const T
                                             int g, int row, int64_t grow, bool active, uint32_t tile_iter,
                                             volatile int* abort_flag) {
     const int sp = warp & 3;
-    if (EPI == MOE_EPI_SILU_MUL_QUANT) {
+    if (EPI == MOE_EPI_SILU_MUL_QUANT && a.sf_packed == 2) {
+        // MXFP8: this thread's 64 values are two whole 1x32 groups of its row; no exchange
+        uint4* dst = reinterpret_cast<uint4*>(a.out_q + grow * (a.N / 2) + t.n * 128 + g * 64);
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = hg * 32; j < hg * 32 + 32; ++j) {
+                const float gate = acc[j];
+                const float h = __fdividef(gate * acc[64 + j], 1.0f + __expf(-gate));
+                acc[j] = h;
+                amax = fmaxf(amax, fabsf(h));
+            }
+            const float sc = group_scale_fmt(amax, MOE_SCALE_UE8M0);
+            const float rsc = __frcp_rn(sc);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t wv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float* h = acc + hg * 32 + c * 16 + j * 4;
+                    const uint32_t lo = e4m3x2(div_by_scale(h[0], sc, rsc), div_by_scale(h[1], sc, rsc));
+                    const uint32_t hi = e4m3x2(div_by_scale(h[2], sc, rsc), div_by_scale(h[3], sc, rsc));
+                    wv[j] = lo | (hi << 16);
+                }
+                dst[hg * 2 + c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+            a.out_sf[packed_sf_offset(grow, t.n * 4 + g * 2 + hg, a.N / 256)] = ue8m0_byte(sc);
+        }
+    } else if (EPI == MOE_EPI_SILU_MUL_QUANT) {
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
@@ -679,7 +708,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 256 : (a.N + 255) / 256;
     const int KB = a.K / BK;
-    const int KB4 = (KB + 3) / 4;   // scale-factor tiles per 128 rows of A or per 128 columns of B
+    // scale-factor tiles per 128 rows of A or per 128 columns of B: one per 4 K blocks (packed UE8M0),
+    // or one per K block (MXFP8: a word holds the K block's four 32-wide groups)
+    const bool mx = a.sf_packed == 2;
+    const int KB4 = mx ? KB : (KB + 3) / 4;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -751,7 +783,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     const uint32_t fb = smem_addr(&ctl->full[stage]);
-                    const bool load_sf = (kb & 3) == 0;
+                    const bool load_sf = mx || (kb & 3) == 0;
                     mbar_arrive_expect_tx(fb, bytes + (load_sf ? sf_bytes : 0u));
                     tma_load_2d(smem_addr(smA + stage * A_TILE), &tmA, kb * BK, static_cast<int32_t>(t.row0), fb);
                     if (t.has1)
@@ -760,7 +792,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(smem_addr(smB + stage * B_TILE), &tmB, kb * bdx, by0 + kb * bdy, fb);
                     if (load_sf) {
                         const uint32_t dst = smem_addr(smSF + stage * SF_STAGE);
-                        const int64_t q = (kb >> 2) * kSfTileBytes;
+                        const int64_t q = static_cast<int64_t>(mx ? kb : kb >> 2) * kSfTileBytes;
                         bulk_load(dst, sfa + q, kSfTileBytes, fb);
                         bulk_load(dst + kSfTileBytes, sfb0 + q, kSfTileBytes, fb);
                         if (t.has1) bulk_load(dst + 2 * kSfTileBytes, sfb1 + q, kSfTileBytes, fb);
@@ -803,7 +835,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    if ((kb & 3) == 0) {
+                    if (mx || (kb & 3) == 0) {
                         const uint32_t col = TMEM_SF + (sf_loads % SF_SLOTS) * 16;
                         const uint32_t src = smem_addr(smSF + stage * SF_STAGE);
                         sfa_t = tmem + col;
@@ -813,13 +845,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (t.has1) tmem_copy_sf_tile(sfb_t + 4, smem_desc_sf_tile(src + 2 * kSfTileBytes));
                         ++sf_loads;
                     }
-                    const uint32_t idesc = idesc_e4m3_ue8m0(BM, n, kb & 3);
                     const uint32_t a0 = smem_addr(smA + stage * A_TILE);
                     const uint32_t b0 = smem_addr(smB + stage * B_TILE);
 #pragma unroll
-                    for (int s = 0; s < BK / 32; ++s)
+                    for (int s = 0; s < BK / 32; ++s) {
+                        // the scale byte: the K block's (packed UE8M0) or the 32-group's (MXFP8)
+                        const uint32_t idesc = idesc_e4m3_ue8m0(BM, n, mx ? s : (kb & 3));
                         mma_e4m3_block_scaled(tmem, smem_desc_k128_sw128(a0 + s * 32), smem_desc_k128_sw128(b0 + s * 32),
                                               idesc, sfa_t, sfb_t, (kb | s) != 0 ? 1u : 0u);
+                    }
                     mma_commit(smem_addr(&ctl->empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;

@@ -83,9 +83,14 @@ cudaError_t launch_masked_map(const int32_t* counts, int E, int M, int Mp, int32
 // s may be null (no fp32 scales); sf != null: the scales (then rounded up to powers of two,
 // MOE_SCALE_UE8M0) also go out as UE8M0 bytes in packed scale-factor tiles (packed_sf_offset,
 // ceil(cols/512) tiles per 128 output rows).
+// scale_fmt MOE_SCALE_MXFP8: groups of 32 with UE8M0 scales (s then unused; s8: the scale bytes
+// [out rows, cols/32]; sf: packed tiles of the 32-group columns, cols/128 tiles per 128 rows).
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf = nullptr);
+                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf = nullptr,
+                               uint8_t* s8 = nullptr);
+// UE8M0 bytes s [rows, C] -> packed scale-factor tiles (packed_sf_offset(r, c, ceil(C/4)))
+cudaError_t launch_pack_scale_bytes(const uint8_t* s, int64_t rows, int C, uint8_t* out, cudaStream_t stream);
 // [E, N/128, K/128] power-of-two block scales -> [E][N/128][ceil(K/512)] scale-factor tiles (out
 // 16-byte aligned); a scale that is not a positive power of two sets MOE_STATUS_BAD_SCALE
 cudaError_t launch_pack_scales(const float* s, int E, int N, int K, uint8_t* out, uint32_t* status,
@@ -151,7 +156,7 @@ struct GemmArgs {
     // rows (tiles start at row 0: tile_row0 must be a multiple of 128); b_sf: B's, [E][N/128]
     // [ceil(K/512)] tiles; out_sf: the SiLU epilogue's requantisation scales, ceil(N/1024) tiles
     // per 128 rows.  a_scale, b_scale and out_scale are then unused.
-    int sf_packed;
+    int sf_packed;             // 1: packed UE8M0 (4 K blocks per word); 2: MXFP8 (4 32-groups per word, one tile per K block)
     const uint8_t* a_sf;
     const uint8_t* b_sf;
     uint8_t* out_sf;

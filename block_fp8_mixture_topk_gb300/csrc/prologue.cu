@@ -123,18 +123,23 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
         }
+        // MXFP8: groups of 32 = 4 threads; otherwise 128 = 16 threads
+        const bool mx = scale_fmt == MOE_SCALE_MXFP8;
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        for (int o = 8; o > 0; o >>= 1)
+            if (!mx || o < 4) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (active) {
-            const float sc = group_scale_fmt(amax, scale_fmt);
+            const float sc = group_scale_fmt(amax, mx ? MOE_SCALE_UE8M0 : scale_fmt);
             const uint2 code = encode8(f, sc, __frcp_rn(sc));
+            const int sc_col = mx ? g * 4 + (sub >> 2) : g;
+            const bool writer = mx ? (sub & 3) == 0 : sub == 0;
             for (int j = 0; j < topk; ++j) {
                 const int64_t o = s_pos[t * topk + j];
                 if (o < 0) continue;
                 *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
-                if (sub == 0) {
+                if (writer) {
                     if (s) s[o * s_rs + g * s_gs] = sc;
-                    if (sf) sf[packed_sf_offset(o, g, sf_kb4)] = ue8m0_byte(sc);
+                    if (sf) sf[packed_sf_offset(o, sc_col, sf_kb4)] = ue8m0_byte(sc);
                 }
             }
         }
@@ -155,7 +160,9 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
     if (blocks > 148) blocks = 148;
     return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
                       padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
-                      q, q_ld, s, s_rs, s_gs, sf ? MOE_SCALE_UE8M0 : scale_fmt, dec, sf, (H / 128 + 3) / 4);
+                      q, q_ld, s, s_rs, s_gs,
+                      scale_fmt == MOE_SCALE_MXFP8 ? MOE_SCALE_MXFP8 : (sf ? MOE_SCALE_UE8M0 : scale_fmt), dec, sf,
+                      scale_fmt == MOE_SCALE_MXFP8 ? H / 128 : (H / 128 + 3) / 4);
 }
 
 }  // namespace mfp8

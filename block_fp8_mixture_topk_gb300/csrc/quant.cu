@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
                                                           int64_t ld, uint8_t* __restrict__ q, int64_t q_ld,
                                                           float* __restrict__ s, int64_t s_rs, int64_t s_gs,
                                                           const int32_t* __restrict__ pos, int topk, int scale_fmt,
-                                                          uint8_t* __restrict__ sf, int sf_kb4) {
+                                                          uint8_t* __restrict__ sf, int sf_kb4,
+                                                          uint8_t* __restrict__ s8) {
     grid_dependency_wait();
     const int G = cols / 128;
     const int64_t total = rows * G;
@@ -53,26 +54,27 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
 #pragma unroll
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
         }
+        // MXFP8: groups of 32 = 4 threads; otherwise 128 = 16 threads
+        const bool mx = scale_fmt == MOE_SCALE_MXFP8;
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        for (int o = 8; o > 0; o >>= 1)
+            if (!mx || o < 4) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (active) {
-            const float sc = group_scale_fmt(amax, scale_fmt);
+            const float sc = group_scale_fmt(amax, mx ? MOE_SCALE_UE8M0 : scale_fmt);
             const uint2 code = encode8(f, sc, __frcp_rn(sc));
-            if (pos) {
-                for (int j = 0; j < topk; ++j) {
-                    const int64_t o = pos[r * topk + j];
-                    if (o < 0) continue;
-                    *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
-                    if (sub == 0) {
-                        if (s) s[o * s_rs + g * s_gs] = sc;
-                        if (sf) sf[packed_sf_offset(o, g, sf_kb4)] = ue8m0_byte(sc);
-                    }
-                }
-            } else {
-                *reinterpret_cast<uint2*>(q + r * q_ld + g * 128 + sub * 8) = code;
-                if (sub == 0) {
-                    if (s) s[r * s_rs + g * s_gs] = sc;
-                    if (sf) sf[packed_sf_offset(r, g, sf_kb4)] = ue8m0_byte(sc);
+            // the scale's column: the 128-group, or (MXFP8) the 32-group g*4 + sub/4
+            const int sc_col = mx ? g * 4 + (sub >> 2) : g;
+            const bool writer = mx ? (sub & 3) == 0 : sub == 0;
+            const int sc_cols = mx ? cols / 32 : cols / 128;
+            const int64_t n_rows = pos ? topk : 1;
+            for (int j = 0; j < n_rows; ++j) {
+                const int64_t o = pos ? pos[r * topk + j] : r;
+                if (o < 0) continue;
+                *reinterpret_cast<uint2*>(q + o * q_ld + g * 128 + sub * 8) = code;
+                if (writer) {
+                    if (s) s[o * s_rs + g * s_gs] = sc;
+                    if (s8) s8[o * sc_cols + sc_col] = ue8m0_byte(sc);
+                    if (sf) sf[packed_sf_offset(o, sc_col, sf_kb4)] = ue8m0_byte(sc);
                 }
             }
         }
@@ -259,12 +261,37 @@ int grid_for(int64_t work_items, int per_block) {
 
 cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_t ld, uint8_t* q, int64_t q_ld,
                                float* s, int64_t s_row_stride, int64_t s_group_stride, const int32_t* pos,
-                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf) {
+                               int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf, uint8_t* s8) {
     const int64_t groups = rows * (cols / 128);
     if (groups == 0) return cudaSuccess;
-    const int sf_kb4 = (cols / 128 + 3) / 4;
+    // packed tiles: 4 scale columns per 32-bit word (MXFP8: 32-groups, 4 per 128-wide K block)
+    const int sf_kb4 = scale_fmt == MOE_SCALE_MXFP8 ? cols / 128 : (cols / 128 + 3) / 4;
+    const int fmt = scale_fmt == MOE_SCALE_MXFP8 ? MOE_SCALE_MXFP8 : (sf ? MOE_SCALE_UE8M0 : scale_fmt);
     return launch_pdl(group_quant_kernel, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, rows, cols, ld, q,
-                      q_ld, s, s_row_stride, s_group_stride, pos, topk, sf ? MOE_SCALE_UE8M0 : scale_fmt, sf, sf_kb4);
+                      q_ld, s, s_row_stride, s_group_stride, pos, topk, fmt, sf, sf_kb4, s8);
+}
+
+// Packing of UE8M0 scale bytes s [rows, C] (row-major) into scale-factor tiles: out at
+// packed_sf_offset(r, c, ceil(C/4)); missing bytes of a last partial word or tile are left alone.
+__global__ void __launch_bounds__(256) pack_scale_bytes_kernel(const uint8_t* __restrict__ s, int64_t rows, int C,
+                                                               uint8_t* __restrict__ out) {
+    grid_dependency_wait();
+    const int C4 = (C + 3) / 4;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * C;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / C;
+        const int c = static_cast<int>(i - r * C);
+        out[packed_sf_offset(r, c, C4)] = s[i];
+    }
+}
+
+cudaError_t launch_pack_scale_bytes(const uint8_t* s, int64_t rows, int C, uint8_t* out, cudaStream_t stream) {
+    const int64_t n = rows * C;
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    return launch_pdl(pack_scale_bytes_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, s, rows,
+                      C, out);
 }
 
 cudaError_t launch_pack_scales(const float* s, int E, int N, int K, uint8_t* out, uint32_t* status,

@@ -20,7 +20,10 @@ MOE_WEIGHTS_NK, MOE_WEIGHTS_TILED, MOE_WEIGHTS_NVFP4 = 0, 1, 2
 NVFP4_UNIT_BYTES = 16 * 64 + 16 * 8   # one 16-row slab x one 128-wide K block: codes, then block scales
 # fp32 amax/448; that scale rounded up to a power of two (FLOAT32_CEIL_UE8M0); the same UE8M0 scales in
 # the packed scale-factor tiles of the block-scaled MMA (MOE_SCALE_UE8M0_PACKED)
-SCALE_FMT = {"f32": 0, "ue8m0": 1, "ue8m0_packed": 2}
+# the same UE8M0 scales in the packed scale-factor tiles of the block-scaled MMA (MOE_SCALE_UE8M0_PACKED);
+# MXFP8: 1x32 groups and blocks along K with UE8M0 scales, on the block-scaled MMA (MOE_SCALE_MXFP8)
+SCALE_FMT = {"f32": 0, "ue8m0": 1, "ue8m0_packed": 2, "mxfp8": 3}
+_PACKED_SCALES = ("ue8m0_packed", "mxfp8")
 SCORING = {"softmax": 0, "sigmoid": 1}
 EPILOGUE = {"store": 0, "silu_mul_quant": 1, "weighted_scatter": 2, "weighted_rows": 3, "weighted_pairs_bf16": 4}
 
@@ -108,6 +111,9 @@ def lib():
                 "moe_fp8_block_pack_weights": ([P, I, I, I, P, P], I),
                 "moe_packed_scale_bytes": ([I64, I], SZ),
                 "moe_fp8_block_pack_scales": ([P, I, I, I, P, P], I),
+                "moe_mxfp8_packed_scale_bytes": ([I64, I], SZ),
+                "moe_mxfp8_quant_weight": ([P, I, I, I, P, P, P], I),
+                "moe_mxfp8_pack_scales": ([P, I64, I, P, P], I),
                 "moe_nvfp4_quant_weight": ([P, I, I, I, P, P, P, P], I),
                 "moe_nvfp4_packed_bytes": ([I, I, I], SZ),
                 "moe_nvfp4_pack_weights": ([P, P, I, I, I, P, P], I),
@@ -217,13 +223,16 @@ def moe_packed_scale_bytes(rows, K) -> int:
 
 def fp8_group_quant(x, scale_fmt="f32"):
     """1x128 group quantisation of bf16 [rows, cols]: returns (codes uint8, scales fp32 [rows, cols/128]).
-    scale_fmt: "f32" (amax/448), "ue8m0" (rounded up to a power of two) or "ue8m0_packed" (the same
-    scales as packed UE8M0 tiles: a uint8 tensor of moe_packed_scale_bytes(rows, cols) bytes)."""
+    scale_fmt: "f32" (amax/448), "ue8m0" (rounded up to a power of two), "ue8m0_packed" (the same
+    scales as packed UE8M0 tiles: a uint8 tensor of moe_packed_scale_bytes(rows, cols) bytes) or
+    "mxfp8" (groups of 32: the UE8M0 scale bytes, uint8 [rows, cols/32])."""
     _cuda(x, torch.bfloat16, "x")
     rows, cols = x.shape
     q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
     if scale_fmt == "ue8m0_packed":
         s = torch.zeros(max(moe_packed_scale_bytes(rows, cols), 16), dtype=torch.uint8, device=x.device)
+    elif scale_fmt == "mxfp8":
+        s = torch.empty(rows, max(cols // 32, 1), dtype=torch.uint8, device=x.device)
     else:
         s = torch.empty(rows, max(cols // 128, 1), dtype=torch.float32, device=x.device)
     rc = lib().fp8_group_quant_ex(_ptr(x), rows, cols, cols, _ptr(q), _ptr(s), SCALE_FMT[scale_fmt], _stream())
@@ -250,6 +259,32 @@ def moe_fp8_block_pack_scales(s):
     out = torch.empty(E, NB, (KB + 3) // 4, 512, dtype=torch.uint8, device=s.device)
     _check("moe_fp8_block_pack_scales", lib().moe_fp8_block_pack_scales(_ptr(s), E, NB * 128, KB * 128, _ptr(out),
                                                                           _stream()))
+    return out
+
+
+def moe_mxfp8_quant_weight(w):
+    """MXFP8 quantisation of bf16 expert weights [E, N, K]: returns (codes uint8 [E, N, K], UE8M0
+    scale bytes uint8 [E, N, K/32]) (load-time)."""
+    _cuda(w, torch.bfloat16, "w")
+    E, N, K = w.shape
+    q = torch.empty(E, N, K, dtype=torch.uint8, device=w.device)
+    s = torch.empty(E, N, max(K // 32, 1), dtype=torch.uint8, device=w.device)
+    _check("moe_mxfp8_quant_weight", lib().moe_mxfp8_quant_weight(_ptr(w), E, N, K, _ptr(q), _ptr(s), _stream()))
+    return q, s
+
+
+def moe_mxfp8_packed_scale_bytes(rows, K) -> int:
+    return int(lib().moe_mxfp8_packed_scale_bytes(rows, K))
+
+
+def moe_mxfp8_pack_scales(s):
+    """UE8M0 scale bytes [..., rows, K/32] (uint8; leading dimensions folded into rows, a multiple of
+    128) -> the MXFP8 packed scale tiles, a uint8 tensor of moe_mxfp8_packed_scale_bytes bytes."""
+    s = _cuda(s, torch.uint8, "s")
+    K = s.shape[-1] * 32
+    rows = s.numel() // s.shape[-1]
+    out = torch.empty(max(moe_mxfp8_packed_scale_bytes(rows, K), 16), dtype=torch.uint8, device=s.device)
+    _check("moe_mxfp8_pack_scales", lib().moe_mxfp8_pack_scales(_ptr(s), rows, K, _ptr(out), _stream()))
     return out
 
 
@@ -395,7 +430,7 @@ def moe_fp8_block_forward(hidden, router_logits, w13, w13_scale, w2, w2_scale, t
     _cuda(hidden, torch.bfloat16, "hidden")
     _cuda(router_logits, torch.float32, "router_logits")
     w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
-    sdt = torch.uint8 if scale_fmt == "ue8m0_packed" else torch.float32
+    sdt = torch.uint8 if scale_fmt in _PACKED_SCALES else torch.float32
     _cuda(w13_scale, sdt, "w13_scale")
     _cuda(w2_scale, sdt, "w2_scale")
     T, H = hidden.shape
@@ -447,7 +482,7 @@ def moe_fp8_block_forward_masked(hidden, counts, w13, w13_scale, w2, w2_scale, o
     _cuda(hidden, torch.bfloat16, "hidden")
     _cuda(counts, torch.int32, "counts")
     w13, w2 = _codes(_cuda(w13, None, "w13")), _codes(_cuda(w2, None, "w2"))
-    sdt = torch.uint8 if scale_fmt == "ue8m0_packed" else torch.float32
+    sdt = torch.uint8 if scale_fmt in _PACKED_SCALES else torch.float32
     _cuda(w13_scale, sdt, "w13_scale")
     _cuda(w2_scale, sdt, "w2_scale")
     E, M, H = hidden.shape

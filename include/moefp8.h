@@ -224,6 +224,25 @@ int moe_nvfp4_pack_weights(const uint8_t* q, const uint8_t* block_scale, int E, 
  * words, each word the scales of 4 consecutive K blocks (byte b = K block 4q + b).  Weights: one
  * set of tiles per expert, [E][N/128][ceil(K/512)] tiles (moe_fp8_block_pack_scales). */
 #define MOE_SCALE_UE8M0_PACKED 2
+/* MOE_SCALE_MXFP8: MXFP8 ("MXFP8 (block [1, 32])", page "vllm.model_executor.layers.fused_moe.oracle.fp8",
+ * make_fp8_moe_quant_config; weights with "e8m0 group-32 scales", _humming_fp8_weight_schema): the
+ * activations and the requantised intermediate in groups of 32 along K, the weights in 1x32 blocks
+ * along K, every scale max(amax, 1e-8)/448 rounded up to a power of two and stored as its UE8M0
+ * byte.  The GEMMs run on the block-scaled MMA, one scale per 32 K per row, as the format defines.
+ * Packed scale tiles of a [rows, K] operand: the same layout as above with the 32-wide groups as
+ * the scale columns, i.e. ceil(rows/128) * (K/128) tiles of 512 bytes, the byte of (row r, group
+ * g = k/32) at ((r / 128) * (K/128) + g / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4. */
+#define MOE_SCALE_MXFP8 3
+/* Bytes of the MXFP8 packed scale tiles of a [rows, K] operand: ceil(rows/128) * (K/128) * 512. */
+size_t moe_mxfp8_packed_scale_bytes(int64_t rows, int K);
+/* MXFP8 weight quantisation of stacked bf16 expert weights w [E, N, K] (load time): 1x32 blocks
+ * along K, q e4m3 [E, N, K], s the UE8M0 scale bytes [E, N, K/32] (the pages' uint8 layout).  w,
+ * q 16-byte aligned; K a multiple of 128. */
+int moe_mxfp8_quant_weight(const uint16_t* w, int E, int N, int K, uint8_t* q, uint8_t* s, void* stream);
+/* Packing of UE8M0 scale bytes s [rows, K/32] (e.g. moe_mxfp8_quant_weight's, rows = E * N) into the
+ * MXFP8 packed tiles: out, moe_mxfp8_packed_scale_bytes(rows, K) bytes, 16-byte aligned.  rows a
+ * multiple of 128 (whole tiles), K a multiple of 128. */
+int moe_mxfp8_pack_scales(const uint8_t* s, int64_t rows, int K, uint8_t* out, void* stream);
 /* Bytes of the packed scale tiles of a [rows, K] operand: ceil(rows/128) * ceil(K/512) * 512
  * (0 for negative sizes or K not a multiple of 128). */
 size_t moe_packed_scale_bytes(int64_t rows, int K);
@@ -236,8 +255,9 @@ int moe_fp8_block_pack_scales(const float* s, int E, int N, int K, uint8_t* out,
 /* fp8_group_quant / fp8_block_quant_weight with a scale format.  fp8_group_quant_ex with
  * MOE_SCALE_UE8M0_PACKED writes the UE8M0 scales as packed tiles: s is then a byte array of
  * moe_packed_scale_bytes(rows, cols) (passed as float*), rows past `rows` in the last tile left as
- * they are.  fp8_block_quant_weight_ex takes MOE_SCALE_F32 or MOE_SCALE_UE8M0 (pack its scales
- * with moe_fp8_block_pack_scales). */
+ * they are.  With MOE_SCALE_MXFP8, groups of 32: s is a byte array of the UE8M0 scales
+ * [rows, cols/32] (passed as float*).  fp8_block_quant_weight_ex takes MOE_SCALE_F32 or
+ * MOE_SCALE_UE8M0 (pack its scales with moe_fp8_block_pack_scales). */
 int fp8_group_quant_ex(const uint16_t* x, int rows, int cols, int ld, uint8_t* q, float* s, int scale_fmt,
                        void* stream);
 int fp8_block_quant_weight_ex(const uint16_t* w, int E, int N, int K, uint8_t* q, float* s, int scale_fmt,

@@ -143,8 +143,9 @@ def test_newer_entry_points_reject_bad_arguments_on_host():
         assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
                                           1 << 30, p, None, None) == -1
     # quantisers: unknown scale format
-    assert L.fp8_group_quant_ex(p, 4, 128, 128, p, p, 3, None) == -1
-    assert L.fp8_block_quant_weight_ex(p, 1, 128, 128, p, p, 3, None) == -1
+    assert L.fp8_group_quant_ex(p, 4, 128, 128, p, p, 7, None) == -1
+    assert L.fp8_block_quant_weight_ex(p, 1, 128, 128, p, p, 3, None) == -1     # weights: f32 / ue8m0 only
+    assert L.fp8_block_quant_weight_ex(p, 1, 128, 128, p, p, 2, None) == -1
     # packing: N not a multiple of 128; in place; empty is a no-op
     assert L.moe_fp8_block_pack_weights(p, 1, 100, 128, big, None) == -2
     assert L.moe_fp8_block_pack_weights(big, 2, 128, 128, ctypes.c_void_p(0x100000 + 4096), None) == -1
@@ -206,3 +207,35 @@ def test_nvfp4_entry_points_reject_bad_arguments_on_host():
     opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, 0, 0)
     assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 8, 256, 256, 128, 65, 1, None, ctypes.byref(opts), big,
                                       1 << 40, p, None, None) == -2
+
+
+def test_block_scaled_formats_reject_bad_arguments_on_host():
+    """Packed UE8M0 and MXFP8 scales: sizes, packing and the layer's options, checked on the host."""
+    L = ops.lib()
+    p = ctypes.c_void_p(0x1000)
+    big = ctypes.c_void_p(0x100000)
+    # packed UE8M0 tiles: ceil(rows/128) * ceil(K/512) * 512 bytes; MXFP8: ceil(rows/128) * (K/128) * 512
+    assert moe.moe_packed_scale_bytes(128, 7168) == 14 * 512
+    assert moe.moe_packed_scale_bytes(129, 640) == 2 * 2 * 512
+    assert moe.moe_packed_scale_bytes(128, 100) == 0
+    assert moe.moe_mxfp8_packed_scale_bytes(128, 7168) == 56 * 512
+    assert moe.moe_mxfp8_packed_scale_bytes(300, 256) == 3 * 2 * 512
+    # packing: shapes and alignment
+    assert L.moe_fp8_block_pack_scales(p, 1, 100, 128, big, None) == -2
+    assert L.moe_fp8_block_pack_scales(p, 1, 128, 128, ctypes.c_void_p(0x100008), None) == -1
+    assert L.moe_fp8_block_pack_scales(None, 0, 128, 128, None, None) == 0
+    assert L.moe_mxfp8_quant_weight(p, 1, 128, 96, p, p, None) == -2
+    assert L.moe_mxfp8_pack_scales(p, 100, 128, big, None) == -2         # whole 128-row tiles
+    assert L.moe_mxfp8_pack_scales(p, 128, 96, big, None) == -2
+    assert L.moe_mxfp8_pack_scales(None, 0, 128, None, None) == 0
+    # the layer: block-scaled formats take neither the decode kernel nor NVFP4 weights
+    for fmt in (2, 3):
+        opts = ops._ForwardOptions(0, fmt, 2)
+        assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                          1 << 30, p, None, None) == -1
+        opts = ops._ForwardOptions(ops.MOE_WEIGHTS_NVFP4, fmt, 0)
+        assert L.moe_fp8_block_forward_ex(p, p, p, p, p, p, 4, 256, 256, 4, 2, 1, None, ctypes.byref(opts), big,
+                                          1 << 30, p, None, None) == -1
+    # grouped GEMM: the block-scaled kernel has the store, SiLU and pair-row epilogues only
+    ep = ops._Epilogue(3, 1, p, None, None, 0, 0, p, p, 1, None, 0, 3)
+    assert L.fp8_block_grouped_gemm(p, p, 1, 1, 128, p, p, 256, 128, 1, p, p, p, 1, ctypes.byref(ep), None) == -1
