@@ -60,9 +60,10 @@ def parse():
                    help="routed: the whole layer (default); masked: moe_fp8_block_forward_masked on rows "
                         "grouped by expert, counts from routing the workload's tokens")
     p.add_argument("--max-tokens", type=int, default=None, help="masked layout: rows per expert (default: max count)")
-    p.add_argument("--scale-fmt", choices=["f32", "ue8m0", "ue8m0_packed"], default="f32",
-                   help="block scales: fp32 amax/448, rounded up to a power of two (FLOAT32_CEIL_UE8M0), or those "
-                        "UE8M0 scales packed for the block-scaled tensor-core MMA (the tile GEMMs only)")
+    p.add_argument("--scale-fmt", choices=["f32", "ue8m0", "ue8m0_packed", "mxfp8"], default="f32",
+                   help="block scales: fp32 amax/448, rounded up to a power of two (FLOAT32_CEIL_UE8M0), those "
+                        "UE8M0 scales packed for the block-scaled tensor-core MMA, or MXFP8 (1x32 groups and blocks, "
+                        "UE8M0; block-scaled MMA); the last two on the tile GEMMs only")
     p.add_argument("--decode", choices=["auto", "off", "on"], default="auto",
                    help="expert GEMMs of small steps: decode-path kernels for up to 8 tokens (auto), never, "
                         "or whenever the step qualifies")
@@ -97,8 +98,8 @@ def describe(wl, world):
 
 def describe_weights(args):
     fmt = {"ue8m0": ", scales rounded up to powers of two (ue8m0)",
-           "ue8m0_packed": ", UE8M0 scales packed for the block-scaled MMA (ue8m0_packed)"}.get(args.scale_fmt,
-                                                                                                 ", fp32 scales")
+           "ue8m0_packed": ", UE8M0 scales packed for the block-scaled MMA (ue8m0_packed)",
+           "mxfp8": ", MXFP8: 1x32 blocks with UE8M0 scales (block-scaled MMA)"}.get(args.scale_fmt, ", fp32 scales")
     if args.weights == "nvfp4":
         return ("NVFP4: e2m1 codes, e4m3 scale per 16 along K, fp32 global scale per expert, packed at load "
                 "time (moe_nvfp4_pack_weights); activations e4m3 1x128 groups" + fmt)
@@ -112,9 +113,13 @@ def touched_per_pass(ids, tokens_per_pass):
                for t0 in range(0, ids.shape[0], tokens_per_pass))
 
 
-def expert_weight_bytes(wl, nvfp4=False, packed_scales=False):
+def expert_weight_bytes(wl, nvfp4=False, packed_scales=False, mxfp8=False):
     """Bytes one expert's w13 and w2 occupy (codes and scales): (w13, both)."""
     H, I = wl.H, wl.I
+    if mxfp8:
+        # one UE8M0 byte per 32 weights
+        w13 = 2 * I * H + 2 * I * H // 32
+        return w13, w13 + H * I + H * I // 32
     if packed_scales:
         # UE8M0 scale tiles: 512 bytes per 128 weight rows and 4 K blocks
         w13 = 2 * I * H + (2 * I // 128) * -(-H // 512) * 512
@@ -360,11 +365,18 @@ def run_ours(args, wl):
         w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
         w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
         wfmt = "ue8m0" if args.scale_fmt == "ue8m0_packed" else args.scale_fmt
+        if args.scale_fmt == "mxfp8":
+            # MXFP8 weights: 1x32 blocks, UE8M0 scale bytes, packed for the MMA (untimed, load time)
+            w13s = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
+            w2s = torch.empty(E, H, I // 32, dtype=torch.uint8, device=dev)
         for e0 in range(0, E, 8):
             ex = range(e0, min(E, e0 + 8))
-            w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex),
-                                                                                        wfmt)
-            w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), wfmt)
+            quant = moe.moe_mxfp8_quant_weight if args.scale_fmt == "mxfp8" else \
+                (lambda w: moe.fp8_block_quant_weight(w, wfmt))
+            w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = quant(mi.w13_bf16(wl, dev, ex))
+            w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = quant(mi.w2_bf16(wl, dev, ex))
+        if args.scale_fmt == "mxfp8":
+            w13s, w2s = moe.moe_mxfp8_pack_scales(w13s), moe.moe_mxfp8_pack_scales(w2s)
         if args.scale_fmt == "ue8m0_packed":
             # load-time packing of the UE8M0 block scales for the block-scaled MMA (untimed)
             w13s, w2s = moe.moe_fp8_block_pack_scales(w13s), moe.moe_fp8_block_pack_scales(w2s)
@@ -382,9 +394,9 @@ def run_ours(args, wl):
     # its own tokens touch
     touched_streamed = touched_per_pass(ids, 8) if args.weights == "nvfp4" else touched
     P = wl.P
-    packed_scales = args.scale_fmt == "ue8m0_packed"
+    packed_scales = args.scale_fmt in ("ue8m0_packed", "mxfp8")
     if packed_scales and (nvfp4 or args.decode == "on"):
-        raise SystemExit("--scale-fmt ue8m0_packed runs on the tile GEMMs: not with NVFP4 weights or --decode on")
+        raise SystemExit(f"--scale-fmt {args.scale_fmt} runs on the tile GEMMs: not with NVFP4 weights or --decode on")
     decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode) and not packed_scales
     # kernels per step (the decode path's one GEMM kernel in place of two)
     launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
@@ -514,11 +526,15 @@ def run_ours(args, wl):
     pk = peaks()
     tokens_s = whole_job_rate(world, wl.T, ms)
     flops = wl.flops()
-    per_expert_w13, per_expert = expert_weight_bytes(wl, nvfp4, packed_scales)
+    per_expert_w13, per_expert = expert_weight_bytes(wl, nvfp4, packed_scales, args.scale_fmt == "mxfp8")
     layer_bytes = touched * per_expert + wl.T * H * 2 * 2 + wl.T * E * 4
     # algorithmic bytes of one w13 GEMM launch: touched experts' w13 + scales, the sorted activation
     # rows and scales read once, the requantised intermediate and its scales written once
     gemm_bytes = touched * per_expert_w13 + P * (H + H // 128 * 4) + P * (I + I // 128 * 4)
+    if packed_scales:
+        # one scale byte per row and 128 (packed UE8M0) or 32 (MXFP8) activations
+        g_act = 32 if args.scale_fmt == "mxfp8" else 128
+        gemm_bytes = touched * per_expert_w13 + P * (H + H // g_act) + P * (I + I // g_act)
     gemm_flops = 4 * P * H * I
     g_ms = stage_ms["gemm_w13"]
     if decode:
@@ -604,10 +620,16 @@ def run_masked(args, wl):
     w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
     w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
     wfmt = "ue8m0" if args.scale_fmt == "ue8m0_packed" else args.scale_fmt
+    if args.scale_fmt == "mxfp8":
+        w13s = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
+        w2s = torch.empty(E, H, I // 32, dtype=torch.uint8, device=dev)
+    quant = moe.moe_mxfp8_quant_weight if args.scale_fmt == "mxfp8" else (lambda w: moe.fp8_block_quant_weight(w, wfmt))
     for e0 in range(0, E, 8):
         ex = range(e0, min(E, e0 + 8))
-        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w13_bf16(wl, dev, ex), wfmt)
-        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = moe.fp8_block_quant_weight(mi.w2_bf16(wl, dev, ex), wfmt)
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = quant(mi.w13_bf16(wl, dev, ex))
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = quant(mi.w2_bf16(wl, dev, ex))
+    if args.scale_fmt == "mxfp8":
+        w13s, w2s = moe.moe_mxfp8_pack_scales(w13s), moe.moe_mxfp8_pack_scales(w2s)
     if args.scale_fmt == "ue8m0_packed":
         w13s, w2s = moe.moe_fp8_block_pack_scales(w13s), moe.moe_fp8_block_pack_scales(w2s)
     w13p, w2p = (moe.moe_fp8_block_pack_weights(w13q), moe.moe_fp8_block_pack_weights(w2q)) \
