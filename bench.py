@@ -34,13 +34,16 @@ import moe_inputs as mi  # noqa: E402
 
 FP8_OVER_BF16 = 2.0        # nominal dense fp8 / bf16 tensor throughput ratio
 CSRC = os.path.join(ROOT, "block_fp8_mixture_topk_gb300", "csrc")
-# ncu summary of each w13 kernel and the sources it was taken on: tile GEMM, decode-path GEMM
+# DRAM traffic of each w13 kernel from an ncu capture (a JSON record beside the profile's summary)
+# and the sources it was taken on: tile GEMM, block-scaled tile GEMM, decode-path GEMM (FP8, NVFP4)
 PROFILES = {
-    "tile": (os.path.join(ROOT, "profiles", "gemm_w13_dsv3.md"),
+    "tile": (os.path.join(ROOT, "profiles", "gemm_w13_dsv3.json"),
              [os.path.join(CSRC, f) for f in ("gemm.cu", "common.cuh")]),
-    "decode": (os.path.join(ROOT, "profiles", "decode_mlp_dsv3_decode.md"),
+    "tile_bs": (os.path.join(ROOT, "profiles", "gemm_bs_w13_dsv3.json"),
+                [os.path.join(CSRC, f) for f in ("gemm.cu", "common.cuh")]),
+    "decode": (os.path.join(ROOT, "profiles", "decode_mlp_dsv3_decode.json"),
                [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
-    "nvfp4": (os.path.join(ROOT, "profiles", "decode_mlp_nvfp4_dsv3_decode.md"),
+    "nvfp4": (os.path.join(ROOT, "profiles", "decode_mlp_nvfp4_dsv3_decode.json"),
               [os.path.join(CSRC, f) for f in ("decode.cu", "common.cuh")]),
 }
 
@@ -299,25 +302,24 @@ def gemm_source_sha(mode="tile"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(wl, mode="tile"):
-    """dram bytes per launch of the w13 GEMM (tile GEMM, decode-path kernel, or the decode-path
-    kernel on NVFP4 weights) from the committed ncu summary, if it was taken on the current kernel
-    source for this workload; else None."""
+def profiled_traffic(wl, mode="tile", scale_fmt="f32"):
+    """dram bytes per launch of the w13 GEMM (tile GEMM, block-scaled tile GEMM, decode-path kernel,
+    or the decode-path kernel on NVFP4 weights) from the committed ncu record, if it was taken on the
+    current kernel source for this workload and scale format; else None."""
     path = PROFILES[mode][0]
     if not os.path.exists(path):
         return None
-    kv = {}
-    for line in open(path):
-        if "=" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split("=", 1)
-            kv[k.strip()] = v.strip().strip("`")
-    if kv.get("source_sha") != gemm_source_sha(mode) or kv.get("workload") != wl.name:
+    try:
+        rec = json.load(open(path))
+    except (OSError, ValueError):
         return None
-    if "tokens" in kv and kv["tokens"] != str(wl.T):
+    if rec.get("source_sha") != gemm_source_sha(mode) or rec.get("workload") != wl.name:
+        return None
+    if rec.get("tokens") not in (None, wl.T) or rec.get("scale_fmt", "f32") != scale_fmt:
         return None
     try:
-        return float(kv["dram_bytes_per_launch_full"])
-    except (KeyError, ValueError):
+        return float(rec["dram_bytes_per_launch_full"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -559,9 +561,12 @@ def run_ours(args, wl):
                       else "grouped_gemm_bs_kernel<silu_mul_quant> (w13 GEMM, block-scaled MMA)" if packed_scales
                       else "grouped_gemm_kernel<silu_mul_quant> (w13 GEMM)")
     roof["algorithmic_bytes_per_launch"] = gemm_bytes
+    if nvfp4 and wl.T > 8:
+        # passes of 8 tokens: each pass streams the experts its own tokens touch
+        roof["bytes_basis"] = "weights streamed: each 8-token pass's touched experts"
     roof["ms_per_launch"] = g_ms
-    roof["traffic"] = None if packed_scales else profiled_traffic(wl, "nvfp4" if nvfp4 else "decode" if decode
-                                                                  else "tile")
+    roof["traffic"] = profiled_traffic(wl, "nvfp4" if nvfp4 else "decode" if decode else "tile_bs" if packed_scales
+                                       else "tile", args.scale_fmt)
 
     line = {"metric": "block-FP8 fused-MoE tokens/s", "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -574,6 +579,7 @@ def run_ours(args, wl):
             "layer_gbs": world * layer_bytes / (ms / 1e3) / 1e9,
             "ms_per_step_eager": eager_ms, "ms_per_step_graph": graph_ms, "launch": launch,
             "experts_touched": touched, "weight_bytes_touched": touched * per_expert, "decode_path": decode,
+            "weight_gbs_unique": world * touched * per_expert / (ms / 1e3) / 1e9,
             "stage_ms": stage_ms, "clocks": clk,
             "e2e": {"value": whole_job_rate(world, wl.T, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": hidden.numel() * 2 + logits.numel() * 4,
