@@ -302,3 +302,51 @@ def test_packed_layer_rejects_the_decode_kernel_and_nvfp4():
                                     scale_fmt="ue8m0_packed")
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("fmt", ["ue8m0_packed", "mxfp8"])
+def test_block_scaled_layer_repeats_and_replays_from_a_cuda_graph(fmt):
+    """Ten calls on one dirty workspace and a CUDA-graph replay on new inputs give the same bytes
+    as a fresh eager call, in both block-scaled formats."""
+    wl = mi.Workload("bs_graph", 163, 300, 256, 384, 6, 2)
+    if fmt == "mxfp8":
+        from test_gpu_mxfp8 import MxLayer
+        layer = MxLayer(wl)
+    else:
+        layer = PackedLayer(wl)
+    rp, _ = routing_of(wl)
+    hid = mi.hidden(wl).to(DEV)
+    log = mi.router_logits(wl).to(DEV)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8,
+                     device=DEV)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=DEV)
+
+    def step():
+        moe.moe_fp8_block_forward(hid, log, layer.w13q, layer.w13sf, layer.w2q, layer.w2sf, wl.topk, True, rp,
+                                  out=out, workspace=ws, scale_fmt=fmt)
+
+    step()
+    first = out.clone()
+    for _ in range(9):
+        step()
+        assert torch.equal(out, first)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in range(2):
+        wl_s = wl.with_(number=wl.number + 300 + seed)
+        h, l = mi.hidden(wl_s).to(DEV), mi.router_logits(wl_s).to(DEV)
+        hid.copy_(h)
+        log.copy_(l)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        want = moe.moe_fp8_block_forward(h, l, layer.w13q, layer.w13sf, layer.w2q, layer.w2sf, wl.topk, True, rp,
+                                         scale_fmt=fmt)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
