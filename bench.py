@@ -70,6 +70,9 @@ def parse():
     p.add_argument("--decode", choices=["auto", "off", "on"], default="auto",
                    help="expert GEMMs of small steps: decode-path kernels for up to 8 tokens (auto), never, "
                         "or whenever the step qualifies")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the extra timings of the default run (the block-scaled formats on the same "
+                        "workload, and the tensor-bound Qwen3-shaped workload in every FP8 scale format)")
     p.add_argument("--weights", choices=["tiled", "nk", "nvfp4"], default="tiled",
                    help="expert weights: e4m3 tile-packed at load time (default), e4m3 in the pages' [E, N, K], "
                         "or NVFP4 (e2m1 codes with e4m3 16-blocks and a global scale, packed; decode-path kernel)")
@@ -586,6 +589,19 @@ def run_ours(args, wl):
                     "d2h_bytes_per_step": out.numel() * 2},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roof}
+    if (world == 1 and not args.no_variants and args.scale_fmt == "f32" and args.weights == "tiled"
+            and args.layout == "routed" and wl == mi.WORKLOADS["dsv3"]):
+        # the same layer in the pages' Blackwell scale format (packed UE8M0) and MXFP8, both on the
+        # block-scaled tensor-core MMA; and the tensor-bound Qwen3-shaped batch in every FP8 format
+        del w13q, w13s, w2q, w2s
+        torch.cuda.empty_cache()
+        var = {}
+        for fmt in ("ue8m0_packed", "mxfp8"):
+            var[f"dsv3/{fmt}"] = time_variant(moe, wl, dev, fmt, args.steps, args.warmup, fp8_peak)
+        q3 = mi.WORKLOADS["qwen3_skew"]
+        for fmt in ("f32", "ue8m0_packed", "mxfp8"):
+            var[f"qwen3_skew/{fmt}"] = time_variant(moe, q3, dev, fmt, args.steps, args.warmup, fp8_peak)
+        line["variants"] = var
     if world == 1 and not args.no_cpu_baseline:
         n = args.cpu_sample or default_sample(wl)
         times, sample, cores = time_oracle(wl, n, dev, runs=1, nvfp4=nvfp4)
@@ -595,6 +611,84 @@ def run_ours(args, wl):
     if dist:
         dist.destroy_process_group()
     _ = np
+
+
+def build_weights(moe, wl, dev, fmt):
+    """Tile-packed e4m3 expert weights of a workload and their scales in scale format `fmt` (load time)."""
+    E, H, I = wl.E, wl.H, wl.I
+    w13q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+    w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+    if fmt == "mxfp8":
+        w13s = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8, device=dev)
+        w2s = torch.empty(E, H, I // 32, dtype=torch.uint8, device=dev)
+        quant = moe.moe_mxfp8_quant_weight
+    else:
+        w13s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+        wfmt = "ue8m0" if fmt == "ue8m0_packed" else fmt
+        quant = (lambda w: moe.fp8_block_quant_weight(w, wfmt))
+    for e0 in range(0, E, 8):
+        ex = range(e0, min(E, e0 + 8))
+        w13q[e0:e0 + len(ex)], w13s[e0:e0 + len(ex)] = quant(mi.w13_bf16(wl, dev, ex))
+        w2q[e0:e0 + len(ex)], w2s[e0:e0 + len(ex)] = quant(mi.w2_bf16(wl, dev, ex))
+    if fmt == "mxfp8":
+        w13s, w2s = moe.moe_mxfp8_pack_scales(w13s), moe.moe_mxfp8_pack_scales(w2s)
+    elif fmt == "ue8m0_packed":
+        w13s, w2s = moe.moe_fp8_block_pack_scales(w13s), moe.moe_fp8_block_pack_scales(w2s)
+    w13q, w2q = moe.moe_fp8_block_pack_weights(w13q), moe.moe_fp8_block_pack_weights(w2q)
+    torch.cuda.synchronize()
+    return w13q, w13s, w2q, w2s
+
+
+def time_variant(moe, wl, dev, fmt, steps, warmup, fp8_peak):
+    """One workload in one scale format: CUDA-graph replay time per step, and each stage's time from
+    one eager pass with events.  The weights are freed before returning."""
+    w13q, w13s, w2q, w2s = build_weights(moe, wl, dev, fmt)
+    hidden, logits = mi.hidden(wl, dev), mi.router_logits(wl, dev)
+    bias = mi.expert_bias(wl, dev)
+    rp = (moe.RoutingParams("sigmoid", wl.n_group, wl.topk_group, wl.routed_scaling, bias)
+          if wl.scoring == mi.SIGMOID else moe.RoutingParams("softmax", 1, 1, wl.routed_scaling))
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,
+                                  workspace=ws, events=events, scale_fmt=fmt)
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(moe.ops.FORWARD_STAGES) + 1)]
+    for _ in range(warmup):
+        step()
+    step(evs)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    if moe.moe_get_device_status(clear=True):
+        raise RuntimeError(f"device status word set during the {fmt} variant")
+    stage = {name: evs[j].elapsed_time(evs[j + 1]) for j, name in enumerate(moe.ops.FORWARD_STAGES)}
+    flops = wl.flops()
+    res = {"ms_per_step": ms, "tokens_per_s": wl.T / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+           "pct_fp8_peak": flops / (ms / 1e3) / 1e12 / fp8_peak,
+           "w13_pct_fp8_peak": 4 * wl.P * wl.H * wl.I / (stage["gemm_w13"] / 1e3) / 1e12 / fp8_peak,
+           "w2_pct_fp8_peak": 2 * wl.P * wl.H * wl.I / (stage["gemm_w2"] / 1e3) / 1e12 / fp8_peak,
+           "stage_ms_eager": stage}
+    del w13q, w13s, w2q, w2s, ws, graph
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_masked(args, wl):
