@@ -403,16 +403,15 @@ def run_ours(args, wl):
     if packed_scales and (nvfp4 or args.decode == "on"):
         raise SystemExit(f"--scale-fmt {args.scale_fmt} runs on the tile GEMMs: not with NVFP4 weights or --decode on")
     decode = moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk, args.decode) and not packed_scales
-    # kernels per step (the decode path's one GEMM kernel in place of two)
-    launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk)
-    if decode != moe.moe_fp8_block_decode_path(wl.T, H, I, wl.topk):
-        launches_per_step += -1 if decode else 1
     if nvfp4:
         if args.decode == "off":
             raise SystemExit("NVFP4 weights run on the decode-path kernel: --decode off does not apply")
-        # route, sort + quantise, the decode kernel, the weighted sum, per 8 tokens
         decode = True
-        launches_per_step = 4 * ((wl.T + 7) // 8)
+    # kernels per step, as the library counts them for these routing parameters and options
+    layout = {"nk": moe.ops.MOE_WEIGHTS_NK, "tiled": moe.ops.MOE_WEIGHTS_TILED,
+              "nvfp4": moe.ops.MOE_WEIGHTS_NVFP4}[args.weights]
+    launches_per_step = moe.moe_fp8_block_forward_kernel_count(wl.T, H, I, E, wl.topk, rp, layout, args.scale_fmt,
+                                                               args.decode)
 
     def step(events=None):
         moe.moe_fp8_block_forward(hidden, logits, w13q, w13s, w2q, w2s, wl.topk, wl.renormalize, rp, out=out,

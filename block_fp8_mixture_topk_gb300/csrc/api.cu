@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "route_select.cuh"
 
 using namespace mfp8;
 
@@ -90,7 +91,7 @@ int64_t mx_sf_bytes(int64_t rows, int K) { return (rows + 127) / 128 * (K / 128)
 
 struct ForwardLayout {
     size_t ids, wts, eoff, poff, sorted, pos, tile_e, tile_r, ntiles, counts, a1, a1s, a2, a2s, a1sf, a2sf, y, dh,
-        dcnt, dtab, total;
+        dcnt, total;
     int64_t rows, tiles;
     int64_t dcnt_n;   // decode-path group counters (0: the step cannot take the decode path)
 };
@@ -105,9 +106,9 @@ constexpr int kDecodeAutoMaxTokens = 2;
 constexpr int64_t kColumnOrderMinExpertBytes = int64_t(16) << 20;
 
 // Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
-// rows per expert), a sort small enough for the one-launch prologue (which writes the decode
-// path's tile records and zeroes its counters), an expert's w13 under 2^31 bytes (the
-// kernels' 32-bit row offsets) and tile records that fit a CTA's shared memory.
+// rows per expert), a sort small enough for a CTA's shared memory (the decode kernel sorts the
+// pairs itself), an expert's w13 under 2^31 bytes (the kernels' 32-bit row offsets) and tile
+// records that fit a CTA's shared memory.
 bool decode_possible(int T, int H, int I, int topk) {
     const int64_t P = static_cast<int64_t>(T) * topk;
     return T > 0 && decode_cols(T) > 0 && P <= kSmallPairs && static_cast<int64_t>(2) * I * H < (int64_t(1) << 31) &&
@@ -116,6 +117,19 @@ bool decode_possible(int T, int H, int I, int topk) {
 bool use_decode(int T, int H, int I, int topk, int mode) {
     if (!decode_possible(T, H, I, topk) || mode == MOE_DECODE_OFF) return false;
     return mode == MOE_DECODE_ON || T <= kDecodeAutoMaxTokens;
+}
+// Copies of the token rows the decode prologue writes (into the a1 rows / a1s scales of the
+// layout): 16, as the rows allow
+int decode_x_copies(int T, int64_t rows) {
+    const int64_t c = (rows - kDecodeCols) / T;
+    return static_cast<int>(c < 1 ? 1 : (c > 16 ? 16 : c));
+}
+// Experts per lane with which the decode kernel routes the step in every CTA (the routing
+// kernel's register-resident selection, up to 8 per lane: E <= 256), 0 when the step takes the
+// routing kernel's ids instead
+int decode_route_v(int E, int n_group) {
+    const int v = reg_experts_per_lane(E, n_group);
+    return v >= 1 && v <= 8 ? v : 0;
 }
 
 ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
@@ -148,11 +162,11 @@ ForwardLayout forward_layout(int T, int H, int I, int E, int topk) {
     L.a1sf = take(mx_sf_bytes(L.rows, H));
     L.a2sf = take(mx_sf_bytes(L.rows, I));
     L.y = take(static_cast<size_t>(P) * H * 2);
-    // decode path: h = silu(gate) * up by pair [P, I] fp32, the counters and the tile records
+    // decode path: h = silu(gate) * up by pair [P, I] fp32 and the counters (the decode path's
+    // activations are copies of the token rows in a1 / a1s: decode_x_copies)
     L.dcnt_n = decode_possible(T, H, I, topk) ? decode_counters(static_cast<int>(L.tiles), I) : 0;
     L.dh = take(L.dcnt_n ? static_cast<size_t>(P) * I * 4 : 0);
     L.dcnt = take(static_cast<size_t>(L.dcnt_n) * 4);
-    L.dtab = take(L.dcnt_n ? static_cast<size_t>(L.tiles) * sizeof(DecodeTile) : 0);
     L.total = off;
     return L;
 }
@@ -544,12 +558,24 @@ int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, in
     return cuda_rc(launch_combine_pairs(y, pos, T, topk, H, out, static_cast<cudaStream_t>(stream)));
 }
 
-int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
+int moe_fp8_block_forward_kernel_count_ex(int T, int H, int I, int E, int topk, const moe_routing_params* rp,
+                                          const moe_forward_options* opts) {
     if (T < 0 || H <= 0 || I <= 0 || E < 1 || topk < 1) return -1;
     if (T == 0) return 0;
+    const int layout = opts ? opts->weight_layout : MOE_WEIGHTS_NK;
+    const int fmt = opts ? opts->scale_fmt : MOE_SCALE_F32;
+    const int mode = opts ? opts->decode_path : MOE_DECODE_AUTO;
+    // the decode path: its prologue, the decode kernel and the weighted sum, after the routing
+    // kernel when the decode kernel cannot route in every CTA
+    const int decode_step = decode_route_v(E, rp ? rp->n_group : 1) > 0 ? 3 : 4;
+    if (layout == MOE_WEIGHTS_NVFP4) return (T + kDecodeCols - 1) / kDecodeCols * decode_step;
+    if (sf_mode(fmt) == 0 && use_decode(T, H, I, topk, mode)) return decode_step;
     const int64_t P = static_cast<int64_t>(T) * topk;
-    if (use_decode(T, H, I, topk, MOE_DECODE_AUTO)) return 1 + 1 + 1 + 1;
     return 1 + (P <= kSmallPairs ? 1 : 4) + 2 + 1;
+}
+
+int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
+    return moe_fp8_block_forward_kernel_count_ex(T, H, I, E, topk, nullptr, nullptr);
 }
 
 int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode) {
@@ -676,29 +702,89 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
     const int scoring = rp ? rp->scoring : MOE_SCORING_SOFTMAX;
-    cudaError_t e = mark(0);
-    if (e == cudaSuccess)
-        e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, rp ? rp->n_group : 1,
-                                      rp ? rp->topk_group : 1, rp ? rp->routed_scaling : 1.0f,
-                                      rp ? rp->bias : nullptr, ids, wts, s);
-    if (e == cudaSuccess) e = mark(1);
-    // a small batch (decode) is sorted and quantised by one block in one launch (the
-    // quantisation stage is then empty); larger ones by the three sort kernels and the
-    // grid-wide quantiser
-    const bool small = P <= kSmallPairs;
+    const int n_group = rp ? rp->n_group : 1;
+    const int topk_group = rp ? rp->topk_group : 1;
+    const float routed_scaling = rp ? rp->routed_scaling : 1.0f;
+    const float* bias = rp ? rp->bias : nullptr;
     if (fp4 && !decode_possible(T, H, I, topk)) return MOE_ERR_UNSUPPORTED_SHAPE;
     const bool decode = fp4 || (!packed && use_decode(T, H, I, topk, decode_mode));
+    cudaError_t e = mark(0);
+    if (decode) {
+        // Up to 8 tokens: the decode prologue (counters zeroed, tokens quantised token-major),
+        // one kernel that routes and sorts the step in every CTA and runs both GEMMs with their
+        // epilogues (decode.cu), and the weighted k-way sum; the routing kernel runs first only
+        // for shapes the in-kernel selection does not take.  Stages: routing (that kernel or
+        // empty), sort (empty), quantisation (the prologue), w13 (the decode kernel), w2 (empty),
+        // the unpermute-sum.
+        const int route_v = decode_route_v(E, n_group);
+        if (e == cudaSuccess && route_v == 0)
+            e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, n_group, topk_group,
+                                  routed_scaling, bias, ids, wts, s);
+        if (e == cudaSuccess) e = mark(1);
+        if (e == cudaSuccess) e = mark(2);
+        const int x_copies = decode_x_copies(T, L.rows);
+        if (e == cudaSuccess)
+            e = launch_decode_prologue(hidden, T, H, x_copies, a1, a1s, reinterpret_cast<int32_t*>(ws + L.dcnt),
+                                       static_cast<int>(L.dcnt_n), scale_fmt, s);
+        if (e == cudaSuccess) e = mark(3);
+        DecodeMlpArgs d{};
+        d.w13 = w13;
+        d.w13_scale = w13_scale;
+        d.w2 = w2;
+        d.w2_scale = w2_scale;
+        d.w_tiled = weight_layout == MOE_WEIGHTS_TILED;
+        d.w_fp4 = fp4;
+        d.H = H;
+        d.I = I;
+        d.E = E;
+        d.T = T;
+        d.topk = topk;
+        d.route_v = route_v;
+        d.logits = router_logits;
+        d.bias = bias;
+        d.renormalize = renormalize;
+        d.scoring = scoring;
+        d.n_group = n_group;
+        d.topk_group = topk_group;
+        d.vec_loads = route_v >= 4 && E == 32 * route_v && aligned(router_logits, 16);
+        d.routed_scaling = routed_scaling;
+        d.ids = ids;
+        d.wts = wts;
+        d.pos = pos;
+        d.a1 = a1;
+        d.a1s = a1s;
+        d.x_copies = x_copies;
+        d.a2 = a2;
+        d.a2s = a2s;
+        d.rows = L.rows;
+        d.max_tiles = static_cast<int>(L.tiles);
+        d.cols = decode_cols(T);
+        d.h = reinterpret_cast<float*>(ws + L.dh);
+        d.counters = reinterpret_cast<int32_t*>(ws + L.dcnt);
+        d.scale_fmt = scale_fmt;
+        d.y = ypairs;
+        d.status = st->status;
+        if (e == cudaSuccess) e = launch_decode_mlp(d, st->num_sms, s);
+        if (e == cudaSuccess) e = mark(4);
+        if (e == cudaSuccess) e = mark(5);
+        if (e == cudaSuccess) e = launch_combine_pairs(ypairs, pos, T, topk, H, out, s);
+        if (e == cudaSuccess) e = mark(6);
+        return cuda_rc(e);
+    }
+    if (e == cudaSuccess)
+        e = launch_route_topk(router_logits, T, E, topk, renormalize, scoring, n_group, topk_group, routed_scaling,
+                              bias, ids, wts, s);
+    if (e == cudaSuccess) e = mark(1);
+    // a small batch is sorted and quantised by one block in one launch (the quantisation stage
+    // is then empty); larger ones by the three sort kernels and the grid-wide quantiser
+    const bool small = P <= kSmallPairs;
     uint8_t* a1sf = packed ? ws + L.a1sf : nullptr;
     uint8_t* a2sf = ws + L.a2sf;
-    int32_t* dcnt = reinterpret_cast<int32_t*>(ws + L.dcnt);
-    DecodeTile* dtab = reinterpret_cast<DecodeTile*>(ws + L.dtab);
-    DecodeSetup dsetup{};
-    if (decode) dsetup = DecodeSetup{dtab, wts, dcnt, static_cast<int>(L.dcnt_n)};
     if (e == cudaSuccess && small)
         e = launch_sort_quant_small(ids, static_cast<int>(P), E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                     reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
                                     st->status, hidden, T, H, topk, a1, H, packed ? nullptr : a1s, 1, L.rows,
-                                    scale_fmt, dsetup, s, a1sf);
+                                    scale_fmt, s, a1sf);
     if (e == cudaSuccess && !small)
         e = launch_align_permute(ids, P, E, MOE_BLOCK_M, reinterpret_cast<int32_t*>(ws + L.eoff),
                                  reinterpret_cast<int32_t*>(ws + L.poff), sorted, pos, tile_e, tile_r, ntiles,
@@ -711,39 +797,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         e = launch_group_quant(hidden, T, H, H, a1, H, packed ? nullptr : a1s, 1, L.rows, pos, topk, scale_fmt, s,
                                a1sf);
     if (e == cudaSuccess) e = mark(3);
-    if (decode) {
-        // up to 8 rows per expert: both GEMMs in one weight-streaming launch (decode.cu); the
-        // requantised intermediate goes to the a2 / a2s regions at the padded rows, as in the
-        // tile path.  Its time is recorded as the w13 stage (the w2 stage is empty).
-        DecodeMlpArgs d{};
-        d.w13 = w13;
-        d.w13_scale = w13_scale;
-        d.w2 = w2;
-        d.w2_scale = w2_scale;
-        d.w_tiled = weight_layout == MOE_WEIGHTS_TILED;
-        d.w_fp4 = fp4;
-        d.H = H;
-        d.I = I;
-        d.E = E;
-        d.a1 = a1;
-        d.a1s = a1s;
-        d.a2 = a2;
-        d.a2s = a2s;
-        d.rows = L.rows;
-        d.tiles = dtab;
-        d.num_tiles = ntiles;
-        d.max_tiles = static_cast<int>(L.tiles);
-        d.cols = decode_cols(T);
-        d.h = reinterpret_cast<float*>(ws + L.dh);
-        d.counters = dcnt;
-        d.scale_fmt = scale_fmt;
-        d.y = ypairs;
-        d.status = st->status;
-        if (e == cudaSuccess) e = launch_decode_mlp(d, st->num_sms, s);
-        if (e == cudaSuccess) e = mark(4);
-        if (e == cudaSuccess) e = mark(5);
-    }
-    if (e == cudaSuccess && !decode) {
+    if (e == cudaSuccess) {
         GemmArgs g{};
         g.a_box_rows = a_box_rows;
         g.A = a1;
@@ -783,7 +837,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         e = launch_grouped_gemm(g, st->num_sms, s);
         if (e == cudaSuccess) e = mark(4);
     }
-    if (e == cudaSuccess && !decode) {
+    if (e == cudaSuccess) {
         GemmArgs g{};
         g.a_box_rows = a_box_rows;
         g.A = a2;

@@ -1,5 +1,8 @@
-// Decode-regime expert MLP: both grouped block-FP8 GEMMs of the layer in one persistent
-// launch, for steps in which every expert holds at most 8 routed rows (up to 8 tokens).
+// Decode-regime expert MLP: the routing, the expert sort and both grouped block-FP8 GEMMs of
+// the layer in one persistent launch, for steps of up to 8 tokens (so every expert holds at
+// most 8 routed rows).  A small prologue kernel (prologue.cu) zeroes the counters and quantises
+// the tokens; it lets this kernel launch at once, and this kernel waits for it only before it
+// takes work.  The weighted k-way sum (moe_combine_pairs) follows as its own launch.
 //
 // The same products as the tile GEMMs (gemm.cu),
 //   C[r, n] = sum_kb a_scale[r, kb] * w_scale[e, n/128, kb] * sum_{k in kb} A[r, k] * W[e, n, k],
@@ -11,7 +14,17 @@
 // the tile GEMMs give a one-token DeepSeek-V3-shaped step only 128 w13 work items for 152
 // SMs (a w13 tile cannot be split further: its 1x128 requantisation groups need all 256 of
 // its gate and up rows), and the w2 launch cannot start streaming before the w13 launch has
-// drained.
+// drained.  For the same reason the steps before the GEMMs run inside this kernel: with separate
+// launches for routing and sort, a one-token step spent 18 us before its first weight load.
+//
+// Prologue of every CTA (before any weight load): warps 1..T each route one token with the
+// routing kernel's selection (route_select.cuh: the same choices, the same arithmetic); the
+// CTA sorts the T*topk pairs by (expert, pair) in shared memory into one tile record per
+// touched expert (expert, rows, their pairs and tokens), the small-batch sort's order.  The
+// fp64 router weights are formed afterwards by the same warps while the producer streams.
+// (Shapes whose scores do not fit the register-resident selection take the routing kernel's
+// ids and weights instead.)  CTA 0 writes the ids, the weights and each pair's row (-1 for a
+// dropped pair) for the k-way sum.
 //
 // Work items (tickets, taken in order from one counter by the CTAs' producers):
 //   first every w13 item: 16 gate rows [16u, 16u+16) and the matching 16 up rows [I+16u, ...)
@@ -27,8 +40,10 @@
 // Roles of a CTA (one per SM, 384 threads):
 //   warp 0      producer: per group of 16 K blocks of an item, TMA loads of its weight rows
 //               over the 16 blocks (w13: two boxes of 16 rows, 32 KB each; w2: one box of 32
-//               rows, 64 KB) and of the expert's activation rows over them (a box of 1, 2, 4
-//               or 8 rows, the fewest that hold the item's rows) into a ring of 2-3 stages, and
+//               rows, 64 KB) and of the activation rows over them (w13: the step's token rows,
+//               from one of the prologue's copies of them, so that the CTAs' reads of these few
+//               lines spread over L2; w2: the tile's rows of the intermediate; a box of 1, 2, 4
+//               or 8 rows, the fewest that hold them) into a ring of 2-4 stages, and
 //               the blocks' weight-block and activation scales by cp.async, all completing
 //               on the stage's mbarrier.  The ring runs on across items and across the two
 //               GEMMs.  (On GB300 an SM streams at the HBM share only with large boxes: a
@@ -45,8 +60,9 @@
 //   warps 9..11 epilogue: add the eight partial sums in warp order (deterministic) and
 //               finish the item while the MMA warps stream the next ones.
 // The k order inside an MMA is free as long as A and B agree: lane (g, t) gives bytes
-// 16t..16t+7 (and 64+16t..) of weight rows g and g+8 and of activation row g to one MMA
-// and bytes 16t+8..16t+15 to the next, so all lanes with the same t hold the same K.
+// 16t..16t+7 (and 64+16t..) of weight rows g and g+8 and of the tile's activation row g (w13:
+// the row of its token) to one MMA and bytes 16t+8..16t+15 to the next, so all lanes with the
+// same t hold the same K.
 //
 // w13 epilogue: h = silu(gate) * up in fp32 for the item's 16 columns, stored to an fp32
 // buffer by routed pair.  The eight items of a 1x128 requantisation group count their
@@ -54,12 +70,15 @@
 // the item that completes the group re-reads the group's 128 values, requantises them
 // (amax/448, e4m3 codes) into the expert's padded rows, as the tile GEMM's fused epilogue
 // does, and counts the group on the tile's ready counter.  No w13 item waits for another.
-// w2 epilogue: bf16(router weight * C) to the pair's row of the [T*topk, H] buffer that
-// the k-way sum (moe_combine_pairs) reads, as the tile GEMM's pairs epilogue.
-// The counters and the ticket are zeroed by the expert sort of the same call.  Every wait
+// w2 epilogue: bf16(router weight * C) to the pair's row of the [T*topk, H] buffer that the
+// k-way sum (moe_combine_pairs) reads, as the tile GEMM's pairs epilogue.  (Forming the sum here
+// -- the item that completes 32 output columns adds them up -- took 13 us more on a one-token
+// step: the count's release and round trip on every short w2 item held up the epilogue.)
+// The counters and the ticket are zeroed by the decode prologue of the same call.  Every wait
 // is bounded (mbar_wait, wait_count); on expiry the CTA records MOE_STATUS_WAIT_TIMEOUT,
 // lets its loads in flight land and exits.
 #include "kernels.cuh"
+#include "route_select.cuh"
 
 namespace mfp8 {
 
@@ -80,6 +99,17 @@ constexpr int kWeightBytes4 = 2 * kTileBytes4;
 constexpr int kStageScales = 2 * kGroupKB + kCols * kGroupKB;   // [tile][kb] weight scales, [kb][row] activation scales
 constexpr int kGroupItems = 128 / 16;           // w13 items per 1x128 group of the intermediate
 constexpr int kRedBufs = 2;                     // items whose partial sums await the epilogue
+constexpr int kTileRows = 128;                  // padded rows per expert tile in a2 (MOE_BLOCK_M)
+
+// Per-expert-tile record of a decode step, built by every CTA in shared memory: the tile's expert,
+// its first padded row (m * 128), its routed rows and, for row j < cnt, the pair index, its token
+// and its router weight (-1, 0, 0 from cnt on).
+struct DecodeTile {
+    int32_t e, poff, cnt, pad;   // pad: set once the tile's intermediate was seen complete
+    int32_t pair[kCols];
+    int32_t tok[kCols];
+    float weight[kCols];
+};
 
 struct Ctl {
     uint64_t full[kMaxStages];                  // a stage landed (1 + 32 arrivals, tx bytes)
@@ -88,15 +118,18 @@ struct Ctl {
     uint64_t red_empty[kRedBufs];               // the epilogue has read them (4 arrivals)
     int abort_flag;
     int last;
+    int ntiles;                                 // tiles of the step (touched experts)
     int stage_item[kMaxStages];                 // the stage's item (ticket), -1: no more work
     int stage_grp[kMaxStages];                  // its group of K blocks
     int stage_rows[kMaxStages];                 // activation rows it holds (1, 2, 4 or 8)
+    uint32_t stage_tok[kMaxStages];             // w13: B column j reads stage row (tok >> 4j) & 15 (j < cnt)
+    int stage_cnt[kMaxStages];                  // the tile's routed rows
     int red_item[kRedBufs];                     // the reduction buffer's item, -1: no more work
     alignas(16) float scl[kMaxStages][kStageScales];
     alignas(16) float red[kRedBufs][kMmaWarps][2][32][4];
 };
 // shared memory: alignment slack, the control block, the ring (stages x stage bytes: a stage's
-// weights, then its activation rows), the step's tile records
+// weights, then its activation rows), the step's tile records, the sort's three ints per pair
 constexpr size_t kCtlBytes = (sizeof(Ctl) + 1023) / 1024 * 1024;
 constexpr size_t kSmemLimit = 232448;
 // a stage holds up to `cols` activation rows in a box of the next power of two rows
@@ -105,9 +138,9 @@ size_t stage_bytes(int cols, bool fp4 = false) {
     while (r < cols) r <<= 1;
     return ((fp4 ? kWeightBytes4 : kWeightBytes) + static_cast<size_t>(r) * 128 * kGroupKB + 1023) / 1024 * 1024;
 }
-size_t smem_bytes(int max_tiles, int stages, int cols, bool fp4 = false) {
+size_t smem_bytes(int max_tiles, int stages, int cols, int pairs, bool fp4 = false) {
     return 1024 + kCtlBytes + static_cast<size_t>(stages) * stage_bytes(cols, fp4) +
-           static_cast<size_t>(max_tiles) * sizeof(DecodeTile);
+           static_cast<size_t>(max_tiles) * sizeof(DecodeTile) + static_cast<size_t>(pairs) * 3 * sizeof(int);
 }
 
 __device__ __forceinline__ uint32_t word(const uint4& v, int i) {
@@ -234,9 +267,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int I = a.I;
     const int GPT = I / 128;                     // 1x128 groups of the intermediate per expert tile
+    const int P = a.T * a.topk;                  // routed pairs of the step
     int32_t* group_count = a.counters;           // [max_tiles][I/128]
     int32_t* ready = a.counters + static_cast<int64_t>(a.max_tiles) * GPT;   // [max_tiles]
     int32_t* ticket = ready + a.max_tiles;
+    int* s_ids = reinterpret_cast<int*>(tab + a.max_tiles);   // [P] chosen expert of pair p
+    int* s_rank = s_ids + P;                     // [P] row of pair p in its tile (-1: dropped)
+    int* s_slot = s_rank + P;                    // [P] tile << 8 | row (-1: dropped)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -248,32 +285,136 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&ctl->red_empty[b]), kEpiWarps);
         }
         ctl->abort_flag = 0;
+        ctl->ntiles = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmW13);
         tma_prefetch_map(&tmW2);
     }
-    // the set-up above overlaps the previous kernel's tail; its outputs are read from here on
-    grid_dependency_wait();
-    // the step's tile records, all of them in one load (no item looks anything up in global memory)
-    {
-        const int4* src = reinterpret_cast<const int4*>(a.tiles);
-        int4* dst = reinterpret_cast<int4*>(tab);
-        const int n = a.max_tiles * static_cast<int>(sizeof(DecodeTile) / sizeof(int4));
-        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+    // The step's routing, in every CTA while the decode prologue still runs: warps 1..T take
+    // token warp - 1 with the routing kernel's selection (route_select.cuh).  The scores are the
+    // caller's input, complete before the prologue let this grid launch.  Without in-kernel
+    // routing (route_v == 0) the routing kernel's ids are read once the earlier grids are done.
+    const bool route_here = a.route_v > 0;
+    const bool router = route_here && warp >= 1 && warp <= a.T;
+    const bool sigmoid = a.scoring == MOE_SCORING_SIGMOID;
+    const float* lrow = a.logits + static_cast<int64_t>(warp >= 1 ? warp - 1 : 0) * a.E;
+    int my_id = -1;
+    double zall = 0.0;
+    if (router) {
+        switch (a.route_v) {
+            case 1:
+                my_id = route_token_reg<1>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                                           a.vec_loads != 0, lane, &zall);
+                break;
+            case 2:
+                my_id = route_token_reg<2>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                                           a.vec_loads != 0, lane, &zall);
+                break;
+            case 4:
+                my_id = route_token_reg<4>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                                           a.vec_loads != 0, lane, &zall);
+                break;
+            default:
+                my_id = route_token_reg<8>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                                           a.vec_loads != 0, lane, &zall);
+                break;
+        }
+        if (lane < a.topk) s_ids[(warp - 1) * a.topk + lane] = my_id;
     }
-    int64_t ntiles = *a.num_tiles;
-    if (ntiles < 0) ntiles = 0;
+    if (!route_here) {
+        grid_dependency_wait();
+        for (int p = threadIdx.x; p < P; p += blockDim.x) s_ids[p] = __ldcg(a.ids + p);
+    }
+    __syncthreads();
+    // The expert sort, in shared memory: pair p's row is the number of earlier pairs with its
+    // expert (a stable order by (expert, pair)); one tile per touched expert, in expert order, at
+    // padded row m * 128 of the intermediate -- the small-batch sort's layout.  An id out of range
+    // drops its pair and is reported.
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int id = s_ids[p];
+        int rank = -1;
+        if (id >= 0 && id < a.E) {
+            rank = 0;
+            for (int o = 0; o < p; ++o) rank += s_ids[o] == id ? 1 : 0;
+            if (rank == 0) atomicAdd(&ctl->ntiles, 1);
+        } else {
+            status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+        }
+        s_rank[p] = rank;
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int id = s_ids[p], rank = s_rank[p];
+        int slot = -1;
+        if (rank >= 0) {
+            int m = 0, cnt = 0;
+            for (int o = 0; o < P; ++o) {
+                m += (s_rank[o] == 0 && s_ids[o] < id) ? 1 : 0;
+                cnt += s_ids[o] == id ? 1 : 0;
+            }
+            if (m < a.max_tiles) {
+                // (an expert with more rows than the kernel takes is reported by the epilogue)
+                if (rank < kCols) slot = (m << 8) | rank;
+                if (rank == 0) {
+                    DecodeTile& d = tab[m];
+                    d.e = id;
+                    d.poff = m * kTileRows;
+                    d.cnt = cnt;
+                    d.pad = 0;
+                    for (int j = cnt; j < kCols; ++j) {
+                        d.pair[j] = -1;
+                        d.tok[j] = 0;
+                        d.weight[j] = 0.0f;
+                    }
+                }
+            }
+        }
+        s_slot[p] = slot;
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+        const int slot = s_slot[p];
+        if (slot < 0) continue;
+        DecodeTile& d = tab[slot >> 8];
+        d.pair[slot & 255] = p;
+        d.tok[slot & 255] = p / a.topk;
+        d.weight[slot & 255] = route_here ? 0.0f : __ldcg(a.wts + p);
+    }
+    __syncthreads();
+    // the decode prologue's outputs (zeroed counters, quantised tokens) from here on
+    if (route_here) grid_dependency_wait();
+    if (blockIdx.x == 0)
+        for (int p = threadIdx.x; p < P; p += blockDim.x) {
+            const int slot = s_slot[p];
+            a.pos[p] = slot < 0 ? -1 : (slot >> 8) * kTileRows + (slot & 255);
+        }
+    int64_t ntiles = ctl->ntiles;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const Gemm G1 = gemm_of(a, false), G2 = gemm_of(a, true);
     const int total1 = static_cast<int>(ntiles * G1.per_tile);
     const int total = total1 + static_cast<int>(ntiles * G2.per_tile);
     volatile int* abort_flag = &ctl->abort_flag;
-    __syncthreads();
+    if (router) {
+        // the router weights in fp64 (as the routing kernel forms them), off the producer's path:
+        // the epilogue reads them for w2 items, after every MMA warp has passed its reduction
+        // barrier at least once
+        const float wgt = route_weight_warp(lrow, my_id, a.topk, a.renormalize, sigmoid, zall, a.routed_scaling, lane);
+        if (lane < a.topk) {
+            const int p = (warp - 1) * a.topk + lane;
+            const int slot = s_slot[p];
+            if (slot >= 0) tab[slot >> 8].weight[slot & 255] = wgt;
+            if (blockIdx.x == 0) {
+                a.ids[p] = my_id;
+                a.wts[p] = wgt;
+            }
+        }
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
+        const int xcopy = static_cast<int>(blockIdx.x) % a.x_copies;   // this CTA's copy of the token rows
         uint32_t q = 0;
         bool ok = true;
         // tickets are taken two items ahead: an atomic's round trip is longer than a w2 item's issue
@@ -313,10 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* wsc = second ? a.w2_scale : a.w13_scale;
             const float* ws[2] = {wsc + (static_cast<int64_t>(e) * NB + row0 / 128) * G.KB,
                                   wsc + (static_cast<int64_t>(e) * NB + row1 / 128) * G.KB};
-            const float* xsc = second ? a.a2s : a.a1s;
-            // activation rows: the item's rows rounded up to a power of two (zero-row records of
-            // invalid tiles load one row)
-            int cnt = tab[m].cnt;
+            // activation scales of K block kb: w13 [copy][kb][token] (ld kCols), w2 [kb][padded row]
+            const float* xsc = second ? a.a2s + poff : a.a1s + static_cast<int64_t>(xcopy) * (a.H / 128) * kCols;
+            const int64_t xs_ld = second ? a.rows : kCols;
+            uint32_t tokmap = 0;
+            if (!second)
+                for (int j = 0; j < kCols; ++j) tokmap |= static_cast<uint32_t>(tab[m].tok[j] & 15) << (4 * j);
+            // activation rows: w13 the step's T token rows, w2 the tile's rows of the intermediate,
+            // rounded up to a power of two
+            int cnt = second ? tab[m].cnt : a.T;
             cnt = cnt < 1 ? 1 : (cnt > a.cols ? a.cols : cnt);
             const int lg = cnt <= 1 ? 0 : cnt <= 2 ? 1 : cnt <= 4 ? 2 : 3;
             const CUtensorMap* tmA = &tmX.m[second ? 1 : 0][lg];
@@ -339,6 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ctl->stage_item[stage] = item;
                     ctl->stage_grp[stage] = grp;
                     ctl->stage_rows[stage] = 1 << lg;
+                    ctl->stage_tok[stage] = tokmap;
+                    ctl->stage_cnt[stage] = tab[m].cnt;
                     // K blocks past K are out of the tensor: zero-filled (and counted), and skipped
                     // by the MMA warps
                     mbar_arrive_expect_tx(fb, stage_tx);
@@ -379,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the activation rows of the stage's K blocks (after a failed wait the load still
                 // goes out, so that the stage's phase completes and the drain below can wait for
                 // it; the status word marks the outputs invalid)
-                if (lane == 0) tma_load_3d(dst + kWB, tmA, 0, kb0, poff, fb);
+                if (lane == 0) tma_load_3d(dst + kWB, tmA, 0, kb0, second ? poff : xcopy * a.T, fb);
                 if constexpr (FP4) {
                     // the expert's 1 / global_scale (the block scales came with the codes)
                     if (lane == 0) cp_async_4(smem_addr(&ctl->scl[stage][0]), wsc + e);
@@ -395,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int kbi = lane >> 1, c = lane & 1, kb = kb0 + kbi;
                     if (kbi < G.GKB && kb < G.KB)
                         cp_async_16(smem_addr(&ctl->scl[stage][2 * kGroupKB + kbi * kCols + 4 * c]),
-                                    xsc + static_cast<int64_t>(kb) * a.rows + poff + 4 * c);
+                                    xsc + static_cast<int64_t>(kb) * xs_ld + 4 * c);
                 }
                 cp_async_arrive(fb);
                 if (!got) {
@@ -445,6 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Gemm& G = second ? G2 : G1;
             const uint8_t* st = ring + static_cast<size_t>(stage) * SB;
             const int xr = ctl->stage_rows[stage];
+            // B column g is the tile's row g: for w13 the row of its token among the stage's token
+            // rows (columns past the tile's rows are zero, their results never read), for w2 row g
+            const uint32_t tokmap = ctl->stage_tok[stage];
+            const int xrow = second ? g : static_cast<int>((tokmap >> (4 * g)) & 15u);
+            const bool xlive = second ? g < xr : g < ctl->stage_cnt[stage];
+            const int sc0 = second ? 2 * t : static_cast<int>((tokmap >> (8 * t)) & 15u);
+            const int sc1 = second ? 2 * t + 1 : static_cast<int>((tokmap >> (8 * t + 4)) & 15u);
             if constexpr (FP4) {
                 // this warp's K blocks of the stage, cw and cw + 8.  Lane (g, t) feeds K positions
                 // [32t, 32t + 32) of a block (any K order works when A and B agree): MMA j takes
@@ -472,11 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        xq[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWB + (g * G.GKB + kbi) * 128 +
-                                                                               32 * t + 16 * c)
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
-                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                        xq[half][c] = xlive ? *reinterpret_cast<const uint4*>(st + kWB + (xrow * G.GKB + kbi) * 128 +
+                                                                              32 * t + 16 * c)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + sc0];
+                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + sc1];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
@@ -567,17 +722,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < 2; ++c)
                                 wv[half][tile][hr][c] = *reinterpret_cast<const uint4*>(rp + 16 * ((4 * c + t) ^ x));
                         }
-                    // the stage holds xr activation rows: B columns past them are zero (their results
-                    // are never read)
     #pragma unroll
                     for (int c = 0; c < 2; ++c)
-                        xv[half][c] = g < xr ? *reinterpret_cast<const uint4*>(st + kWB +
-                                                                               (g * G.GKB + kbi) * 128 + 64 * c + 16 * t)
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                        xv[half][c] = xlive ? *reinterpret_cast<const uint4*>(st + kWB + (xrow * G.GKB + kbi) * 128 +
+                                                                              64 * c + 16 * t)
+                                            : make_uint4(0u, 0u, 0u, 0u);
                     ws[half][0] = ctl->scl[stage][kbi];
                     ws[half][1] = ctl->scl[stage][kGroupKB + kbi];
-                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t];
-                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + 2 * t + 1];
+                    xa[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + sc0];
+                    xb[half] = ctl->scl[stage][2 * kGroupKB + kbi * kCols + sc1];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[stage]));
@@ -723,8 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 int decode_cols(int T) { return T >= 1 && T <= kCols ? T : 0; }
 
 size_t decode_max_tiles() {
-    // room for two stages of 8 activation rows
-    return (kSmemLimit - smem_bytes(0, 2, kCols)) / sizeof(DecodeTile);
+    // room for two stages of 8 activation rows and the sort of the most pairs a step can have
+    return (kSmemLimit - smem_bytes(0, 2, kCols, kSmallPairs)) / sizeof(DecodeTile);
 }
 
 int64_t decode_counters(int max_tiles, int I) { return static_cast<int64_t>(max_tiles) * (I / 128 + 1) + 1; }
@@ -787,15 +940,20 @@ cudaError_t act_map(CUtensorMap* map, const uint8_t* x, int64_t rows, int K, uin
 cudaError_t launch_decode_mlp(const DecodeMlpArgs& args, int num_sms, cudaStream_t stream) {
     if (args.max_tiles <= 0) return cudaSuccess;
     if (args.cols < 1 || args.cols > kCols || args.H % 128 != 0 || args.I % 128 != 0) return cudaErrorInvalidValue;
+    if (args.T < 1 || args.T > kCols || args.topk < 1 || args.T * args.topk > kSmallPairs) return cudaErrorInvalidValue;
+    if (args.route_v != 0 && args.route_v != 1 && args.route_v != 2 && args.route_v != 4 && args.route_v != 8)
+        return cudaErrorInvalidValue;
+    if (args.x_copies < 1 || static_cast<int64_t>(args.x_copies) * args.T + kCols > args.rows) return cudaErrorInvalidValue;
     DecodeMlpArgs a = args;
     // as many ring stages as fit next to the control block and the tile records
     const bool fp4 = a.w_fp4 != 0;
     a.stage_bytes = static_cast<int>(stage_bytes(a.cols, fp4));
-    const size_t fixed = smem_bytes(a.max_tiles, 0, a.cols, fp4);
+    const int pairs = a.T * a.topk;
+    const size_t fixed = smem_bytes(a.max_tiles, 0, a.cols, pairs, fp4);
     if (fixed + 2 * static_cast<size_t>(a.stage_bytes) > kSmemLimit) return cudaErrorInvalidValue;
     a.stages = static_cast<int>((kSmemLimit - fixed) / a.stage_bytes);
     if (a.stages > kMaxStages) a.stages = kMaxStages;
-    const size_t smem = smem_bytes(a.max_tiles, a.stages, a.cols, fp4);
+    const size_t smem = smem_bytes(a.max_tiles, a.stages, a.cols, pairs, fp4);
     CUtensorMap tmW13, tmW2;
     cudaError_t err;
     if (fp4) {

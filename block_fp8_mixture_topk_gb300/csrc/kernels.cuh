@@ -42,33 +42,22 @@ cudaError_t launch_align_permute(const int32_t* ids, int64_t P, int E, int block
                                  int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles,
                                  int32_t* chunk_counts, uint32_t* status, cudaStream_t stream);
 
-// Per-expert-tile record of a decode step (at most kDecodeCols rows per expert, so one tile per
-// expert), written by the small-batch sort and read by the decode-path GEMMs: the tile's
-// expert, its first padded row, its routed rows and, for row j < cnt, the pair index and its
-// router weight (-1 and 0 from cnt on).
+// The most routed rows per expert the decode-path kernel takes (a step of at most 8 tokens).
 constexpr int kDecodeCols = 8;
-struct DecodeTile {
-    int32_t e, poff, cnt, pad;   // pad: zero (the decode kernel marks tiles it has seen ready in its own copy)
-    int32_t pair[kDecodeCols];
-    float weight[kDecodeCols];
-};
-// What the small-batch sort also writes for the decode path (tiles == nullptr: nothing).
-struct DecodeSetup {
-    DecodeTile* tiles;           // [max_tiles]
-    const float* topk_weights;   // [P]
-    int32_t* counters;           // zeroed: the decode kernel's counters
-    int ncounters;
-};
 
-// prologue.cu: expert sort + scattering quantisation of a small batch in one launch, and the
-// decode path's tile records
+// prologue.cu: expert sort + scattering quantisation of a small batch in one launch
 constexpr int kSmallPairs = 512;   // routed pairs the one-block path takes
 cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_m, int32_t* expert_offsets,
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec, cudaStream_t stream,
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream,
                                     uint8_t* sf = nullptr);
+// prologue.cu: the decode path's prologue (1 <= T <= kDecodeCols): counters[0, ncounters) zeroed,
+// the T tokens' 1x128 groups quantised into `copies` copies of token-major rows q [copy][T][H] and
+// scales s [copy][H/128][kDecodeCols]; lets the decode kernel launch before it ends
+cudaError_t launch_decode_prologue(const uint16_t* x, int T, int H, int copies, uint8_t* q, float* s,
+                                   int32_t* counters, int ncounters, int scale_fmt, cudaStream_t stream);
 
 // masked.cu: row maps and tile table of the masked batched layout [E, M, H] (Mp = M rounded
 // up to 128): row_map [E*Mp] (input row or -1), pos [E*M] (padded row or -1), ones [E*M]
@@ -184,14 +173,23 @@ struct DecodeMlpArgs {
     int w_tiled;
     int w_fp4;                 // NVFP4 weights in the packed layout of nvfp4.cu
     int H, I, E;
-    const uint8_t* a1;         // activation codes [rows, H]: a tile's j-th row at padded row poff + j
-    const float* a1s;          // their scales [H/128][rows]
-    uint8_t* a2;               // requantised intermediate [rows, I] at the same rows (written here)
+    // the step's routing: T tokens, topk pairs each (pair p = t * topk + j)
+    int T, topk;
+    int route_v;               // experts per lane of the in-kernel routing (1, 2, 4, 8), 0: ids / wts are inputs
+    const float* logits;       // [T, E] router logits (route_v > 0)
+    const float* bias;         // [E] selection bias or null
+    int renormalize, scoring, n_group, topk_group, vec_loads;
+    float routed_scaling;
+    int32_t* ids;              // [P] chosen experts: written by CTA 0 (route_v > 0) or read
+    float* wts;                // [P] router weights: likewise
+    int32_t* pos;              // [P] written by CTA 0: the pair's padded row, -1 for a dropped pair
+    const uint8_t* a1;         // activation codes: x_copies copies of the T token rows [copy][T][H]
+    const float* a1s;          // their scales [copy][H/128][kDecodeCols] (the decode prologue's)
+    int x_copies;
+    uint8_t* a2;               // requantised intermediate [rows, I]: tile m's j-th row at padded row m*128 + j
     float* a2s;                // its scales [I/128][rows]
     int64_t rows;
-    const DecodeTile* tiles;   // [max_tiles] (the small-batch sort's records)
-    const int32_t* num_tiles;
-    int max_tiles;
+    int max_tiles;             // >= the step's tiles (one per touched expert)
     int cols;                  // the most routed rows an expert can hold, 1..8 (decode_cols: T)
     float* h;                  // h = silu(gate) * up [P, I] fp32 by pair
     int32_t* counters;         // decode_counters(max_tiles, I) ints, zero on entry

@@ -11,10 +11,9 @@
 // same, element for element: per-expert counts, exclusive scans, the stable order by
 // (expert, pair) -- a pair's rank is the number of earlier pairs with its expert,
 // counted, so no atomics -- the tile table, and the codes and scales.  In a decode step
-// this removes three launches and the gaps between them.  For the decode-path GEMMs it also
-// writes one record per expert tile (expert, first row, rows, their pairs and router
-// weights), so that those kernels read everything about a tile in one load, and zeroes their
-// group counters.
+// this removes three launches and the gaps between them.
+//
+// decode_prologue_kernel is the decode path's own prologue (below).
 #include "kernels.cuh"
 
 namespace mfp8 {
@@ -26,8 +25,8 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row0, int32_t* __restrict__ num_tiles,
     uint32_t* status, const uint16_t* __restrict__ x, int T, int H, int topk, uint8_t* __restrict__ q,
-    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec,
-    uint8_t* __restrict__ sf, int sf_kb4) {
+    int64_t q_ld, float* __restrict__ s, int64_t s_rs, int64_t s_gs, int scale_fmt, uint8_t* __restrict__ sf,
+    int sf_kb4) {
     grid_dependency_wait();
     __shared__ int s_id[kSmallPairs];
     __shared__ int s_pos[kSmallPairs];
@@ -54,8 +53,6 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     const int off = block_exclusive_scan(total, warp_sums);
     const int poff = block_exclusive_scan(padded, warp_sums);
     const bool writer = blockIdx.x == 0;
-    if (writer)
-        for (int i = tid; i < dec.ncounters; i += blockDim.x) dec.counters[i] = 0;
     if (tid < E) s_poff[tid] = poff;
     if (writer && tid < E) {
         expert_offsets[tid] = off;
@@ -70,18 +67,6 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
             tile_row0[i] = i * block_m;
         }
         for (int r = poff + total; r < poff + padded; ++r) sorted_pair_ids[r] = -1;
-        if (dec.tiles && total > 0) {
-            // the decode path takes at most kDecodeCols rows per expert: one tile each
-            DecodeTile& dt = dec.tiles[poff / block_m];
-            dt.e = tid;
-            dt.poff = poff;
-            dt.cnt = total;
-            dt.pad = 0;
-            for (int j = total; j < kDecodeCols; ++j) {
-                dt.pair[j] = -1;
-                dt.weight[j] = 0.0f;
-            }
-        }
     }
     __syncthreads();
 
@@ -94,11 +79,6 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
             for (int o = 0; o < p; ++o) before += s_id[o] == id ? 1 : 0;
             r = s_poff[id] + before;
             if (writer) sorted_pair_ids[r] = p;
-            if (writer && dec.tiles && before < kDecodeCols) {
-                DecodeTile& dt = dec.tiles[s_poff[id] / block_m];
-                dt.pair[before] = p;
-                dt.weight[before] = dec.topk_weights[p];
-            }
         }
         if (writer) pos[p] = r;
         s_pos[p] = r;
@@ -146,14 +126,70 @@ __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     }
 }
 
+// The decode path's prologue: zeroes the decode kernel's counters and quantises the step's T
+// tokens in 1x128 groups (section Fp8Config; kFp8Dynamic128Sym) into `copies` copies of
+// token-major rows q [copy][T][H] with their scales s [copy][H/128][kDecodeCols]
+// (s[(copy * H/128 + g) * kDecodeCols + t]); 16 threads per group, as the small sort's quantiser.
+// Every CTA of the decode kernel reads these few rows; the copies spread those reads over L2.
+// Right after its own dependency wait it lets the decode kernel launch: that kernel routes and
+// sorts the step's tokens itself in every CTA meanwhile, and waits for this grid only before it
+// takes work.
+__global__ void __launch_bounds__(1024) decode_prologue_kernel(const uint16_t* __restrict__ x, int T, int H,
+                                                               int copies, uint8_t* __restrict__ q,
+                                                               float* __restrict__ s, int32_t* __restrict__ counters,
+                                                               int ncounters, int scale_fmt) {
+    grid_dependency_wait();
+    grid_dependency_trigger();
+    const int tid = threadIdx.x;
+    if (blockIdx.x == 0)
+        for (int i = tid; i < ncounters; i += blockDim.x) counters[i] = 0;
+    const int G = H / 128;
+    const int half = (tid >> 4) & 1, sub = tid & 15;
+    const int per_pass = (blockDim.x >> 5) * 2;   // groups per block and pass
+    for (int gi0 = blockIdx.x * per_pass + (tid >> 5) * 2; gi0 < T * G; gi0 += gridDim.x * per_pass) {
+        const int gi = gi0 + half;
+        const bool active = gi < T * G;
+        float f[8];
+        float amax = 0.0f;
+        int t = 0, g = 0;
+        if (active) {
+            t = gi / G;
+            g = gi - t * G;
+            unpack8(__ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + g * 128 + sub * 8)), f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (active) {
+            const float sc = group_scale_fmt(amax, scale_fmt);
+            const uint2 code = encode8(f, sc, __frcp_rn(sc));
+            for (int c = 0; c < copies; ++c) {
+                *reinterpret_cast<uint2*>(q + (static_cast<int64_t>(c) * T + t) * H + g * 128 + sub * 8) = code;
+                if (sub == 0) s[(static_cast<int64_t>(c) * G + g) * kDecodeCols + t] = sc;
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_prologue(const uint16_t* x, int T, int H, int copies, uint8_t* q, float* s,
+                                   int32_t* counters, int ncounters, int scale_fmt, cudaStream_t stream) {
+    if (T < 1 || T > kDecodeCols || H % 128 != 0 || copies < 1) return cudaErrorInvalidValue;
+    int blocks = (T * (H / 128) + 63) / 64;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 148) blocks = 148;
+    return launch_pdl(decode_prologue_kernel, dim3(blocks), dim3(1024), 0, stream, x, T, H, copies, q, s, counters,
+                      ncounters, scale_fmt);
+}
 
 cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_m, int32_t* expert_offsets,
                                     int32_t* padded_offsets, int32_t* sorted_pair_ids, int32_t* pos,
                                     int32_t* tile_expert, int32_t* tile_row0, int32_t* num_tiles, uint32_t* status,
                                     const uint16_t* x, int T, int H, int topk, uint8_t* q, int64_t q_ld, float* s,
-                                    int64_t s_rs, int64_t s_gs, int scale_fmt, DecodeSetup dec,
-                                    cudaStream_t stream, uint8_t* sf) {
+                                    int64_t s_rs, int64_t s_gs, int scale_fmt, cudaStream_t stream,
+                                    uint8_t* sf) {
     const int groups = T * (H / 128);
     int blocks = (groups + 63) / 64;
     if (blocks < 1) blocks = 1;
@@ -161,7 +197,7 @@ cudaError_t launch_sort_quant_small(const int32_t* ids, int P, int E, int block_
     return launch_pdl(sort_quant_small_kernel, dim3(blocks), dim3(1024), 0, stream, ids, P, E, block_m, expert_offsets,
                       padded_offsets, sorted_pair_ids, pos, tile_expert, tile_row0, num_tiles, status, x, T, H, topk,
                       q, q_ld, s, s_rs, s_gs,
-                      scale_fmt == MOE_SCALE_MXFP8 ? MOE_SCALE_MXFP8 : (sf ? MOE_SCALE_UE8M0 : scale_fmt), dec, sf,
+                      scale_fmt == MOE_SCALE_MXFP8 ? MOE_SCALE_MXFP8 : (sf ? MOE_SCALE_UE8M0 : scale_fmt), sf,
                       scale_fmt == MOE_SCALE_MXFP8 ? H / 128 : (H / 128 + 3) / 4);
 }
 

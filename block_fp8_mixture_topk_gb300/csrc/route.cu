@@ -9,36 +9,16 @@
 // scores are defined as fp64 sigmoids rounded to fp32; the selection first runs on
 // fp32 sigmoids and keeps the result when every decision clears the fp32 error
 // (nearly always), else repeats the token on the exact scores.  Weights are formed
-// in fp64 from the exact scores of the chosen experts and rounded to fp32.
+// in fp64 from the exact scores of the chosen experts and rounded to fp32.  The register-
+// resident selection (route_select.cuh) is shared with the decode-path kernel.
 #include "kernels.cuh"
+#include "route_select.cuh"
 
 namespace mfp8 {
 
 namespace {
 
 constexpr int kWarps = 4;
-
-struct Cand {
-    float v;
-    int idx;  // INT32_MAX when empty
-};
-
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-    if (a.idx == INT32_MAX) return false;
-    if (b.idx == INT32_MAX) return true;
-    return a.v > b.v || (a.v == b.v && a.idx < b.idx);
-}
-
-__device__ __forceinline__ Cand warp_argmax(Cand c) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Cand other;
-        other.v = __shfl_xor_sync(0xffffffffu, c.v, o);
-        other.idx = __shfl_xor_sync(0xffffffffu, c.idx, o);
-        if (better(other, c)) c = other;
-    }
-    return c;
-}
 
 // Chooses the experts from the scores sel[0..E) (shared memory): with n_group > 1,
 // the topk_group groups with the largest sum of their two best scores are kept
@@ -113,11 +93,6 @@ __device__ int select_experts(const float* sel, int E, int topk, int n_group, in
     return my_id;
 }
 
-// Sigmoid score of a logit as the layer defines it: evaluated in fp64, rounded to fp32.
-__device__ __forceinline__ float sigmoid_exact(float l) {
-    return static_cast<float>(1.0 / (1.0 + exp(-static_cast<double>(l))));
-}
-
 __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int T, int E, int topk, int renormalize, int scoring, int n_group,
     int topk_group, float routed_scaling, const float* __restrict__ bias, int32_t* __restrict__ ids,
@@ -183,144 +158,6 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_kernel(
     }
 }
 
-// ---------------------------------------------------------------- register-resident variant
-// The same routing with each lane holding V consecutive experts (e = lane*V + v) in
-// registers: for E <= 32*V and groups that are whole runs of lanes (n_group == 1, or a
-// group's G = E/n_group experts a multiple of V spanning a power-of-two number of lanes).
-// A group's two best scores are merged across its lanes with shuffles (the group score
-// is the fp32 sum of the two largest values, whichever experts hold them); the topk_group
-// best groups are found by ranking the group scores; the k winners by k rounds of a lane
-// maximum plus a warp argmax (ties to the lower expert index).  Same fast path, margin
-// checks and exact fallback as route_topk_kernel.
-template <int V>
-__device__ int select_experts_reg(const float (&sel)[V], uint32_t live, int E, int topk, int n_group,
-                                  int topk_group, int lane, bool check, bool* thin) {
-    bool close = false;
-    if (n_group > 1) {
-        const int lpg = (E / n_group) / V;   // lanes per group
-        float a1 = -INFINITY, a2 = -INFINITY;
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            if (!((live >> v) & 1u)) continue;
-            if (sel[v] > a1) {
-                a2 = a1;
-                a1 = sel[v];
-            } else if (sel[v] > a2) {
-                a2 = sel[v];
-            }
-        }
-        for (int o = 1; o < lpg; o <<= 1) {
-            const float b1 = __shfl_xor_sync(0xffffffffu, a1, o);
-            const float b2 = __shfl_xor_sync(0xffffffffu, a2, o);
-            const float hi = fmaxf(a1, b1);
-            a2 = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
-            a1 = hi;
-        }
-        const float gs = a1 + a2;
-        const int my_group = lane / lpg;
-        int rank = 0;
-        for (int g = 0; g < n_group; ++g) {
-            const float o = __shfl_sync(0xffffffffu, gs, g * lpg);
-            rank += (o > gs || (o == gs && g < my_group)) ? 1 : 0;
-        }
-        if (check && topk_group < n_group) {
-            float last = (my_group < n_group && rank == topk_group - 1) ? gs : -INFINITY;
-            float next = (my_group < n_group && rank == topk_group) ? gs : -INFINITY;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                last = fmaxf(last, __shfl_xor_sync(0xffffffffu, last, o));
-                next = fmaxf(next, __shfl_xor_sync(0xffffffffu, next, o));
-            }
-            const float bound = 0x1p-17f + 0x1p-19f * fmaxf(fabsf(last), fabsf(next));
-            if (last - next <= bound) close = true;
-        }
-        if (my_group >= n_group || rank >= topk_group) live = 0;
-    }
-    int my_id = -1;
-    float prev = 0.0f;
-    const int rounds = check ? topk + 1 : topk;
-    if constexpr (V <= 16) {
-        // Each lane sorts its live candidates (value descending, expert index ascending) once;
-        // a round is then one warp-wide unsigned max over the lanes' heads (values mapped to
-        // order-preserving keys; -0 counted as +0, 0 = no candidate), a ballot for the lowest lane
-        // holding it (lanes hold consecutive experts, so the lowest lane has the lowest index
-        // among equal values), and the winning lane dropping its head: the same winners, in the
-        // same order, as the argmax rounds below.
-        uint32_t key[V];
-        int ix[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-            const uint32_t b = __float_as_uint(sel[v] + 0.0f);
-            key[v] = ((live >> v) & 1u) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
-            ix[v] = v;
-        }
-#pragma unroll
-        for (int k = 2; k <= V; k <<= 1)
-#pragma unroll
-            for (int jj = k >> 1; jj > 0; jj >>= 1)
-#pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    const int l = i ^ jj;
-                    if (l <= i) continue;
-                    // first / second: the pair's required order ((i & k) == 0: i before l)
-                    const int f = (i & k) == 0 ? i : l, g2 = (i & k) == 0 ? l : i;
-                    const bool ok = key[f] > key[g2] || (key[f] == key[g2] && ix[f] < ix[g2]);
-                    if (!ok) {
-                        const uint32_t tk = key[i];
-                        key[i] = key[l];
-                        key[l] = tk;
-                        const int ti = ix[i];
-                        ix[i] = ix[l];
-                        ix[l] = ti;
-                    }
-                }
-        for (int j = 0; j < rounds; ++j) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-            if (m == 0u) break;   // fewer candidates than rounds (only the extra round)
-            const int wl = __ffs(__ballot_sync(0xffffffffu, key[0] == m)) - 1;
-            const int widx = wl * V + __shfl_sync(0xffffffffu, ix[0], wl);
-            const float wv = __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
-            if (check && j > 0) {
-                const float bound = 0x1p-19f + 0x1p-20f * fmaxf(fabsf(prev), fabsf(wv));
-                if (prev - wv <= bound) close = true;
-            }
-            prev = wv;
-            if (j < topk) {
-                if (lane == wl) {
-#pragma unroll
-                    for (int v = 0; v + 1 < V; ++v) {
-                        key[v] = key[v + 1];
-                        ix[v] = ix[v + 1];
-                    }
-                    key[V - 1] = 0u;
-                }
-                if (lane == j) my_id = widx;
-            }
-        }
-        if (thin) *thin = close;
-        return my_id;
-    }
-    for (int j = 0; j < rounds; ++j) {
-        Cand c{0.0f, INT32_MAX};
-#pragma unroll
-        for (int v = 0; v < V; ++v)
-            if (((live >> v) & 1u) && (c.idx == INT32_MAX || sel[v] > c.v)) c = Cand{sel[v], lane * V + v};
-        const Cand win = warp_argmax(c);
-        if (win.idx == INT32_MAX) break;  // fewer candidates than rounds (only the extra round)
-        if (check && j > 0) {
-            const float bound = 0x1p-19f + 0x1p-20f * fmaxf(fabsf(prev), fabsf(win.v));
-            if (prev - win.v <= bound) close = true;
-        }
-        prev = win.v;
-        if (j < topk) {
-            if (win.idx / V == lane) live &= ~(1u << (win.idx % V));
-            if (lane == j) my_id = win.idx;
-        }
-    }
-    if (thin) *thin = close;
-    return my_id;
-}
-
 // One warp selects the experts of one token (fp32 registers); the fp64 weights of the
 // block's kWarps tokens are then formed together, one thread per (token, choice), so that
 // the fp64 instructions (a small fraction of the fp32 rate on this GPU) run on full warps.
@@ -338,63 +175,10 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_reg_kernel(
     const long t = tb + warp;
     const bool sigmoid = scoring == MOE_SCORING_SIGMOID;
     if (t < T) {
-        const float* lrow = logits + t * E;
-        const int e0 = lane * V;
-        uint32_t live = 0;
-        float x[V];
-        if (vec_loads) {
-            // E == 32*V, V >= 4, rows 16-byte aligned
-#pragma unroll
-            for (int v = 0; v < V; v += 4) {
-                const float4 q = __ldg(reinterpret_cast<const float4*>(lrow + e0 + v));
-                x[v] = q.x;
-                x[v + 1] = q.y;
-                x[v + 2] = q.z;
-                x[v + 3] = q.w;
-            }
-            live = V >= 32 ? 0xffffffffu : (1u << V) - 1u;
-        } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const bool ok = e0 + v < E;
-                x[v] = ok ? __ldg(lrow + e0 + v) : 0.0f;
-                if (ok) live |= 1u << v;
-            }
-        }
-        float sel[V];
-        int my_id;
-        if (sigmoid) {
-            // fast path on fp32 sigmoids, kept only when every decision clears their error
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-                const float sg = 1.0f / (1.0f + expf(-x[v]));
-                sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldg(bias + e0 + v) : sg;
-            }
-            bool thin = false;
-            my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, true, &thin);
-            if (__any_sync(0xffffffffu, thin)) {
-#pragma unroll
-                for (int v = 0; v < V; ++v) {
-                    const float sg = sigmoid_exact(x[v]);
-                    sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldg(bias + e0 + v) : sg;
-                }
-                my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
-            }
-        } else {
-#pragma unroll
-            for (int v = 0; v < V; ++v) sel[v] = x[v];
-            my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
-            if (!renormalize) {
-                const double lmax = static_cast<double>(lrow[__shfl_sync(0xffffffffu, my_id, 0)]);
-                double part = 0.0;
-#pragma unroll
-                for (int v = 0; v < V; ++v)
-                    if ((live >> v) & 1u) part += exp(static_cast<double>(x[v]) - lmax);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                if (lane == 0) s_zall[warp] = part;
-            }
-        }
+        double zall = 0.0;
+        const int my_id = route_token_reg<V>(logits + t * E, E, topk, renormalize, sigmoid, n_group,
+                                             topk_group, bias, vec_loads, lane, &zall);
+        if (!sigmoid && !renormalize && lane == 0) s_zall[warp] = zall;
         if (lane < topk) s_id[warp * topk + lane] = my_id;
     }
     __syncthreads();
@@ -420,20 +204,6 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_reg_kernel(
         ids[tb * topk + sl] = s_id[sl];
         weights[tb * topk + sl] = static_cast<float>(s_val[sl] / z * static_cast<double>(routed_scaling));
     }
-}
-
-// experts per lane of the register variant for this shape, or 0 when it does not apply
-int reg_experts_per_lane(int E, int n_group) {
-    int V = 1;
-    while (32 * V < E) V *= 2;
-    if (V > 32) return 0;
-    if (n_group > 1) {
-        const int G = E / n_group;
-        if (G % V != 0) return 0;
-        const int lpg = G / V;
-        if (lpg > 32 || (lpg & (lpg - 1)) != 0) return 0;
-    }
-    return V;
 }
 
 }  // namespace

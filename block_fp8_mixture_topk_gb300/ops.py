@@ -104,6 +104,7 @@ def lib():
                 "fp8_block_grouped_gemm": ([P, P, I64, I64, I64, P, P, I, I, I, P, P, P, I64, P, P], I),
                 "moe_fp8_block_workspace_size": ([I, I, I, I, I], SZ),
                 "moe_fp8_block_forward_kernel_count": ([I, I, I, I, I], I),
+                "moe_fp8_block_forward_kernel_count_ex": ([I, I, I, I, I, P, P], I),
                 "moe_fp8_block_decode_path": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
@@ -391,9 +392,16 @@ def moe_fp8_block_decode_path(T, H, I, topk, decode="auto") -> bool:
     return bool(r)
 
 
-def moe_fp8_block_forward_kernel_count(T, H, I, E, topk) -> int:
-    """Kernels one moe_fp8_block_forward launches for these sizes."""
-    return int(lib().moe_fp8_block_forward_kernel_count(T, H, I, E, topk))
+def moe_fp8_block_forward_kernel_count(T, H, I, E, topk, routing: RoutingParams | None = None, layout=None,
+                                       scale_fmt="f32", decode="auto") -> int:
+    """Kernels one moe_fp8_block_forward with these routing parameters and options launches
+    (layout: MOE_WEIGHTS_NK / _TILED / _NVFP4, default NK)."""
+    if routing is None and layout is None and scale_fmt == "f32" and decode == "auto":
+        return int(lib().moe_fp8_block_forward_kernel_count(T, H, I, E, topk))
+    rp = routing.to_c() if routing else None
+    opts = _ForwardOptions(MOE_WEIGHTS_NK if layout is None else layout, SCALE_FMT[scale_fmt], DECODE_PATH[decode])
+    return int(lib().moe_fp8_block_forward_kernel_count_ex(T, H, I, E, topk, ctypes.byref(rp) if rp else None,
+                                                           ctypes.byref(opts)))
 
 
 def moe_fp8_block_workspace_size(T, H, I, E, topk) -> int:

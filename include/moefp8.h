@@ -370,12 +370,8 @@ int moe_combine_pairs(const uint16_t* y, const int32_t* pos, int T, int topk, in
  * bytes (256-byte aligned).  hidden, w13, w2 and out 16-byte aligned.  out may
  * not alias any input.  T == 0 is a no-op. */
 size_t moe_fp8_block_workspace_size(int T, int H, int I, int E, int topk);
-/* Number of kernels one moe_fp8_block_forward launches for these sizes (host only):
- * routing, the expert sort and quantisation (one kernel for up to 512 routed pairs,
- * four otherwise), the two grouped GEMMs (one kernel on the decode path) and the weighted
- * sum, under MOE_DECODE_AUTO; 0 when T == 0, -1 for invalid sizes.  (With MOE_WEIGHTS_NVFP4
- * a forward launches 4 kernels per 8 tokens: routing, sort and quantisation, the decode
- * kernel, the weighted sum.) */
+/* Number of kernels one moe_fp8_block_forward launches for these sizes (host only), with
+ * rp == NULL and default options: see moe_fp8_block_forward_kernel_count_ex. */
 int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk);
 int moe_fp8_block_forward(const uint16_t* hidden, const float* router_logits,
                           const uint8_t* w13, const float* w13_scale,
@@ -400,9 +396,14 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
  * and multiplied on the warp-level tensor core MMA, so that every SM streams weights even
  * when only a few experts are touched (a one-token DeepSeek-V3-shaped step touches 8 experts:
  * 1024 w13 items instead of 128 tiles of 128 x 256) and the w2 weights stream while the last
- * w13 items finish.  Same operands, block scales and epilogues as the tile GEMMs; the sums
- * run in another order, so results agree with the tile path to fp32 rounding, not bit for
- * bit.  With events, its time is recorded as the w13 GEMM stage and the w2 stage is empty.
+ * w13 items finish.  The same kernel routes the step's tokens in every CTA (the routing
+ * kernel's selection, so the same experts and weights; for E <= 256 with groups the register-
+ * resident selection takes, otherwise the routing kernel runs first) and sorts the pairs; a small
+ * prologue kernel zeroes its counters and quantises the tokens, and the weighted sum follows.
+ * Same operands, block scales and epilogues as the tile GEMMs; the sums run in another order, so
+ * results agree with the tile path to fp32 rounding, not bit for bit.  With events, the prologue
+ * is recorded as the quantisation stage and the decode kernel as the w13 GEMM stage (the routing
+ * stage holds the routing kernel or nothing; the sort and w2 stages are empty).
  *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300: the decode
  *                    path for steps of one or two tokens, the tile GEMMs otherwise
  *   MOE_DECODE_OFF:  always the tile GEMMs
@@ -422,7 +423,7 @@ int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode);
  * per-expert global scales [E] (moe_nvfp4_quant_weight); activations and the intermediate keep
  * their FP8 1x128 groups.  Both GEMMs then run on the decode-path kernel (decode_path
  * MOE_DECODE_OFF is rejected with MOE_ERR_INVALID_ARG), a step of more than 8 tokens 8 tokens
- * at a time (4 launches each); moe_fp8_block_workspace_size(T, ...) still suffices.  Shapes the
+ * at a time (3 or 4 launches each); moe_fp8_block_workspace_size(T, ...) still suffices.  Shapes the
  * decode kernel cannot take give MOE_ERR_UNSUPPORTED_SHAPE.
  * MOE_SCALE_UE8M0_PACKED: w13_scale / w2_scale are the packed UE8M0 weight scales
  * (moe_fp8_block_pack_scales outputs, passed as const float*) and both GEMMs run on the block-scaled
@@ -433,6 +434,16 @@ typedef struct moe_forward_options {
     int32_t scale_fmt;                /* MOE_SCALE_F32, MOE_SCALE_UE8M0 or MOE_SCALE_UE8M0_PACKED */
     int32_t decode_path;              /* MOE_DECODE_AUTO, MOE_DECODE_OFF or MOE_DECODE_ON */
 } moe_forward_options;
+
+/* Number of kernels one moe_fp8_block_forward_ex with these routing parameters and options
+ * (either may be NULL) launches (host only): on the tile path routing, the expert sort and
+ * quantisation (one kernel for up to 512 routed pairs, four otherwise), the two grouped GEMMs
+ * and the weighted sum; on the decode path the prologue, the decode kernel and the weighted sum,
+ * plus the routing kernel when the decode kernel cannot route in every CTA (E > 256, or groups
+ * the register-resident selection does not take), per 8 tokens with MOE_WEIGHTS_NVFP4.  0 when T == 0, -1 for
+ * invalid sizes. */
+int moe_fp8_block_forward_kernel_count_ex(int T, int H, int I, int E, int topk, const moe_routing_params* rp,
+                                          const moe_forward_options* opts);
 
 /* The same layer with options, optionally recording CUDA events between its stages for
  * per-stage timing (events: host array of MOE_FORWARD_NUM_EVENTS cudaEvent_t created by the

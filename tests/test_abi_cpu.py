@@ -55,13 +55,31 @@ def test_host_only_queries():
     # sorted activation codes, the sorted intermediate, bf16 weighted rows in pair order
     assert ws >= rows * 7168 + rows * 2048 + 32768 * 7168 * 2
     assert moe.moe_fp8_block_workspace_size(16, 256, 256, 4, 2) > 0
+    # decode path (up to 2 tokens by default): its prologue + the decode kernel + the weighted sum
+    assert moe.moe_fp8_block_forward_kernel_count(2, 7168, 2048, 256, 8) == 3
     # route + sort/quantise (one kernel up to 512 pairs, four above) + two GEMMs + weighted sum
-    assert moe.moe_fp8_block_forward_kernel_count(2, 7168, 2048, 256, 8) == 4
     assert moe.moe_fp8_block_forward_kernel_count(3, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(64, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(65, 7168, 2048, 256, 8) == 8
     assert moe.moe_fp8_block_forward_kernel_count(0, 7168, 2048, 256, 8) == 0
     assert moe.moe_fp8_block_forward_kernel_count(-1, 7168, 2048, 256, 8) == -1
+
+
+def test_forward_kernel_count_with_options():
+    """The decode kernel routes in every CTA for E <= 256 (with groups the register-resident
+    selection takes); otherwise the routing kernel runs first.  NVFP4 steps count per 8 tokens;
+    block-scaled formats always take the tile GEMMs."""
+    kc = moe.moe_fp8_block_forward_kernel_count
+    dsv3 = moe.RoutingParams("sigmoid", 8, 4, 2.5, None)
+    assert kc(1, 7168, 2048, 256, 8, dsv3) == 3
+    assert kc(1, 4096, 14336, 8, 2, None, moe.ops.MOE_WEIGHTS_TILED) == 3
+    assert kc(1, 2048, 768, 512, 8) == 4                        # 16 experts per lane: routing kernel
+    assert kc(1, 256, 256, 96, 4, moe.RoutingParams("softmax", 4, 2)) == 4   # groups of 24 on 4-expert lanes
+    assert kc(4, 7168, 2048, 256, 8, dsv3, decode="on") == 3
+    assert kc(4, 7168, 2048, 256, 8, dsv3, decode="off") == 5
+    assert kc(1, 7168, 2048, 256, 8, dsv3, scale_fmt="ue8m0_packed") == 5
+    assert kc(17, 7168, 2048, 256, 8, dsv3, moe.ops.MOE_WEIGHTS_NVFP4) == 3 * 3
+    assert kc(0, 7168, 2048, 256, 8, dsv3) == 0
 
 
 def test_decode_path_selection():
@@ -72,8 +90,8 @@ def test_decode_path_selection():
     assert dp(1, 7168, 2048, 8, "on") and dp(8, 7168, 2048, 8, "on")
     assert dp(1, 7168, 2048, 8) and dp(2, 7168, 2048, 8) and not dp(3, 7168, 2048, 8)
     assert not dp(9, 7168, 2048, 8) and not dp(4096, 7168, 2048, 8)
-    # route + sort/quantise + both GEMMs in one kernel + weighted sum
-    assert moe.moe_fp8_block_forward_kernel_count(1, 7168, 2048, 256, 8) == 4
+    # the decode prologue + the decode kernel (routing, sort, both GEMMs) + the weighted sum
+    assert moe.moe_fp8_block_forward_kernel_count(1, 7168, 2048, 256, 8) == 3
     assert not dp(1, 7168, 2048, 8, "off")
     assert dp(8, 256, 256, 32, "on") and not dp(9, 256, 256, 2, "on") and not dp(0, 256, 256, 8, "on")
     assert not dp(1, 65536, 16384, 8, "on")

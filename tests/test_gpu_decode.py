@@ -1,7 +1,9 @@
-"""The decode-path GEMMs (steps of up to 8 tokens): the whole layer against the oracle on
-every token, the same steps through the tile GEMMs, both weight layouts, both scale formats,
-and repeated calls on one workspace (the per-group completion counters start from zero on
-every call)."""
+"""The decode path (steps of up to 8 tokens: a prologue kernel, one kernel that routes, sorts
+and runs both GEMMs, then the weighted sum): the whole layer against the oracle on every
+token, the same steps through the tile GEMMs, both weight layouts, both scale formats, the
+in-kernel routing against the routing kernel bit for bit, the routing kernel's ids where the
+in-kernel selection does not apply, and repeated calls on one workspace (the counters start
+from zero on every call)."""
 import numpy as np
 import pytest
 import torch
@@ -96,8 +98,7 @@ def test_decode_path_ue8m0_scales():
 
 def test_decode_path_repeated_calls_on_one_workspace():
     """Ten calls on one workspace, on changing inputs: each equals a call on a fresh workspace
-    (the group counters are zeroed by every call's sort and reset by the item that completes
-    a group)."""
+    (the counters and the ticket are zeroed by every call's decode prologue)."""
     wl = workload("dsv3_decode", 2)
     layer = Layer(wl)
     rp, _ = routing_of(wl)
@@ -156,3 +157,86 @@ def test_decode_path_replays_from_a_cuda_graph(T):
         torch.cuda.synchronize()
         assert torch.equal(got, want)
     assert moe.moe_get_device_status(clear=True) == 0
+
+
+def routing_in_workspace(ws, T, topk):
+    """The decode kernel's CTA 0 writes the step's chosen experts and router weights at the start
+    of the forward workspace: ids [T*topk] int32, then the weights [T*topk] fp32 at the next
+    256-byte boundary (the layout's first two regions)."""
+    P = T * topk
+    off = (P * 4 + 255) // 256 * 256
+    return ws[:P * 4].view(torch.int32).view(T, topk), ws[off:off + P * 4].view(torch.float32).view(T, topk)
+
+
+ROUTE_CASES = [
+    ("dsv3_decode", 1, True), ("dsv3_decode", 2, True), ("dsv3_decode", 8, True),   # sigmoid, 8 groups, bias
+    ("mixtral", 1, True), ("mixtral", 8, True), ("mixtral", 4, False),               # softmax, 1 expert per lane
+    ("qwen3_skew", 4, True), ("qwen3_skew", 3, False),                               # 4 experts per lane
+    ("tiny", 8, True),
+]
+
+
+@pytest.mark.parametrize("name,T,renorm", ROUTE_CASES)
+def test_decode_kernel_routes_like_the_routing_kernel(name, T, renorm):
+    """Every CTA of the decode kernel routes the step's tokens itself with the routing kernel's
+    selection: the ids and weights it writes are bit-identical to moe_route_topk's, and the
+    layer equals the oracle."""
+    wl = workload(name, T).with_(renormalize=renorm)
+    layer = Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    h, l = hidden.to(DEV), logits.to(DEV)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8, device=DEV)
+    out = forward(layer, h, l, rp, "on", workspace=ws)
+    ids, wts = moe.moe_route_topk(l, wl.topk, wl.renormalize, rp)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(clear=True) == 0
+    got_ids, got_wts = routing_in_workspace(ws, T, wl.topk)
+    assert torch.equal(got_ids, ids)
+    assert torch.equal(got_wts.view(torch.int32), wts.view(torch.int32))
+    oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    assert_output_close(out, oracle_out(layer, hidden, logits, okw))
+
+
+def test_decode_kernel_routing_on_tied_scores():
+    """Logits on a coarse grid: many equal scores, so the fp32 fast path hands the token to the
+    exact fp64 scores and equal values go to the lower expert index -- in the decode kernel as in
+    the routing kernel and the oracle."""
+    wl = workload("dsv3_decode", 8)
+    layer = Layer(wl)
+    hidden = mi.hidden(wl)
+    logits = torch.round(mi.router_logits(wl) * 2.0) / 2.0
+    rp, okw = routing_of(wl)
+    h, l = hidden.to(DEV), logits.to(DEV)
+    ws = torch.empty(moe.moe_fp8_block_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.topk), dtype=torch.uint8,
+                     device=DEV)
+    out = forward(layer, h, l, rp, "on", workspace=ws)
+    ids, wts = moe.moe_route_topk(l, wl.topk, wl.renormalize, rp)
+    torch.cuda.synchronize()
+    got_ids, got_wts = routing_in_workspace(ws, wl.T, wl.topk)
+    assert torch.equal(got_ids, ids) and torch.equal(got_wts, wts)
+    oids, _ = oracle.route(logits.numpy(), wl.topk, wl.renormalize, **okw)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    assert_output_close(out, oracle_out(layer, hidden, logits, okw))
+
+
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+def test_decode_path_with_the_routing_kernel(scoring):
+    """512 experts (16 per lane): the decode kernel takes the routing kernel's ids and weights
+    instead of routing in every CTA; the layer still equals the oracle and the tile path."""
+    wl = mi.Workload("dec_e512", 77, 2, 256, 256, 512, 8)
+    if scoring == "sigmoid":
+        wl = wl.with_(scoring=mi.SIGMOID, n_group=8, topk_group=4, routed_scaling=2.5, bias_std=0.01)
+    assert moe.moe_fp8_block_forward_kernel_count(wl.T, wl.H, wl.I, wl.E, wl.topk, decode="on") == 4
+    layer = Layer(wl)
+    hidden, logits = mi.hidden(wl), mi.router_logits(wl)
+    rp, okw = routing_of(wl)
+    h, l = hidden.to(DEV), logits.to(DEV)
+    out = forward(layer, h, l, rp, "on")
+    tile = forward(layer, h, l, rp, "off")
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(clear=True) == 0
+    ref = oracle_out(layer, hidden, logits, okw)
+    assert_output_close(out, ref)
+    assert_output_close(tile, ref)
