@@ -119,10 +119,10 @@ bool use_decode(int T, int H, int I, int topk, int mode) {
     return mode == MOE_DECODE_ON || T <= kDecodeAutoMaxTokens;
 }
 // Copies of the token rows the decode prologue writes (into the a1 rows / a1s scales of the
-// layout): 16, as the rows allow
+// layout): 4, as the rows allow
 int decode_x_copies(int T, int64_t rows) {
     const int64_t c = (rows - kDecodeCols) / T;
-    return static_cast<int>(c < 1 ? 1 : (c > 16 ? 16 : c));
+    return static_cast<int>(c < 1 ? 1 : (c > 4 ? 4 : c));
 }
 // Experts per lane with which the decode kernel routes the step in every CTA (the routing
 // kernel's register-resident selection, up to 8 per lane: E <= 256), 0 when the step takes the

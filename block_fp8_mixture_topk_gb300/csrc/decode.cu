@@ -21,7 +21,9 @@
 // routing kernel's selection (route_select.cuh: the same choices, the same arithmetic); the
 // CTA sorts the T*topk pairs by (expert, pair) in shared memory into one tile record per
 // touched expert (expert, rows, their pairs and tokens), the small-batch sort's order.  The
-// fp64 router weights are formed afterwards by the same warps while the producer streams.
+// fp64 router weights (a few microseconds of dependent fp64 operations on this GPU) are formed
+// afterwards by the epilogue warps, idle until the first item is done; on an MMA warp they held
+// up the ring for all eight.
 // (Shapes whose scores do not fit the register-resident selection take the routing kernel's
 // ids and weights instead.)  CTA 0 writes the ids, the weights and each pair's row (-1 for a
 // dropped pair) for the k-way sum.
@@ -119,6 +121,7 @@ struct Ctl {
     int abort_flag;
     int last;
     int ntiles;                                 // tiles of the step (touched experts)
+    double zall[kCols];                         // softmax without renormalisation: each token's sum
     int stage_item[kMaxStages];                 // the stage's item (ticket), -1: no more work
     int stage_grp[kMaxStages];                  // its group of K blocks
     int stage_rows[kMaxStages];                 // activation rows it holds (1, 2, 4 or 8)
@@ -299,10 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool route_here = a.route_v > 0;
     const bool router = route_here && warp >= 1 && warp <= a.T;
     const bool sigmoid = a.scoring == MOE_SCORING_SIGMOID;
-    const float* lrow = a.logits + static_cast<int64_t>(warp >= 1 ? warp - 1 : 0) * a.E;
-    int my_id = -1;
-    double zall = 0.0;
     if (router) {
+        const float* lrow = a.logits + static_cast<int64_t>(warp - 1) * a.E;
+        double zall = 0.0;
+        int my_id;
         switch (a.route_v) {
             case 1:
                 my_id = route_token_reg<1>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
@@ -322,12 +325,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
         }
         if (lane < a.topk) s_ids[(warp - 1) * a.topk + lane] = my_id;
+        if (lane == 0) ctl->zall[warp - 1] = zall;
     }
     if (!route_here) {
         grid_dependency_wait();
         for (int p = threadIdx.x; p < P; p += blockDim.x) s_ids[p] = __ldcg(a.ids + p);
     }
     __syncthreads();
+    // the decode prologue's outputs (zeroed counters, quantised tokens) from here on; the first two
+    // tickets go out now, their round trip under the sort
+    if (route_here) grid_dependency_wait();
+    int ticket0 = 0, ticket1 = 0;
+    if (warp == 0 && lane == 0) {
+        ticket0 = atomicAdd(ticket, 1);
+        ticket1 = atomicAdd(ticket, 1);
+    }
     // The expert sort, in shared memory: pair p's row is the number of earlier pairs with its
     // expert (a stable order by (expert, pair)); one tile per touched expert, in expert order, at
     // padded row m * 128 of the intermediate -- the small-batch sort's layout.  An id out of range
@@ -376,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
         const int slot = s_slot[p];
+        if (blockIdx.x == 0) a.pos[p] = slot < 0 ? -1 : (slot >> 8) * kTileRows + (slot & 255);
         if (slot < 0) continue;
         DecodeTile& d = tab[slot >> 8];
         d.pair[slot & 255] = p;
@@ -383,34 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         d.weight[slot & 255] = route_here ? 0.0f : __ldcg(a.wts + p);
     }
     __syncthreads();
-    // the decode prologue's outputs (zeroed counters, quantised tokens) from here on
-    if (route_here) grid_dependency_wait();
-    if (blockIdx.x == 0)
-        for (int p = threadIdx.x; p < P; p += blockDim.x) {
-            const int slot = s_slot[p];
-            a.pos[p] = slot < 0 ? -1 : (slot >> 8) * kTileRows + (slot & 255);
-        }
     int64_t ntiles = ctl->ntiles;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const Gemm G1 = gemm_of(a, false), G2 = gemm_of(a, true);
     const int total1 = static_cast<int>(ntiles * G1.per_tile);
     const int total = total1 + static_cast<int>(ntiles * G2.per_tile);
     volatile int* abort_flag = &ctl->abort_flag;
-    if (router) {
-        // the router weights in fp64 (as the routing kernel forms them), off the producer's path:
-        // the epilogue reads them for w2 items, after every MMA warp has passed its reduction
-        // barrier at least once
-        const float wgt = route_weight_warp(lrow, my_id, a.topk, a.renormalize, sigmoid, zall, a.routed_scaling, lane);
-        if (lane < a.topk) {
-            const int p = (warp - 1) * a.topk + lane;
-            const int slot = s_slot[p];
-            if (slot >= 0) tab[slot >> 8].weight[slot & 255] = wgt;
-            if (blockIdx.x == 0) {
-                a.ids[p] = my_id;
-                a.wts[p] = wgt;
-            }
-        }
-    }
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
@@ -418,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t q = 0;
         bool ok = true;
         // tickets are taken two items ahead: an atomic's round trip is longer than a w2 item's issue
-        int item = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(ticket, 1) : 0, 0);
-        int next = lane == 0 ? atomicAdd(ticket, 1) : 0;
+        int item = __shfl_sync(0xffffffffu, ticket0, 0);
+        int next = ticket1;
         while (ok) {
             if (item >= total) {
                 // no more work: a stage that says so
@@ -789,6 +780,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ epilogue warps
         const int et = threadIdx.x - kFirstEpiWarp * 32;   // 0..95
         const int ew = warp - kFirstEpiWarp;
+        if (route_here) {
+            // the router weights in fp64, as the routing kernel forms them: lane groups of topk
+            // lanes take one token each (all of a step's tokens in one round for topk <= 8); read
+            // by the w2 epilogue after the barrier below; CTA 0 writes ids and weights out
+            const int per_warp = 32 / a.topk;
+            for (int t0 = ew * per_warp; t0 < a.T; t0 += kEpiWarps * per_warp) {
+                const int j = lane % a.topk, t = t0 + lane / a.topk;
+                const bool active = lane / a.topk < per_warp && t < a.T;
+                const int p = active ? t * a.topk + j : 0;
+                const int id = active ? s_ids[p] : -1;
+                const float wgt = route_weight_group(a.logits + static_cast<int64_t>(active ? t : 0) * a.E, id, active,
+                                                     lane - j, a.topk, a.renormalize, sigmoid,
+                                                     ctl->zall[active ? t : 0], a.routed_scaling);
+                if (active) {
+                    const int slot = s_slot[p];
+                    if (slot >= 0) tab[slot >> 8].weight[slot & 255] = wgt;
+                    if (blockIdx.x == 0) {
+                        a.ids[p] = id;
+                        a.wts[p] = wgt;
+                    }
+                }
+            }
+            epilogue_barrier();
+        }
         uint32_t iter = 0;
         while (true) {
             const uint32_t buf = iter % kRedBufs;

@@ -250,23 +250,28 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
     return my_id;
 }
 
-// The router weight of lane j's expert (lane j < topk; my_id as route_token_reg returns it): the
-// fp64 terms of the chosen experts (sigmoid: the exact score; softmax: exp(l - l_first)), summed
-// in the order of the chosen list (renormalize) or 1 / zall, times routed_scaling, rounded once to
-// fp32 -- the same operations in the same order as the routing kernel's weight stage.
-__device__ __forceinline__ float route_weight_warp(const float* lrow, int my_id, int topk, int renormalize,
-                                                   bool sigmoid, double zall, float routed_scaling, int lane) {
-    const int first = __shfl_sync(0xffffffffu, my_id, 0);
+// The router weight of one token's j-th choice, for the tokens of lane groups: lanes
+// [base, base + topk) of the warp hold one token's choices, lane base + j its j-th expert my_id
+// (as route_token_reg returns it on lane j) and that token's score row lrow; the first choice is
+// lane base's.  The fp64 terms of the chosen experts (sigmoid: the exact score; softmax:
+// exp(l - l_first)), summed in the order of the chosen list (renormalize) or 1 / zall, times
+// routed_scaling, rounded once to fp32 -- the same operations in the same order as the routing
+// kernel's weight stage.  Every lane of the warp takes part (shuffles); a lane outside any group
+// passes active = false and gets 0.
+__device__ __forceinline__ float route_weight_group(const float* lrow, int my_id, bool active, int base, int topk,
+                                                    int renormalize, bool sigmoid, double zall,
+                                                    float routed_scaling) {
+    const int first = __shfl_sync(0xffffffffu, my_id, base & 31);
     double v = 0.0;
-    if (lane < topk && my_id >= 0) {
+    if (active && my_id >= 0) {
         const float l = __ldcg(lrow + my_id);
         v = sigmoid ? static_cast<double>(sigmoid_exact(l))
                     : exp(static_cast<double>(l) - static_cast<double>(__ldcg(lrow + first)));
     }
     double z = 0.0;
-    for (int jj = 0; jj < topk; ++jj) z += __shfl_sync(0xffffffffu, v, jj);
+    for (int jj = 0; jj < topk; ++jj) z += __shfl_sync(0xffffffffu, v, (base + jj) & 31);
     if (!renormalize) z = sigmoid ? 1.0 : zall;
-    return static_cast<float>(v / z * static_cast<double>(routed_scaling));
+    return active ? static_cast<float>(v / z * static_cast<double>(routed_scaling)) : 0.0f;
 }
 
 }  // namespace
