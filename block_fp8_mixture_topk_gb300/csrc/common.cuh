@@ -26,9 +26,6 @@ __device__ __forceinline__ void status_set(uint32_t* status, uint32_t bits) {
 // the previous grid to complete and its memory to be visible.  Every kernel calls it on
 // every path, so the wait also covers all grids before that one.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Lets the next kernel of the stream (launched with programmatic serialisation) start before this
-// one ends; it still sees this grid's writes only after its own grid_dependency_wait.
-__device__ __forceinline__ void grid_dependency_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -20,6 +20,10 @@ namespace mfp8 {
 
 namespace {
 
+// Lets the next kernel of the stream (launched with programmatic serialisation) start before this
+// one ends; it still sees this grid's writes only after its own grid_dependency_wait.
+__device__ __forceinline__ void grid_dependency_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __global__ void __launch_bounds__(1024, 1) sort_quant_small_kernel(
     const int32_t* __restrict__ ids, int P, int E, int block_m, int32_t* __restrict__ expert_offsets,
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ sorted_pair_ids, int32_t* __restrict__ pos,
