@@ -308,19 +308,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int my_id;
         switch (a.route_v) {
             case 1:
-                my_id = route_token_reg<1>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                my_id = route_token_reg<1, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
                                            a.vec_loads != 0, lane, &zall);
                 break;
             case 2:
-                my_id = route_token_reg<2>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                my_id = route_token_reg<2, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
                                            a.vec_loads != 0, lane, &zall);
                 break;
             case 4:
-                my_id = route_token_reg<4>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                my_id = route_token_reg<4, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
                                            a.vec_loads != 0, lane, &zall);
                 break;
             default:
-                my_id = route_token_reg<8>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
+                my_id = route_token_reg<8, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
                                            a.vec_loads != 0, lane, &zall);
                 break;
         }

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kWarps * 32) route_topk_reg_kernel(
     const bool sigmoid = scoring == MOE_SCORING_SIGMOID;
     if (t < T) {
         double zall = 0.0;
-        const int my_id = route_token_reg<V>(logits + t * E, E, topk, renormalize, sigmoid, n_group,
+        const int my_id = route_token_reg<V, true>(logits + t * E, E, topk, renormalize, sigmoid, n_group,
                                              topk_group, bias, vec_loads, lane, &zall);
         if (!sigmoid && !renormalize && lane == 0) s_zall[warp] = zall;
         if (lane < topk) s_id[warp * topk + lane] = my_id;

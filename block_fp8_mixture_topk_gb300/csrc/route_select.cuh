@@ -8,14 +8,27 @@
 // defined as fp64 sigmoids rounded to fp32; the selection first runs on fp32 sigmoids and keeps
 // the result when every decision clears the fp32 error (nearly always), else repeats the token on
 // the exact scores.  Weights are formed in fp64 from the exact scores of the chosen experts and
-// rounded to fp32.  Scores and bias are read through L2 (ld.global.cg): the decode kernel reads
-// them while an earlier kernel of the stream may have just written them.
+// rounded to fp32.  The routing kernel reads scores and bias through L1 (every token of a block
+// reads the same bias); the decode kernel reads them through L2 (ld.global.cg), before it waits
+// for the grids ahead of it.
 #pragma once
 #include "common.cuh"
 
 namespace mfp8 {
 
 namespace {
+
+// a read-only load through L1 (L1 = true) or through L2 only
+template <bool L1>
+__device__ __forceinline__ float ld_score(const float* p) {
+    if constexpr (L1) return __ldg(p);
+    else return __ldcg(p);
+}
+template <bool L1>
+__device__ __forceinline__ float4 ld_score4(const float4* p) {
+    if constexpr (L1) return __ldg(p);
+    else return __ldcg(p);
+}
 
 
 struct Cand {
@@ -187,7 +200,7 @@ __device__ int select_experts_reg(const float (&sel)[V], uint32_t live, int E, i
 // (vec_loads: E == 32*V, V >= 4, lrow 16-byte aligned).  Returns, on lane j < topk, the j-th
 // chosen expert.  zall: for softmax scoring without renormalisation, the fp64 sum over all experts
 // of exp(l - l_first) (each lane's experts in order, then a shuffle tree), on every lane.
-template <int V>
+template <int V, bool L1>
 __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int topk, int renormalize, bool sigmoid,
                                                int n_group, int topk_group, const float* bias, bool vec_loads,
                                                int lane, double* zall) {
@@ -198,7 +211,7 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
         // E == 32*V, V >= 4, rows 16-byte aligned
 #pragma unroll
         for (int v = 0; v < V; v += 4) {
-            const float4 q = __ldcg(reinterpret_cast<const float4*>(lrow + e0 + v));
+            const float4 q = ld_score4<L1>(reinterpret_cast<const float4*>(lrow + e0 + v));
             x[v] = q.x;
             x[v + 1] = q.y;
             x[v + 2] = q.z;
@@ -209,7 +222,7 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const bool ok = e0 + v < E;
-            x[v] = ok ? __ldcg(lrow + e0 + v) : 0.0f;
+            x[v] = ok ? ld_score<L1>(lrow + e0 + v) : 0.0f;
             if (ok) live |= 1u << v;
         }
     }
@@ -220,7 +233,7 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
 #pragma unroll
         for (int v = 0; v < V; ++v) {
             const float sg = 1.0f / (1.0f + expf(-x[v]));
-            sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldcg(bias + e0 + v) : sg;
+            sel[v] = (bias && ((live >> v) & 1u)) ? sg + ld_score<L1>(bias + e0 + v) : sg;
         }
         bool thin = false;
         my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, true, &thin);
@@ -228,7 +241,7 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 const float sg = sigmoid_exact(x[v]);
-                sel[v] = (bias && ((live >> v) & 1u)) ? sg + __ldcg(bias + e0 + v) : sg;
+                sel[v] = (bias && ((live >> v) & 1u)) ? sg + ld_score<L1>(bias + e0 + v) : sg;
             }
             my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
         }
@@ -237,7 +250,7 @@ __device__ __forceinline__ int route_token_reg(const float* lrow, int E, int top
         for (int v = 0; v < V; ++v) sel[v] = x[v];
         my_id = select_experts_reg<V>(sel, live, E, topk, n_group, topk_group, lane, false, nullptr);
         if (!renormalize) {
-            const double lmax = static_cast<double>(__ldcg(lrow + __shfl_sync(0xffffffffu, my_id, 0)));
+            const double lmax = static_cast<double>(ld_score<L1>(lrow + __shfl_sync(0xffffffffu, my_id, 0)));
             double part = 0.0;
 #pragma unroll
             for (int v = 0; v < V; ++v)
