@@ -250,6 +250,33 @@ struct ActMaps {
     CUtensorMap m[2][4];
 };
 
+// The step's routing, out of line: called once per token and CTA, these functions hold the
+// selection's instantiations and the fp64 exp and division.  Inlined into the kernel they made
+// its weight stream slower by 10% at one token (TMA issue-to-landing time per stage 2.2 us
+// instead of 1.9 us, measured with the kernel instrumented), and the routing itself slower too.
+__device__ __noinline__ int route_token(int route_v, const float* lrow, int E, int topk, int renormalize,
+                                        bool sigmoid, int n_group, int topk_group, const float* bias, bool vec_loads,
+                                        int lane, double* zall) {
+    switch (route_v) {
+        case 1:
+            return route_token_reg<1, false>(lrow, E, topk, renormalize, sigmoid, n_group, topk_group, bias,
+                                             vec_loads, lane, zall);
+        case 2:
+            return route_token_reg<2, false>(lrow, E, topk, renormalize, sigmoid, n_group, topk_group, bias,
+                                             vec_loads, lane, zall);
+        case 4:
+            return route_token_reg<4, false>(lrow, E, topk, renormalize, sigmoid, n_group, topk_group, bias,
+                                             vec_loads, lane, zall);
+        default:
+            return route_token_reg<8, false>(lrow, E, topk, renormalize, sigmoid, n_group, topk_group, bias,
+                                             vec_loads, lane, zall);
+    }
+}
+__device__ __noinline__ float route_weight(const float* lrow, int my_id, bool active, int base, int topk,
+                                           int renormalize, bool sigmoid, double zall, float routed_scaling) {
+    return route_weight_group(lrow, my_id, active, base, topk, renormalize, sigmoid, zall, routed_scaling);
+}
+
 // FP4: NVFP4 weights (nvfp4.cu's packed units); the MMA warps expand each code times its block
 // scale to f16 (exact: at most 6 significant bits, |w| <= 6 * 448) and the activation codes to
 // f16 (exact), and run f16 MMAs; the expert's 1 / global_scale joins the promotion's scale.
@@ -305,25 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (router) {
         const float* lrow = a.logits + static_cast<int64_t>(warp - 1) * a.E;
         double zall = 0.0;
-        int my_id;
-        switch (a.route_v) {
-            case 1:
-                my_id = route_token_reg<1, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
-                                           a.vec_loads != 0, lane, &zall);
-                break;
-            case 2:
-                my_id = route_token_reg<2, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
-                                           a.vec_loads != 0, lane, &zall);
-                break;
-            case 4:
-                my_id = route_token_reg<4, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
-                                           a.vec_loads != 0, lane, &zall);
-                break;
-            default:
-                my_id = route_token_reg<8, false>(lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group, a.bias,
-                                           a.vec_loads != 0, lane, &zall);
-                break;
-        }
+        const int my_id = route_token(a.route_v, lrow, a.E, a.topk, a.renormalize, sigmoid, a.n_group, a.topk_group,
+                                      a.bias, a.vec_loads != 0, lane, &zall);
         if (lane < a.topk) s_ids[(warp - 1) * a.topk + lane] = my_id;
         if (lane == 0) ctl->zall[warp - 1] = zall;
     }
@@ -790,9 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool active = lane / a.topk < per_warp && t < a.T;
                 const int p = active ? t * a.topk + j : 0;
                 const int id = active ? s_ids[p] : -1;
-                const float wgt = route_weight_group(a.logits + static_cast<int64_t>(active ? t : 0) * a.E, id, active,
-                                                     lane - j, a.topk, a.renormalize, sigmoid,
-                                                     ctl->zall[active ? t : 0], a.routed_scaling);
+                const float wgt = route_weight(a.logits + static_cast<int64_t>(active ? t : 0) * a.E, id, active,
+                                               lane - j, a.topk, a.renormalize, sigmoid, ctl->zall[active ? t : 0],
+                                               a.routed_scaling);
                 if (active) {
                     const int slot = s_slot[p];
                     if (slot >= 0) tab[slot >> 8].weight[slot & 255] = wgt;
