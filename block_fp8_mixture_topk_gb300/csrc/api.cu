@@ -98,9 +98,9 @@ struct ForwardLayout {
 
 // Steps of up to this many tokens take the decode path by default (MOE_DECODE_AUTO).  Measured on
 // GB300 with the DeepSeek-V3-shaped layer (E=256, top-8, tile-packed weights, CUDA-graph replay),
-// ms per step, decode path against the tile GEMMs: one token 0.085 / 0.090, two 0.140 / 0.141,
-// four 0.249 / 0.245, eight 0.421 / 0.387.
-constexpr int kDecodeAutoMaxTokens = 2;
+// ms per step, decode path against the tile GEMMs: two tokens 0.128 / 0.142, three 0.195 / 0.201,
+// four 0.242 / 0.249, five 0.280 / 0.269, six 0.333 / 0.318.
+constexpr int kDecodeAutoMaxTokens = 4;
 // the w13 GEMM visits an expert's few tiles column by column when one expert's w13 has at least
 // this many bytes (see GemmArgs::padded_offsets)
 constexpr int64_t kColumnOrderMinExpertBytes = int64_t(16) << 20;

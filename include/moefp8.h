@@ -405,7 +405,7 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
  * is recorded as the quantisation stage and the decode kernel as the w13 GEMM stage (the routing
  * stage holds the routing kernel or nothing; the sort and w2 stages are empty).
  *   MOE_DECODE_AUTO: the faster path for the step's size as measured on GB300: the decode
- *                    path for steps of one or two tokens, the tile GEMMs otherwise
+ *                    path for steps of up to four tokens, the tile GEMMs otherwise
  *   MOE_DECODE_OFF:  always the tile GEMMs
  *   MOE_DECODE_ON:   the decode path whenever the step qualifies */
 #define MOE_DECODE_AUTO 0

@@ -55,10 +55,11 @@ def test_host_only_queries():
     # sorted activation codes, the sorted intermediate, bf16 weighted rows in pair order
     assert ws >= rows * 7168 + rows * 2048 + 32768 * 7168 * 2
     assert moe.moe_fp8_block_workspace_size(16, 256, 256, 4, 2) > 0
-    # decode path (up to 2 tokens by default): its prologue + the decode kernel + the weighted sum
+    # decode path (up to 4 tokens by default): its prologue + the decode kernel + the weighted sum
     assert moe.moe_fp8_block_forward_kernel_count(2, 7168, 2048, 256, 8) == 3
+    assert moe.moe_fp8_block_forward_kernel_count(4, 7168, 2048, 256, 8) == 3
     # route + sort/quantise (one kernel up to 512 pairs, four above) + two GEMMs + weighted sum
-    assert moe.moe_fp8_block_forward_kernel_count(3, 7168, 2048, 256, 8) == 5
+    assert moe.moe_fp8_block_forward_kernel_count(5, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(64, 7168, 2048, 256, 8) == 5
     assert moe.moe_fp8_block_forward_kernel_count(65, 7168, 2048, 256, 8) == 8
     assert moe.moe_fp8_block_forward_kernel_count(0, 7168, 2048, 256, 8) == 0
@@ -88,7 +89,7 @@ def test_decode_path_selection():
     "on"."""
     dp = moe.moe_fp8_block_decode_path
     assert dp(1, 7168, 2048, 8, "on") and dp(8, 7168, 2048, 8, "on")
-    assert dp(1, 7168, 2048, 8) and dp(2, 7168, 2048, 8) and not dp(3, 7168, 2048, 8)
+    assert dp(1, 7168, 2048, 8) and dp(4, 7168, 2048, 8) and not dp(5, 7168, 2048, 8)
     assert not dp(9, 7168, 2048, 8) and not dp(4096, 7168, 2048, 8)
     # the decode prologue + the decode kernel (routing, sort, both GEMMs) + the weighted sum
     assert moe.moe_fp8_block_forward_kernel_count(1, 7168, 2048, 256, 8) == 3
