@@ -83,14 +83,18 @@ __global__ void __launch_bounds__(256) group_quant_kernel(const uint16_t* __rest
 
 // The same quantisation for the layer's common case, written to keep the instruction count low
 // (the general kernel above issued about 580 warp instructions per two groups and was bound by
-// instruction issue, not HBM): fp32 or UE8M0 scales only, every token's codes scattered to the
-// K sorted rows pos[r*K + j] (K fixed at compile time, the K row indices loaded as vectors once per
-// group; pos 16-byte aligned), 32-bit index arithmetic where the sizes allow (checked by the launcher).
-template <int K, bool UE8M0>
+// instruction issue, not HBM): 1x128 groups with fp32 or UE8M0 scales (s [groups][rows]), or
+// UE8M0 scale bytes in packed tiles (PACKED: sf, sf_kb4 as the general kernel's), or MXFP8 (MX:
+// 1x32 groups of four threads, their UE8M0 bytes in packed tiles), every token's
+// codes scattered to the K sorted rows pos[r*K + j] (K fixed at compile time, the K row indices
+// loaded as vectors once per group; pos 16-byte aligned), 32-bit index arithmetic where the
+// sizes allow (checked by the launcher).
+template <int K, bool UE8M0, bool PACKED, bool MX = false>
 __global__ void __launch_bounds__(256) group_quant_scatter_kernel(const uint16_t* __restrict__ x, int rows, int G,
                                                                   int ld, uint8_t* __restrict__ q, int q_ld,
                                                                   float* __restrict__ s, int s_gs,
-                                                                  const int32_t* __restrict__ pos) {
+                                                                  const int32_t* __restrict__ pos,
+                                                                  uint8_t* __restrict__ sf, int sf_kb4) {
     grid_dependency_wait();
     const int total = rows * G;
     const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
@@ -124,17 +128,23 @@ __global__ void __launch_bounds__(256) group_quant_scatter_kernel(const uint16_t
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
-        for (int o2 = 8; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+        for (int o2 = MX ? 2 : 8; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
         if (!active) continue;
         const float sc = group_scale_fmt(amax, UE8M0 ? MOE_SCALE_UE8M0 : MOE_SCALE_F32);
         const uint2 code = encode8(f, sc, __frcp_rn(sc));
         uint8_t* qg = q + g * 128 + sub * 8;
-        float* sg = s + g * s_gs;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             if (o[j] < 0) continue;
             *reinterpret_cast<uint2*>(qg + static_cast<int64_t>(o[j]) * q_ld) = code;
-            if (sub == 0) sg[o[j]] = sc;
+            if constexpr (MX) {
+                if ((sub & 3) == 0) sf[packed_sf_offset(o[j], g * 4 + (sub >> 2), sf_kb4)] = ue8m0_byte(sc);
+            } else if (sub == 0) {
+                if constexpr (PACKED)
+                    sf[packed_sf_offset(o[j], g, sf_kb4)] = ue8m0_byte(sc);
+                else
+                    s[g * s_gs + o[j]] = sc;
+            }
         }
     }
 }
@@ -322,28 +332,39 @@ cudaError_t launch_group_quant(const uint16_t* x, int64_t rows, int cols, int64_
                                int topk, int scale_fmt, cudaStream_t stream, uint8_t* sf, uint8_t* s8) {
     const int64_t groups = rows * (cols / 128);
     if (groups == 0) return cudaSuccess;
-    // the common case on its lean kernel: fp32 or UE8M0 scales [groups][rows] (row stride 1), rows
-    // scattered to pos with top-k 2 or 8, every offset within 32 bits
-    const bool lean = pos && s && !sf && !s8 && s_row_stride == 1 && (topk == 2 || topk == 8) &&
-                      (scale_fmt == MOE_SCALE_F32 || scale_fmt == MOE_SCALE_UE8M0) && ld <= INT32_MAX &&
+    // packed tiles: 4 scale columns per 32-bit word (MXFP8: 32-groups, 4 per 128-wide K block)
+    const int sf_kb4 = scale_fmt == MOE_SCALE_MXFP8 ? cols / 128 : (cols / 128 + 3) / 4;
+    // the common case on its lean kernel: fp32 or UE8M0 scales [groups][rows] (row stride 1), or
+    // only packed UE8M0 tiles, rows scattered to pos with top-k 2 or 8, every offset within 32 bits
+    const bool packed_only = sf && !s;   // packed UE8M0 tiles, or MXFP8 (its 32-group tiles)
+    const bool mx = scale_fmt == MOE_SCALE_MXFP8;
+    const bool lean = pos && ((s && !sf) || packed_only) && !s8 && s_row_stride == 1 && (topk == 2 || topk == 8) &&
+                      (scale_fmt == MOE_SCALE_F32 || scale_fmt == MOE_SCALE_UE8M0 || packed_only) && ld <= INT32_MAX &&
                       q_ld <= INT32_MAX && s_group_stride <= INT32_MAX && groups < (int64_t(1) << 30) &&
                       rows * topk < INT32_MAX && rows * ld < INT32_MAX && (cols / 128) * s_group_stride < INT32_MAX &&
                       (reinterpret_cast<uintptr_t>(pos) & 15) == 0;
     if (lean) {
         const int r32 = static_cast<int>(rows), G = cols / 128;
-#define MOE_QUANT_LEAN(KK, U8)                                                                              \
-    return launch_pdl(group_quant_scatter_kernel<KK, U8>, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, \
-                      r32, G, static_cast<int>(ld), q, static_cast<int>(q_ld), s, static_cast<int>(s_group_stride), pos)
+#define MOE_QUANT_LEAN(KK, U8, PK)                                                                           \
+    return launch_pdl(group_quant_scatter_kernel<KK, U8, PK>, dim3(grid_for(groups, 16)), dim3(256), 0, stream, \
+                      x, r32, G, static_cast<int>(ld), q, static_cast<int>(q_ld), s,                              \
+                      static_cast<int>(s_group_stride), pos, sf, sf_kb4)
         if (topk == 8) {
-            if (scale_fmt == MOE_SCALE_UE8M0) MOE_QUANT_LEAN(8, true);
-            MOE_QUANT_LEAN(8, false);
+            if (mx) return launch_pdl(group_quant_scatter_kernel<8, true, true, true>, dim3(grid_for(groups, 16)),
+                                      dim3(256), 0, stream, x, r32, G, static_cast<int>(ld), q, static_cast<int>(q_ld),
+                                      s, static_cast<int>(s_group_stride), pos, sf, sf_kb4);
+            if (packed_only) MOE_QUANT_LEAN(8, true, true);
+            if (scale_fmt == MOE_SCALE_UE8M0) MOE_QUANT_LEAN(8, true, false);
+            MOE_QUANT_LEAN(8, false, false);
         }
-        if (scale_fmt == MOE_SCALE_UE8M0) MOE_QUANT_LEAN(2, true);
-        MOE_QUANT_LEAN(2, false);
+        if (mx) return launch_pdl(group_quant_scatter_kernel<2, true, true, true>, dim3(grid_for(groups, 16)),
+                                  dim3(256), 0, stream, x, r32, G, static_cast<int>(ld), q, static_cast<int>(q_ld), s,
+                                  static_cast<int>(s_group_stride), pos, sf, sf_kb4);
+        if (packed_only) MOE_QUANT_LEAN(2, true, true);
+        if (scale_fmt == MOE_SCALE_UE8M0) MOE_QUANT_LEAN(2, true, false);
+        MOE_QUANT_LEAN(2, false, false);
 #undef MOE_QUANT_LEAN
     }
-    // packed tiles: 4 scale columns per 32-bit word (MXFP8: 32-groups, 4 per 128-wide K block)
-    const int sf_kb4 = scale_fmt == MOE_SCALE_MXFP8 ? cols / 128 : (cols / 128 + 3) / 4;
     const int fmt = scale_fmt == MOE_SCALE_MXFP8 ? MOE_SCALE_MXFP8 : (sf ? MOE_SCALE_UE8M0 : scale_fmt);
     return launch_pdl(group_quant_kernel, dim3(grid_for(groups, 16)), dim3(256), 0, stream, x, rows, cols, ld, q,
                       q_ld, s, s_row_stride, s_group_stride, pos, topk, fmt, sf, sf_kb4, s8);
