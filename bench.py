@@ -320,6 +320,13 @@ def profiled_traffic(wl, mode="tile", scale_fmt="f32"):
         return None
     if rec.get("tokens") not in (None, wl.T) or rec.get("scale_fmt", "f32") != scale_fmt:
         return None
+    # a record without a token count holds the named workload's own sizes; the expert counts it
+    # holds for are listed, else the named workload's
+    canon = mi.WORKLOADS.get(wl.name)
+    if rec.get("tokens") is None and canon is not None and wl.T != canon.T:
+        return None
+    if wl.E not in rec.get("experts", [canon.E if canon is not None else wl.E]):
+        return None
     try:
         return float(rec["dram_bytes_per_launch_full"])
     except (KeyError, TypeError, ValueError):
