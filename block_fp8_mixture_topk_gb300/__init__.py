@@ -21,6 +21,7 @@ from .ops import (  # noqa: F401
     moe_fp8_block_masked_workspace_size,
     moe_fp8_block_forward_kernel_count,
     moe_fp8_block_decode_path,
+    moe_fp8_block_pair_path,
     moe_fp8_block_pack_scales,
     moe_fp8_block_pack_weights,
     moe_fp8_block_workspace_size,

@@ -104,6 +104,13 @@ constexpr int kDecodeAutoMaxTokens = 4;
 // the w13 GEMM visits an expert's few tiles column by column when one expert's w13 has at least
 // this many bytes (see GemmArgs::padded_offsets)
 constexpr int64_t kColumnOrderMinExpertBytes = int64_t(16) << 20;
+// the block-scaled w2 GEMM runs on the CTA-pair kernel (gemm.cu) when the routed rows average at
+// least this many per expert: there the tensor pipe bounds it, and an expert's tiles pair up with
+// little padding (with fewer rows most experts have one or two tiles).  Measured on GB300 with the
+// Qwen3-30B-A3B-shaped skewed batch (16384 tokens, 1024 rows per expert), ms per layer: packed
+// UE8M0 0.735 with the pair kernel for w2 against 0.754 without it; with it for w13 too, 0.779 (the
+// w13 pair kernel, whose epilogue spills, ran 0.376 ms against 0.356 on the one-CTA kernel).
+constexpr int64_t kPairMinRowsPerExpert = 512;
 
 // Whether a step can take the decode-path GEMMs (decode.cu): at most 8 tokens (so at most 8
 // rows per expert), a sort small enough for a CTA's shared memory (the decode kernel sorts the
@@ -209,6 +216,13 @@ inline bool known_scale_fmt(int f) {
 }
 // formats whose GEMMs run on the block-scaled MMA: 1 = packed UE8M0, 2 = MXFP8, 0 = neither
 inline int sf_mode(int f) { return f == MOE_SCALE_UE8M0_PACKED ? 1 : f == MOE_SCALE_MXFP8 ? 2 : 0; }
+
+// Whether a step's block-scaled w2 GEMM qualifies for the CTA-pair kernel (besides the device's
+// clusters): a packed scale format, a hidden size of whole 256-column items and at least
+// kPairMinRowsPerExpert routed rows per expert on average (more than 32 tokens follows).
+bool pair_shape(int T, int H, int E, int topk, bool packed) {
+    return packed && H % 256 == 0 && static_cast<int64_t>(T) * topk >= kPairMinRowsPerExpert * E;
+}
 
 }  // namespace
 
@@ -578,6 +592,15 @@ int moe_fp8_block_forward_kernel_count(int T, int H, int I, int E, int topk) {
     return moe_fp8_block_forward_kernel_count_ex(T, H, I, E, topk, nullptr, nullptr);
 }
 
+int moe_fp8_block_pair_path(int T, int H, int E, int topk, int scale_fmt) {
+    if (T < 0 || H < 0 || E < 1 || topk < 1 || !known_scale_fmt(scale_fmt)) return MOE_ERR_INVALID_ARG;
+    if (!pair_shape(T, H, E, topk, sf_mode(scale_fmt) != 0)) return 0;
+    DeviceState* st = nullptr;
+    const int rc = device_state(&st);
+    if (rc != MOE_OK) return rc;
+    return gemm_pair_clusters();
+}
+
 int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode) {
     if (T < 0 || H < 0 || I < 0 || topk < 1) return -1;
     if (mode != MOE_DECODE_AUTO && mode != MOE_DECODE_OFF && mode != MOE_DECODE_ON) return -1;
@@ -697,6 +720,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
     // an expert holds at most T rows: with T <= 32 only the first 32 rows of a tile can be
     // real, so the GEMMs load 32-row activation boxes
     const int a_box_rows = T <= 32 ? 32 : 128;
+    const bool pair = pair_shape(T, H, E, topk, packed) && a_box_rows == 128 && gemm_pair_clusters() > 0;
 
     auto mark = [&](int i) {
         return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
@@ -865,6 +889,7 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
             g.sf_packed = sfm;
             g.a_sf = a2sf;
             g.b_sf = reinterpret_cast<const uint8_t*>(w2_scale);
+            if (pair) g.pair_offsets = reinterpret_cast<const int32_t*>(ws + L.poff);
         }
         g.status = st->status;
         e = launch_grouped_gemm(g, st->num_sms, s);

@@ -55,11 +55,21 @@ constexpr int NUM_THREADS = (FIRST_EPI_WARP + NUM_EPI_WARPS) * 32;
 // registers per thread: 168 at launch (384 threads).  Warpgroup 0 (the TMA, MMA and
 // scale warps) gives some back and the two epilogue warpgroups take them: 128*c + 256*e
 // <= 384*168.  The SiLU epilogue holds more live values (gate and up halves); the
-// splits are the ones with the fewest spills.
+// splits are the ones with the fewest spills.  A spill in a control warp is a local-memory
+// round trip in the loop that feeds the tensor pipe; with most of the SM's L1 given to shared
+// memory it can reach L2.
 template <int EPI>
 struct RegSplit {
-    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 72 : 104;
-    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 216 : 192;
+    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 72 : 120;
+    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 216 : 184;
+    static_assert(128 * control + 256 * epilogue <= 384 * 168, "register split over the launch budget");
+};
+// the block-scaled kernels (no promotion in the epilogue): the SiLU epilogue needs fewer registers
+// and the control warps more (none spill at 88 / 208; at 72 / 216 the control warps spilled)
+template <int EPI>
+struct RegSplitBs {
+    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 88 : 104;
+    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 208 : 192;
     static_assert(128 * control + 256 * epilogue <= 384 * 168, "register split over the launch budget");
 };
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
@@ -747,7 +757,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     if (warp < FIRST_EPI_WARP) {
-      regs_decrease<RegSplit<EPI>::control>();
+      regs_decrease<RegSplitBs<EPI>::control>();
       if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
@@ -871,7 +881,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     } else {
-        regs_increase<RegSplit<EPI>::epilogue>();
+        regs_increase<RegSplitBs<EPI>::epilogue>();
         // ---------------------------------------------------------------- epilogue
         const int g = (warp - FIRST_EPI_WARP) >> 2;   // column half
         const int sp = warp & 3;                      // TMEM lane quarter
@@ -925,12 +935,512 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair block-scaled variant
+// The block-scaled GEMM on the two-SM MMA.  A cluster of two CTAs computes a 256-row x 256-column
+// work item (two 128-row tiles of one expert): each CTA keeps its own 128 rows of A and one of the
+// item's two 128-row weight bands in its shared memory, and CTA 0 issues tcgen05.mma.cta_group::2
+// (M = 256), which reads both CTAs' operands and accumulates each CTA's 128 rows x 256 columns in
+// that CTA's tensor memory.  A K block then brings 32 KB into each SM instead of 48 KB for the same
+// multiply-adds: the operand feed that bounds the one-CTA kernel on batches with many rows per
+// expert drops by a third.
+// Facts about the pair forms that this layout relies on (checked on GB300 with one 256 x 256 x 128
+// item, exact against a host computation): the allocation is collective (both CTAs allocate and get
+// the same base); tcgen05.cp.cta_group::2 copies each CTA's shared memory into its own tensor
+// memory; each CTA needs the weight scale factors of all 256 columns (both bands' tiles) beside its
+// own rows' activation scale factors; CTA 0's band supplies columns 0..127.
+// Synchronisation: the ring holds P_SUPER stages of P_SUB K blocks.  Both CTAs' loads of a stage
+// (TMA with .cta_group::2: operand and scale-factor tiles into each CTA's own shared memory)
+// complete their bytes on CTA 0's full barrier, which CTA 0's producer armed with the stage's bytes
+// of both CTAs.  A second thread of CTA 0 copies the scale-factor tiles of the stage into a ring of
+// tensor-memory slots (tcgen05.cp.cta_group::2) and signals each slot on its own barrier; the MMA
+// thread waits for the stage and the slots it reads, issues the stage's MMAs and commits them to
+// both CTAs' empty barriers (multicast), so each producer refills its own stage; an item's last
+// commit arrives on both CTAs' tfull; the epilogue warps of both CTAs arrive on CTA 0's tempty
+// before the next item's MMAs overwrite the accumulators.
+// The single MMA thread bounds these kernels: issuing a pair MMA takes 60-80 cycles of its time
+// against 128 for the tensor pipe to run it, and each barrier wait, commit and scale-factor copy
+// another 100-200 (cycle counts of an instrumented copy on GB300).  Hence two K blocks (eight MMAs)
+// per barrier wait and commit, and the copies on another thread.  (Forwarding each stage from a
+// thread of CTA 1 to CTA 0 instead of the .cta_group::2 loads cost about 0.3 us per stage.)
+// Work: candidate w of the tile-major order (tile m, column block n) is an item when tile m sits at
+// an even position among its expert's tiles; CTA 0 takes tile m and CTA 1 tile m + 1, or, when
+// the expert has no tile m + 1, a copy of tile m's rows whose results it discards.
+constexpr int P_SUB = 2;                       // K blocks per stage
+constexpr int P_SUPER = 3;                     // stages
+constexpr int P_STAGES = P_SUB * P_SUPER;      // K-block buffers
+constexpr int P_SF_STAGE = 3 * kSfTileBytes;   // per K block: this CTA's rows' A tile, then both bands' B tiles
+constexpr int P_SF_SLOTS = 8;                  // > P_STAGES: a slot's last MMAs completed before its reuse
+constexpr int P_ITEMS = 128;                   // candidates of a cluster cached in shared memory
+
+struct SmemCtlPair {
+    uint64_t full[P_SUPER];            // (CTA 0) both CTAs' loads of the stage landed
+    uint64_t empty[P_SUPER];           // the stage's MMAs completed (commit from CTA 0, both CTAs)
+    uint64_t sf_ready[P_SF_SLOTS];     // (CTA 0) the slot's scale-factor copies completed
+    uint64_t sf_drain;                 // (CTA 0) all scale-factor copies completed
+    uint64_t tfull;                    // the item's accumulators are complete (both CTAs)
+    uint64_t tempty;                   // (CTA 0) both CTAs' epilogue warps moved them out (16 arrivals)
+    uint64_t amax_bar[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    float amax_x[2][2][BM];
+    alignas(16) float stage[NUM_EPI_WARPS][32 * 20];
+    int item_n[P_ITEMS];               // the cluster's candidates in visiting order: column block,
+    int item_e[P_ITEMS];               // expert (-1: not an item, -2: an item with a bad tile entry),
+    int item_r0[P_ITEMS];              // first row of this CTA's tile,
+    int item_live[P_ITEMS];            // and whether that tile is one of the expert's
+};
+constexpr size_t SMEM_BYTES_PAIR = 1024 + P_STAGES * (A_TILE + B_HALF + P_SF_STAGE) + sizeof(SmemCtlPair);
+static_assert(SMEM_BYTES_PAIR <= 232448, "shared memory per CTA exceeds the sm_103 limit");
+static_assert(TMEM_SF + P_SF_SLOTS * 16 <= TMEM_COLS, "scale-factor slots exceed the tensor-memory allocation");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// TMA tile loads into this CTA's shared memory whose bytes complete on `bar`, a shared::cluster
+// address that may be the other CTA's barrier (the .cta_group::2 form).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t smem_dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+// Arrive on a barrier of either CTA of the pair (shared::cluster address).  CTA-scope release, like
+// the waits (mbar_wait): the arrivals hand over tensor memory (ordered by the tcgen05 fences around
+// the barrier) and shared-memory stages (written by TMA, completion counted on the barrier), never
+// data the arriving thread wrote itself; a cluster-scope release made every arrival of the
+// epilogue warps wait for their earlier global stores.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// All threads of both CTAs.
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Each CTA's 512-byte scale-factor tile at this shared-memory address into its own tensor memory.
+__device__ __forceinline__ void tmem_copy_sf_tile_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// D (256 x N over both CTAs) (+)= (A * sfA) * (B * sfB)^T, K = 32, issued by one thread of CTA 0.
+__device__ __forceinline__ void mma_e4m3_block_scaled_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                           uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the barrier at this offset in each CTA of `mask` when the MMAs issued so far complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+struct PairItem {
+    int64_t row0;   // this CTA's tile's first row
+    int e, n;
+    bool take;      // candidate is an item
+    bool ok;        // its tile entries are valid
+    bool live;      // this CTA's tile is one of the expert's
+};
+
+// Candidate w (tile m, column block n) from the tile table and the experts' padded row offsets.
+// Everything but row0 and live is the same in both CTAs, so both skip the same candidates.
+__device__ __forceinline__ PairItem pair_item_lookup(const GemmArgs& a, int64_t w, int NT, uint32_t rank,
+                                                     int64_t ntiles) {
+    PairItem p;
+    const int64_t mt = w / NT;
+    const int m = static_cast<int>(mt);
+    p.n = static_cast<int>(w - mt * NT);
+    p.e = a.tile_expert[m];
+    p.take = true;
+    p.ok = false;
+    p.live = false;
+    p.row0 = 0;
+    if (p.e < 0 || p.e >= a.E) return p;
+    const int f = a.pair_offsets[p.e] / BM, end = a.pair_offsets[p.e + 1] / BM;
+    if (m < f || m >= end) return p;
+    if (((m - f) & 1) != 0) {
+        p.take = false;
+        return p;
+    }
+    const bool has2 = m + 1 < end && m + 1 < ntiles;
+    const int64_t r_first = a.tile_row0[m];
+    const int64_t r_second = has2 ? a.tile_row0[m + 1] : r_first;
+    const auto valid = [&](int64_t r) { return r >= 0 && (r & (BM - 1)) == 0 && r + BM <= a.a_rows; };
+    p.ok = valid(r_first) && valid(r_second);
+    p.live = rank == 0 || has2;
+    p.row0 = rank == 0 ? r_first : r_second;
+    return p;
+}
+
+__device__ __forceinline__ PairItem pair_item(const GemmArgs& a, const SmemCtlPair* ctl, int64_t k, int64_t w, int NT,
+                                              uint32_t rank, int64_t ntiles) {
+    if (k < P_ITEMS) {
+        PairItem p;
+        const int ce = ctl->item_e[k];
+        p.n = ctl->item_n[k];
+        p.e = ce;
+        p.take = ce != -1;
+        p.ok = ce >= 0;
+        p.row0 = ctl->item_r0[k];
+        p.live = ctl->item_live[k] != 0;
+        return p;
+    }
+    return pair_item_lookup(a, w, NT, rank, ntiles);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                             const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint8_t* smA = base;
+    uint8_t* smB = base + P_STAGES * A_TILE;
+    uint8_t* smSF = smB + P_STAGES * B_HALF;
+    SmemCtlPair* ctl = reinterpret_cast<SmemCtlPair*>(smSF + P_STAGES * P_SF_STAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    const int NT = a.N / 256;   // silu: gate band n with up band N/256 + n; otherwise bands 2n, 2n + 1
+    const int KB = a.K / BK;
+    const bool mx = a.sf_packed == 2;
+    const int KB4 = mx ? KB : (KB + 3) / 4;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_SUPER; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int s = 0; s < P_SF_SLOTS; ++s) mbar_init(smem_addr(&ctl->sf_ready[s]), 1);
+        mbar_init(smem_addr(&ctl->sf_drain), 1);
+        mbar_init(smem_addr(&ctl->tfull), 1);
+        mbar_init(smem_addr(&ctl->tempty), 2 * NUM_EPI_WARPS);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_addr(&ctl->amax_bar[b]), NUM_EPI_WARPS * 32);
+        mbar_init(smem_addr(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmSFA);
+        tma_prefetch_map(&tmSFB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();   // both CTAs' barriers initialised before any arrival from the other
+    tc_fence_after();
+    grid_dependency_wait();
+    int64_t ntiles = *a.num_tiles;
+    if (ntiles < 0) ntiles = 0;
+    if (ntiles > a.max_tiles) ntiles = a.max_tiles;
+    const int64_t total = ntiles * NT;
+    for (int64_t k = threadIdx.x; k < P_ITEMS; k += blockDim.x) {
+        const int64_t w = cid + k * ncl;
+        if (w >= total) break;
+        const PairItem p = pair_item_lookup(a, w, NT, rank, ntiles);
+        ctl->item_n[k] = p.n;
+        ctl->item_e[k] = !p.take ? -1 : (p.ok ? p.e : -2);
+        ctl->item_r0[k] = static_cast<int>(p.row0);
+        ctl->item_live[k] = p.live ? 1 : 0;
+    }
+    __syncthreads();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int* abort_flag = &ctl->abort_flag;
+    if (warp < FIRST_EPI_WARP) {
+      regs_decrease<RegSplitBs<EPI>::control>();
+      if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0, issued = 0;
+            bool ok = true;
+            int64_t k = 0;
+            const int NBn = a.N / 128;
+            for (int64_t w = cid; w < total && ok; w += ncl, ++k) {
+                const PairItem p = pair_item(a, ctl, k, w, NT, rank, ntiles);
+                if (!p.take) continue;
+                if (!p.ok) {
+                    status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
+                    continue;
+                }
+                const int bcol0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? p.n * 128 : p.n * 256;
+                const int bcol1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 2 + p.n * 128 : bcol0 + 128;
+                const int band = rank == 0 ? bcol0 : bcol1;   // the weight rows this CTA holds
+                int32_t by0, bdx, bdy;
+                if (a.b_tiled) {
+                    by0 = ((p.e * NBn + band / 128) * KB) * 128;
+                    bdx = 0;
+                    bdy = 128;
+                } else {
+                    by0 = p.e * a.N + band;
+                    bdx = BK;
+                    bdy = 0;
+                }
+                // scale-factor tiles (index into the packed arrays, tensor maps of 512-byte tiles)
+                const int32_t sfa = static_cast<int32_t>((p.row0 >> 7) * KB4);
+                const int32_t sfb0 = (p.e * NBn + bcol0 / 128) * KB4;
+                const int32_t sfb1 = (p.e * NBn + bcol1 / 128) * KB4;
+                for (int kb0 = 0; kb0 < KB; kb0 += P_SUB) {
+                    const int nsub = KB - kb0 < P_SUB ? KB - kb0 : P_SUB;
+                    if (!mbar_wait(smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb0 = smem_addr(&ctl->full[stage]);
+                    const uint32_t fb = cluster_map(fb0, 0);   // CTA 0's full barrier
+                    uint32_t bytes = 0;
+                    for (int j = 0; j < nsub; ++j)
+                        bytes += A_TILE + B_HALF + ((mx || ((kb0 + j) & 3) == 0) ? P_SF_STAGE : 0u);
+                    if (rank == 0) mbar_arrive_expect_tx(fb0, 2 * bytes);
+                    for (int j = 0; j < nsub; ++j) {
+                        const int kb = kb0 + j, buf = stage * P_SUB + j;
+                        tma_load_2d_pair(smem_addr(smA + buf * A_TILE), &tmA, kb * BK, static_cast<int32_t>(p.row0), fb);
+                        tma_load_2d_pair(smem_addr(smB + buf * B_HALF), &tmB, kb * bdx, by0 + kb * bdy, fb);
+                        if (mx || (kb & 3) == 0) {
+                            const uint32_t dst = smem_addr(smSF + buf * P_SF_STAGE);
+                            const int32_t q = mx ? kb : kb >> 2;
+                            tma_load_3d_pair(dst, &tmSFA, 0, 0, sfa + q, fb);
+                            tma_load_3d_pair(dst + kSfTileBytes, &tmSFB, 0, 0, sfb0 + q, fb);
+                            tma_load_3d_pair(dst + 2 * kSfTileBytes, &tmSFB, 0, 0, sfb1 + q, fb);
+                        }
+                    }
+                    ++issued;
+                    if (++stage == P_SUPER) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // after an abort, CTA 0 waits (bounded) for the loads of the stages it armed, both
+            // CTAs' bytes; CTA 1 cannot see its loads' completion, and waits at the closing
+            // cluster barrier for CTA 0 (its own loads land within microseconds, its producer
+            // leaves the loop only after a wait of kWaitLimitNs gave up or after its last stage)
+            if (!ok && rank == 0) {
+                for (int s = 0; s < P_SUPER; ++s) {
+                    const uint32_t n_s = (issued + P_SUPER - 1 - s) / P_SUPER;
+                    if (n_s > 0) mbar_wait(smem_addr(&ctl->full[s]), (n_s - 1) & 1u, nullptr, a.status);
+                }
+            }
+        }
+      } else if (warp == 2 && lane == 0 && rank == 0) {
+        // ---------------------------------------------------------------- CTA 0: scale factors
+        // Slot u % P_SF_SLOTS takes the u-th scale-factor load.  It is rewritten P_SF_SLOTS loads
+        // (at least P_SF_SLOTS K blocks) later, after this thread waited for the stage bringing the
+        // new tiles, which was refilled only once the MMAs P_STAGES K blocks back had completed.
+        int stage = 0;
+        uint32_t phase = 0, sf_loads = 0;
+        bool ok = true;
+        int64_t k = 0;
+        for (int64_t w = cid; w < total && ok; w += ncl, ++k) {
+            const PairItem p = pair_item(a, ctl, k, w, NT, rank, ntiles);
+            if (!p.take || !p.ok) continue;
+            for (int kb0 = 0; kb0 < KB; kb0 += P_SUB) {
+                const int nsub = KB - kb0 < P_SUB ? KB - kb0 : P_SUB;
+                bool any = false;
+                for (int j = 0; j < nsub; ++j) any = any || mx || ((kb0 + j) & 3) == 0;
+                if (any) {
+                    if (!mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < nsub; ++j) {
+                        if (!(mx || ((kb0 + j) & 3) == 0)) continue;
+                        const uint32_t slot = sf_loads % P_SF_SLOTS;
+                        const uint32_t t_sf = tmem + TMEM_SF + slot * 16;
+                        const uint32_t src = smem_addr(smSF + (stage * P_SUB + j) * P_SF_STAGE);
+                        tmem_copy_sf_tile_pair(t_sf, smem_desc_sf_tile(src));
+                        tmem_copy_sf_tile_pair(t_sf + 4, smem_desc_sf_tile(src + kSfTileBytes));
+                        tmem_copy_sf_tile_pair(t_sf + 8, smem_desc_sf_tile(src + 2 * kSfTileBytes));
+                        mma_commit_pair(smem_addr(&ctl->sf_ready[slot]), 1);
+                        ++sf_loads;
+                    }
+                }
+                if (++stage == P_SUPER) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        mma_commit_pair(smem_addr(&ctl->sf_drain), 1);
+        mbar_wait(smem_addr(&ctl->sf_drain), 0, nullptr, a.status);
+      } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------------------------------------------------------- CTA 0: MMA issuer
+        int stage = 0;
+        uint32_t phase = 0, items = 0, sf_loads = 0;
+        bool ok = true;
+        int64_t k = 0;
+        for (int64_t w = cid; w < total && ok; w += ncl, ++k) {
+            const PairItem p = pair_item(a, ctl, k, w, NT, rank, ntiles);
+            if (!p.take || !p.ok) continue;
+            if (!mbar_wait(smem_addr(&ctl->tempty), (items & 1u) ^ 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sfa_t = 0, sfb_t = 0;
+            for (int kb0 = 0; kb0 < KB && ok; kb0 += P_SUB) {
+                const int nsub = KB - kb0 < P_SUB ? KB - kb0 : P_SUB;
+                if (!mbar_wait(smem_addr(&ctl->full[stage]), phase, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < nsub; ++j) {
+                    const int kb = kb0 + j;
+                    if (mx || (kb & 3) == 0) {
+                        const uint32_t slot = sf_loads % P_SF_SLOTS;
+                        if (!mbar_wait(smem_addr(&ctl->sf_ready[slot]), (sf_loads / P_SF_SLOTS) & 1u, abort_flag,
+                                       a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        sfa_t = tmem + TMEM_SF + slot * 16;
+                        sfb_t = sfa_t + 4;
+                        ++sf_loads;
+                    }
+                    const uint32_t a0 = smem_addr(smA + (stage * P_SUB + j) * A_TILE);
+                    const uint32_t b0 = smem_addr(smB + (stage * P_SUB + j) * B_HALF);
+#pragma unroll
+                    for (int s = 0; s < BK / 32; ++s) {
+                        const uint32_t idesc = idesc_e4m3_ue8m0(2 * BM, 256, mx ? s : (kb & 3));
+                        mma_e4m3_block_scaled_pair(tmem, smem_desc_k128_sw128(a0 + s * 32),
+                                                   smem_desc_k128_sw128(b0 + s * 32), idesc, sfa_t, sfb_t,
+                                                   (kb | s) != 0 ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(smem_addr(&ctl->empty[stage]), 3);
+                if (++stage == P_SUPER) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit_pair(smem_addr(&ctl->tfull), 3);
+            ++items;
+        }
+        // every MMA complete before the CTAs can leave (they read both CTAs' shared memory)
+        mma_commit_pair(smem_addr(&ctl->drain), 1);
+        mbar_wait(smem_addr(&ctl->drain), 0, nullptr, a.status);
+      }
+    } else {
+        regs_increase<RegSplitBs<EPI>::epilogue>();
+        // ---------------------------------------------------------------- epilogue (both CTAs)
+        const int g = (warp - FIRST_EPI_WARP) >> 2;   // column half
+        const int sp = warp & 3;                      // TMEM lane quarter
+        const int row = sp * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        const uint32_t tempty0 = cluster_map(smem_addr(&ctl->tempty), 0);
+        uint32_t acc_iter = 0, epi_iter = 0;
+        bool ok = true;
+        int64_t k = 0;
+        for (int64_t w = cid; w < total && ok; w += ncl, ++k) {
+            const PairItem p = pair_item(a, ctl, k, w, NT, rank, ntiles);
+            if (!p.take || !p.ok) continue;
+            Tile t;
+            t.row0 = p.row0;
+            t.e = p.e;
+            t.n = p.n;
+            t.bcol0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? p.n * 128 : p.n * 256;
+            t.bcol1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 2 + p.n * 128 : t.bcol0 + 128;
+            t.has1 = true;
+            t.ok = true;
+            const int64_t grow = t.row0 + row;
+            const bool row_real = p.live && (a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0);
+            const bool active = __any_sync(0xffffffffu, row_real);
+            float acc[128];
+            if (!mbar_wait(smem_addr(&ctl->tfull), acc_iter & 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (active) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t c0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? lane_base + r * 128 + g * 64
+                                                                        : lane_base + g * 128 + r * 64;
+                    tmem_ld32x2(c0, c0 + 32, acc + r * 64, acc + r * 64 + 32);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty0);
+            ++acc_iter;
+            if (p.live) {
+                if (!finish_item<EPI>(a, ctl, t, acc, warp, lane, g, row, grow, active, epi_iter, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++epi_iter;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();   // neither CTA leaves while the other's MMAs or arrivals may still reach it
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn g_encode = nullptr;
+int g_pair_clusters = 0;   // clusters of two CTAs of the pair kernel resident at once (0: unavailable)
 std::once_flag g_encode_once;
 
 cudaError_t get_encoder() {
@@ -1061,7 +1571,55 @@ cudaError_t gemm_init_device() {
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(grouped_gemm_bs_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_bs);
+    const int bytes_pair = static_cast<int>(SMEM_BYTES_PAIR);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_pair);
+    if (err == cudaSuccess) {
+        // clusters of two that fit on the device at once (one CTA per SM; pairs within a GPC)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES_PAIR;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<MOE_EPI_WEIGHTED_PAIRS_BF16>, &cfg) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        g_pair_clusters = n;
+    }
     return err;
+}
+
+int gemm_pair_clusters() { return g_pair_clusters; }
+
+// The CTA-pair kernel: clusters of two CTAs, launched like the others with programmatic serialisation.
+template <int EPI>
+cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmSFA,
+                        const CUtensorMap& tmSFB, const GemmArgs& args, unsigned clusters, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES_PAIR;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<EPI>, tmA, tmB, tmSFA, tmSFB, args);
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t stream) {
@@ -1069,6 +1627,31 @@ cudaError_t launch_grouped_gemm(const GemmArgs& args, int num_sms, cudaStream_t 
     const int64_t bound = args.max_tiles * NT;
     if (bound == 0) return cudaSuccess;
     CUtensorMap tmA, tmB;
+    if (args.pair_offsets) {
+        if (!args.sf_packed || args.N % 256 != 0 || args.a_box_rows != 128 || args.epi != MOE_EPI_WEIGHTED_PAIRS_BF16)
+            return cudaErrorInvalidValue;
+        if (g_pair_clusters < 1) return cudaErrorNotSupported;
+        cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows, 128);
+        if (err != cudaSuccess) return err;
+        if (args.b_tiled)
+            err = make_map(&tmB, args.B, 128, static_cast<int64_t>(args.E) * args.N * (args.K / 128));
+        else
+            err = make_map(&tmB, args.B, args.K, static_cast<int64_t>(args.E) * args.N);
+        if (err != cudaSuccess) return err;
+        // the packed scale-factor arrays as rows of 512-byte tiles (box: one tile)
+        if (args.a_rows % 128 != 0) return cudaErrorInvalidValue;
+        const uint64_t KB = args.K / 128, kb4 = args.sf_packed == 2 ? KB : (KB + 3) / 4;
+        const uint64_t sf_strides[2] = {256, 512};
+        const uint32_t sf_box[3] = {256, 2, 1};
+        const uint64_t a_dims[3] = {256, 2, static_cast<uint64_t>(args.a_rows / 128) * kb4};
+        const uint64_t b_dims[3] = {256, 2, static_cast<uint64_t>(args.E) * (args.N / 128) * kb4};
+        CUtensorMap tmSFA, tmSFB;
+        err = encode_u8_map_nd(&tmSFA, args.a_sf, 3, a_dims, sf_strides, sf_box, false);
+        if (err == cudaSuccess) err = encode_u8_map_nd(&tmSFB, args.b_sf, 3, b_dims, sf_strides, sf_box, false);
+        if (err != cudaSuccess) return err;
+        const unsigned clusters = static_cast<unsigned>(bound < g_pair_clusters ? bound : g_pair_clusters);
+        return launch_pair<MOE_EPI_WEIGHTED_PAIRS_BF16>(tmA, tmB, tmSFA, tmSFB, args, clusters, stream);
+    }
     if (args.a_box_rows != 32 && args.a_box_rows != 128) return cudaErrorInvalidValue;
     cudaError_t err = make_map(&tmA, args.A, args.K, args.a_rows, static_cast<uint32_t>(args.a_box_rows));
     if (err != cudaSuccess) return err;

@@ -149,9 +149,15 @@ struct GemmArgs {
     const uint8_t* a_sf;
     const uint8_t* b_sf;
     uint8_t* out_sf;
+    // non-null (with sf_packed and the weighted-pairs epilogue): the CTA-pair kernel (gemm.cu),
+    // whose items are two consecutive tiles of one expert; [E + 1] padded row offsets of the tile
+    // table (tile m = rows [128m, 128m + 128)).  Needs N % 256 == 0 and a_box_rows == 128.
+    const int32_t* pair_offsets;
     uint32_t* status;
 };
 cudaError_t gemm_init_device();
+// Clusters of two CTAs of the pair GEMM kernel that are resident at once (0 if it cannot run).
+int gemm_pair_clusters();
 // Tensor map of a 2-D byte matrix [rows, cols] (row stride = cols bytes), boxes of
 // box_cols x box_rows, with the 128-byte swizzle or none.
 cudaError_t encode_u8_map(CUtensorMap* map, const uint8_t* ptr, int64_t cols, int64_t rows, uint32_t box_cols,

@@ -106,6 +106,7 @@ def lib():
                 "moe_fp8_block_forward_kernel_count": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward_kernel_count_ex": ([I, I, I, I, I, P, P], I),
                 "moe_fp8_block_decode_path": ([I, I, I, I, I], I),
+                "moe_fp8_block_pair_path": ([I, I, I, I, I], I),
                 "moe_fp8_block_forward": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_packed": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, SZ, P, P], I),
                 "moe_fp8_block_forward_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P, P, P], I),
@@ -382,6 +383,15 @@ def moe_combine_pairs(y, pos, T, topk, out=None):
     rc = lib().moe_combine_pairs(_ptr(y), _ptr(pos), T, topk, H, _ptr(out), _stream())
     _check("moe_combine_pairs", rc)
     return out
+
+
+def moe_fp8_block_pair_path(T, H, E, topk, scale_fmt="f32") -> int:
+    """Two-CTA clusters that the step's tile GEMMs launch on the CTA-pair kernel (0: the one-CTA
+    kernels)."""
+    r = int(lib().moe_fp8_block_pair_path(T, H, E, topk, SCALE_FMT[scale_fmt]))
+    if r < 0:
+        raise MoeError("moe_fp8_block_pair_path", r)
+    return r
 
 
 def moe_fp8_block_decode_path(T, H, I, topk, decode="auto") -> bool:

@@ -415,6 +415,19 @@ int moe_fp8_block_forward_packed(const uint16_t* hidden, const float* router_log
  * under `mode`, 0 if it takes the tile GEMMs, -1 for a negative size, topk < 1 or an unknown
  * mode.  Host only. */
 int moe_fp8_block_decode_path(int T, int H, int I, int topk, int mode);
+/* Whether the w2 GEMM of a step of T tokens (hidden H, E experts, this top-k) in `scale_fmt`
+ * runs on the CTA-pair kernel: two CTAs of a cluster compute two consecutive 128-row tiles of one
+ * expert with the two-SM tensor-core MMA (tcgen05.mma.cta_group::2, M = 256), each CTA holding its
+ * own rows of the activations and half of the 256 weight rows of the item, so that an SM takes in
+ * a third fewer operand bytes per multiply-add.  Taken with the packed block-scaled formats
+ * (MOE_SCALE_UE8M0_PACKED, MOE_SCALE_MXFP8) when H is a multiple of 256 and the step routes at
+ * least 512 rows per expert on average (the tensor-bound regime, where an expert's tiles pair up
+ * with little padding); the w13 GEMM stays on the one-CTA kernel (faster there as measured).
+ * Returns the number of two-CTA clusters the w2 GEMM launches (> 0), 0 if the step takes the
+ * one-CTA kernels, MOE_ERR_INVALID_ARG for a negative size, E or topk < 1 or an unknown format, or
+ * an error code if no usable device is present (the cluster count is the device's: pairs of SMs
+ * within a GPC). */
+int moe_fp8_block_pair_path(int T, int H, int E, int topk, int scale_fmt);
 
 /* Options of the layer: the expert weights' layout, the scale format of the activations
  * and of the requantised intermediate, and the GEMM kernels of small steps

@@ -83,6 +83,21 @@ def test_forward_kernel_count_with_options():
     assert kc(0, 7168, 2048, 256, 8, dsv3) == 0
 
 
+def test_pair_path_selection_without_a_device():
+    """The shape rule of the CTA-pair GEMMs is host logic: steps that do not qualify give 0 with or
+    without a device; invalid arguments give MOE_ERR_INVALID_ARG."""
+    L = ops.lib()
+    f32, packed, mx = (ops.SCALE_FMT[k] for k in ("f32", "ue8m0_packed", "mxfp8"))
+    assert L.moe_fp8_block_pair_path(16384, 2048, 128, 8, f32) == 0            # fp32 scales
+    assert L.moe_fp8_block_pair_path(4096, 7168, 256, 8, packed) == 0          # 128 rows per expert
+    assert L.moe_fp8_block_pair_path(16384, 2176, 128, 8, packed) == 0         # H not whole 256-column items
+    assert L.moe_fp8_block_pair_path(8191, 2048, 128, 8, mx) == 0              # 511.9 rows per expert
+    assert L.moe_fp8_block_pair_path(-1, 2048, 128, 8, packed) == -1
+    assert L.moe_fp8_block_pair_path(16, 2048, 0, 8, packed) == -1
+    assert L.moe_fp8_block_pair_path(16, 2048, 4, 0, packed) == -1
+    assert L.moe_fp8_block_pair_path(16, 2048, 4, 2, 9) == -1
+
+
 def test_decode_path_selection():
     """"on" takes the decode-path GEMMs for any step they can serve (at most 8 tokens, at most
     512 routed pairs, an expert's w13 under 2^31 bytes), "off" never, "auto" never more than

@@ -304,11 +304,13 @@ def test_packed_layer_rejects_the_decode_kernel_and_nvfp4():
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("pair", [False, True], ids=["one_cta", "cta_pair"])
 @pytest.mark.parametrize("fmt", ["ue8m0_packed", "mxfp8"])
-def test_block_scaled_layer_repeats_and_replays_from_a_cuda_graph(fmt):
+def test_block_scaled_layer_repeats_and_replays_from_a_cuda_graph(fmt, pair):
     """Ten calls on one dirty workspace and a CUDA-graph replay on new inputs give the same bytes
-    as a fresh eager call, in both block-scaled formats."""
-    wl = mi.Workload("bs_graph", 163, 300, 256, 384, 6, 2)
+    as a fresh eager call, in both block-scaled formats, on the one-CTA GEMMs (50 rows per expert)
+    and on the CTA-pair GEMMs (600 rows per expert)."""
+    wl = mi.Workload("bs_graph", 163, 1200, 256, 384, 2, 1) if pair else mi.Workload("bs_graph", 163, 300, 256, 384, 6, 2)
     if fmt == "mxfp8":
         from test_gpu_mxfp8 import MxLayer
         layer = MxLayer(wl)

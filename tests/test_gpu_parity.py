@@ -532,14 +532,18 @@ def test_forward_full_size_every_tile_sampled(name):
     assert_output_close(out, ref["out"], rows=tokens)
 
 
-def test_forward_more_items_than_a_cta_caches():
+@pytest.mark.parametrize("fmt", ["f32", "ue8m0_packed"])
+def test_forward_more_items_than_a_cta_caches(fmt):
     """Both grouped GEMMs with more than 256 work items per CTA on every SM (a CTA caches its first
     256 items' tile, column block, expert and first row in shared memory and looks up later ones
     in global memory).  H=4096, I=2048: 16 column blocks per tile in each GEMM; 50000 tokens, top-8
     over 32 experts: about 3150 tiles, so the items of tiles from 16 x (SM count) on come after a
     CTA's 256th.  Experts 28-31 hold exactly 300 rows each (three tiles, a w13 of 16 MB: the w13
     GEMM visits their tiles column by column) and sit in the last tiles.  Tokens whose rows lie
-    past the cached items are compared with the oracle."""
+    past the cached items are compared with the oracle.  With packed UE8M0 scales (12500 rows per
+    expert) the GEMMs run on the CTA-pair kernel, whose clusters (at most half the SM count) cache
+    their first 256 candidates, i.e. tiles below 16 x (SM count) / 2 x 2: the same bound; the small
+    experts' third tiles are pairs whose second CTA has no rows."""
     T, H, I, E, topk = 50000, 4096, 2048, 32, 8
     wl = mi.Workload("items", 95, T, H, I, E, topk)
     logits = mi.router_logits(wl)
@@ -547,7 +551,12 @@ def test_forward_more_items_than_a_cta_caches():
     logits[:, small] -= 1000.0                 # experts 28-31 never chosen ...
     chosen = torch.arange(0, T, T // 300)[:300]
     logits[chosen.unsqueeze(1), small.unsqueeze(0)] += 2000.0   # ... except by these 300 tokens
-    layer = Layer(wl)
+    packed = fmt == "ue8m0_packed"
+    if packed:
+        from test_gpu_block_scaled import PackedLayer
+        layer = PackedLayer(wl)
+    else:
+        layer = Layer(wl)
     rp, _ = routing_of(wl)
     out = layer.forward(mi.hidden(wl).to(DEV), logits.to(DEV), rp)
     oids, _ = oracle.route(logits.numpy(), topk, True)
@@ -573,7 +582,8 @@ def test_forward_more_items_than_a_cta_caches():
             toks.add(int(sorted_[off[e]]) // topk)
     tokens = sorted(toks)
     w13q, w13s, w2q, w2s = layer.oracle_weights(set(oids[tokens].reshape(-1).tolist()))
-    ref = oracle.moe_forward(bits(mi.hidden(wl)), logits.numpy(), w13q, w13s, w2q, w2s, topk, True, tokens=tokens)
+    ref = oracle.moe_forward(bits(mi.hidden(wl)), logits.numpy(), w13q, w13s, w2q, w2s, topk, True, tokens=tokens,
+                             scale_fmt=oracle.SCALE_UE8M0 if packed else oracle.SCALE_F32)
     assert_output_close(out, ref["out"], rows=tokens)
 
 
