@@ -936,7 +936,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ CTA-pair block-scaled variant
-// The block-scaled GEMM on the two-SM MMA.  A cluster of two CTAs computes a 256-row x 256-column
+// The block-scaled w2 GEMM (router-weighted pair rows) on the two-SM MMA, for batches with many
+// rows per expert (the layer takes it from 512 routed rows per expert on average).  A cluster of
+// two CTAs computes a 256-row x 256-column
 // work item (two 128-row tiles of one expert): each CTA keeps its own 128 rows of A and one of the
 // item's two 128-row weight bands in its shared memory, and CTA 0 issues tcgen05.mma.cta_group::2
 // (M = 256), which reads both CTAs' operands and accumulates each CTA's 128 rows x 256 columns in
@@ -1128,6 +1130,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                              const GemmArgs a) {
+    // the w2 GEMM's epilogue only (the w13 GEMM ran faster on the one-CTA kernel, whose epilogue
+    // does not spill; this kernel's SiLU epilogue did at every register split)
+    static_assert(EPI == MOE_EPI_WEIGHTED_PAIRS_BF16, "the pair kernel runs the weighted-pairs epilogue");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t* base = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -1139,7 +1144,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
-    const int NT = a.N / 256;   // silu: gate band n with up band N/256 + n; otherwise bands 2n, 2n + 1
+    const int NT = a.N / 256;   // item n: weight bands 2n (CTA 0) and 2n + 1 (CTA 1)
     const int KB = a.K / BK;
     const bool mx = a.sf_packed == 2;
     const int KB4 = mx ? KB : (KB + 3) / 4;
@@ -1206,8 +1211,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
                     continue;
                 }
-                const int bcol0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? p.n * 128 : p.n * 256;
-                const int bcol1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 2 + p.n * 128 : bcol0 + 128;
+                const int bcol0 = p.n * 256, bcol1 = bcol0 + 128;
                 const int band = rank == 0 ? bcol0 : bcol1;   // the weight rows this CTA holds
                 int32_t by0, bdx, bdy;
                 if (a.b_tiled) {
@@ -1386,8 +1390,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             t.row0 = p.row0;
             t.e = p.e;
             t.n = p.n;
-            t.bcol0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? p.n * 128 : p.n * 256;
-            t.bcol1 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? a.N / 2 + p.n * 128 : t.bcol0 + 128;
+            t.bcol0 = p.n * 256;
+            t.bcol1 = t.bcol0 + 128;
             t.has1 = true;
             t.ok = true;
             const int64_t grow = t.row0 + row;
@@ -1402,8 +1406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (active) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const uint32_t c0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? lane_base + r * 128 + g * 64
-                                                                        : lane_base + g * 128 + r * 64;
+                    const uint32_t c0 = lane_base + g * 128 + r * 64;
                     tmem_ld32x2(c0, c0 + 32, acc + r * 64, acc + r * 64 + 32);
                 }
             } else {
