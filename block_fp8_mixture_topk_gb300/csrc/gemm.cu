@@ -64,12 +64,13 @@ struct RegSplit {
     static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 216 : 184;
     static_assert(128 * control + 256 * epilogue <= 384 * 168, "register split over the launch budget");
 };
-// the block-scaled kernels (no promotion in the epilogue): the SiLU epilogue needs fewer registers
-// and the control warps more (none spill at 88 / 208; at 72 / 216 the control warps spilled)
+// the block-scaled kernels (no promotion in the epilogue): the epilogues need fewer registers
+// and the control warps more (the SiLU kernel spills nothing at 88 / 208, its control warps did at
+// 72 / 216; the pair kernel spills nothing at 136 / 176, 8 / 48 bytes at 104 / 192)
 template <int EPI>
 struct RegSplitBs {
-    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 88 : 104;
-    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 208 : 192;
+    static constexpr uint32_t control = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 88 : 136;
+    static constexpr uint32_t epilogue = (EPI == MOE_EPI_SILU_MUL_QUANT) ? 208 : 176;
     static_assert(128 * control + 256 * epilogue <= 384 * 168, "register split over the launch budget");
 };
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
@@ -131,6 +132,40 @@ __device__ __forceinline__ void item_of(const GemmArgs& a, int64_t w, int NT, in
     m = f + static_cast<int>(l - static_cast<int64_t>(n) * c);
 }
 
+// The w2 GEMM's (router-weighted pair rows) last wave: when its R = total mod gridDim items would
+// keep at most half of the CTAs busy, each of them runs as two 128-column half items, so that 2R
+// SMs stream half an item's weights each instead of R SMs a whole item's (Mixtral-shaped layer:
+// ~190 items of 112 K blocks on 152 SMs).  Only when every unit is among the items the CTAs cache
+// (fill_item_cache), so that decode_tile's lookup of a later item never meets a half item.
+// Returns R, or 0 for no split.
+template <int EPI>
+__device__ __forceinline__ int64_t tail_halves(const GemmArgs& a, int64_t total) {
+    if constexpr (EPI != MOE_EPI_WEIGHTED_PAIRS_BF16) {
+        return 0;
+    } else {
+        if (a.N % 256 != 0) return 0;
+        const int64_t G = gridDim.x, R = total % G;
+        return (R > 0 && 2 * R <= G && total + R <= static_cast<int64_t>(ITEMS) * G) ? R : 0;
+    }
+}
+
+// Unit w of the non-SiLU GEMMs -> tile m and column block n (256 columns), or for a half item of
+// the split last wave n = -(128-column band + 1).  Units: total - halves whole items, then two
+// units for each of the last `halves` items.
+__device__ __forceinline__ void unit_of(int64_t w, int NT, int64_t total, int64_t halves, int& m, int& n) {
+    if (halves > 0 && w >= total - halves) {
+        const int64_t h = w - (total - halves);
+        const int64_t item = total - halves + (h >> 1);
+        const int64_t mt = item / NT;
+        m = static_cast<int>(mt);
+        n = -(2 * static_cast<int>(item - mt * NT) + static_cast<int>(h & 1) + 1);
+    } else {
+        const int64_t mt = w / NT;
+        m = static_cast<int>(mt);
+        n = static_cast<int>(w - mt * NT);
+    }
+}
+
 template <int EPI, class Ctl>
 __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, int64_t k, int64_t w, int NT) {
     Tile t;
@@ -140,6 +175,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, i
         t.e = ctl->item_e[k];
         t.row0 = ctl->item_r0[k];
     } else {
+        // (past the cached items there are no half items: tail_halves)
         int m, n;
         if constexpr (EPI != MOE_EPI_SILU_MUL_QUANT) {
             m = static_cast<int>(w / NT);
@@ -158,10 +194,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, i
         t.bcol0 = t.n * 128;
         t.bcol1 = a.N / 2 + t.n * 128;
         t.has1 = true;
-    } else {
+    } else if (t.n >= 0) {
         t.bcol0 = t.n * 256;
         t.bcol1 = t.bcol0 + 128;
         t.has1 = t.bcol1 < a.N;
+    } else {
+        t.bcol0 = (-t.n - 1) * 128;   // a half item of the split last wave
+        t.bcol1 = t.bcol0 + 128;
+        t.has1 = false;
     }
     return t;
 }
@@ -195,16 +235,15 @@ __device__ __forceinline__ void load_b_pair(uint32_t dst, const CUtensorMap* m, 
 // tile-by-tile order (its column blocks of one expert run in the same wave for the shapes served,
 // and the reorder gained nothing measurable there).
 template <int EPI, class Ctl>
-__device__ __forceinline__ void fill_item_cache(const GemmArgs& a, Ctl* ctl, int64_t total, int NT) {
+__device__ __forceinline__ void fill_item_cache(const GemmArgs& a, Ctl* ctl, int64_t total, int64_t halves, int NT) {
     for (int64_t k = threadIdx.x; k < ITEMS; k += blockDim.x) {
         const int64_t w = blockIdx.x + k * gridDim.x;
-        if (w >= total) break;
+        if (w >= total + halves) break;
         int m, n;
         if constexpr (EPI == MOE_EPI_SILU_MUL_QUANT) {
             item_of(a, w, NT, m, n);
         } else {
-            m = static_cast<int>(w / NT);
-            n = static_cast<int>(w - static_cast<int64_t>(m) * NT);
+            unit_of(w, NT, total, halves, m, n);
         }
         ctl->item_n[k] = n;
         ctl->item_e[k] = a.tile_expert[m];
@@ -432,7 +471,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const int64_t total = ntiles * NT;
-    fill_item_cache<EPI>(a, ctl, total, NT);
+    const int64_t halves = tail_halves<EPI>(a, total);
+    const int64_t units = total + halves;
+    fill_item_cache<EPI>(a, ctl, total, halves, NT);
     __syncthreads();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -447,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0, issued = 0;
             bool ok = true;
             int64_t k = 0;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
                 const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) {
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
@@ -507,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t q = 0;
         bool ok = true;
         int64_t k = 0;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+        for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
             const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int nb0 = (EPI == MOE_EPI_SILU_MUL_QUANT) ? t.n : t.bcol0 / 128;
@@ -547,7 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0, buf = 0, bphase = 0;
             bool ok = true;
             int64_t k = 0;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
                 const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) continue;
                 const uint32_t idesc = t.has1 ? idesc_full : idesc_half;
@@ -591,7 +632,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t buf = 0, bphase = 0, tile_iter = 0, q = 0;
         bool ok = true;
         int64_t k = 0;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+        for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
             const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int64_t grow = t.row0 + row;
@@ -752,7 +793,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ntiles < 0) ntiles = 0;
     if (ntiles > a.max_tiles) ntiles = a.max_tiles;
     const int64_t total = ntiles * NT;
-    fill_item_cache<EPI>(a, ctl, total, NT);
+    const int64_t halves = tail_halves<EPI>(a, total);
+    const int64_t units = total + halves;
+    fill_item_cache<EPI>(a, ctl, total, halves, NT);
     __syncthreads();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -766,7 +809,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             int64_t k = 0;
             const int NBn = a.N / 128;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
                 const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) {
                     status_set(a.status, MOE_STATUS_BAD_EXPERT_ID);
@@ -828,7 +871,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t phase = 0, items = 0, sf_loads = 0;
             bool ok = true;
             int64_t k = 0;
-            for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+            for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
                 const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
                 if (!t.ok) continue;
                 const int n = t.has1 ? 256 : 128;
@@ -890,7 +933,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t tile_iter = 0;
         bool ok = true;
         int64_t k = 0;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x, ++k) {
+        for (int64_t w = blockIdx.x; w < units && ok; w += gridDim.x, ++k) {
             const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int64_t grow = t.row0 + row;

@@ -602,6 +602,21 @@ def test_forward_small_shapes(T, H, I, E, topk):
     assert_output_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("fmt", ["f32", "ue8m0_packed"])
+def test_forward_w2_last_wave_in_half_items(fmt):
+    """The w2 GEMM runs a last wave that would keep at most half of the CTAs busy as 128-column half
+    items.  200 tokens, top-2 over 4 experts, H=768: four tiles of three 256-column items each, all
+    in the one partial wave, so every item is split (bands 0..5); every token against the oracle,
+    for the fp32-scale and the block-scaled kernel."""
+    wl = mi.Workload("halves", 196, 200, 768, 256, 4, 2)
+    if fmt == "f32":
+        out, ref = run_layer(wl)
+    else:
+        from test_gpu_block_scaled import run_packed_layer
+        out, ref = run_packed_layer(wl)
+    assert_output_close(out, ref["out"])
+
+
 @pytest.mark.parametrize("T,H,I,E,topk", [
     (64, 128, 128, 16, 8),       # 512 routed pairs: the one-launch sort + quantisation
     (65, 128, 128, 16, 8),       # 520 pairs: the three sort kernels and the grid-wide quantiser
