@@ -847,6 +847,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.epi = MOE_EPI_SILU_MUL_QUANT;
         g.scale_fmt = scale_fmt;
         g.sorted_pair_ids = sorted;
+        g.row_offsets = reinterpret_cast<const int32_t*>(ws + L.eoff);
+        g.row_padded = reinterpret_cast<const int32_t*>(ws + L.poff);
         g.out_q = a2;
         g.out_scale = a2s;
         g.os_row_stride = 1;
@@ -882,6 +884,8 @@ int moe_fp8_block_forward_ex(const uint16_t* hidden, const float* router_logits,
         g.epi = MOE_EPI_WEIGHTED_PAIRS_BF16;
         g.out_bf16 = ypairs;
         g.sorted_pair_ids = sorted;
+        g.row_offsets = reinterpret_cast<const int32_t*>(ws + L.eoff);
+        g.row_padded = reinterpret_cast<const int32_t*>(ws + L.poff);
         g.topk_weights = wts;
         g.topk = topk;
         g.num_pairs = P;

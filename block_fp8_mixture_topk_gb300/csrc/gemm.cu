@@ -94,8 +94,9 @@ struct SmemCtl {
     alignas(16) float stage[NUM_EPI_WARPS][32 * 20];   // per-warp store staging: 32 rows x 16 floats (+4 pad)
     alignas(16) float scl[SR][SCL];    // scale ring: a_scale of the tile's 128 rows, then the two weight scales
     int item_n[ITEMS];                 // the CTA's work items (see item_of), in its visiting order: column block,
-    int item_e[ITEMS];                 // the tile's expert
-    int item_r0[ITEMS];                // and first row
+    int item_e[ITEMS];                 // the tile's expert,
+    int item_r0[ITEMS];                // first row
+    int item_live[ITEMS];              // and real rows (Tile::live)
 };
 constexpr int STAGE_ROW = 20;          // floats per staged row (80 B: conflict-free 16-byte slots)
 constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE + B_TILE) + sizeof(SmemCtl);
@@ -106,6 +107,7 @@ struct Tile {
     int e;
     int n;
     int bcol0, bcol1;
+    int live;       // real rows of the tile (its first `live` rows), or -1: check sorted_pair_ids
     bool has1;
     bool ok;
 };
@@ -174,6 +176,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, i
         t.n = ctl->item_n[k];
         t.e = ctl->item_e[k];
         t.row0 = ctl->item_r0[k];
+        t.live = ctl->item_live[k];
     } else {
         // (past the cached items there are no half items: tail_halves)
         int m, n;
@@ -186,6 +189,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const Ctl* ctl, i
         t.n = n;
         t.e = a.tile_expert[m];
         t.row0 = a.tile_row0[m];
+        t.live = -1;
     }
     t.ok = t.e >= 0 && t.e < a.E && t.row0 >= 0 && t.row0 + BM <= a.a_rows;
     // the packed scale-factor tiles of A cover rows 128q .. 128q + 127
@@ -245,9 +249,17 @@ __device__ __forceinline__ void fill_item_cache(const GemmArgs& a, Ctl* ctl, int
         } else {
             unit_of(w, NT, total, halves, m, n);
         }
+        const int e = a.tile_expert[m];
+        const int32_t r0 = a.tile_row0[m];
+        int live = -1;
+        if (a.row_offsets && a.row_padded && e >= 0 && e < a.E) {
+            const int64_t l = static_cast<int64_t>(a.row_offsets[e + 1]) - a.row_offsets[e] - (r0 - a.row_padded[e]);
+            live = static_cast<int>(l < 0 ? 0 : (l > BM ? BM : l));
+        }
         ctl->item_n[k] = n;
-        ctl->item_e[k] = a.tile_expert[m];
-        ctl->item_r0[k] = a.tile_row0[m];
+        ctl->item_e[k] = e;
+        ctl->item_r0[k] = r0;
+        ctl->item_live[k] = live;
     }
 }
 
@@ -638,7 +650,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t grow = t.row0 + row;
             // rows whose sorted pair id is -1 are padding: a warp with no real row skips the
             // promotion (decode tiles hold a few real rows out of 128)
-            const bool row_real = a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0;
+            const bool row_real = t.live >= 0 ? row < t.live
+                                              : (a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0);
             const bool warp_live = __any_sync(0xffffffffu, row_real);
             const bool active = ((EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1) && warp_live;
             float acc[128];
@@ -740,6 +753,7 @@ struct SmemCtlBs {
     int item_n[ITEMS];
     int item_e[ITEMS];
     int item_r0[ITEMS];
+    int item_live[ITEMS];
 };
 constexpr size_t SMEM_BYTES_BS = 1024 + STAGES * (A_TILE + B_TILE + SF_STAGE) + sizeof(SmemCtlBs);
 static_assert(SMEM_BYTES_BS <= 232448, "shared memory per CTA exceeds the sm_103 limit");
@@ -937,7 +951,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const Tile t = decode_tile<EPI>(a, ctl, k, w, NT);
             if (!t.ok) continue;
             const int64_t grow = t.row0 + row;
-            const bool row_real = a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0;
+            const bool row_real = t.live >= 0 ? row < t.live
+                                              : (a.sorted_pair_ids == nullptr || a.sorted_pair_ids[grow] >= 0);
             const bool warp_live = __any_sync(0xffffffffu, row_real);
             const bool active = ((EPI == MOE_EPI_SILU_MUL_QUANT) || g == 0 || t.has1) && warp_live;
             float acc[128];

@@ -129,6 +129,12 @@ struct GemmArgs {
     // few tiles column by column (see item_of in gemm.cu); nullptr, and the other epilogues, keep
     // the tile-by-tile order
     const int32_t* padded_offsets;
+    // optional [E + 1] offsets of each expert's real rows and of its padded rows in the sorted layout
+    // (the sort places an expert's real rows first in its padded region): the epilogues then take a
+    // tile's real rows from them, cached per work item, instead of loading sorted_pair_ids for
+    // every row at the start of an item
+    const int32_t* row_offsets;
+    const int32_t* row_padded;
     int epi;
     float* out_f32;
     uint8_t* out_q;
