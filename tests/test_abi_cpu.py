@@ -81,6 +81,9 @@ def test_forward_kernel_count_with_options():
     assert kc(1, 7168, 2048, 256, 8, dsv3, scale_fmt="ue8m0_packed") == 5
     assert kc(17, 7168, 2048, 256, 8, dsv3, moe.ops.MOE_WEIGHTS_NVFP4) == 3 * 3
     assert kc(0, 7168, 2048, 256, 8, dsv3) == 0
+    # the CTA-pair w2 GEMM replaces the one-CTA launch: the same 8 launches per step
+    for fmt in ("f32", "ue8m0_packed", "mxfp8"):
+        assert kc(16384, 2048, 768, 128, 8, scale_fmt=fmt) == 8
 
 
 def test_pair_path_selection_without_a_device():
